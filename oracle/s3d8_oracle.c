@@ -1,0 +1,198 @@
+/*
+ * Plain CPU oracle for the S3D8 W2.7A8 linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the test suite, the package smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header, table or
+ * constant with the CUDA library.
+ *
+ * Everything here is a direct, slow, scalar restatement of the definitions on
+ * two pages:
+ *   [P]  "Llama-Mobile: Efficient 2.7-Bit Quantization of VLMs" (arXiv
+ *        2608.21134), section 3.4 "The S3D8 Format", Equation 1 and the
+ *        domains that follow it; section 4.3 for Y = X W^T.
+ *   [B]  "11 billion parameters on a phone" (Graphcore Research blog), section
+ *        "S3D8 design notes" -> "Bit layout" and "Output channel packing", and
+ *        the fused matrix-vector example (scale dtypes and epilogue order).
+ *
+ * Readings taken where the pages leave a step open (each is listed with its
+ * reason in the design notes of the repository):
+ *   - bits 1..5 of a byte hold Q with Q0 at bit 1 (so I0 = 2Q + S0 and
+ *     I1 = 32 S1 + Q are both plain indices, as [B] "Bit layout" states);
+ *   - sign selector 0 means +, 1 means - ([B] "Bit layout");
+ *   - byte (g, k) carries output channels 3g, 3g+1, 3g+2 at input column k,
+ *     selector S_d and centroid column d going with channel 3g+d
+ *     ([P] Eq. 1: C[q][i mod 3]; [B] "Output channel packing");
+ *   - N is padded up to 3*ceil(N/3); the padded lanes never reach an output;
+ *   - activations: one fp32 scale per token row, s = absmax / 127 (the same
+ *     absmax rule [P] gives for the weight channel scale alpha), q =
+ *     round-half-even(x / s) clamped to [-127, 127]; an all-zero row gives
+ *     s = 0 and q = 0;
+ *   - output: out[m,n] = xscale[m] * acc[m,n] * chan_scale[n], evaluated here
+ *     in fp64 (the GPU evaluates it in fp32 and rounds once to bf16).
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math, no
+ * FMA contraction, so that the fp32 activation quantiser is plain IEEE
+ * single-precision division and rounding on every host).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* bfloat16 is the upper half of an IEEE binary32; widening is exact. */
+static float bf16_bits_to_float(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* ---------------------------------------------------------------------------
+ * Byte layout, [B] "Bit layout": the byte is [S2 xor S0, S1, Q4..Q0, S0] from
+ * bit 7 down to bit 0.
+ * ------------------------------------------------------------------------- */
+
+/* Split one packed byte into its centroid index Q and the three sign
+ * selectors S0, S1, S2. */
+void s3d8o_byte_fields(uint8_t b, int32_t *Q, int32_t *S0, int32_t *S1, int32_t *S2)
+{
+    int s0 = b & 1;                 /* bit 0            */
+    int q = (b >> 1) & 31;          /* bits 1..5        */
+    int s1 = (b >> 6) & 1;          /* bit 6            */
+    int s2_xor_s0 = (b >> 7) & 1;   /* bit 7            */
+    *Q = q;
+    *S0 = s0;
+    *S1 = s1;
+    *S2 = s2_xor_s0 ^ s0;           /* recover S2       */
+}
+
+/* Inverse of s3d8o_byte_fields: build the byte from its fields. */
+uint8_t s3d8o_pack_byte(int32_t Q, int32_t S0, int32_t S1, int32_t S2)
+{
+    return (uint8_t)((S0 & 1) | ((Q & 31) << 1) | ((S1 & 1) << 6) | (((S2 ^ S0) & 1) << 7));
+}
+
+/* One decoded INT8 weight: component d (0, 1, 2) of the byte, i.e. the
+ * s * C[Q][d] factor of [P] Eq. 1 without the channel scale alpha.
+ * C is the 32 x 3 absolute-value centroid table, row-major C[q*3 + d]. */
+int32_t s3d8o_decode_component(uint8_t b, const int8_t *C, int32_t d)
+{
+    int32_t Q, S[3];
+    s3d8o_byte_fields(b, &Q, &S[0], &S[1], &S[2]);
+    int32_t c = C[Q * 3 + d];
+    return S[d] ? -c : c;
+}
+
+/* Dense INT8 weight matrix W[n, k] (n < N) from packed[G, K], G = ceil(N/3).
+ * Output row n comes from packed row n / 3, component n % 3 ([P] Eq. 1 with
+ * q_{floor(i/3), j} and C_{q, i mod 3}). */
+void s3d8o_decode(const uint8_t *packed, const int8_t *C, int64_t N, int64_t K, int8_t *w)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        int64_t g = n / 3;
+        int32_t d = (int32_t)(n % 3);
+        for (int64_t k = 0; k < K; ++k)
+            w[n * K + k] = (int8_t)s3d8o_decode_component(packed[g * K + k], C, d);
+    }
+}
+
+/* Pack a dense sign/index description into bytes.
+ *   Q[G, K]     centroid index per (group, column), 0..31
+ *   S[3G, K]    sign selector per (channel, column), 0 or 1 (padded channels
+ *               included, so that the caller controls every bit)
+ * Output packed[G, K]. */
+void s3d8o_pack(const int32_t *Q, const int32_t *S, int64_t G, int64_t K, uint8_t *packed)
+{
+    for (int64_t g = 0; g < G; ++g)
+        for (int64_t k = 0; k < K; ++k)
+            packed[g * K + k] = s3d8o_pack_byte(Q[g * K + k], S[(3 * g + 0) * K + k],
+                                                S[(3 * g + 1) * K + k], S[(3 * g + 2) * K + k]);
+}
+
+/* ---------------------------------------------------------------------------
+ * Activation quantisation (per-token absmax INT8), fp32 throughout.
+ * x is bf16 bit patterns, row-major [M, K].
+ * ------------------------------------------------------------------------- */
+void s3d8o_quantize_act(const uint16_t *x, int64_t M, int64_t K, int8_t *xq, float *xscale)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = x + m * K;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(bf16_bits_to_float(row[k]));
+            if (a > amax)
+                amax = a;
+        }
+        float s = amax / 127.0f;
+        xscale[m] = s;
+        for (int64_t k = 0; k < K; ++k) {
+            int32_t q = 0;
+            if (s != 0.0f) {
+                float r = rintf(bf16_bits_to_float(row[k]) / s); /* ties to even */
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
+                q = (int32_t)r;
+            }
+            xq[m * K + k] = (int8_t)q;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * The linear layer, Y = X W^T ([P] section 4.3), split into the exact integer
+ * accumulation and the scaled output.
+ * ------------------------------------------------------------------------- */
+
+/* acc[m, n] = sum_k xq[m, k] * Wq[n, k] in int64, Wq decoded byte by byte.
+ * Returns the number of accumulators that fall outside int32. */
+int64_t s3d8o_linear_acc(const uint8_t *packed, const int8_t *C, const int8_t *xq,
+                         int64_t M, int64_t N, int64_t K, int64_t *acc)
+{
+    int64_t out_of_range = 0;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t g = n / 3;
+            int32_t d = (int32_t)(n % 3);
+            int64_t sum = 0;
+            for (int64_t k = 0; k < K; ++k)
+                sum += (int64_t)xq[m * K + k] *
+                       (int64_t)s3d8o_decode_component(packed[g * K + k], C, d);
+            acc[m * N + n] = sum;
+            if (sum > INT32_MAX || sum < INT32_MIN)
+                ++out_of_range;
+        }
+    }
+    return out_of_range;
+}
+
+/* Same sum for a list of (m, n) pairs only, for spot checks at full size. */
+void s3d8o_linear_acc_at(const uint8_t *packed, const int8_t *C, const int8_t *xq,
+                         int64_t M, int64_t N, int64_t K,
+                         const int64_t *ms, const int64_t *ns, int64_t count, int64_t *acc)
+{
+    (void)M;
+    (void)N;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m = ms[i], n = ns[i];
+        int64_t g = n / 3;
+        int32_t d = (int32_t)(n % 3);
+        int64_t sum = 0;
+        for (int64_t k = 0; k < K; ++k)
+            sum += (int64_t)xq[m * K + k] *
+                   (int64_t)s3d8o_decode_component(packed[g * K + k], C, d);
+        acc[i] = sum;
+    }
+}
+
+/* out[m, n] = xscale[m] * acc[m, n] * alpha[n], in fp64 (exact products of the
+ * stored fp32 / bf16 / integer values up to one fp64 rounding each).
+ * chan_scale is bf16 bit patterns [N]. */
+void s3d8o_linear_out(const int64_t *acc, const float *xscale, const uint16_t *chan_scale,
+                      int64_t M, int64_t N, double *out)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            out[m * N + n] = (double)xscale[m] * (double)acc[m * N + n] *
+                             (double)bf16_bits_to_float(chan_scale[n]);
+}

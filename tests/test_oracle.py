@@ -1,0 +1,349 @@
+"""Pins for the CPU oracle, against what the pages and plain mathematics fix.
+
+No GPU.  Each test pins the oracle to something other than itself: values
+decoded by hand from the pages' bit layout, the pages' second description of
+the decoder (three permuted signed 64-entry tables indexed by I0, I1, I2),
+the reflection structure of the codebook, closed forms, textbook integer
+matrix products, and exact rational arithmetic.
+
+Pages: "11 billion parameters on a phone" (Graphcore Research blog),
+sections "Bit layout", "Fusing sign selection into lookups", "Absolute-value
+centroids and sign selection", "Output channel packing", "Format decoding on
+Arm CPUs"; "Llama-Mobile: Efficient 2.7-Bit Quantization of VLMs", section
+3.4 (Eq. 1, domains, bits per element, alpha = absmax / 127).
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import s3d8_inputs as si
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def hand_table():
+    """C[q][d] = 4q + d + 1, the table the golden fixture was decoded with."""
+    return np.array([[4 * q + d + 1 for d in range(3)] for q in range(32)], dtype=np.int8)
+
+
+def load_fixture():
+    rows = []
+    with open(os.path.join(HERE, "golden", "byte_layout.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tok = line.split()
+            rows.append([int(tok[0], 16)] + [int(t) for t in tok[1:]])
+    return rows
+
+
+def signed_tables_from_pages(C):
+    """The decoder as the blog's "Format decoding on Arm CPUs" describes it.
+
+    Each column of the 32 x 3 absolute table is expanded over both signs into
+    a 64-entry signed table: components 0 and 2 in sign-minor order (index =
+    2Q + s), component 1 in sign-major order (index = 32 s + Q).
+    """
+    C = np.asarray(C, dtype=np.int64)
+    T0 = np.zeros(64, np.int64)
+    T1 = np.zeros(64, np.int64)
+    T2 = np.zeros(64, np.int64)
+    for q in range(32):
+        for s in (0, 1):
+            sign = -1 if s else 1
+            T0[2 * q + s] = sign * C[q, 0]
+            T1[32 * s + q] = sign * C[q, 1]
+            T2[2 * q + s] = sign * C[q, 2]
+    return T0, T1, T2
+
+
+def decode_by_pages_lut(b, tables):
+    """Three lookups with indices built by the blog's 5 logical operations."""
+    T0, T1, T2 = tables
+    i0 = b & 0x3F
+    i1 = (b >> 1) & 0x3F
+    i2 = i0 ^ (b >> 7)
+    return int(T0[i0]), int(T1[i1]), int(T2[i2])
+
+
+def dense_by_pages_lut(packed, C, N):
+    tables = signed_tables_from_pages(C)
+    G, K = packed.shape
+    W = np.zeros((3 * G, K), np.int64)
+    lut = np.array([decode_by_pages_lut(b, tables) for b in range(256)], dtype=np.int64)
+    for d in range(3):
+        W[d::3] = lut[packed.astype(np.int64), d]
+    return W[:N]
+
+
+def some_tables():
+    rng = np.random.default_rng(1234)
+    yield hand_table()
+    yield rng.integers(0, 128, size=(32, 3)).astype(np.int8)        # includes 0 and 127
+    t = rng.integers(1, 128, size=(32, 3)).astype(np.int8)
+    t[0] = 0
+    t[31] = 127
+    yield t
+    yield np.zeros((32, 3), np.int8)
+
+
+# --------------------------------------------------------------------------
+# Byte layout
+# --------------------------------------------------------------------------
+
+def test_fixture_fields_and_values():
+    C = hand_table()
+    for b, Q, S0, S1, S2, I0, I1, I2, w0, w1, w2 in load_fixture():
+        assert oracle.byte_fields(b) == (Q, S0, S1, S2), hex(b)
+        assert oracle.pack_byte(Q, S0, S1, S2) == b, hex(b)
+        # the fixture's indices are the blog's I0 / I1 / I2 of the same byte
+        assert (b & 0x3F, (b >> 1) & 0x3F, (b & 0x3F) ^ (b >> 7)) == (I0, I1, I2)
+        assert (I0, I1, I2) == (2 * Q + S0, 32 * S1 + Q, 2 * Q + S2)
+        got = tuple(oracle.decode_component(b, C, d) for d in range(3))
+        assert got == (w0, w1, w2), hex(b)
+
+
+@pytest.mark.parametrize("which", range(4))
+def test_exhaustive_decode_matches_pages_lut_reading(which):
+    C = list(some_tables())[which]
+    tables = signed_tables_from_pages(C)
+    for b in range(256):
+        want = decode_by_pages_lut(b, tables)
+        got = tuple(oracle.decode_component(b, C, d) for d in range(3))
+        assert got == want, (hex(b), got, want)
+
+
+def test_layout_is_a_bijection():
+    seen = set()
+    for b in range(256):
+        f = oracle.byte_fields(b)
+        assert 0 <= f[0] < 32 and all(s in (0, 1) for s in f[1:])
+        assert oracle.pack_byte(*f) == b
+        seen.add(f)
+    assert len(seen) == 256
+
+
+def test_reflections():
+    """The 256 signed codewords are the 8 sign reflections of 32 absolute rows
+    (blog, "Absolute-value centroids and sign selection"); in the physical
+    layout each reflection is a fixed XOR on the byte."""
+    rng = np.random.default_rng(7)
+    C = rng.integers(1, 128, size=(32, 3)).astype(np.int8)
+    flips = {0x41: (-1, -1, -1), 0x81: (-1, 1, 1), 0x40: (1, -1, 1), 0x80: (1, 1, -1)}
+    for b in range(256):
+        base = [oracle.decode_component(b, C, d) for d in range(3)]
+        assert [abs(v) for v in base] == [int(C[oracle.byte_fields(b)[0], d]) for d in range(3)]
+        for mask, sgn in flips.items():
+            got = [oracle.decode_component(b ^ mask, C, d) for d in range(3)]
+            assert got == [s * v for s, v in zip(sgn, base)], (hex(b), hex(mask))
+    # the 8 reflections of one row are all distinct when the row has no zero
+    row = {tuple(oracle.decode_component(b, C, d) for d in range(3)) for b in range(256)
+           if oracle.byte_fields(b)[0] == 5}
+    assert len(row) == 8
+
+
+def test_output_channel_packing_and_padding():
+    """Byte (g, k) feeds channels 3g, 3g+1, 3g+2 at column k; N is padded up to
+    a multiple of 3 and the pad lanes never reach an output."""
+    rng = np.random.default_rng(3)
+    C = rng.integers(1, 128, size=(32, 3)).astype(np.int8)
+    for N in (1, 2, 3, 4, 5, 7, 96):
+        G = oracle.groups(N)
+        K = 32
+        packed = rng.integers(0, 256, size=(G, K), dtype=np.uint8)
+        W = oracle.decode(packed, C, N)
+        assert W.shape == (N, K)
+        np.testing.assert_array_equal(W.astype(np.int64), dense_by_pages_lut(packed, C, N))
+        # flipping every pad-lane sign selector changes nothing
+        if 3 * G > N:
+            Q = np.array([[oracle.byte_fields(b)[0] for b in r] for r in packed], np.int32)
+            S = np.zeros((3 * G, K), np.int32)
+            for g in range(G):
+                for k in range(K):
+                    f = oracle.byte_fields(int(packed[g, k]))
+                    S[3 * g:3 * g + 3, k] = f[1:]
+            S[N:] ^= 1
+            packed2 = oracle.pack(Q, S)
+            assert not np.array_equal(packed2, packed)
+            np.testing.assert_array_equal(oracle.decode(packed2, C, N), W)
+
+
+def test_pack_roundtrip_matrix():
+    rng = np.random.default_rng(11)
+    G, K = 5, 48
+    Q = rng.integers(0, 32, size=(G, K)).astype(np.int32)
+    S = rng.integers(0, 2, size=(3 * G, K)).astype(np.int32)
+    packed = oracle.pack(Q, S)
+    for g in range(G):
+        for k in range(K):
+            f = oracle.byte_fields(int(packed[g, k]))
+            assert f == (Q[g, k], S[3 * g, k], S[3 * g + 1, k], S[3 * g + 2, k])
+
+
+# --------------------------------------------------------------------------
+# Accumulation: textbook integer products and closed forms
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 16), (2, 2, 16), (3, 4, 32), (5, 5, 256), (4, 96, 256),
+                                   (2, 7, 48)])
+def test_linear_acc_matches_textbook_matmul(M, N, K):
+    rng = np.random.default_rng(M * 1000 + N * 10 + K)
+    C = rng.integers(0, 128, size=(32, 3)).astype(np.int8)
+    packed = rng.integers(0, 256, size=(oracle.groups(N), K), dtype=np.uint8)
+    xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    W = dense_by_pages_lut(packed, C, N)
+    want = xq.astype(np.int64) @ W.T
+    acc, bad = oracle.linear_acc(packed, C, xq, N)
+    assert bad == 0
+    np.testing.assert_array_equal(acc, want)
+    ms = rng.integers(0, M, size=17)
+    ns = rng.integers(0, N, size=17)
+    np.testing.assert_array_equal(oracle.linear_acc_at(packed, C, xq, N, ms, ns), want[ms, ns])
+
+
+def test_constant_bytes_closed_form():
+    """All bytes equal with every selector positive: acc[m, 3g+d] = C[Q][d] * sum_k xq[m, k]."""
+    rng = np.random.default_rng(5)
+    C = rng.integers(1, 128, size=(32, 3)).astype(np.int8)
+    M, N, K = 3, 9, 64
+    for Q in (0, 17, 31):
+        b = oracle.pack_byte(Q, 0, 0, 0)
+        packed = np.full((oracle.groups(N), K), b, np.uint8)
+        xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+        acc, _ = oracle.linear_acc(packed, C, xq, N)
+        rs = xq.astype(np.int64).sum(axis=1)
+        for n in range(N):
+            np.testing.assert_array_equal(acc[:, n], int(C[Q, n % 3]) * rs)
+        # the all-negative reflection negates every accumulator exactly
+        acc_neg, _ = oracle.linear_acc(packed ^ np.uint8(0x41), C, xq, N)
+        np.testing.assert_array_equal(acc_neg, -acc)
+
+
+def test_int32_edge():
+    """|acc| <= 127 * 127 * K; at K = 14336 the extreme 231,225,344 still fits
+    int32, and at K = 133,145 it does not."""
+    C = np.full((32, 3), 127, np.int8)
+    for K, fits in ((14336, True), (133145, False)):
+        packed = np.full((1, K), oracle.pack_byte(3, 0, 0, 0), np.uint8)
+        xq = np.full((1, K), 127, np.int8)
+        acc, bad = oracle.linear_acc(packed, C, xq, 3)
+        assert (acc == 16129 * K).all()
+        assert (bad == 0) == fits
+    assert 16129 * 14336 == 231_225_344
+
+
+# --------------------------------------------------------------------------
+# Activation quantisation (per-token absmax INT8)
+# --------------------------------------------------------------------------
+
+def bf16(vals):
+    return si.f32_to_bf16_bits(np.asarray(vals, np.float32))
+
+
+def test_quantize_ties_to_even_with_unit_scale():
+    # absmax 127 gives s = 127 / 127 = 1 exactly, so x / s = x
+    x = bf16([[127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -0.5, 126.5, 0.0, -127.0, 64.0, 1.0, -1.0,
+               0.25, 0.75]])
+    xq, xs = oracle.quantize_act(x)
+    assert xs[0] == np.float32(1.0)
+    assert xq.tolist() == [[127, 2, 4, -2, -4, 0, 2, 0, 126, 0, -127, 64, 1, -1, 0, 1]]
+
+
+def test_quantize_zero_row_and_signs():
+    rng = np.random.default_rng(9)
+    xf = rng.standard_normal((4, 64)).astype(np.float32)
+    xf[2] = 0.0
+    x = bf16(xf)
+    xq, xs = oracle.quantize_act(x)
+    assert xs[2] == 0.0 and (xq[2] == 0).all()
+    xneg = x ^ np.uint16(0x8000)          # flip the bf16 sign bit: exact negation
+    xneg[2] = 0
+    xqn, xsn = oracle.quantize_act(xneg)
+    np.testing.assert_array_equal(xsn, xs)
+    np.testing.assert_array_equal(xqn, -xq)
+
+
+def test_quantize_properties():
+    rng = np.random.default_rng(10)
+    x = si.activations(rng, 8, 512, outliers=True)
+    xf = si.bf16_bits_to_f32(x).astype(np.float64)
+    xq, xs = oracle.quantize_act(x)
+    amax = np.abs(xf).max(axis=1)
+    # the scale is absmax / 127 rounded once to fp32
+    for m in range(8):
+        exact = Fraction(float(amax[m])) / 127
+        half_ulp = Fraction(float(np.spacing(np.float32(xs[m])))) / 2
+        assert abs(Fraction(float(xs[m])) - exact) <= half_ulp
+        # the absmax element lands on +-127
+        assert np.abs(xq[m]).max() == 127
+        r = xf[m] / float(xs[m])
+        assert np.all(np.abs(r - xq[m]) <= 0.5 + 1e-5)
+    # scaling a row by 2 (exact in bf16) doubles the scale and keeps the codes
+    x2 = si.f32_to_bf16_bits(si.bf16_bits_to_f32(x) * np.float32(2.0))
+    xq2, xs2 = oracle.quantize_act(x2)
+    np.testing.assert_array_equal(xq2, xq)
+    np.testing.assert_array_equal(xs2, xs * np.float32(2.0))
+
+
+def test_quantize_agrees_with_fp64_rounding_away_from_ties():
+    rng = np.random.default_rng(12)
+    x = si.activations(rng, 16, 1024)
+    xf = si.bf16_bits_to_f32(x).astype(np.float64)
+    xq, xs = oracle.quantize_act(x)
+    r = xf / xs.astype(np.float64)[:, None]
+    frac = np.abs(r - np.floor(r) - 0.5)
+    safe = frac > 1e-4
+    np.testing.assert_array_equal(xq[safe], np.rint(r[safe]).astype(np.int8))
+
+
+# --------------------------------------------------------------------------
+# Output scaling and bits per element
+# --------------------------------------------------------------------------
+
+def test_linear_out_exact_rationals():
+    rng = np.random.default_rng(13)
+    M, N = 3, 5
+    acc = rng.integers(-2**31, 2**31, size=(M, N)).astype(np.int64)
+    xs = rng.random(M).astype(np.float32)
+    cs = si.f32_to_bf16_bits(rng.random(N).astype(np.float32) * 0.01)
+    out = oracle.linear_out(acc, xs, cs)
+    csf = si.bf16_bits_to_f32(cs)
+    for m in range(M):
+        for n in range(N):
+            exact = Fraction(float(xs[m])) * int(acc[m, n]) * Fraction(float(csf[n]))
+            assert abs(Fraction(out[m, n]) - exact) <= abs(exact) * Fraction(2, 2**52)
+
+
+@pytest.mark.parametrize("K,N", [(4096, 14336), (14336, 4096), (4096, 4096), (4096, 1024)])
+def test_bits_per_element_closed_form(K, N):
+    """Buffer sizes give 8/3 + 16/K bits per element up to padding and the
+    96-byte table (Llama-Mobile section 3.4)."""
+    G = oracle.groups(N)
+    bits = 8 * G * K + 16 * N + 8 * 96
+    bpp = bits / (N * K)
+    slack = (8 * (3 * G - N) * K / 3 + 8 * 96) / (N * K)
+    assert abs(bpp - (8 / 3 + 16 / K)) <= slack + 1e-12
+    assert 2.66 < bpp < 2.68
+
+
+def test_bits_per_element_whole_text_stack():
+    total_bits = 0
+    total_params = 0
+    for _, K, N in list(si.LLAMA_11B_LAYER) * si.LLAMA_11B_LAYERS + [si.LLAMA_11B_HEAD]:
+        total_bits += 8 * si.groups(N) * K + 16 * N + 8 * 96
+        total_params += N * K
+    bpp = total_bits / total_params
+    # the pages report 2.68 bits/parameter for the whole VLM
+    assert 2.66 < bpp < 2.69
+
+
+def test_input_bf16_conversion_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(14)
+    f = (rng.standard_normal(4096) * np.exp(rng.uniform(-30, 30, 4096))).astype(np.float32)
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(si.f32_to_bf16_bits(f), want)
