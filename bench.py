@@ -1,0 +1,511 @@
+"""Benchmark: S3D8 W2.7A8 linear layers of a Llama-3.2-11B text decoder layer at M = 1.
+
+One step is one pass of the whole hot path over one token: per-token INT8
+quantisation of the four distinct activations of a decoder layer (attention
+input, attention output, MLP input, MLP hidden), then the seven S3D8 linears
+(q, k, v, o, gate, up, down) through the library's C ABI.  Weights are
+synthetic (seeded recipe in s3d8_inputs) and resident in HBM; the step cycles
+through 8 independent copies of the layer (582 MB of packed weights, well
+above the 129 MB L2) so that every step streams its weights from HBM.
+
+Printed JSON (one line, rank 0):
+  value      weight GB/s = (packed bytes + bf16 channel scales + tables) per
+             step / device time per step, over all ranks (weak scaling);
+  roofline   the GEMV kernel's algorithmic bytes (weights, activations,
+             scales, outputs) per launch / its average launch time, measured
+             with CUDA events inside the timed graphs, against the measured
+             HBM copy bandwidth;
+  e2e        the same metric with per-step host->device copies of the
+             activations from pinned memory and device->host copies of the
+             seven outputs, through the Python binding;
+  prefill    INT8 tensor-op rate of the same library at M = 2048 on the
+             gate/up and down shapes;
+  cpu_baseline  the plain CPU oracle, timed on this host on a bounded sample.
+
+`--impl reference` times the CPU oracle alone on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import s3d8_inputs as si  # noqa: E402
+
+METRIC = "S3D8 linear weight GB/s (M=1) & INT8 TOPS (prefill), % of roofline"
+UNIT = "GB/s"
+COPIES = 8
+WORKLOAD = ("Llama-3.2-11B text decoder layer, decode M=1: S3D8 linears q 4096->4096, "
+            "k/v 4096->1024, o 4096->4096, gate/up 4096->14336, down 14336->4096")
+
+
+def weight_bytes(K, N):
+    """Packed bytes + bf16 channel scales + the 32x3 int8 table."""
+    return si.groups(N) * K + 2 * N + 96
+
+
+def linear_bytes(M, K, N):
+    """Algorithmic bytes of one linear launch: weights, xq, xscale, output."""
+    return weight_bytes(K, N) + M * K + 4 * M + 2 * M * N
+
+
+LAYER_WEIGHT_BYTES = sum(weight_bytes(K, N) for _, K, N in si.LLAMA_11B_LAYER)
+ACT_K = {"attn": 4096, "o": 4096, "mlp": 4096, "down": 14336}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def gemv_source_sha():
+    h = hashlib.sha256()
+    for name in ("gemv.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "s3d8_a8_linear_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch():
+    """DRAM bytes per GEMV launch from the committed ncu summary, or None when
+    the kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "gemv_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("source_sha") != gemv_source_sha():
+            return None
+        return float(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def to_dev_bf16(bits, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+class LayerCopy:
+    def __init__(self, layer, dev, seed=0):
+        import torch
+        self.mats = []
+        for mat in si.layer_matrices(layer=layer, seed=seed):
+            self.mats.append(dict(
+                name=mat.name, K=mat.K, N=mat.N,
+                packed=torch.from_numpy(mat.packed).to(dev),
+                C=torch.from_numpy(mat.C).to(dev),
+                cs=to_dev_bf16(mat.chan_scale, dev)))
+
+
+class Step:
+    """Device buffers of one decoder-layer step at M tokens."""
+
+    def __init__(self, M, dev, seed=0):
+        import torch
+        self.M = M
+        self.x = {k: to_dev_bf16(si.acts(M, K, seed=seed, index=i), dev)
+                  for i, (k, K) in enumerate(ACT_K.items())}
+        self.xq = {k: torch.empty((M, K), dtype=torch.int8, device=dev) for k, K in ACT_K.items()}
+        self.xs = {k: torch.empty((M,), dtype=torch.float32, device=dev) for k in ACT_K}
+        self.out = {n: torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                    for n, _, N in si.LLAMA_11B_LAYER}
+
+    def run(self, s3d8, copy, events=None):
+        for k in ACT_K:
+            s3d8.quantize_act(self.x[k], self.xq[k], self.xs[k])
+        for j, m in enumerate(copy.mats):
+            a = si.LLAMA_11B_INPUT_OF[m["name"]]
+            if events is not None:
+                events[j][0].record()
+            s3d8.linear(m["packed"], m["C"], m["cs"], self.xq[a], self.xs[a], m["N"],
+                        out=self.out[m["name"]])
+            if events is not None:
+                events[j][1].record()
+
+
+def make_timing_events(torch):
+    try:
+        return [(torch.cuda.Event(enable_timing=True, external=True),
+                 torch.cuda.Event(enable_timing=True, external=True))
+                for _ in si.LLAMA_11B_LAYER]
+    except TypeError:
+        return None
+
+
+def gpu_arm(args):
+    import torch
+
+    import s3d8_a8_linear_gb300 as s3d8
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    s3d8.load(build_if_missing=True)
+
+    copies = [LayerCopy(r, dev) for r in range(COPIES)]
+    step = Step(1, dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize()
+
+    # eager warm-up (also sets kernel attributes outside capture)
+    with torch.cuda.stream(stream):
+        for r in range(COPIES):
+            step.run(s3d8, copies[r])
+    stream.synchronize()
+
+    # one graph per weight copy, each with per-linear timing events
+    graphs, events = [], []
+    for r in range(COPIES):
+        ev = make_timing_events(torch)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step.run(s3d8, copies[r], ev)
+        graphs.append(g)
+        events.append(ev)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % COPIES].replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(args.steps):
+            graphs[i % COPIES].replay()
+        t1.record(stream)
+    t1.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    ms_step = ms_total / args.steps
+
+    # per-linear launch durations from the events recorded inside the graphs
+    lin_ms, lin_bytes = [], []
+    if events[0] is not None:
+        for r in range(COPIES):
+            for j, (name, K, N) in enumerate(si.LLAMA_11B_LAYER):
+                lin_ms.append(events[r][j][0].elapsed_time(events[r][j][1]))
+                lin_bytes.append(linear_bytes(1, K, N))
+    status = s3d8.device_status()
+
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    value = world * LAYER_WEIGHT_BYTES / (ms_step * 1e-3) / 1e9
+    hbm_peak, _, peak_kind = load_peaks()
+    roofline = None
+    if lin_ms:
+        achieved = sum(lin_bytes) / (sum(lin_ms) * 1e-3) / 1e9
+        tr = traffic_per_launch()
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                    "traffic": tr, "kernel": "s3d8 gemv (M=1), 7 linears of the layer",
+                    "peak_kind": peak_kind,
+                    "per_linear_us": {n: round(1e3 * statistics.mean(
+                        lin_ms[r * 7 + j] for r in range(COPIES)), 2)
+                        for j, (n, _, _) in enumerate(si.LLAMA_11B_LAYER)}}
+
+    e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 2000))
+    prefill = prefill_measure(torch, s3d8, dev) if not args.skip_prefill else None
+    unpack = unpack_measure(torch, s3d8, dev)
+
+    if rank != 0:
+        return
+    cpu = None if args.skip_cpu else cpu_baseline(args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded S3D8 fields, bf16 N(0,1) activations; no trained weights)",
+        "config": {"workload": WORKLOAD, "M": 1, "weight_bytes_per_step": LAYER_WEIGHT_BYTES,
+                   "weight_copies": COPIES,
+                   "l2": f"inputs larger than L2: {COPIES} rotating layer copies "
+                         f"({COPIES * LAYER_WEIGHT_BYTES / 1e6:.0f} MB of weights)",
+                   "launch": "one CUDA graph per step (4 quantize_act + 7 linear)",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps * (len(ACT_K) + len(si.LLAMA_11B_LAYER)),
+        "device_status": status,
+        "roofline": roofline, "e2e": e2e, "prefill": prefill, "unpack": unpack,
+        "clocks": clocks, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+def e2e_measure(torch, s3d8, copies, dev, steps):
+    """Same metric through the Python binding, with the activations copied in
+    from pinned host memory and the seven outputs copied back every step."""
+    step = Step(1, dev)
+    host_x = {k: torch.from_numpy(si.acts(1, K, seed=5, index=i).view(np.int16)).view(
+        torch.bfloat16).pin_memory() for i, (k, K) in enumerate(ACT_K.items())}
+    host_out = {n: torch.empty((1, N), dtype=torch.bfloat16).pin_memory()
+                for n, _, N in si.LLAMA_11B_LAYER}
+    stream = torch.cuda.Stream(dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        step.run(s3d8, copies[0])
+    stream.synchronize()
+    for r in range(COPIES):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step.run(s3d8, copies[r])
+        graphs.append(g)
+    h2d = sum(t.numel() * 2 for t in host_x.values())
+    d2h = sum(t.numel() * 2 for t in host_out.values())
+
+    def one(i):
+        for k in ACT_K:
+            step.x[k].copy_(host_x[k], non_blocking=True)
+        graphs[i % COPIES].replay()
+        for n in host_out:
+            host_out[n].copy_(step.out[n], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            one(i)
+    stream.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(steps):
+            one(i)
+        t1.record(stream)
+    t1.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": round(LAYER_WEIGHT_BYTES / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
+            "steps": steps, "path": "Python binding captured in a CUDA graph, pinned copies"}
+
+
+def prefill_measure(torch, s3d8, dev, M=2048, reps=3):
+    res = {}
+    tot_ops, tot_ms = 0, 0.0
+    for name, K, N in si.SWEEP_SHAPES:
+        mat = si.matrix(name, K, N, seed=3)
+        packed = torch.from_numpy(mat.packed).to(dev)
+        C = torch.from_numpy(mat.C).to(dev)
+        cs = to_dev_bf16(mat.chan_scale, dev)
+        x = to_dev_bf16(si.acts(M, K, seed=3), dev)
+        xq, xs = s3d8.quantize_act(x)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        s3d8.linear(packed, C, cs, xq, xs, N, out=out)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            s3d8.linear(packed, C, cs, xq, xs, N, out=out)
+        t1.record()
+        t1.synchronize()
+        ms = t0.elapsed_time(t1) / reps
+        ops = 2 * M * N * K
+        res[name] = {"M": M, "K": K, "N": N, "us": round(ms * 1e3, 1),
+                     "tops": round(ops / (ms * 1e-3) / 1e12, 2)}
+        tot_ops += ops
+        tot_ms += ms
+    res["tops"] = round(tot_ops / (tot_ms * 1e-3) / 1e12, 2)
+    res["unit"] = "TOPS (int8 multiply-adds x2)"
+    return res
+
+
+def unpack_measure(torch, s3d8, dev, reps=20):
+    name, K, N = "gate", 4096, 14336
+    mats = [si.matrix(name, K, N, seed=4, index=i) for i in range(COPIES)]
+    packed = [torch.from_numpy(m.packed).to(dev) for m in mats]
+    Cs = [torch.from_numpy(m.C).to(dev) for m in mats]
+    w = torch.empty((N, K), dtype=torch.int8, device=dev)
+    s3d8.decode(packed[0], Cs[0], N, w)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(reps):
+        s3d8.decode(packed[i % COPIES], Cs[i % COPIES], N, w)
+    t1.record()
+    t1.synchronize()
+    ms = t0.elapsed_time(t1) / reps
+    rd = si.groups(N) * K
+    return {"shape": "4096x14336 (gate)", "us": round(ms * 1e3, 2),
+            "read_gbs": round(rd / (ms * 1e-3) / 1e9, 1),
+            "total_gbs": round((rd + N * K) / (ms * 1e-3) / 1e9, 1)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_layer_step(oracle, mats, xs_bits):
+    q = {k: oracle.quantize_act(xs_bits[k]) for k in ACT_K}
+    for m in mats:
+        xq, xsc = q[si.LLAMA_11B_INPUT_OF[m.name]]
+        oracle.linear(m.packed, m.C, m.chan_scale, xq, xsc, m.N)
+
+
+def cpu_baseline(seconds, max_steps=None):
+    import oracle
+    mats = si.layer_matrices(layer=0, seed=0)
+    xs_bits = {k: si.acts(1, K, seed=0, index=i) for i, (k, K) in enumerate(ACT_K.items())}
+    oracle.lib()
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle_layer_step(oracle, mats, xs_bits)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_steps and n >= max_steps):
+            break
+    return {"value": round(n * LAYER_WEIGHT_BYTES / el / 1e9, 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle", "seconds": round(el, 2),
+            "sample": f"{n} full layer steps at M=1 (4 activation quantisations + 7 linears), "
+                      "single-threaded plain C oracle"}
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    mats = si.layer_matrices(layer=0, seed=0)
+    xs_bits = {k: si.acts(1, K, seed=0, index=i) for i, (k, K) in enumerate(ACT_K.items())}
+    oracle.lib()
+    for _ in range(args.warmup):
+        oracle_layer_step(oracle, mats, xs_bits)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_layer_step(oracle, mats, xs_bits)
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    value = LAYER_WEIGHT_BYTES / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded S3D8 fields, bf16 N(0,1) activations)",
+        "config": {"workload": WORKLOAD, "M": 1, "weight_bytes_per_step": LAYER_WEIGHT_BYTES},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} full layer steps at M=1, single-threaded "
+                                   "plain C oracle"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=("s3d8", "reference"), default="s3d8")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-prefill", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        args.steps = 10 if args.steps is None else args.steps
+        args.warmup = 3 if args.warmup is None else args.warmup
+        reference_arm(args)
+        return
+    args.steps = 40000 if args.steps is None else args.steps
+    args.warmup = 400 if args.warmup is None else args.warmup
+    if args.warmup < 3:
+        args.warmup = 3
+    gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

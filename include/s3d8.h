@@ -1,0 +1,144 @@
+/*
+ * s3d8.h - C ABI of the GB300 (sm_103a) S3D8 W2.7A8 linear-layer library.
+ *
+ * The layer (Llama-Mobile: Efficient 2.7-Bit Quantization of VLMs, section 3.4,
+ * Eq. 1, and section 4.3 for Y = X W^T) is
+ *
+ *     out[m, n] = bf16( xscale[m] * chan_scale[n] * sum_k xq[m, k] * Wq[n, k] )
+ *
+ * where Wq[n, k] = s * C[q][n mod 3] is decoded on the fly from one packed byte
+ * per (n / 3, k).  Byte layout ("11 billion parameters on a phone", Graphcore
+ * Research blog, section "Bit layout"): bit 0 = S0, bits 1..5 = Q (Q0 in bit
+ * 1), bit 6 = S1, bit 7 = S2 xor S0; a selector of 0 is +, 1 is -.  Selector
+ * S_d and table column d belong to output channel 3g + d of packed row g
+ * (blog, "Output channel packing").
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer is caller-owned DEVICE memory unless stated otherwise.  The
+ *     library allocates nothing per call and keeps no state except one device
+ *     status word (see s3d8_device_status).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *     is the legacy default stream).  They neither synchronise nor read device
+ *     memory from the host.
+ *   - Arguments are checked before anything is launched; a failed check returns
+ *     a negative s3d8_status and touches no memory.  A launch failure returns
+ *     S3D8_ERR_CUDA.
+ *   - Shapes: M tokens, N output channels, K input columns.  G = ceil(N / 3)
+ *     packed rows.  M == 0 or N == 0 is a valid empty call (returns S3D8_OK and
+ *     launches nothing).  K must be a positive multiple of 16 (the pages' fused
+ *     kernel steps K by 16) and at most S3D8_MAX_K, so that every int32
+ *     accumulator is exact (127 * 127 * K < 2^31).
+ *   - Not checked, for speed: centroid values must lie in 0..127 and the bf16
+ *     inputs must be finite.
+ */
+#ifndef S3D8_H
+#define S3D8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define S3D8_MAX_K 133144
+#define S3D8_MAX_M (1 << 24)
+#define S3D8_MAX_N (1 << 26)
+
+typedef enum {
+    S3D8_OK = 0,
+    S3D8_ERR_INVALID_ARG = -1, /* null pointer, bad shape, K % 16 != 0, K too large */
+    S3D8_ERR_ALIGNMENT = -2,   /* a pointer misses its required alignment         */
+    S3D8_ERR_UNSUPPORTED = -3, /* algorithm not available for this shape/device   */
+    S3D8_ERR_CUDA = -4,        /* a CUDA call or kernel launch failed             */
+    S3D8_ERR_TIMEOUT = -5,     /* a bounded device-side wait ran out (sticky)     */
+    S3D8_ERR_WORKSPACE = -6    /* workspace missing or smaller than required      */
+} s3d8_status;
+
+/* Algorithm choice for s3d8_linear_ex.  AUTO picks by M. */
+typedef enum {
+    S3D8_ALGO_AUTO = 0,
+    S3D8_ALGO_GEMV = 1,    /* CUDA-core decode + dp4a GEMV, weights streamed once per 8 tokens */
+    S3D8_ALGO_SKINNY = 2,  /* decode in registers + mma.sync s8 (M up to a few hundred)       */
+    S3D8_ALGO_TC = 3       /* tcgen05 bf16 tensor-core GEMM with exact chunked int32 sums      */
+} s3d8_algo;
+
+/*
+ * Per-token INT8 activation quantisation (the pages fix channel-scaled INT8
+ * activations with one float scale per activation vector; the absmax/127 rule
+ * follows the paper's channel scale alpha_i = max_j |W_ij| / 127, section 3.4).
+ *   x_bf16 : [M, K] bfloat16, row-major, 16-byte aligned
+ *   xq     : [M, K] int8 output, row-major, 16-byte aligned
+ *   xscale : [M] fp32 output, xscale[m] = absmax_k |x[m,k]| / 127 (IEEE division)
+ * xq[m,k] = clamp(round_half_even(x[m,k] / xscale[m]), -127, 127) with IEEE fp32
+ * division; an all-zero row gives xscale 0 and codes 0.
+ */
+int s3d8_quantize_act(const void *x_bf16, int64_t M, int64_t K, int8_t *xq, float *xscale,
+                      void *stream);
+
+/*
+ * Standalone S3D8 -> INT8 unpack (the pages' dequantisation kernel, blog
+ * section "Fast? How fast?"; paper section 4.3).
+ *   packed    : [G, K] uint8, row-major, 16-byte aligned
+ *   centroids : [32 * 3] int8, row-major C[q][d] (any alignment)
+ *   w         : [N, K] int8 output, row-major, 16-byte aligned; row n is
+ *               component n % 3 of packed row n / 3.  Padded rows are not written.
+ */
+int s3d8_decode(const uint8_t *packed, const int8_t *centroids, int64_t N, int64_t K, int8_t *w,
+                void *stream);
+
+/* Bytes of device workspace s3d8_linear_ex needs for this shape and algorithm
+ * (0 when none).  Pure host function. */
+size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo);
+
+/*
+ * The S3D8 linear layer, Y = X W^T (paper section 4.3, Eq. 1; blog fused
+ * matrix-vector example for the epilogue order and dtypes):
+ *   out[m,n] = bf16_rn( (xscale[m] * float(acc[m,n])) * float(chan_scale[n]) )
+ * with acc the exact int32 sum over k of xq[m,k] * Wq[n,k].
+ *   packed     : [G, K] uint8, row-major (k contiguous), 16-byte aligned
+ *   centroids  : [32 * 3] int8, row-major C[q][d]
+ *   chan_scale : [N] bfloat16, 2-byte aligned
+ *   xq         : [M, K] int8, row-major, 16-byte aligned
+ *   xscale     : [M] fp32, 4-byte aligned
+ *   out_bf16   : [M, N] bfloat16 output, row-major, 2-byte aligned
+ *   workspace  : device scratch of s3d8_linear_workspace_size(M, N, K, AUTO)
+ *                bytes (may be NULL when that size is 0); caller-owned, must
+ *                not be shared by calls that overlap on the GPU.
+ */
+int s3d8_linear(const uint8_t *packed, const int8_t *centroids, const void *chan_scale_bf16,
+                const int8_t *xq, const float *xscale, int64_t M, int64_t N, int64_t K,
+                void *out_bf16, void *workspace, size_t workspace_bytes, void *stream);
+
+/* As s3d8_linear with an explicit algorithm (s3d8_algo).  Returns
+ * S3D8_ERR_UNSUPPORTED when that algorithm cannot run the shape. */
+int s3d8_linear_ex(const uint8_t *packed, const int8_t *centroids, const void *chan_scale_bf16,
+                   const int8_t *xq, const float *xscale, int64_t M, int64_t N, int64_t K,
+                   void *out_bf16, void *workspace, size_t workspace_bytes, int algo,
+                   void *stream);
+
+/*
+ * The exact integer part of the layer alone: acc[m, n] = sum_k xq[m,k] * Wq[n,k]
+ * as int32 [M, N] row-major (4-byte aligned), through the same kernels as
+ * s3d8_linear_ex with `algo`.  Exists so that the accumulators can be checked
+ * bit for bit.
+ */
+int s3d8_linear_acc_i32(const uint8_t *packed, const int8_t *centroids, const int8_t *xq,
+                        int64_t M, int64_t N, int64_t K, int32_t *acc, void *workspace,
+                        size_t workspace_bytes, int algo, void *stream);
+
+/* Synchronises `stream`, then returns and clears the sticky device status word
+ * (S3D8_OK or S3D8_ERR_TIMEOUT), or S3D8_ERR_CUDA if the synchronisation fails. */
+int s3d8_device_status(void *stream);
+
+/* Static English text for a status code. */
+const char *s3d8_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int s3d8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* S3D8_H */

@@ -1,0 +1,194 @@
+"""GB300 (sm_103a) S3D8 W2.7A8 linear layer: thin Python binding.
+
+Every step of the layer runs in the CUDA library ``_build/libs3d8.so`` behind
+the C ABI of ``include/s3d8.h``; this module only checks tensor dtypes,
+shapes and devices, and passes raw device pointers and the current CUDA
+stream.  There is no CPU or PyTorch fallback: if the library has not been
+built, every call raises.
+
+Format: "11 billion parameters on a phone" (Graphcore Research blog),
+sections "Bit layout" and "Output channel packing"; math: "Llama-Mobile:
+Efficient 2.7-Bit Quantization of VLMs", section 3.4, Eq. 1.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+ALGO_AUTO, ALGO_GEMV, ALGO_SKINNY, ALGO_TC = 0, 1, 2, 3
+
+STATUS = {
+    0: "ok",
+    -1: "invalid argument",
+    -2: "misaligned pointer",
+    -3: "unsupported",
+    -4: "CUDA error",
+    -5: "timeout",
+    -6: "workspace",
+}
+
+_lib = None
+
+
+class S3D8Error(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed with status {status} ({msg})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load the CUDA library (optionally building it first)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        if not build_if_missing:
+            raise RuntimeError(
+                f"S3D8 CUDA library missing at {_build.LIB}; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        _build.build()
+    L = ctypes.CDLL(_build.LIB)
+    P, I64, SZ, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+    L.s3d8_quantize_act.argtypes = [P, I64, I64, P, P, P]
+    L.s3d8_decode.argtypes = [P, P, I64, I64, P, P]
+    L.s3d8_linear_workspace_size.argtypes = [I64, I64, I64, I]
+    L.s3d8_linear_workspace_size.restype = SZ
+    L.s3d8_linear.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, SZ, P]
+    L.s3d8_linear_ex.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, SZ, I, P]
+    L.s3d8_linear_acc_i32.argtypes = [P, P, P, I64, I64, I64, P, P, SZ, I, P]
+    L.s3d8_device_status.argtypes = [P]
+    L.s3d8_status_string.argtypes = [I]
+    L.s3d8_status_string.restype = ctypes.c_char_p
+    L.s3d8_version.argtypes = []
+    for fn in ("s3d8_quantize_act", "s3d8_decode", "s3d8_linear", "s3d8_linear_ex",
+               "s3d8_linear_acc_i32", "s3d8_device_status", "s3d8_version"):
+        getattr(L, fn).restype = I
+    _lib = L
+    return L
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise S3D8Error(fn, status, load().s3d8_status_string(status).decode())
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def groups(N: int) -> int:
+    return (N + 2) // 3
+
+
+def quantize_act(x: torch.Tensor, xq: torch.Tensor | None = None,
+                 xscale: torch.Tensor | None = None):
+    """Per-token INT8 quantisation of bf16 x[M, K] -> (xq int8 [M, K], xscale fp32 [M])."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if xscale is None:
+        xscale = torch.empty((M,), dtype=torch.float32, device=x.device)
+    st = load().s3d8_quantize_act(_dev(x, "x", torch.bfloat16), M, K,
+                                  _dev(xq, "xq", torch.int8, (M, K)),
+                                  _dev(xscale, "xscale", torch.float32, (M,)), _stream(x.device))
+    _check("s3d8_quantize_act", st)
+    return xq, xscale
+
+
+def decode(packed: torch.Tensor, centroids: torch.Tensor, N: int,
+           w: torch.Tensor | None = None) -> torch.Tensor:
+    """S3D8 -> dense int8 W[N, K]."""
+    G, K = packed.shape
+    if G != groups(N):
+        raise ValueError(f"packed has {G} rows, expected ceil(N/3) = {groups(N)}")
+    if w is None:
+        w = torch.empty((N, K), dtype=torch.int8, device=packed.device)
+    st = load().s3d8_decode(_dev(packed, "packed", torch.uint8),
+                            _dev(centroids, "centroids", torch.int8, (32, 3)), N, K,
+                            _dev(w, "w", torch.int8, (N, K)), _stream(packed.device))
+    _check("s3d8_decode", st)
+    return w
+
+
+def workspace_size(M: int, N: int, K: int, algo: int = ALGO_AUTO) -> int:
+    return int(load().s3d8_linear_workspace_size(M, N, K, algo))
+
+
+def _workspace(M, N, K, algo, device, workspace):
+    need = workspace_size(M, N, K, algo)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=device)
+    if workspace.numel() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    return workspace, workspace.numel()
+
+
+def linear(packed: torch.Tensor, centroids: torch.Tensor, chan_scale: torch.Tensor,
+           xq: torch.Tensor, xscale: torch.Tensor, N: int, out: torch.Tensor | None = None,
+           algo: int = ALGO_AUTO, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """out[M, N] bf16 = xscale[m] * chan_scale[n] * sum_k xq[m,k] Wq[n,k]."""
+    G, K = packed.shape
+    if G != groups(N):
+        raise ValueError(f"packed has {G} rows, expected ceil(N/3) = {groups(N)}")
+    M = xq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=packed.device)
+    ws, ws_bytes = _workspace(M, N, K, algo, packed.device, workspace)
+    st = load().s3d8_linear_ex(
+        _dev(packed, "packed", torch.uint8), _dev(centroids, "centroids", torch.int8, (32, 3)),
+        _dev(chan_scale, "chan_scale", torch.bfloat16, (N,)), _dev(xq, "xq", torch.int8, (M, K)),
+        _dev(xscale, "xscale", torch.float32, (M,)), M, N, K,
+        _dev(out, "out", torch.bfloat16, (M, N)),
+        None if ws is None else ws.data_ptr(), ws_bytes, algo, _stream(packed.device))
+    _check("s3d8_linear_ex", st)
+    return out
+
+
+def linear_acc_i32(packed: torch.Tensor, centroids: torch.Tensor, xq: torch.Tensor, N: int,
+                   algo: int = ALGO_AUTO, acc: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Exact int32 accumulators acc[M, N] = sum_k xq[m,k] Wq[n,k]."""
+    G, K = packed.shape
+    if G != groups(N):
+        raise ValueError(f"packed has {G} rows, expected ceil(N/3) = {groups(N)}")
+    M = xq.shape[0]
+    if acc is None:
+        acc = torch.empty((M, N), dtype=torch.int32, device=packed.device)
+    ws, ws_bytes = _workspace(M, N, K, algo, packed.device, workspace)
+    st = load().s3d8_linear_acc_i32(
+        _dev(packed, "packed", torch.uint8), _dev(centroids, "centroids", torch.int8, (32, 3)),
+        _dev(xq, "xq", torch.int8, (M, K)), M, N, K, _dev(acc, "acc", torch.int32, (M, N)),
+        None if ws is None else ws.data_ptr(), ws_bytes, algo, _stream(packed.device))
+    _check("s3d8_linear_acc_i32", st)
+    return acc
+
+
+def device_status() -> int:
+    """Synchronise the current stream and return (and clear) the device status."""
+    return int(load().s3d8_device_status(_stream(None)))

@@ -1,0 +1,237 @@
+// C ABI of the S3D8 library: argument checks, algorithm choice, launches.
+// Every check runs before the first CUDA call so that a rejected call touches
+// neither the device nor any memory.
+#include "../../include/s3d8.h"
+#include "launch.h"
+
+#include <cuda_runtime.h>
+
+namespace s3d8 {
+
+__device__ int g_device_status;  // sticky S3D8_ERR_TIMEOUT set by bounded waits
+
+static constexpr int kMaxDevices = 64;
+
+int device_sm_count()
+{
+    static int cached[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+static int *device_status_ptr()
+{
+    static int *cached[kMaxDevices] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    if (!cached[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess)
+            return nullptr;
+        cached[dev] = static_cast<int *>(p);
+    }
+    return cached[dev];
+}
+
+}  // namespace s3d8
+
+using namespace s3d8;
+
+static bool aligned(const void *p, size_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+static int check_k(int64_t K)
+{
+    if (K < 16 || (K % 16) != 0 || K > S3D8_MAX_K)
+        return S3D8_ERR_INVALID_ARG;
+    return S3D8_OK;
+}
+
+static int check_mn(int64_t M, int64_t N)
+{
+    if (M < 0 || N < 0 || M > S3D8_MAX_M || N > S3D8_MAX_N)
+        return S3D8_ERR_INVALID_ARG;
+    return S3D8_OK;
+}
+
+static int cuda_status(cudaError_t e)
+{
+    return e == cudaSuccess ? S3D8_OK : S3D8_ERR_CUDA;
+}
+
+extern "C" {
+
+int s3d8_version(void) { return 100; }
+
+const char *s3d8_status_string(int status)
+{
+    switch (status) {
+    case S3D8_OK: return "ok";
+    case S3D8_ERR_INVALID_ARG: return "invalid argument";
+    case S3D8_ERR_ALIGNMENT: return "misaligned pointer";
+    case S3D8_ERR_UNSUPPORTED: return "unsupported algorithm for this shape or device";
+    case S3D8_ERR_CUDA: return "CUDA error";
+    case S3D8_ERR_TIMEOUT: return "device-side wait timed out";
+    case S3D8_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+int s3d8_quantize_act(const void *x_bf16, int64_t M, int64_t K, int8_t *xq, float *xscale,
+                      void *stream)
+{
+    int st = check_k(K);
+    if (st == S3D8_OK)
+        st = check_mn(M, 1);
+    if (st != S3D8_OK)
+        return st;
+    if (M == 0)
+        return S3D8_OK;
+    if (!x_bf16 || !xq || !xscale)
+        return S3D8_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(xq, 16) || !aligned(xscale, 4))
+        return S3D8_ERR_ALIGNMENT;
+    return cuda_status(launch_quantize_act(static_cast<const __nv_bfloat16 *>(x_bf16), (int)M,
+                                           (int)K, xq, xscale, static_cast<cudaStream_t>(stream)));
+}
+
+int s3d8_decode(const uint8_t *packed, const int8_t *centroids, int64_t N, int64_t K, int8_t *w,
+                void *stream)
+{
+    int st = check_k(K);
+    if (st == S3D8_OK)
+        st = check_mn(0, N);
+    if (st != S3D8_OK)
+        return st;
+    if (N == 0)
+        return S3D8_OK;
+    if (!packed || !centroids || !w)
+        return S3D8_ERR_INVALID_ARG;
+    if (!aligned(packed, 16) || !aligned(w, 16))
+        return S3D8_ERR_ALIGNMENT;
+    return cuda_status(launch_decode(packed, centroids, (int)N, (int)K, w,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo)
+{
+    (void)M;
+    (void)N;
+    (void)K;
+    (void)algo;
+    return 0;
+}
+
+static int linear_common(const uint8_t *packed, const int8_t *centroids, const void *chan_scale,
+                         const int8_t *xq, const float *xscale, int64_t M, int64_t N, int64_t K,
+                         void *out_bf16, int32_t *acc, void *workspace, size_t workspace_bytes,
+                         int algo, void *stream)
+{
+    int st = check_k(K);
+    if (st == S3D8_OK)
+        st = check_mn(M, N);
+    if (st != S3D8_OK)
+        return st;
+    if (algo < S3D8_ALGO_AUTO || algo > S3D8_ALGO_TC)
+        return S3D8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0)
+        return S3D8_OK;
+    if (!packed || !centroids || !xq)
+        return S3D8_ERR_INVALID_ARG;
+    if (acc) {
+        if (!aligned(acc, 4))
+            return S3D8_ERR_ALIGNMENT;
+    } else {
+        if (!chan_scale || !xscale || !out_bf16)
+            return S3D8_ERR_INVALID_ARG;
+        if (!aligned(chan_scale, 2) || !aligned(xscale, 4) || !aligned(out_bf16, 2))
+            return S3D8_ERR_ALIGNMENT;
+    }
+    if (!aligned(packed, 16) || !aligned(xq, 16))
+        return S3D8_ERR_ALIGNMENT;
+    const size_t need = s3d8_linear_workspace_size(M, N, K, algo);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return S3D8_ERR_WORKSPACE;
+    if (algo != S3D8_ALGO_AUTO && algo != S3D8_ALGO_GEMV)
+        return S3D8_ERR_UNSUPPORTED;
+
+    LinearArgs a;
+    a.packed = packed;
+    a.C = centroids;
+    a.cs = static_cast<const __nv_bfloat16 *>(chan_scale);
+    a.xq = xq;
+    a.xscale = xscale;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.out = static_cast<__nv_bfloat16 *>(out_bf16);
+    a.acc = acc;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+    a.status = device_status_ptr();
+    return cuda_status(launch_gemv(a, static_cast<cudaStream_t>(stream)));
+}
+
+int s3d8_linear(const uint8_t *packed, const int8_t *centroids, const void *chan_scale_bf16,
+                const int8_t *xq, const float *xscale, int64_t M, int64_t N, int64_t K,
+                void *out_bf16, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return linear_common(packed, centroids, chan_scale_bf16, xq, xscale, M, N, K, out_bf16,
+                         nullptr, workspace, workspace_bytes, S3D8_ALGO_AUTO, stream);
+}
+
+int s3d8_linear_ex(const uint8_t *packed, const int8_t *centroids, const void *chan_scale_bf16,
+                   const int8_t *xq, const float *xscale, int64_t M, int64_t N, int64_t K,
+                   void *out_bf16, void *workspace, size_t workspace_bytes, int algo, void *stream)
+{
+    return linear_common(packed, centroids, chan_scale_bf16, xq, xscale, M, N, K, out_bf16,
+                         nullptr, workspace, workspace_bytes, algo, stream);
+}
+
+int s3d8_linear_acc_i32(const uint8_t *packed, const int8_t *centroids, const int8_t *xq,
+                        int64_t M, int64_t N, int64_t K, int32_t *acc, void *workspace,
+                        size_t workspace_bytes, int algo, void *stream)
+{
+    if (!acc) {
+        int st = check_k(K);
+        if (st == S3D8_OK)
+            st = check_mn(M, N);
+        if (st != S3D8_OK)
+            return st;
+        return (M == 0 || N == 0) ? S3D8_OK : S3D8_ERR_INVALID_ARG;
+    }
+    return linear_common(packed, centroids, nullptr, xq, nullptr, M, N, K, nullptr, acc,
+                         workspace, workspace_bytes, algo, stream);
+}
+
+int s3d8_device_status(void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return S3D8_ERR_CUDA;
+    int *p = device_status_ptr();
+    if (!p)
+        return S3D8_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return S3D8_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return S3D8_ERR_CUDA;
+    }
+    return v == 0 ? S3D8_OK : v;
+}
+
+}  // extern "C"

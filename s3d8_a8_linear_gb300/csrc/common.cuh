@@ -1,0 +1,131 @@
+// Shared device helpers of the S3D8 CUDA library (sm_103a).
+//
+// Decoding follows "11 billion parameters on a phone" (Graphcore Research
+// blog), sections "Bit layout" and "Format decoding on Arm CPUs": each column
+// of the 32 x 3 absolute-value centroid table is expanded over both signs into
+// a 64-entry signed table (components 0 and 2 in sign-minor order, component 1
+// in sign-major order), and the three lookup indices come from the byte by
+//   I0 = b & 0x3F,  I1 = (b >> 1) & 0x3F,  I2 = I0 ^ (b >> 7).
+// On the GPU the three lookups are folded once per CTA into one 256-entry
+// table of 32-bit words [w0, w1, w2, 0] (one signed byte per output channel
+// of the group), so that a packed byte costs one shared-memory load.  The
+// table is replicated once per lane (word index = byte * 32 + lane), which
+// makes every warp-wide lookup conflict-free whatever the byte values.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace s3d8 {
+
+constexpr int kLutEntries = 256;
+constexpr int kLutWords = kLutEntries * 32;     // lane-replicated
+constexpr int kLutBytes = kLutWords * 4;        // 32 KiB
+constexpr int kLutStageWords = kLutEntries;     // one unreplicated copy
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_stream_v4(const void *p)
+{
+    // Read-only, streamed once: bypass L1 allocation.
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    return __byte_perm(a, b, sel);
+}
+
+// Signed value of one of the blog's 64-entry tables.
+//   sign-minor (components 0 and 2): index = 2 q + s
+//   sign-major (component 1):        index = 32 s + q
+__device__ __forceinline__ int signed_minor(const int8_t *C, int d, uint32_t idx)
+{
+    int c = C[(idx >> 1) * 3 + d];
+    return (idx & 1) ? -c : c;
+}
+__device__ __forceinline__ int signed_major(const int8_t *C, int d, uint32_t idx)
+{
+    int c = C[(idx & 31) * 3 + d];
+    return (idx >> 5) ? -c : c;
+}
+
+// Expanded table word for packed byte b: bytes 0..2 = decoded weights of
+// components 0..2, byte 3 = 0.
+__device__ __forceinline__ uint32_t expanded_entry(const int8_t *C, uint32_t b)
+{
+    const uint32_t i0 = b & 0x3Fu;
+    const uint32_t i1 = (b >> 1) & 0x3Fu;
+    const uint32_t i2 = i0 ^ (b >> 7);
+    const int w0 = signed_minor(C, 0, i0);
+    const int w1 = signed_major(C, 1, i1);
+    const int w2 = signed_minor(C, 2, i2);
+    return (uint32_t)(uint8_t)w0 | ((uint32_t)(uint8_t)w1 << 8) | ((uint32_t)(uint8_t)w2 << 16);
+}
+
+// Builds the lane-replicated table in shared memory.  `stage` holds 256 words.
+// Every thread of the block must call it; it ends with __syncthreads().
+__device__ __forceinline__ void build_lut(uint32_t *lut, uint32_t *stage, const int8_t *C_global)
+{
+    __shared__ int8_t Cs[96];
+    for (int i = threadIdx.x; i < 96; i += blockDim.x)
+        Cs[i] = C_global[i];
+    __syncthreads();
+    for (int b = threadIdx.x; b < kLutEntries; b += blockDim.x)
+        stage[b] = expanded_entry(Cs, (uint32_t)b);
+    __syncthreads();
+    for (int w = threadIdx.x; w < kLutWords; w += blockDim.x)
+        lut[w] = stage[w >> 5];
+    __syncthreads();
+}
+
+// Four packed bytes of one group (consecutive k) -> the three per-channel
+// k-quads V[d] = [w_d(k0), w_d(k1), w_d(k2), w_d(k3)], ready for dp4a / IMMA.
+// `lane_base` = shared address of lut + 4 * lane.
+__device__ __forceinline__ void decode_quad(uint32_t word, uint32_t lane_base, uint32_t &V0,
+                                            uint32_t &V1, uint32_t &V2)
+{
+    const uint32_t L0 = lds_u32(lane_base + ((word & 0xFFu) << 7));
+    const uint32_t L1 = lds_u32(lane_base + (((word >> 8) & 0xFFu) << 7));
+    const uint32_t L2 = lds_u32(lane_base + (((word >> 16) & 0xFFu) << 7));
+    const uint32_t L3 = lds_u32(lane_base + ((word >> 24) << 7));
+    const uint32_t T01 = prmt(L0, L1, 0x5140);   // [w0k0 w0k1 w1k0 w1k1]
+    const uint32_t T23 = prmt(L2, L3, 0x5140);   // [w0k2 w0k3 w1k2 w1k3]
+    const uint32_t U01 = prmt(L0, L1, 0x0062);   // [w2k0 w2k1 . .]
+    const uint32_t U23 = prmt(L2, L3, 0x0062);   // [w2k2 w2k3 . .]
+    V0 = prmt(T01, T23, 0x5410);
+    V1 = prmt(T01, T23, 0x7632);
+    V2 = prmt(U01, U23, 0x5410);
+}
+
+__device__ __forceinline__ __nv_bfloat16 epilogue_bf16(int acc, float xs, __nv_bfloat16 cs)
+{
+    // (x_s * float(acc)) * W_s, rounded once to bf16 (blog, fused matrix-vector example)
+    const float a = __fmul_rn(xs, __int2float_rn(acc));
+    return __float2bfloat16_rn(__fmul_rn(a, __bfloat162float(cs)));
+}
+
+__device__ __forceinline__ int warp_sum(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace s3d8

@@ -1,0 +1,33 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace s3d8 {
+
+struct LinearArgs {
+    const uint8_t *packed;      // [G, K]
+    const int8_t *C;            // [32 * 3]
+    const __nv_bfloat16 *cs;    // [N]            (unused when acc != nullptr)
+    const int8_t *xq;           // [M, K]
+    const float *xscale;        // [M]            (unused when acc != nullptr)
+    int M, N, K;
+    __nv_bfloat16 *out;         // [M, N] bf16 output, or
+    int32_t *acc;               // [M, N] int32 accumulators (test entry)
+    void *ws;                   // device workspace
+    size_t ws_bytes;
+    int *status;                // device status word
+};
+
+int device_sm_count();
+
+cudaError_t launch_quantize_act(const __nv_bfloat16 *x, int M, int K, int8_t *xq, float *xscale,
+                                cudaStream_t stream);
+cudaError_t launch_decode(const uint8_t *packed, const int8_t *C, int N, int K, int8_t *w,
+                          cudaStream_t stream);
+cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t stream);
+
+}  // namespace s3d8

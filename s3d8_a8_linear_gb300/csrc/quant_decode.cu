@@ -1,0 +1,144 @@
+// Activation quantisation and the standalone S3D8 -> INT8 unpack.
+#include "common.cuh"
+#include "launch.h"
+
+namespace s3d8 {
+
+// ---------------------------------------------------------------------------
+// Per-token absmax INT8 quantisation.  One CTA per row (grid-stride over rows),
+// 16-byte vector loads, two passes over the row (the second hits L1/L2).
+// xscale = absmax / 127 with IEEE division; q = rint(x / xscale), ties to even,
+// clamped to +-127; a zero row gives scale 0 and codes 0.
+// ---------------------------------------------------------------------------
+constexpr int kQuantThreads = 256;
+
+__global__ __launch_bounds__(kQuantThreads) void quantize_act_kernel(
+    const __nv_bfloat16 *__restrict__ x, int M, int K, int8_t *__restrict__ xq,
+    float *__restrict__ xscale)
+{
+    __shared__ float red[kQuantThreads / 32];
+    const int chunks = K / 8;  // 8 bf16 per 16 bytes; K % 16 == 0
+    for (int m = blockIdx.x; m < M; m += gridDim.x) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
+        float amax = 0.0f;
+        for (int c = threadIdx.x; c < chunks; c += kQuantThreads) {
+            const uint4 v = __ldg(row + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
+                amax = fmaxf(amax, fabsf(__low2float(h)));
+                amax = fmaxf(amax, fabsf(__high2float(h)));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if ((threadIdx.x & 31) == 0)
+            red[threadIdx.x >> 5] = amax;
+        __syncthreads();
+        amax = red[0];
+#pragma unroll
+        for (int i = 1; i < kQuantThreads / 32; ++i)
+            amax = fmaxf(amax, red[i]);
+        __syncthreads();  // red is reused by the next row
+        const float s = __fdiv_rn(amax, 127.0f);
+        if (threadIdx.x == 0)
+            xscale[m] = s;
+        uint2 *qrow = reinterpret_cast<uint2 *>(xq + (size_t)m * K);
+        for (int c = threadIdx.x; c < chunks; c += kQuantThreads) {
+            const uint4 v = __ldg(row + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
+                const float f[2] = {__low2float(h), __high2float(h)};
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    int q = 0;
+                    if (s != 0.0f) {
+                        q = __float2int_rn(__fdiv_rn(f[e], s));
+                        q = max(-127, min(127, q));
+                    }
+                    const int byte = 2 * j + e;
+                    packed[byte >> 2] |= ((uint32_t)(uint8_t)q) << (8 * (byte & 3));
+                }
+            }
+            qrow[c] = make_uint2(packed[0], packed[1]);
+        }
+    }
+}
+
+cudaError_t launch_quantize_act(const __nv_bfloat16 *x, int M, int K, int8_t *xq, float *xscale,
+                                cudaStream_t stream)
+{
+    const int grid = M < device_sm_count() * 8 ? M : device_sm_count() * 8;
+    quantize_act_kernel<<<grid, kQuantThreads, 0, stream>>>(x, M, K, xq, xscale);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Standalone unpack: packed[G, K] -> w[N, K] int8.  Each thread takes one
+// 16-byte chunk of a packed row, looks every byte up once in the expanded
+// table and writes 16 bytes to each of the (up to) three output rows.
+// Persistent grid so that the 32 KiB table build is amortised.
+// ---------------------------------------------------------------------------
+constexpr int kDecodeThreads = 256;
+
+__global__ __launch_bounds__(kDecodeThreads) void decode_kernel(const uint8_t *__restrict__ packed,
+                                                                const int8_t *__restrict__ C,
+                                                                int N, int K,
+                                                                int8_t *__restrict__ w)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
+    uint32_t *stage = lut + kLutWords;
+    build_lut(lut, stage, C);
+    const uint32_t lane_base = smem_addr(lut) + 4u * (threadIdx.x & 31);
+    const int G = (N + 2) / 3;
+    const int chunks_per_row = K / 16;
+    const long long total = (long long)G * chunks_per_row;
+    for (long long i = (long long)blockIdx.x * kDecodeThreads + threadIdx.x; i < total;
+         i += (long long)gridDim.x * kDecodeThreads) {
+        const int g = (int)(i / chunks_per_row);
+        const int k = (int)(i % chunks_per_row) * 16;
+        const uint4 p = ldg_stream_v4(packed + (size_t)g * K + k);
+        uint32_t V[3][4];
+        decode_quad(p.x, lane_base, V[0][0], V[1][0], V[2][0]);
+        decode_quad(p.y, lane_base, V[0][1], V[1][1], V[2][1]);
+        decode_quad(p.z, lane_base, V[0][2], V[1][2], V[2][2]);
+        decode_quad(p.w, lane_base, V[0][3], V[1][3], V[2][3]);
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const int n = 3 * g + d;
+            if (n < N)
+                *reinterpret_cast<uint4 *>(w + (size_t)n * K + k) =
+                    make_uint4(V[d][0], V[d][1], V[d][2], V[d][3]);
+        }
+    }
+}
+
+cudaError_t launch_decode(const uint8_t *packed, const int8_t *C, int N, int K, int8_t *w,
+                          cudaStream_t stream)
+{
+    const size_t smem = (size_t)(kLutWords + kLutStageWords) * 4;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
+    const long long G = (N + 2) / 3;
+    const long long work = G * (K / 16);
+    long long grid = (work + kDecodeThreads - 1) / kDecodeThreads;
+    const long long cap = (long long)device_sm_count() * 4;
+    if (grid > cap)
+        grid = cap;
+    decode_kernel<<<(int)grid, kDecodeThreads, smem, stream>>>(packed, C, N, K, w);
+    return cudaGetLastError();
+}
+
+}  // namespace s3d8

@@ -1,0 +1,140 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must build for sm_103a, load, export every entry point that
+include/s3d8.h declares, and reject bad arguments before it makes any CUDA
+call.  The rejection tests pass non-null dummy addresses that are never
+dereferenced; they run only on a machine without a CUDA device so that no
+code path can ever hand such an address to a GPU.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import s3d8_a8_linear_gb300 as s3d8
+from s3d8_a8_linear_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _has_cuda_device():
+    try:
+        import torch
+
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+no_device_only = pytest.mark.skipif(_has_cuda_device(),
+                                    reason="dummy-pointer rejection tests run only without a GPU")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return s3d8.load()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "s3d8.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(s3d8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("s3d8_quantize_act", "s3d8_linear", "s3d8_decode", "s3d8_linear_ex",
+               "s3d8_linear_acc_i32", "s3d8_linear_workspace_size", "s3d8_device_status",
+               "s3d8_status_string", "s3d8_version"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (s3d8_[a-z0-9_]+)$", out, flags=re.M))
+    missing = [fn for fn in declared_functions() if fn not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for fn in declared_functions():
+        getattr(lib, fn)
+
+
+def test_status_strings(lib):
+    for code, word in ((0, b"ok"), (-1, b"invalid"), (-2, b"misaligned"), (-3, b"unsupported"),
+                       (-4, b"CUDA"), (-5, b"timed out"), (-6, b"workspace")):
+        assert word in lib.s3d8_status_string(code)
+    assert lib.s3d8_version() >= 100
+
+
+A16 = 0x10000        # dummy, 16-byte aligned, never dereferenced
+A16B = 0x20000
+A16C = 0x30000
+
+
+@no_device_only
+def test_linear_rejects_bad_shapes(lib):
+    f = lib.s3d8_linear
+    ok_ptrs = (A16, A16B, A16C, A16, A16B)
+    for K in (0, 8, 15, 17, 100, 133145, -16):
+        assert f(*ok_ptrs, 1, 3, K, A16C, None, 0, None) == -1, K
+    assert f(*ok_ptrs, -1, 3, 16, A16C, None, 0, None) == -1
+    assert f(*ok_ptrs, 1, -3, 16, A16C, None, 0, None) == -1
+    assert f(*ok_ptrs, (1 << 24) + 1, 3, 16, A16C, None, 0, None) == -1
+
+
+@no_device_only
+def test_linear_rejects_null_and_misaligned(lib):
+    f = lib.s3d8_linear
+    base = [A16, A16B, A16C, A16, A16B]
+    for i in range(5):
+        args = list(base)
+        args[i] = None
+        assert f(*args, 2, 3, 32, A16C, None, 0, None) == -1, i
+    assert f(*base, 2, 3, 32, None, None, 0, None) == -1
+    mis = list(base)
+    mis[0] = A16 + 8     # packed must be 16-byte aligned
+    assert f(*mis, 2, 3, 32, A16C, None, 0, None) == -2
+    mis = list(base)
+    mis[3] = A16 + 4     # xq must be 16-byte aligned
+    assert f(*mis, 2, 3, 32, A16C, None, 0, None) == -2
+    mis = list(base)
+    mis[4] = A16 + 2     # xscale must be 4-byte aligned
+    assert f(*mis, 2, 3, 32, A16C, None, 0, None) == -2
+    assert f(*base, 2, 3, 32, A16C + 1, None, 0, None) == -2
+
+
+@no_device_only
+def test_empty_calls_are_no_ops(lib):
+    # M == 0 or N == 0 returns OK without touching any pointer (all NULL here)
+    assert lib.s3d8_linear(None, None, None, None, None, 0, 3, 32, None, None, 0, None) == 0
+    assert lib.s3d8_linear(None, None, None, None, None, 2, 0, 32, None, None, 0, None) == 0
+    assert lib.s3d8_quantize_act(None, 0, 32, None, None, None) == 0
+    assert lib.s3d8_decode(None, None, 0, 32, None, None) == 0
+    assert lib.s3d8_linear_acc_i32(None, None, None, 0, 5, 32, None, None, 0, 0, None) == 0
+
+
+@no_device_only
+def test_other_entry_points_reject(lib):
+    assert lib.s3d8_quantize_act(A16, 2, 24, A16B, A16C, None) == -1        # K % 16
+    assert lib.s3d8_quantize_act(A16 + 2, 2, 32, A16B, A16C, None) == -2    # x alignment
+    assert lib.s3d8_quantize_act(None, 2, 32, A16B, A16C, None) == -1
+    assert lib.s3d8_decode(A16, A16B, 5, 20, A16C, None) == -1
+    assert lib.s3d8_decode(A16 + 1, A16B, 5, 32, A16C, None) == -2
+    assert lib.s3d8_decode(A16, A16B, 5, 32, A16C + 8, None) == -2
+    assert lib.s3d8_linear_acc_i32(A16, A16B, A16C, 2, 5, 32, None, None, 0, 0, None) == -1
+    assert lib.s3d8_linear_acc_i32(A16, A16B, A16C, 2, 5, 32, A16 + 2, None, 0, 0, None) == -2
+    assert lib.s3d8_linear_ex(A16, A16B, A16C, A16, A16B, 2, 3, 32, A16C, None, 0, 7, None) == -1
+    assert lib.s3d8_linear_ex(A16, A16B, A16C, A16, A16B, 2, 3, 32, A16C, None, 0, -1, None) == -1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    packed = torch.zeros((1, 16), dtype=torch.uint8)
+    C = torch.zeros((32, 3), dtype=torch.int8)
+    with pytest.raises(ValueError):
+        s3d8.decode(packed, C, 3)

@@ -1,0 +1,242 @@
+"""GPU parity: the CUDA library against the CPU oracle, through the C ABI.
+
+Bar: activation codes and scales, decoded int8 weights and int32 accumulators
+bit-exact; bf16 outputs within |gpu - ref| <= 1e-3 + 1e-2 |ref| of the fp64
+oracle.  Inputs follow the seeded recipe in s3d8_inputs; the oracle never sees
+anything the GPU produced.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import s3d8_a8_linear_gb300 as s3d8
+import s3d8_inputs as si
+from gpu_util import (assert_out_close, bf16_bits, bf16_to_f64, dev, f32, guarded, i8, to_np,
+                      u8)
+
+pytestmark = pytest.mark.gpu
+
+ALGOS = [s3d8.ALGO_GEMV]
+ALGO_IDS = {s3d8.ALGO_AUTO: "auto", s3d8.ALGO_GEMV: "gemv", s3d8.ALGO_SKINNY: "skinny",
+            s3d8.ALGO_TC: "tc"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    s3d8.load(build_if_missing=True)
+    torch.cuda.set_device(0)
+    yield
+    assert s3d8.device_status() == 0
+
+
+def rand_case(M, N, K, seed, outliers=False):
+    rng = np.random.default_rng(seed)
+    C = si.centroids(rng)
+    packed = si.packed_bytes(rng, si.groups(N), K)
+    cs = si.chan_scale(rng, N)
+    x = si.activations(rng, M, K, outliers)
+    return C, packed, cs, x
+
+
+def gpu_linear(C, packed, cs, xq, xs, N, algo):
+    return s3d8.linear(u8(packed), i8(C), bf16_bits(cs), i8(xq), f32(xs), N, algo=algo)
+
+
+def gpu_acc(C, packed, xq, N, algo):
+    return to_np(s3d8.linear_acc_i32(u8(packed), i8(C), i8(xq), N, algo=algo)).astype(np.int64)
+
+
+# --------------------------------------------------------------------------
+# Activation quantisation
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,outliers", [(4, 256, False), (1, 16, False), (3, 48, False),
+                                          (1, 4096, False), (1, 14336, False), (7, 1040, True),
+                                          (64, 14336, True), (2048, 14336, False)])
+def test_quantize_act_bitexact(M, K, outliers):
+    rng = np.random.default_rng(M * 7 + K)
+    x = si.activations(rng, M, K, outliers)
+    if M > 2:
+        x[1] = 0                      # an all-zero row
+    xq_o, xs_o = oracle.quantize_act(x)
+    xq, xs = s3d8.quantize_act(bf16_bits(x))
+    np.testing.assert_array_equal(to_np(xs), xs_o)
+    np.testing.assert_array_equal(to_np(xq), xq_o)
+
+
+def test_quantize_act_ties_and_guards():
+    # absmax 127 gives a unit scale: halves round to even
+    vals = [127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -0.5, 126.5, 0.0, -127.0, 64.0, 1.0, -1.0,
+            0.25, 0.75]
+    x = si.f32_to_bf16_bits(np.array([vals], np.float32))
+    xq_o, xs_o = oracle.quantize_act(x)
+    xq, check_q = guarded((1, 16), torch.int8, 99)
+    xs, check_s = guarded((1,), torch.float32, -7.0)
+    s3d8.quantize_act(bf16_bits(x), xq, xs)
+    torch.cuda.synchronize()
+    check_q()
+    check_s()
+    np.testing.assert_array_equal(to_np(xq), xq_o)
+    assert to_np(xs)[0] == 1.0
+
+
+# --------------------------------------------------------------------------
+# Standalone unpack
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K", [(96, 256), (1, 16), (2, 32), (4, 48), (5, 64), (7, 1040),
+                                 (1024, 4096), (14336, 4096), (4096, 14336)])
+def test_decode_bitexact(N, K):
+    rng = np.random.default_rng(N + K)
+    C = si.centroids(rng)
+    packed = si.packed_bytes(rng, si.groups(N), K)
+    want = oracle.decode(packed, C, N)
+    w, check = guarded((N, K), torch.int8, 77)
+    s3d8.decode(u8(packed), i8(C), N, w)
+    torch.cuda.synchronize()
+    check()
+    np.testing.assert_array_equal(to_np(w), want)
+
+
+def test_decode_every_byte_every_table():
+    """All 256 byte values against tables with 0 and 127 entries."""
+    rng = np.random.default_rng(5)
+    packed = np.tile(np.arange(256, dtype=np.uint8), (4, 1))   # 4 groups x 256 columns
+    for C in (rng.integers(0, 128, (32, 3)).astype(np.int8), np.full((32, 3), 127, np.int8),
+              np.zeros((32, 3), np.int8)):
+        for N in (12, 11, 10):
+            want = oracle.decode(packed, C, N)
+            np.testing.assert_array_equal(to_np(s3d8.decode(u8(packed), i8(C), N)), want)
+
+
+# --------------------------------------------------------------------------
+# Linear: exact int32 accumulators and bf16 output
+# --------------------------------------------------------------------------
+
+SMALL = [(1, 1, 16), (2, 2, 32), (3, 4, 48), (4, 96, 256), (5, 5, 256), (7, 100, 1040),
+         (8, 33, 512), (9, 1000, 512), (16, 64, 2048), (17, 10, 64)]
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=lambda a: ALGO_IDS[a])
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_linear_small_exact(M, N, K, algo):
+    C, packed, cs, x = rand_case(M, N, K, seed=M * 100003 + N * 101 + K)
+    xq, xs = oracle.quantize_act(x)
+    ref, acc_o = oracle.linear(packed, C, cs, xq, xs, N)
+    np.testing.assert_array_equal(gpu_acc(C, packed, xq, N, algo), acc_o)
+    out, check = guarded((M, N), torch.bfloat16, 3.0)
+    s3d8.linear(u8(packed), i8(C), bf16_bits(cs), i8(xq), f32(xs), N, out=out, algo=algo)
+    torch.cuda.synchronize()
+    check()
+    assert_out_close(bf16_to_f64(out), ref)
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=lambda a: ALGO_IDS[a])
+def test_tiny_config(algo):
+    """K=256, N=96, M=4 with the seeded recipe (the small case)."""
+    mat, x = si.tiny_case(0)
+    xq, xs = oracle.quantize_act(x)
+    ref, acc_o = oracle.linear(mat.packed, mat.C, mat.chan_scale, xq, xs, mat.N)
+    np.testing.assert_array_equal(gpu_acc(mat.C, mat.packed, xq, mat.N, algo), acc_o)
+    assert_out_close(bf16_to_f64(gpu_linear(mat.C, mat.packed, mat.chan_scale, xq, xs, mat.N, algo)),
+                     ref)
+
+
+@pytest.mark.parametrize("algo", [s3d8.ALGO_AUTO] + ALGOS, ids=lambda a: ALGO_IDS[a])
+def test_llama_layer_decode_m1_full(algo):
+    """Every projection of one 11B decoder layer at M = 1, compared in full."""
+    for i, mat in enumerate(si.layer_matrices(layer=0, seed=0)):
+        x = si.acts(1, mat.K, seed=0, index=i)
+        xq, xs = oracle.quantize_act(x)
+        ref, acc_o = oracle.linear(mat.packed, mat.C, mat.chan_scale, xq, xs, mat.N)
+        np.testing.assert_array_equal(gpu_acc(mat.C, mat.packed, xq, mat.N, algo), acc_o,
+                                      err_msg=mat.name)
+        got = bf16_to_f64(gpu_linear(mat.C, mat.packed, mat.chan_scale, xq, xs, mat.N, algo))
+        assert_out_close(got, ref)
+
+
+def sample_positions(M, N, rng, count=1500):
+    ms = list(rng.integers(0, M, count)) + [0, 0, M - 1, M - 1, M // 2]
+    ns = list(rng.integers(0, N, count)) + [0, N - 1, 0, N - 1, N - 2]
+    return np.array(ms, np.int64), np.array(ns, np.int64)
+
+
+@pytest.mark.parametrize("algo", [s3d8.ALGO_AUTO] + ALGOS, ids=lambda a: ALGO_IDS[a])
+@pytest.mark.parametrize("M", list(si.DECODE_SWEEP_M) + list(si.PREFILL_M))
+@pytest.mark.parametrize("shape", si.SWEEP_SHAPES, ids=lambda s: s[0])
+def test_sweep_sampled(shape, M, algo):
+    """Batched decode (with 1 % activation outliers) and prefill sizes at full
+    shape; the oracle computes a sample of outputs one by one."""
+    name, K, N = shape
+    mat = si.matrix(name, K, N, seed=2)
+    x = si.acts(M, K, seed=2, outliers=M <= 64)
+    xq, xs = oracle.quantize_act(x)
+    acc = gpu_acc(mat.C, mat.packed, xq, N, algo)
+    out = bf16_to_f64(gpu_linear(mat.C, mat.packed, mat.chan_scale, xq, xs, N, algo))
+    rng = np.random.default_rng(M)
+    ms, ns = sample_positions(M, N, rng)
+    want = oracle.linear_acc_at(mat.packed, mat.C, xq, N, ms, ns)
+    np.testing.assert_array_equal(acc[ms, ns], want)
+    ref = xs.astype(np.float64)[ms] * want * si.bf16_bits_to_f32(mat.chan_scale).astype(
+        np.float64)[ns]
+    assert_out_close(out[ms, ns], ref)
+    # property at any size: the bf16 output is the epilogue of the exact accumulators
+    csf = si.bf16_bits_to_f32(mat.chan_scale).astype(np.float64)
+    full_ref = xs.astype(np.float64)[:, None] * acc * csf[None, :]
+    assert_out_close(out, full_ref)
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=lambda a: ALGO_IDS[a])
+@pytest.mark.parametrize("K", [16, 4096, 14336])
+def test_int32_extremes(K, algo):
+    """All centroids 127, all codes 127: acc = +-16129 K (231,225,344 at K = 14336)."""
+    C = np.full((32, 3), 127, np.int8)
+    M, N = 3, 8
+    G = si.groups(N)
+    pos = oracle.pack_byte(9, 0, 0, 0)
+    packed = np.full((G, K), pos, np.uint8)
+    packed[1] ^= 0x41                 # group 1: all three weights negative
+    packed[2] ^= 0x80                 # group 2: only component 2 negative
+    xq = np.full((M, K), 127, np.int8)
+    xq[1] = -127
+    xq[2, ::2] = -127                 # alternating signs
+    acc_o, bad = oracle.linear_acc(packed, C, xq, N)
+    assert bad == 0
+    np.testing.assert_array_equal(gpu_acc(C, packed, xq, N, algo), acc_o)
+    assert acc_o[0, 0] == 16129 * K and acc_o[0, 3] == -16129 * K
+
+
+@pytest.mark.parametrize("algo", ALGOS, ids=lambda a: ALGO_IDS[a])
+def test_zero_activation_row_gives_zero(algo):
+    C, packed, cs, x = rand_case(3, 30, 64, seed=4)
+    x[1] = 0
+    xq, xs = oracle.quantize_act(x)
+    out = to_np(gpu_linear(C, packed, cs, xq, xs, 30, algo).float())
+    assert (out[1] == 0).all()
+
+
+def test_empty_and_rejected_calls():
+    packed = torch.zeros((2, 32), dtype=torch.uint8, device=dev())
+    C = torch.zeros((32, 3), dtype=torch.int8, device=dev())
+    cs = torch.zeros((5,), dtype=torch.bfloat16, device=dev())
+    xq = torch.zeros((0, 32), dtype=torch.int8, device=dev())
+    xs = torch.zeros((0,), dtype=torch.float32, device=dev())
+    out = s3d8.linear(packed, C, cs, xq, xs, 5)
+    assert out.shape == (0, 5)
+    # misaligned packed (1-byte offset view) is rejected before any launch
+    big = torch.zeros((2 * 32 + 16,), dtype=torch.uint8, device=dev())
+    mis = big[1:1 + 64].view(2, 32)
+    xq1 = torch.zeros((1, 32), dtype=torch.int8, device=dev())
+    xs1 = torch.ones((1,), dtype=torch.float32, device=dev())
+    with pytest.raises(s3d8.S3D8Error) as e:
+        s3d8.linear(mis, C, cs, xq1, xs1, 5)
+    assert e.value.status == -2
+    # K not a multiple of 16
+    with pytest.raises(s3d8.S3D8Error) as e:
+        s3d8.linear(torch.zeros((2, 24), dtype=torch.uint8, device=dev()), C, cs,
+                    torch.zeros((1, 24), dtype=torch.int8, device=dev()), xs1, 5)
+    assert e.value.status == -1
+    assert s3d8.device_status() == 0
