@@ -180,7 +180,10 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;
     a.status = device_status_ptr();
-    return cuda_status(launch_gemv(a, static_cast<cudaStream_t>(stream)));
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    if (gemv_tma_supported(a.M, a.K))
+        return cuda_status(launch_gemv_tma(a, strm));
+    return cuda_status(launch_gemv(a, strm));
 }
 
 int s3d8_linear(const uint8_t *packed, const int8_t *centroids, const void *chan_scale_bf16,

@@ -128,4 +128,91 @@ __device__ __forceinline__ int warp_sum(int v)
     return v;
 }
 
+
+// ---------------------------------------------------------------------------
+// Wide-stride table for the streaming kernels: entry b of lane l sits at
+// lut_win + 256 b + 4 l, with lut_win a multiple of 64 KiB in the shared
+// window.  A single PRMT then forms the lookup address: byte 0 from the lane
+// offset, byte 1 = the packed byte, bytes 2..3 from lut_win.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kWideLutBytes = 0x10000;
+
+__device__ __forceinline__ uint32_t wide_lut_window(uint32_t dyn_base)
+{
+    return (dyn_base + 0xFFFFu) & ~0xFFFFu;
+}
+
+// Fills the wide table (all threads of the block; ends with __syncthreads()).
+__device__ __forceinline__ void build_wide_lut(unsigned char *lut_ptr, uint32_t *stage,
+                                               const int8_t *C_global)
+{
+    __shared__ int8_t Cw[96];
+    for (int i = threadIdx.x; i < 96; i += blockDim.x)
+        Cw[i] = C_global[i];
+    __syncthreads();
+    for (int b = threadIdx.x; b < kLutEntries; b += blockDim.x)
+        stage[b] = expanded_entry(Cw, (uint32_t)b);
+    __syncthreads();
+    uint32_t *w = reinterpret_cast<uint32_t *>(lut_ptr);
+    for (int i = threadIdx.x; i < kLutEntries * 32; i += blockDim.x)
+        w[(i >> 5) * 64 + (i & 31)] = stage[i >> 5];
+    __syncthreads();
+}
+
+__device__ __forceinline__ uint32_t lds_u32_nv(uint32_t addr)
+{
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t mad_lo_u32(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// As decode_quad, against the wide table (`lane_base` = lut_win | 4 lane).
+// The third channel is merged on the FMA pipe (U01 + U23 * 2^16; both halves
+// are zero-padded because byte 3 of every table entry is 0).
+__device__ __forceinline__ void decode_quad_wide(uint32_t word, uint32_t lane_base, uint32_t &V0,
+                                                 uint32_t &V1, uint32_t &V2)
+{
+    const uint32_t L0 = lds_u32_nv(prmt(word, lane_base, 0x7604));
+    const uint32_t L1 = lds_u32_nv(prmt(word, lane_base, 0x7614));
+    const uint32_t L2 = lds_u32_nv(prmt(word, lane_base, 0x7624));
+    const uint32_t L3 = lds_u32_nv(prmt(word, lane_base, 0x7634));
+    const uint32_t T01 = prmt(L0, L1, 0x5140);   // [w0k0 w0k1 w1k0 w1k1]
+    const uint32_t T23 = prmt(L2, L3, 0x5140);
+    const uint32_t U01 = prmt(L0, L1, 0x3362);   // [w2k0 w2k1 0 0]
+    const uint32_t U23 = prmt(L2, L3, 0x3362);
+    V0 = prmt(T01, T23, 0x5410);
+    V1 = prmt(T01, T23, 0x7632);
+    V2 = mad_lo_u32(U23, 65536u, U01);
+}
+
+// Sum over the warp of P values per lane (P a power of two, 2..32), returned
+// transposed: afterwards every lane of group j (lanes j * 32/P .. +32/P - 1)
+// holds the full sum of value j.  Costs P - 1 + log2(32/P) shuffles.
+template <int P>
+__device__ __forceinline__ int warp_reduce_transposed(int (&v)[P], int lane)
+{
+#pragma unroll
+    for (int n = P, o = 16; n > 1; n >>= 1, o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const int keep = upper ? v[i + n / 2] : v[i];
+            const int send = upper ? v[i] : v[i + n / 2];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    int r = v[0];
+#pragma unroll
+    for (int o = 16 / P; o > 0; o >>= 1)
+        r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
 }  // namespace s3d8

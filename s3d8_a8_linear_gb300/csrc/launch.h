@@ -29,5 +29,7 @@ cudaError_t launch_quantize_act(const __nv_bfloat16 *x, int M, int K, int8_t *xq
 cudaError_t launch_decode(const uint8_t *packed, const int8_t *C, int N, int K, int8_t *w,
                           cudaStream_t stream);
 cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t stream);
+bool gemv_tma_supported(int M, int K);
+cudaError_t launch_gemv_tma(const LinearArgs &a, cudaStream_t stream);
 
 }  // namespace s3d8
