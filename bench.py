@@ -2,8 +2,11 @@
 
 One step is one pass of the whole hot path over one token: per-token INT8
 quantisation of the four distinct activations of a decoder layer (attention
-input, attention output, MLP input, MLP hidden), then the seven S3D8 linears
-(q, k, v, o, gate, up, down) through the library's C ABI.  Weights are
+input, attention output, MLP input, MLP hidden) and the seven S3D8 linears
+(q, k, v, o, gate, up, down), through the library's C ABI.  The headline
+step is one grouped launch (s3d8_linear_batch, quantisation fused); the JSON
+also reports the four-launch structure of a real decoder layer and the
+eleven-launch form (separate quantisation + single-matrix linears).  Weights are
 synthetic (seeded recipe in s3d8_inputs) and resident in HBM; the step cycles
 through 8 independent copies of the layer (582 MB of packed weights, well
 above the 129 MB L2) so that every step streams its weights from HBM.
@@ -11,10 +14,10 @@ above the 129 MB L2) so that every step streams its weights from HBM.
 Printed JSON (one line, rank 0):
   value      weight GB/s = (packed bytes + bf16 channel scales + tables) per
              step / device time per step, over all ranks (weak scaling);
-  roofline   the GEMV kernel's algorithmic bytes (weights, activations,
-             scales, outputs) per launch / its average launch time, measured
-             with CUDA events inside the timed graphs, against the measured
-             HBM copy bandwidth;
+  roofline   the grouped GEMV kernel's algorithmic bytes (weights, tables,
+             scales, bf16 activations, outputs) per launch / its average launch
+             time, measured with CUDA events recorded inside captured graphs,
+             against the measured HBM copy bandwidth;
   e2e        the same metric with per-step host->device copies of the
              activations from pinned memory and device->host copies of the
              seven outputs, through the Python binding;
@@ -77,7 +80,7 @@ def load_peaks():
 
 def gemv_source_sha():
     h = hashlib.sha256()
-    for name in ("gemv.cu", "common.cuh"):
+    for name in ("gemv_tma.cu", "common.cuh", "tma.cuh"):
         with open(os.path.join(ROOT, "s3d8_a8_linear_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -173,7 +176,16 @@ class LayerCopy:
 
 
 class Step:
-    """Device buffers of one decoder-layer step at M tokens."""
+    """Device buffers of one decoder-layer step at M tokens, and the three ways
+    the library can run it:
+      group1    one grouped launch for all seven projections, activation
+                quantisation fused (the inputs of the synthetic step are
+                independent, so they can stream together);
+      group4    the launch structure a real decoder layer allows: q/k/v, o,
+                gate/up and down as four grouped launches with fused quantisation;
+      separate  four quantisation launches and seven single-matrix launches."""
+
+    GROUP4 = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
 
     def __init__(self, M, dev, seed=0):
         import torch
@@ -185,7 +197,27 @@ class Step:
         self.out = {n: torch.empty((M, N), dtype=torch.bfloat16, device=dev)
                     for n, _, N in si.LLAMA_11B_LAYER}
 
-    def run(self, s3d8, copy, events=None):
+    def job(self, m):
+        a = si.LLAMA_11B_INPUT_OF[m["name"]]
+        return dict(packed=m["packed"], centroids=m["C"], chan_scale=m["cs"], N=m["N"],
+                    x=self.x[a], out=self.out[m["name"]])
+
+    def run(self, s3d8, copy, mode="group1", events=None):
+        mats = {m["name"]: m for m in copy.mats}
+        if mode == "group1":
+            groups_ = (tuple(mats),)
+        elif mode == "group4":
+            groups_ = self.GROUP4
+        else:
+            groups_ = None
+        if groups_ is not None:
+            for gi, names in enumerate(groups_):
+                if events is not None:
+                    events[gi][0].record()
+                s3d8.linear_batch([self.job(mats[n]) for n in names], self.M)
+                if events is not None:
+                    events[gi][1].record()
+            return
         for k in ACT_K:
             s3d8.quantize_act(self.x[k], self.xq[k], self.xs[k])
         for j, m in enumerate(copy.mats):
@@ -198,11 +230,30 @@ class Step:
                 events[j][1].record()
 
 
-def make_timing_events(torch):
+def n_launches(mode):
+    return {"group1": 1, "group4": 4, "separate": len(ACT_K) + len(si.LLAMA_11B_LAYER)}[mode]
+
+
+def group_bytes(names, M=1):
+    """Algorithmic bytes of one grouped launch: weights, scales and tables, each
+    distinct bf16 activation once, the bf16 outputs."""
+    shapes = {n: (K, N) for n, K, N in si.LLAMA_11B_LAYER}
+    acts = {si.LLAMA_11B_INPUT_OF[n] for n in names}
+    total = sum(weight_bytes(*shapes[n]) + 2 * M * shapes[n][1] for n in names)
+    return total + sum(2 * M * ACT_K[a] + 4 * M for a in acts)
+
+
+def capture(torch, stream, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def make_timing_events(torch, n):
     try:
         return [(torch.cuda.Event(enable_timing=True, external=True),
-                 torch.cuda.Event(enable_timing=True, external=True))
-                for _ in si.LLAMA_11B_LAYER]
+                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
     except TypeError:
         return None
 
@@ -227,56 +278,79 @@ def gpu_arm(args):
     step = Step(1, dev)
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
-
-    # eager warm-up (also sets kernel attributes outside capture)
-    with torch.cuda.stream(stream):
-        for r in range(COPIES):
-            step.run(s3d8, copies[r])
+    with torch.cuda.stream(stream):       # eager warm-up of every path
+        for mode in ("group1", "group4", "separate"):
+            for r in range(COPIES):
+                step.run(s3d8, copies[r], mode)
     stream.synchronize()
 
-    # one graph per weight copy, each with per-linear timing events
-    graphs, events = [], []
-    for r in range(COPIES):
-        ev = make_timing_events(torch)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step.run(s3d8, copies[r], ev)
-        graphs.append(g)
-        events.append(ev)
+    # One graph holds the COPIES consecutive steps (one per weight copy), the way a
+    # decode loop captures its layers; consecutive launches inside it overlap
+    # through programmatic dependent launch.  Single-step graphs cover the rest.
+    def run_all(mode):
+        for r in range(COPIES):
+            step.run(s3d8, copies[r], mode)
+
+    multi = {mode: capture(torch, stream, lambda mode=mode: run_all(mode))
+             for mode in ("group1", "group4", "separate")}
+    single = [capture(torch, stream, lambda r=r: step.run(s3d8, copies[r], "group1"))
+              for r in range(COPIES)]
     torch.cuda.synchronize()
 
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % COPIES].replay()
-    stream.synchronize()
+    def replay_steps(mode, steps):
+        full, rest = divmod(steps, COPIES)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(full):
+                multi[mode].replay()
+            for r in range(rest):
+                single[r].replay()
+            t1.record(stream)
+        t1.synchronize()
+        return t0.elapsed_time(t1) / steps
 
+    replay_steps("group1", max(args.warmup, 3))
+
+    # ---- timed region: exactly args.steps steps of the headline structure ----
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for i in range(args.steps):
-            graphs[i % COPIES].replay()
-        t1.record(stream)
-    t1.synchronize()
+    ms_step = replay_steps("group1", args.steps)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    ms_total = t0.elapsed_time(t1)
-    ms_step = ms_total / args.steps
 
-    # per-linear launch durations from the events recorded inside the graphs
-    lin_ms, lin_bytes = [], []
-    if events[0] is not None:
-        for r in range(COPIES):
-            for j, (name, K, N) in enumerate(si.LLAMA_11B_LAYER):
-                lin_ms.append(events[r][j][0].elapsed_time(events[r][j][1]))
-                lin_bytes.append(linear_bytes(1, K, N))
+    # ---- other launch structures (same weights, same rotation) --------------
+    variants = {}
+    for mode in ("group4", "separate"):
+        n = max(COPIES, (args.steps // 4) // COPIES * COPIES)
+        replay_steps(mode, COPIES * 4)
+        ms = replay_steps(mode, n)
+        variants[mode] = {"ms_per_step": round(ms, 6), "launches_per_step": n_launches(mode),
+                          "value": round(LAYER_WEIGHT_BYTES / (ms * 1e-3) / 1e9, 1)}
+
+    # ---- per-launch duration of the grouped kernel (events inside graphs) -----
+    launch_ms, launch_bytes = [], []
+    evgraphs = []
+    for r in range(COPIES):
+        ev = make_timing_events(torch, 1)
+        if ev is None:
+            break
+        evgraphs.append((capture(torch, stream,
+                                 lambda r=r, ev=ev: step.run(s3d8, copies[r], "group1", ev)), ev))
+    if evgraphs:
+        with torch.cuda.stream(stream):
+            for rep in range(4):
+                for g, _ in evgraphs:
+                    g.replay()
+                stream.synchronize()
+                launch_ms += [ev[0][0].elapsed_time(ev[0][1]) for _, ev in evgraphs]
+        launch_bytes = [group_bytes([n for n, _, _ in si.LLAMA_11B_LAYER])] * len(launch_ms)
     status = s3d8.device_status()
 
     if world > 1:
@@ -287,18 +361,17 @@ def gpu_arm(args):
     value = world * LAYER_WEIGHT_BYTES / (ms_step * 1e-3) / 1e9
     hbm_peak, _, peak_kind = load_peaks()
     roofline = None
-    if lin_ms:
-        achieved = sum(lin_bytes) / (sum(lin_ms) * 1e-3) / 1e9
-        tr = traffic_per_launch()
+    if launch_ms:
+        avg_ms = sum(launch_ms) / len(launch_ms)
+        achieved = launch_bytes[0] / (avg_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                    "traffic": tr, "kernel": "s3d8 gemv (M=1), 7 linears of the layer",
-                    "peak_kind": peak_kind,
-                    "per_linear_us": {n: round(1e3 * statistics.mean(
-                        lin_ms[r * 7 + j] for r in range(COPIES)), 2)
-                        for j, (n, _, _) in enumerate(si.LLAMA_11B_LAYER)}}
+                    "traffic": traffic_per_launch(),
+                    "kernel": "gemv_group_kernel<1>: one launch, 7 projections, fused quantisation",
+                    "bytes_per_launch": launch_bytes[0], "avg_launch_us": round(avg_ms * 1e3, 3),
+                    "launches_timed": len(launch_ms), "peak_kind": peak_kind}
 
-    e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 2000))
+    e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 4000))
     prefill = prefill_measure(torch, s3d8, dev) if not args.skip_prefill else None
     unpack = unpack_measure(torch, s3d8, dev)
 
@@ -314,34 +387,34 @@ def gpu_arm(args):
                    "weight_copies": COPIES,
                    "l2": f"inputs larger than L2: {COPIES} rotating layer copies "
                          f"({COPIES * LAYER_WEIGHT_BYTES / 1e6:.0f} MB of weights)",
-                   "launch": "one CUDA graph per step (4 quantize_act + 7 linear)",
+                   "launch": "one grouped launch per step (7 projections, activation "
+                             "quantisation fused); the 8 rotating steps captured in one CUDA "
+                             "graph, consecutive launches overlapping by programmatic "
+                             "dependent launch",
                    "parallelism": f"replicas x{world}"},
-        "gpu_launches": args.steps * (len(ACT_K) + len(si.LLAMA_11B_LAYER)),
+        "gpu_launches": args.steps * n_launches("group1"),
         "device_status": status,
-        "roofline": roofline, "e2e": e2e, "prefill": prefill, "unpack": unpack,
-        "clocks": clocks, "cpu_baseline": cpu,
+        "roofline": roofline, "variants": variants, "e2e": e2e, "prefill": prefill,
+        "unpack": unpack, "clocks": clocks, "cpu_baseline": cpu,
     }
     print(json.dumps(line))
 
 
 def e2e_measure(torch, s3d8, copies, dev, steps):
-    """Same metric through the Python binding, with the activations copied in
-    from pinned host memory and the seven outputs copied back every step."""
+    """Same metric through the Python binding, with the four activations copied
+    in from pinned host memory and the seven outputs copied back every step
+    (the step itself is the captured grouped launch)."""
     step = Step(1, dev)
     host_x = {k: torch.from_numpy(si.acts(1, K, seed=5, index=i).view(np.int16)).view(
         torch.bfloat16).pin_memory() for i, (k, K) in enumerate(ACT_K.items())}
     host_out = {n: torch.empty((1, N), dtype=torch.bfloat16).pin_memory()
                 for n, _, N in si.LLAMA_11B_LAYER}
     stream = torch.cuda.Stream(dev)
-    graphs = []
     with torch.cuda.stream(stream):
-        step.run(s3d8, copies[0])
+        step.run(s3d8, copies[0], "group1")
     stream.synchronize()
-    for r in range(COPIES):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step.run(s3d8, copies[r])
-        graphs.append(g)
+    graphs = [capture(torch, stream, lambda r=r: step.run(s3d8, copies[r], "group1"))
+              for r in range(COPIES)]
     h2d = sum(t.numel() * 2 for t in host_x.values())
     d2h = sum(t.numel() * 2 for t in host_out.values())
 
@@ -367,7 +440,8 @@ def e2e_measure(torch, s3d8, copies, dev, steps):
     ms = t0.elapsed_time(t1) / steps
     return {"value": round(LAYER_WEIGHT_BYTES / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
-            "steps": steps, "path": "Python binding captured in a CUDA graph, pinned copies"}
+            "steps": steps, "path": "Python binding (grouped launch) captured in a CUDA graph, "
+                                    "pinned host copies in and out every step"}
 
 
 def prefill_measure(torch, s3d8, dev, M=2048, reps=3):

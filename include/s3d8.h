@@ -127,6 +127,47 @@ int s3d8_linear_acc_i32(const uint8_t *packed, const int8_t *centroids, const in
                         int64_t M, int64_t N, int64_t K, int32_t *acc, void *workspace,
                         size_t workspace_bytes, int algo, void *stream);
 
+/*
+ * One linear of a grouped call (s3d8_linear_batch).  All pointers are device
+ * memory and follow the layouts of s3d8_linear.  Exactly one of x_bf16 and xq
+ * is given:
+ *   x_bf16      [M, K] bfloat16 activations, quantised inside the kernel with
+ *               the s3d8_quantize_act rule (16-byte aligned; M * K <= 28672);
+ *   xq, xscale  [M, K] int8 codes and [M] fp32 scales, already quantised.
+ * xq_out / xscale_out (optional, used only with x_bf16) receive the codes and
+ * scales the kernel computed.  out_bf16 receives the layer output unless acc is
+ * given, in which case acc receives the exact int32 accumulators instead.
+ */
+typedef struct {
+    const uint8_t *packed;
+    const int8_t *centroids;
+    const void *chan_scale_bf16;
+    const void *x_bf16;
+    const int8_t *xq;
+    const float *xscale;
+    int8_t *xq_out;
+    float *xscale_out;
+    void *out_bf16;
+    int32_t *acc;
+    int64_t N;
+    int64_t K;
+} s3d8_linear_job;
+
+#define S3D8_MAX_BATCH 8
+
+/*
+ * Several independent S3D8 linears (the same token count M, 1 <= M <= 4) in one
+ * launch: the GPU's SMs are divided among the jobs in proportion to their
+ * packed bytes and every job streams its weights concurrently.  With x_bf16 the
+ * activation quantisation is fused into the launch (each CTA quantises the
+ * activation row(s) it needs).  This is the decode-step form of the layer: for
+ * example the q, k and v projections of one token, or the seven projections of
+ * a decoder layer when their inputs are available together.
+ * Up to S3D8_MAX_BATCH jobs; each job's K must satisfy the s3d8_linear rules and
+ * K <= 65536.  Returns S3D8_ERR_UNSUPPORTED for M > 4.
+ */
+int s3d8_linear_batch(const s3d8_linear_job *jobs, int count, int64_t M, void *stream);
+
 /* Synchronises `stream`, then returns and clears the sticky device status word
  * (S3D8_OK or S3D8_ERR_TIMEOUT), or S3D8_ERR_CUDA if the synchronisation fails. */
 int s3d8_device_status(void *stream);

@@ -33,6 +33,17 @@ STATUS = {
 
 _lib = None
 
+MAX_BATCH = 8
+
+
+class LinearJob(ctypes.Structure):
+    """Mirror of s3d8_linear_job (include/s3d8.h)."""
+    _fields_ = [("packed", ctypes.c_void_p), ("centroids", ctypes.c_void_p),
+                ("chan_scale_bf16", ctypes.c_void_p), ("x_bf16", ctypes.c_void_p),
+                ("xq", ctypes.c_void_p), ("xscale", ctypes.c_void_p), ("xq_out", ctypes.c_void_p),
+                ("xscale_out", ctypes.c_void_p), ("out_bf16", ctypes.c_void_p),
+                ("acc", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
 
 class S3D8Error(RuntimeError):
     def __init__(self, fn: str, status: int, msg: str):
@@ -64,12 +75,13 @@ def load(build_if_missing: bool = False):
     L.s3d8_linear.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, SZ, P]
     L.s3d8_linear_ex.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, SZ, I, P]
     L.s3d8_linear_acc_i32.argtypes = [P, P, P, I64, I64, I64, P, P, SZ, I, P]
+    L.s3d8_linear_batch.argtypes = [ctypes.POINTER(LinearJob), I, I64, P]
     L.s3d8_device_status.argtypes = [P]
     L.s3d8_status_string.argtypes = [I]
     L.s3d8_status_string.restype = ctypes.c_char_p
     L.s3d8_version.argtypes = []
     for fn in ("s3d8_quantize_act", "s3d8_decode", "s3d8_linear", "s3d8_linear_ex",
-               "s3d8_linear_acc_i32", "s3d8_device_status", "s3d8_version"):
+               "s3d8_linear_acc_i32", "s3d8_linear_batch", "s3d8_device_status", "s3d8_version"):
         getattr(L, fn).restype = I
     _lib = L
     return L
@@ -187,6 +199,52 @@ def linear_acc_i32(packed: torch.Tensor, centroids: torch.Tensor, xq: torch.Tens
         None if ws is None else ws.data_ptr(), ws_bytes, algo, _stream(packed.device))
     _check("s3d8_linear_acc_i32", st)
     return acc
+
+
+def linear_batch(jobs, M: int):
+    """Several independent S3D8 linears with the same token count M (1..4) in one
+    launch.  Each job is a dict with keys packed, centroids, chan_scale, N and
+    either x (bf16 [M, K], quantised inside the launch) or xq + xscale; optional
+    out (bf16 [M, N]), acc (int32 [M, N], replaces out), xq_out, xscale_out.
+    Returns the list of output tensors (out, or acc when given)."""
+    if len(jobs) > MAX_BATCH:
+        raise ValueError(f"at most {MAX_BATCH} jobs per launch")
+    arr = (LinearJob * max(1, len(jobs)))()
+    results = []
+    device = None
+    for i, j in enumerate(jobs):
+        packed, C, N = j["packed"], j["centroids"], int(j["N"])
+        G, K = packed.shape
+        if G != groups(N):
+            raise ValueError(f"job {i}: packed has {G} rows, expected ceil(N/3) = {groups(N)}")
+        device = packed.device
+        d = arr[i]
+        d.packed = _dev(packed, "packed", torch.uint8)
+        d.centroids = _dev(C, "centroids", torch.int8, (32, 3))
+        d.N, d.K = N, K
+        if j.get("x") is not None:
+            d.x_bf16 = _dev(j["x"], "x", torch.bfloat16, (M, K))
+            if j.get("xq_out") is not None:
+                d.xq_out = _dev(j["xq_out"], "xq_out", torch.int8, (M, K))
+            if j.get("xscale_out") is not None:
+                d.xscale_out = _dev(j["xscale_out"], "xscale_out", torch.float32, (M,))
+        else:
+            d.xq = _dev(j["xq"], "xq", torch.int8, (M, K))
+            if j.get("xscale") is not None:
+                d.xscale = _dev(j["xscale"], "xscale", torch.float32, (M,))
+        if j.get("acc") is not None:
+            d.acc = _dev(j["acc"], "acc", torch.int32, (M, N))
+            results.append(j["acc"])
+        else:
+            out = j.get("out")
+            if out is None:
+                out = torch.empty((M, N), dtype=torch.bfloat16, device=packed.device)
+            d.out_bf16 = _dev(out, "out", torch.bfloat16, (M, N))
+            d.chan_scale_bf16 = _dev(j["chan_scale"], "chan_scale", torch.bfloat16, (N,))
+            results.append(out)
+    st = load().s3d8_linear_batch(arr, len(jobs), M, _stream(device))
+    _check("s3d8_linear_batch", st)
+    return results
 
 
 def device_status() -> int:

@@ -218,6 +218,65 @@ int s3d8_linear_acc_i32(const uint8_t *packed, const int8_t *centroids, const in
                          workspace, workspace_bytes, algo, stream);
 }
 
+int s3d8_linear_batch(const s3d8_linear_job *jobs, int count, int64_t M, void *stream)
+{
+    if (count < 0 || count > S3D8_MAX_BATCH || M < 0 || M > S3D8_MAX_M)
+        return S3D8_ERR_INVALID_ARG;
+    if (count == 0 || M == 0)
+        return S3D8_OK;
+    if (!jobs)
+        return S3D8_ERR_INVALID_ARG;
+    if (M > 4)
+        return S3D8_ERR_UNSUPPORTED;
+    GroupArgs g = {};
+    g.M = (int)M;
+    g.njobs = 0;
+    for (int i = 0; i < count; ++i) {
+        const s3d8_linear_job &j = jobs[i];
+        int st = check_k(j.K);
+        if (st == S3D8_OK)
+            st = check_mn(M, j.N);
+        if (st != S3D8_OK)
+            return st;
+        if (j.N == 0)
+            continue;
+        const bool fused = j.x_bf16 != nullptr;
+        if (!j.packed || !j.centroids || (fused == (j.xq != nullptr)))
+            return S3D8_ERR_INVALID_ARG;
+        if (!j.acc && (!j.chan_scale_bf16 || !j.out_bf16))
+            return S3D8_ERR_INVALID_ARG;
+        if (!fused && !j.acc && !j.xscale)
+            return S3D8_ERR_INVALID_ARG;
+        if (!aligned(j.packed, 16) || (j.acc && !aligned(j.acc, 4)) ||
+            (j.out_bf16 && !aligned(j.out_bf16, 2)) || (j.chan_scale_bf16 && !aligned(j.chan_scale_bf16, 2)))
+            return S3D8_ERR_ALIGNMENT;
+        if (fused && (!aligned(j.x_bf16, 16) || (j.xq_out && !aligned(j.xq_out, 16)) ||
+                      (j.xscale_out && !aligned(j.xscale_out, 4))))
+            return S3D8_ERR_ALIGNMENT;
+        if (!fused && (!aligned(j.xq, 16) || (j.xscale && !aligned(j.xscale, 4))))
+            return S3D8_ERR_ALIGNMENT;
+        if (!gemv_group_job_ok((int)M, (int)j.K, fused))
+            return S3D8_ERR_UNSUPPORTED;
+        GroupJob &d = g.jobs[g.njobs++];
+        d.packed = j.packed;
+        d.C = j.centroids;
+        d.cs = static_cast<const __nv_bfloat16 *>(j.chan_scale_bf16);
+        d.x = static_cast<const __nv_bfloat16 *>(j.x_bf16);
+        d.xq = j.xq;
+        d.xscale = j.xscale;
+        d.xq_out = fused ? j.xq_out : nullptr;
+        d.xscale_out = fused ? j.xscale_out : nullptr;
+        d.out = static_cast<__nv_bfloat16 *>(j.out_bf16);
+        d.acc = j.acc;
+        d.N = (int)j.N;
+        d.K = (int)j.K;
+    }
+    if (g.njobs == 0)
+        return S3D8_OK;
+    g.status = device_status_ptr();
+    return cuda_status(launch_gemv_group(g, static_cast<cudaStream_t>(stream)));
+}
+
 int s3d8_device_status(void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -120,6 +120,74 @@ __device__ __forceinline__ __nv_bfloat16 epilogue_bf16(int acc, float xs, __nv_b
     return __float2bfloat16_rn(__fmul_rn(a, __bfloat162float(cs)));
 }
 
+// ---------------------------------------------------------------------------
+// Activation code q = clamp(rint(RN(x / s)), -127, 127) without a division per
+// element.  With r = RN(1/s) and t = RN(x * r):
+//   |t - x/s| <= |x/s| (2^-23 + 2^-48)  and  |RN(x/s) - x/s| <= |x/s| 2^-24,
+// so for |x/s| <= 127.5 the two quotients differ by less than 2.3e-5.  Unless t
+// lies within kTieMargin of a half-integer, rint(t) == rint(RN(x/s)); otherwise
+// (and for scales below 2^-100, where 1/s could overflow) the exact IEEE
+// quotient decides.  Parity with the division-based rule is tested bit for bit.
+// ---------------------------------------------------------------------------
+constexpr float kTieMargin = 1.0e-4f;
+constexpr float kTinyScale = 7.8886090522101181e-31f;   // 2^-100
+
+// The rare exact path, kept out of line so that the common path stays small.
+static __device__ __noinline__ float exact_quotient(float x, float s)
+{
+    return __fdiv_rn(x, s);
+}
+
+__device__ __forceinline__ int quant_code(float x, float s, float r)
+{
+    if (s == 0.0f)
+        return 0;
+    float t = __fmul_rn(x, r);
+    const float f = t - floorf(t);                         // exact for |t| < 2^23
+    if (s < kTinyScale || fabsf(f - 0.5f) < kTieMargin)
+        t = exact_quotient(x, s);
+    return max(-127, min(127, __float2int_rn(t)));
+}
+
+// Eight bf16 values (one 16-byte chunk) -> eight codes (8 bytes).  The common
+// path is branch-free over the eight values (one multiply, floor, compare and
+// convert each, all independent); the rare near-tie values are redone exactly
+// afterwards.  Out of line so that unrolled prologue loops share one copy.
+static __device__ __noinline__ uint2 quant_chunk8(uint4 v, float s, float r)
+{
+    if (s == 0.0f)
+        return make_uint2(0u, 0u);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
+        x[2 * j] = __low2float(h);
+        x[2 * j + 1] = __high2float(h);
+    }
+    int q[8];
+    bool redo = s < kTinyScale;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float t = __fmul_rn(x[e], r);
+        const float f = t - floorf(t);
+        redo |= fabsf(f - 0.5f) < kTieMargin;
+        q[e] = max(-127, min(127, __float2int_rn(t)));
+    }
+    if (redo) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            q[e] = quant_code(x[e], s, r);
+    }
+    uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        lo |= ((uint32_t)(uint8_t)q[e]) << (8 * e);
+        hi |= ((uint32_t)(uint8_t)q[e + 4]) << (8 * e);
+    }
+    return make_uint2(lo, hi);
+}
+
 __device__ __forceinline__ int warp_sum(int v)
 {
 #pragma unroll
@@ -152,6 +220,23 @@ __device__ __forceinline__ void build_wide_lut(unsigned char *lut_ptr, uint32_t 
     __syncthreads();
     for (int b = threadIdx.x; b < kLutEntries; b += blockDim.x)
         stage[b] = expanded_entry(Cw, (uint32_t)b);
+    __syncthreads();
+    uint32_t *w = reinterpret_cast<uint32_t *>(lut_ptr);
+    for (int i = threadIdx.x; i < kLutEntries * 32; i += blockDim.x)
+        w[(i >> 5) * 64 + (i & 31)] = stage[i >> 5];
+    __syncthreads();
+}
+
+// As build_wide_lut, with the 96 table bytes already loaded: thread t < 96
+// passes C[t] in `cval`.
+__device__ __forceinline__ void build_wide_lut_from(unsigned char *lut_ptr, uint32_t *stage, int8_t cval)
+{
+    __shared__ int8_t Cv[96];
+    if (threadIdx.x < 96)
+        Cv[threadIdx.x] = cval;
+    __syncthreads();
+    for (int b = threadIdx.x; b < kLutEntries; b += blockDim.x)
+        stage[b] = expanded_entry(Cv, (uint32_t)b);
     __syncthreads();
     uint32_t *w = reinterpret_cast<uint32_t *>(lut_ptr);
     for (int i = threadIdx.x; i < kLutEntries * 32; i += blockDim.x)

@@ -1,21 +1,31 @@
-// Streaming S3D8 GEMV for the decode regime (M <= 4 tokens), GB300 design.
+// Streaming S3D8 GEMV for the decode regime (M <= 4 tokens), grouped form.
 //
-// Per CTA (one per SM, 16 warps):
-//   * the 64 KiB wide decode table (one PRMT per lookup address, see
-//     common.cuh), built once;
+// One launch runs up to kMaxJobs independent linears.  The CTAs (one per SM,
+// 16 warps) are divided among the jobs in proportion to their packed bytes, so
+// every CTA works on exactly one matrix and all matrices stream concurrently.
+// Per CTA:
+//   * the 64 KiB wide decode table (one PRMT builds each lookup address, see
+//     common.cuh), built once for the CTA's matrix;
 //   * one private ring of kDepth stages per warp in shared memory, filled by
-//     1-D bulk copies (cp.async.bulk + mbarrier complete_tx).  Each warp
-//     refills the stage it has just consumed, so HBM keeps streaming while the
-//     same warp decodes, and the bytes in flight do not occupy registers;
-//   * the activations of the warp's fixed K-slice live in registers.
-// Work: the CTA owns a contiguous range of packed rows.  A row's K is split
-// into T slices of CC x 512 bytes; warp w always handles slice w % T of rows
-// r0 + w / T, r0 + w / T + 16 / T, ...  A warp spans 512 contiguous bytes per
-// step (16 per lane), so each bulk copy is one contiguous row slice.
-// The three partial channel sums (per token) of a row slice are reduced across
-// the warp with a transposed butterfly; with T > 1 the slices of a row are
-// combined with shared-memory atomics and written after a CTA barrier.
-// Output: bf16 epilogue (x_s * acc) * W_s, or the raw int32 accumulators.
+//     1-D bulk copies (cp.async.bulk + mbarrier complete_tx).  A warp refills
+//     the stage it has just consumed, so HBM keeps streaming while the same warp
+//     decodes and the bytes in flight occupy no registers;
+//   * the int8 activations of the warp's fixed K-slice in registers.  With bf16
+//     activations the CTA first quantises the whole row into shared memory
+//     (per-token absmax / 127 with IEEE division, round-half-even), so that no
+//     separate quantisation launch is needed.
+// Work inside a CTA: a contiguous range of packed rows of its job.  A row's K
+// is cut into T slices of 4 KiB (the last may be shorter); warp w always takes
+// slice w % T of rows r0 + w / T + i * (16 / T).  A warp covers 512 contiguous
+// bytes per step (16 per lane), so each bulk copy is one contiguous row slice.
+// The channel sums of a row slice are reduced with a transposed butterfly; with
+// T > 1 the slices of a row meet in shared-memory atomics, written out after a
+// CTA barrier.  Output: bf16 epilogue (x_s * acc) * W_s, or raw int32 sums.
+//
+// Programmatic dependent launch: the kernel lets the next grid launch early and
+// reads no input before griddepcontrol.wait; after it, the 96-byte table and the
+// activations are requested before the bulk weight copies so that the prologue
+// (table build, quantisation) overlaps the first slices in flight.
 #include "common.cuh"
 #include "launch.h"
 #include "tma.cuh"
@@ -25,7 +35,13 @@ namespace s3d8 {
 constexpr int kTmaWarps = 16;
 constexpr int kTmaThreads = kTmaWarps * 32;
 constexpr int kDepth = 2;
-constexpr int kMaxRangeRows = 512;      // rows per CTA pass (bounds the T > 1 accumulator)
+// 512-byte chunks per slice: 8 (4 KiB) for up to 2 tokens, 4 for 3..4 tokens so
+// that the activations of the slice still fit in registers.
+__host__ __device__ constexpr int chunks_for(int MT)
+{
+    return MT <= 2 ? 8 : 4;
+}
+constexpr int kUnionBytes = 28672;               // fused activations, then T > 1 sums
 constexpr int kTmaDynSmem = 232448 - 4096;
 
 __host__ __device__ constexpr int pow2_at_least(int v)
@@ -34,133 +50,165 @@ __host__ __device__ constexpr int pow2_at_least(int v)
 }
 
 struct TmaLayout {
-    uint32_t lut;        // wide table (64 KiB, window-aligned)
-    uint32_t bars;       // kTmaWarps * kDepth mbarriers
-    uint32_t acc;        // kMaxRangeRows * 3 * MT ints
-    uint32_t ring;       // this warp's ring
+    uint32_t lut;    // wide table (64 KiB, window-aligned)
+    uint32_t bars;   // kTmaWarps * kDepth mbarriers
+    uint32_t uni;    // kUnionBytes: quantised activations, later the T > 1 sums
+    uint32_t ring;   // this warp's ring
     bool ok;
 };
 
 // Carves the dynamic shared window [base, base + size) around the 64 KiB-aligned
-// table.  Small blocks and rings go below the table first, then above it.
-__device__ __forceinline__ TmaLayout tma_layout(uint32_t base, uint32_t size, uint32_t ring_bytes,
-                                                uint32_t acc_bytes, int warp)
+// table: the mbarriers and the union buffer go first, then as many rings as fit
+// below the table, the rest above it.
+__device__ __forceinline__ TmaLayout tma_layout(uint32_t base, uint32_t size, int warp, uint32_t stage)
 {
     TmaLayout L;
     L.lut = wide_lut_window(base);
     const uint32_t end = base + size;
-    uint32_t lo = base, hi = L.lut + kWideLutBytes;
-    auto take = [&](uint32_t bytes, uint32_t align) -> uint32_t {
-        uint32_t a = (lo + align - 1) & ~(align - 1);
-        if (a + bytes <= L.lut) {
-            lo = a + bytes;
-            return a;
-        }
-        uint32_t b = (hi + align - 1) & ~(align - 1);
-        hi = b + bytes;
-        return b;
-    };
-    L.bars = take(kTmaWarps * kDepth * 8, 8);
-    L.acc = take(acc_bytes, 16);
-    L.ring = 0;
-    for (int w = 0; w < kTmaWarps; ++w) {
-        const uint32_t r = take(ring_bytes, 128);
-        if (w == warp)
-            L.ring = r;
+    const uint32_t ring_bytes = kDepth * stage;
+    uint32_t lo = (base + 7) & ~7u;
+    uint32_t hi = L.lut + kWideLutBytes;
+    const uint32_t small = kTmaWarps * kDepth * 8 + 16 + kUnionBytes;
+    uint32_t small_at;
+    if (lo + small <= L.lut) {
+        small_at = lo;
+        lo += small;
+    } else {
+        small_at = hi;
+        hi += small;
     }
-    L.ok = hi <= end && L.lut + kWideLutBytes <= end;
+    L.bars = small_at;
+    L.uni = (small_at + kTmaWarps * kDepth * 8 + 15) & ~15u;
+    lo = (lo + 127) & ~127u;
+    hi = (hi + 127) & ~127u;
+    const uint32_t below = L.lut > lo ? (L.lut - lo) / ring_bytes : 0;
+    const uint32_t n_below = below < (uint32_t)kTmaWarps ? below : (uint32_t)kTmaWarps;
+    L.ring = (uint32_t)warp < n_below ? lo + warp * ring_bytes : hi + (warp - n_below) * ring_bytes;
+    L.ok = hi + (kTmaWarps - n_below) * ring_bytes <= end && L.lut + kWideLutBytes <= end;
     return L;
 }
 
-template <int MT, int CC>
-__global__ __launch_bounds__(kTmaThreads, 1) void gemv_tma_kernel(LinearArgs a, int T, int smem_size)
+__device__ __forceinline__ void pdl_launch_dependents()
 {
-    constexpr int STAGE = CC * 512;
-    constexpr int NV = 3 * MT;
-    constexpr int P = pow2_at_least(NV);
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint32_t stage_tab[kLutEntries];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
-    const uint32_t dyn = smem_addr(smem);
-    const TmaLayout L = tma_layout(dyn, (uint32_t)smem_size, kDepth * STAGE,
-                                   kMaxRangeRows * NV * 4, (int)(threadIdx.x >> 5));
-    if (!L.ok) {  // cannot happen for the sizes the host requests; never silently wrong
-        if (threadIdx.x == 0 && a.status)
-            atomicExch(a.status, -3);
-        return;
+// Per-token absmax quantisation of x[M, K] (bf16, M * K <= kUnionBytes) into
+// shared int8 codes and shared fp32 scales, by the whole CTA.  Same rule as the
+// standalone kernel.  The row is read once into registers (stage 1, issued
+// before the bulk weight copies so that it does not queue behind them) and
+// quantised from there (stage 2).
+constexpr int kActChunksPerThread = kUnionBytes / 8 / kTmaThreads;   // 16-byte chunks
+
+struct ActRegs {
+    uint4 v[kActChunksPerThread];
+};
+
+// Volatile loads: all chunks leave at once, here, instead of being sunk one by
+// one to their first use (which would serialise their latencies).
+__device__ __forceinline__ void act_load(const __nv_bfloat16 *__restrict__ x, int M, int K, ActRegs &r)
+{
+    const int chunks = M * K / 8;
+#pragma unroll
+    for (int i = 0; i < kActChunksPerThread; ++i) {
+        const int c = threadIdx.x + i * kTmaThreads;
+        r.v[i] = c < chunks ? ldg_stream_v4(reinterpret_cast<const uint4 *>(x) + c)
+                            : make_uint4(0u, 0u, 0u, 0u);
     }
+}
+
+// Phase A of the fused quantisation: per-warp absmax of each token's row part
+// held in `r`, written to red[warp * MT + m].
+template <int MT>
+__device__ __forceinline__ void act_amax_partial(const ActRegs &r, int M, int K, float *red)
+{
+    const int chunks = M * K / 8;
+    const int per_row = K / 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int *sacc = reinterpret_cast<int *>(smem + (L.acc - dyn));
-    for (int i = threadIdx.x; i < kMaxRangeRows * NV; i += kTmaThreads)
-        sacc[i] = 0;
-    if (lane == 0)
-        for (int s = 0; s < kDepth; ++s)
-            mbar_init(L.bars + (warp * kDepth + s) * 8, 1);
-    fence_proxy_async_smem();
-    build_wide_lut(smem + (L.lut - dyn), stage_tab, a.C);   // ends with __syncthreads()
-
-    const int G = (a.N + 2) / 3;
-    const int sets = kTmaWarps / T;
-    const int rs = warp / T, t = warp - rs * T;
-    const bool active = rs < sets;
-    const uint32_t lane_base = L.lut | (uint32_t)(lane << 2);
-    const int slice_off = t * STAGE;
-    const int slice_len = max(0, min(STAGE, a.K - slice_off));
-    const uint32_t ring = L.ring;
-    const uint32_t bar0 = L.bars + warp * kDepth * 8;
-
-    // activations of this warp's K-slice, per token (zero beyond K or M)
-    uint32_t xr[MT][CC][4];
+    float amax[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m)
+        amax[m] = 0.0f;
 #pragma unroll
-        for (int j = 0; j < CC; ++j) {
-            const int k = slice_off + j * 512 + lane * 16;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (m < a.M && k < a.K)
-                v = __ldg(reinterpret_cast<const uint4 *>(a.xq + (size_t)m * a.K + k));
-            xr[m][j][0] = v.x;
-            xr[m][j][1] = v.y;
-            xr[m][j][2] = v.z;
-            xr[m][j][3] = v.w;
+    for (int i = 0; i < kActChunksPerThread; ++i) {
+        const int c = threadIdx.x + i * kTmaThreads;
+        if (c < chunks) {
+            const int m = c / per_row;
+            const uint32_t w[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
+            float a = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
+                a = fmaxf(a, fmaxf(fabsf(__low2float(h)), fabsf(__high2float(h))));
+            }
+#pragma unroll
+            for (int mm = 0; mm < MT; ++mm)
+                if (mm == m)
+                    amax[mm] = fmaxf(amax[mm], a);
         }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            amax[m] = fmaxf(amax[m], __shfl_xor_sync(0xffffffffu, amax[m], o));
+        if (lane == 0)
+            red[warp * MT + m] = amax[m];
+    }
+}
 
-    bool timed_out = false;
-    int consumed = 0;   // uses of this warp's ring so far (identical in all lanes)
-    int issued = 0;     // bulk copies issued into it so far
-    // Contiguous row partition over the grid, cut into ranges of kMaxRangeRows rows.
-    const int per_cta = (G + gridDim.x - 1) / gridDim.x;
-    const int cta_beg = blockIdx.x * per_cta;
-    const int cta_end = min(G, cta_beg + per_cta);
-    for (int r0 = cta_beg; r0 < cta_end; r0 += kMaxRangeRows) {
-        const int nrow = min(kMaxRangeRows, cta_end - r0);
-        const int nmine = (active && !timed_out) ? max(0, (nrow - rs + sets - 1) / sets) : 0;
-        for (int i = 0; i < kDepth && i < nmine; ++i) {
-            if (lane == 0) {
-                const uint32_t bar = bar0 + (issued % kDepth) * 8;
-                mbar_arrive_expect_tx(bar, (uint32_t)slice_len);
-                bulk_load(ring + (issued % kDepth) * STAGE,
-                          a.packed + (size_t)(r0 + rs + i * sets) * a.K + slice_off,
-                          (uint32_t)slice_len, bar);
-            }
-            ++issued;
+// Phase B: every thread folds the warp maxima into the per-token scale
+// (absmax / 127, IEEE division) and writes the codes of its own chunks into
+// the shared row `xs`.  Thread 0 also publishes the scales.
+template <int MT>
+__device__ __forceinline__ void act_codes(const ActRegs &r, int M, int K, const float *red, int8_t *xs,
+                                          float *scale_s)
+{
+    const int chunks = M * K / 8;
+    const int per_row = K / 8;
+    float sc[MT], rcp[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        float a = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kTmaWarps; ++w)
+            a = fmaxf(a, red[w * MT + m]);
+        sc[m] = __fdiv_rn(a, 127.0f);
+        rcp[m] = sc[m] > 0.0f ? __frcp_rn(sc[m]) : 0.0f;
+        if (threadIdx.x == 0)
+            scale_s[m] = sc[m];
+    }
+#pragma unroll
+    for (int i = 0; i < kActChunksPerThread; ++i) {
+        const int c = threadIdx.x + i * kTmaThreads;
+        if (c < chunks) {
+            const int m = c / per_row;
+            float s = 0.0f, inv = 0.0f;
+#pragma unroll
+            for (int mm = 0; mm < MT; ++mm)
+                if (mm == m) {
+                    s = sc[mm];
+                    inv = rcp[mm];
+                }
+            reinterpret_cast<uint2 *>(xs)[c] = quant_chunk8(r.v[i], s, inv);
         }
-        for (int i = 0; i < nmine; ++i) {
-            const int u = consumed;          // global use index of this warp's ring
-            const int s = u % kDepth;
-            const uint32_t bar = bar0 + s * 8;
-            if (!mbar_wait_bounded(bar, (uint32_t)((u / kDepth) & 1))) {
-                timed_out = true;
-                break;
-            }
-            ++consumed;
-            const uint32_t st = ring + s * STAGE + lane * 16;
-            int acc[MT][3];
+    }
+}
+
+template <int MT, int CH>
+struct SliceCompute {
+    // Decodes `nch` 512-byte chunks of a staged slice and accumulates all tokens.
+    template <bool FULL>
+    __device__ __forceinline__ static void run(uint32_t st, int nch, uint32_t lane_base,
+                                               const uint32_t (&xr)[MT][CH][4], int (&acc)[MT][3])
+    {
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-                acc[m][0] = acc[m][1] = acc[m][2] = 0;
-#pragma unroll
-            for (int j = 0; j < CC; ++j) {
+        for (int j = 0; j < CH; ++j) {
+            if (FULL || j < nch) {
                 const uint4 p = lds_v4(st + j * 512);
                 const uint32_t pw[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
@@ -175,13 +223,204 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_tma_kernel(LinearArgs a, 
                     }
                 }
             }
+        }
+    }
+};
+
+template <int MT>
+__global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g, int smem_size)
+{
+    constexpr int CH = chunks_for(MT);
+    constexpr int kStage = CH * 512;
+    constexpr int NV = 3 * MT;
+    constexpr int P = pow2_at_least(NV);
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint32_t stage_tab[kLutEntries];
+    __shared__ float red[kTmaWarps * MT];
+    __shared__ float scale_s[MT];
+
+    // ---- which job, which rows ------------------------------------------------
+    int jb = 0;
+#pragma unroll
+    for (int j = 1; j < kMaxJobs; ++j)
+        jb += (j < g.njobs && (int)blockIdx.x >= g.cta_begin[j]) ? 1 : 0;
+    const GroupJob job = g.jobs[jb];
+    const int nctas = g.cta_begin[jb + 1] - g.cta_begin[jb];
+    const int b = (int)blockIdx.x - g.cta_begin[jb];
+    const int M = g.M, N = job.N, K = job.K;
+    const int G = (N + 2) / 3;
+    const int T = (K + kStage - 1) / kStage;
+    const int sets = kTmaWarps / T;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rs = warp / T, t = warp - rs * T;
+    const bool active = rs < sets;
+    const int slice_off = t * kStage;
+    const int slice_len = max(0, min(kStage, K - slice_off));
+    const int nch = (slice_len + 511) / 512;
+    const int per_cta = (G + nctas - 1) / nctas;
+    const int cta_beg = b * per_cta;
+    const int cta_end = min(G, cta_beg + per_cta);
+
+    const uint32_t dyn = smem_addr(smem);
+    const TmaLayout L = tma_layout(dyn, (uint32_t)smem_size, warp, kStage);
+    if (!L.ok) {   // the host never requests a size this can happen for
+        if (threadIdx.x == 0 && g.status)
+            atomicExch(g.status, -3);
+        return;
+    }
+    const uint32_t ring = L.ring;
+    const uint32_t bar0 = L.bars + warp * kDepth * 8;
+    int8_t *xs = reinterpret_cast<int8_t *>(smem + (L.uni - dyn));
+    int *sacc = reinterpret_cast<int *>(smem + (L.uni - dyn));
+    const int range_rows = kUnionBytes / (4 * NV);
+
+    if (lane == 0)
+        for (int s = 0; s < kDepth; ++s)
+            mbar_init(bar0 + s * 8, 1);
+    fence_proxy_async_smem();
+    pdl_launch_dependents();
+    pdl_wait();   // inputs may come from the previous grid: read nothing before this
+
+    // ---- phase A: small inputs first (table bytes, activations), then the ring
+    // fill, so that the small loads are not queued behind the bulk copies -------
+    __shared__ int8_t Cv[96];
+    int8_t cval = 0;
+    if (threadIdx.x < 96) {
+        short t;
+        asm volatile("ld.global.nc.s8 %0, [%1];" : "=h"(t) : "l"(job.C + threadIdx.x));
+        cval = (int8_t)t;
+    }
+    const bool fused = job.x != nullptr;
+    ActRegs act;
+    uint32_t xr[MT][CH][4];
+    if (fused) {
+        act_load(job.x, M, K, act);
+    } else {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                const int k = slice_off + j * 512 + lane * 16;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (m < M && k < K && j * 512 < slice_len)
+                    v = ldg_stream_v4(job.xq + (size_t)m * K + k);
+                xr[m][j][0] = v.x;
+                xr[m][j][1] = v.y;
+                xr[m][j][2] = v.z;
+                xr[m][j][3] = v.w;
+            }
+    }
+    int issued = 0, consumed = 0;
+    const int nrow0 = min(range_rows, cta_end - cta_beg);
+    const int nmine0 = active ? max(0, (nrow0 - rs + sets - 1) / sets) : 0;
+    for (int i = 0; i < kDepth && i < nmine0; ++i) {
+        if (lane == 0) {
+            const uint32_t bar = bar0 + (issued % kDepth) * 8;
+            mbar_arrive_expect_tx(bar, (uint32_t)slice_len);
+            bulk_load(ring + (issued % kDepth) * kStage,
+                      job.packed + (size_t)(cta_beg + rs + i * sets) * K + slice_off,
+                      (uint32_t)slice_len, bar);
+        }
+        ++issued;
+    }
+    if (threadIdx.x < 96)
+        Cv[threadIdx.x] = cval;
+    if (fused)
+        act_amax_partial<MT>(act, M, K, red);
+    __syncthreads();
+
+    // ---- phase B: table entries, scales and activation codes ------------------
+    if (threadIdx.x < kLutEntries)
+        stage_tab[threadIdx.x] = expanded_entry(Cv, threadIdx.x);
+    if (fused)
+        act_codes<MT>(act, M, K, red, xs, scale_s);
+    else if (threadIdx.x < MT)   // scales are read only for the bf16 output (none on the int32 path)
+        scale_s[threadIdx.x] =
+            ((int)threadIdx.x < M && job.xscale != nullptr) ? job.xscale[threadIdx.x] : 0.0f;
+    __syncthreads();
+
+    // ---- phase C: replicate the table, take the activation slice ---------------
+    {
+        uint32_t *wt = reinterpret_cast<uint32_t *>(smem + (L.lut - dyn));
+        for (int e = threadIdx.x; e < kLutEntries * 32; e += kTmaThreads)
+            wt[(e >> 5) * 64 + (e & 31)] = stage_tab[e >> 5];
+    }
+    if (fused) {
+        if (b == 0) {   // optional copies of the codes and scales for the caller
+            if (job.xq_out)
+                for (int c = threadIdx.x; c < M * K / 16; c += kTmaThreads)
+                    reinterpret_cast<uint4 *>(job.xq_out)[c] = reinterpret_cast<const uint4 *>(xs)[c];
+            if (job.xscale_out && (int)threadIdx.x < M)
+                job.xscale_out[threadIdx.x] = scale_s[threadIdx.x];
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                const int k = slice_off + j * 512 + lane * 16;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (m < M && k < K && j * 512 < slice_len)
+                    v = *reinterpret_cast<const uint4 *>(xs + (size_t)m * K + k);
+                xr[m][j][0] = v.x;
+                xr[m][j][1] = v.y;
+                xr[m][j][2] = v.z;
+                xr[m][j][3] = v.w;
+            }
+    }
+    __syncthreads();   // table complete; the union buffer is free for the T > 1 sums
+    if (T > 1) {
+        for (int i = threadIdx.x; i < nrow0 * NV; i += kTmaThreads)
+            sacc[i] = 0;
+        __syncthreads();
+    }
+    float xsc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+        xsc[m] = scale_s[m];
+
+    // ---- stream ---------------------------------------------------------------
+    const uint32_t lane_base = L.lut | (uint32_t)(lane << 2);
+    bool timed_out = false;
+    for (int r0 = cta_beg; r0 < cta_end; r0 += range_rows) {
+        const int nrow = min(range_rows, cta_end - r0);
+        const int nmine = (active && !timed_out) ? max(0, (nrow - rs + sets - 1) / sets) : 0;
+        if (r0 != cta_beg) {   // the first range's copies were issued above
+            for (int i = 0; i < kDepth && i < nmine; ++i) {
+                if (lane == 0) {
+                    const uint32_t bar = bar0 + (issued % kDepth) * 8;
+                    mbar_arrive_expect_tx(bar, (uint32_t)slice_len);
+                    bulk_load(ring + (issued % kDepth) * kStage,
+                              job.packed + (size_t)(r0 + rs + i * sets) * K + slice_off,
+                              (uint32_t)slice_len, bar);
+                }
+                ++issued;
+            }
+        }
+        for (int i = 0; i < nmine; ++i) {
+            const int u = consumed;
+            const int s = u % kDepth;
+            const uint32_t bar = bar0 + s * 8;
+            if (!mbar_wait_bounded(bar, (uint32_t)((u / kDepth) & 1))) {
+                timed_out = true;
+                break;
+            }
+            ++consumed;
+            int acc[MT][3];
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                acc[m][0] = acc[m][1] = acc[m][2] = 0;
+            const uint32_t st = ring + s * kStage + lane * 16;
+            if (slice_len == kStage)
+                SliceCompute<MT, CH>::template run<true>(st, nch, lane_base, xr, acc);
+            else
+                SliceCompute<MT, CH>::template run<false>(st, nch, lane_base, xr, acc);
             __syncwarp();
             if (i + kDepth < nmine) {
                 if (lane == 0) {
-                    fence_proxy_async_smem();   // our reads of stage s before the refill
+                    fence_proxy_async_smem();   // this warp's reads of stage s precede the refill
                     mbar_arrive_expect_tx(bar, (uint32_t)slice_len);
-                    bulk_load(ring + s * STAGE,
-                              a.packed + (size_t)(r0 + rs + (i + kDepth) * sets) * a.K + slice_off,
+                    bulk_load(ring + s * kStage,
+                              job.packed + (size_t)(r0 + rs + (i + kDepth) * sets) * K + slice_off,
                               (uint32_t)slice_len, bar);
                 }
                 ++issued;
@@ -197,11 +436,11 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_tma_kernel(LinearArgs a, 
             if (leader && idx < NV) {
                 const int m = idx / 3, n = 3 * row + (idx - 3 * m);
                 if (T == 1) {
-                    if (m < a.M && n < a.N) {
-                        if (a.acc)
-                            a.acc[(size_t)m * a.N + n] = sum;
+                    if (m < M && n < N) {
+                        if (job.acc)
+                            job.acc[(size_t)m * N + n] = sum;
                         else
-                            a.out[(size_t)m * a.N + n] = epilogue_bf16(sum, a.xscale[m], a.cs[n]);
+                            job.out[(size_t)m * N + n] = epilogue_bf16(sum, xsc[m], job.cs[n]);
                     }
                 } else {
                     atomicAdd(&sacc[(row - r0) * NV + idx], sum);
@@ -213,11 +452,11 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_tma_kernel(LinearArgs a, 
             for (int e = threadIdx.x; e < nrow * NV; e += kTmaThreads) {
                 const int rl = e / NV, idx = e - rl * NV;
                 const int m = idx / 3, n = 3 * (r0 + rl) + (idx - 3 * m);
-                if (m < a.M && n < a.N) {
-                    if (a.acc)
-                        a.acc[(size_t)m * a.N + n] = sacc[e];
+                if (m < M && n < N) {
+                    if (job.acc)
+                        job.acc[(size_t)m * N + n] = sacc[e];
                     else
-                        a.out[(size_t)m * a.N + n] = epilogue_bf16(sacc[e], a.xscale[m], a.cs[n]);
+                        job.out[(size_t)m * N + n] = epilogue_bf16(sacc[e], xsc[m], job.cs[n]);
                 }
                 sacc[e] = 0;
             }
@@ -225,11 +464,10 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_tma_kernel(LinearArgs a, 
         }
     }
     if (timed_out) {
-        // drain the copies still in flight into this warp's ring (bounded), then leave
-        for (int u = consumed + 1; u < issued; ++u)
+        for (int u = consumed + 1; u < issued; ++u)   // drain this warp's copies in flight
             mbar_wait_bounded(bar0 + (u % kDepth) * 8, (uint32_t)((u / kDepth) & 1));
         if (lane == 0)
-            record_timeout(a.status);
+            record_timeout(g.status);
     }
 }
 
@@ -237,107 +475,137 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_tma_kernel(LinearArgs a, 
 // Host side
 // ---------------------------------------------------------------------------
 
-template <int MT, int CC>
-static cudaError_t launch_tma_mt_cc(const LinearArgs &a, int T, int grid, cudaStream_t stream)
-{
-    cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<MT, CC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaDynSmem);
-    if (e != cudaSuccess)
-        return e;
-    gemv_tma_kernel<MT, CC><<<grid, kTmaThreads, kTmaDynSmem, stream>>>(a, T, kTmaDynSmem);
-    return cudaGetLastError();
-}
-
-// Worst-case layout check on the host (the table window starts at 64 KiB; the
-// dynamic region may begin anywhere up to 4 KiB into the window).
-static bool tma_layout_fits(int CC, int MT)
-{
-    const long ring = (long)kDepth * CC * 512;
-    const long below = 0x10000 - 0x1000 - kTmaWarps * kDepth * 8 - (long)kMaxRangeRows * 3 * MT * 4;
-    const long above = (long)kTmaDynSmem + 0x400 - 0x20000;
-    const long rings_below = below > 0 ? below / ring : 0;
-    const long rings_above = above / (ring + 128);
-    return rings_below + rings_above >= kTmaWarps;
-}
-
-// Chooses the slice width (CC chunks of 512 bytes) for a shape: the widest
-// that still gives every warp of every CTA work and wastes little of K.
-static int choose_cc(int G, int K, int ctas, int MT)
-{
-    // first choice: wide slices that keep every warp busy and waste < 1/8 of K;
-    // second choice: any slice width that fits the 16 warps and the layout
-    const int options_mt1[] = {8, 7, 4, 2, 1};
-    const int options_mt2[] = {4, 2, 1};
-    const int options_mt4[] = {2, 1};
-    const int *opts = MT == 1 ? options_mt1 : MT == 2 ? options_mt2 : options_mt4;
-    const int nopts = MT == 1 ? 5 : MT == 2 ? 3 : 2;
-    const int rows_per_cta = (G + ctas - 1) / ctas;
-    for (int i = 0; i < nopts; ++i) {
-        const int cc = opts[i];
-        const int T = (K + cc * 512 - 1) / (cc * 512);
-        if (T > kTmaWarps || (kTmaWarps % T != 0 && T != 1))
-            continue;
-        const long waste = (long)T * cc * 512 - K;
-        if (waste * 8 > (long)K && cc > 1)
-            continue;
-        if ((long)rows_per_cta * T < kTmaWarps && cc > 1)
-            continue;
-        if (!tma_layout_fits(cc, MT))
-            continue;
-        return cc;
-    }
-    for (int i = nopts - 1; i >= 0; --i) {
-        const int cc = opts[i];
-        const int T = (K + cc * 512 - 1) / (cc * 512);
-        if (T <= kTmaWarps && tma_layout_fits(cc, MT))
-            return cc;
-    }
-    return 0;
-}
-
 static int tma_token_block(int M)
 {
     return M <= 1 ? 1 : M <= 2 ? 2 : 4;
 }
 
-bool gemv_tma_supported(int M, int K)
+static int stage_bytes(int M)
+{
+    return chunks_for(tma_token_block(M)) * 512;
+}
+
+bool gemv_group_job_ok(int M, int K, bool fused)
 {
     if (M < 1 || M > 4)
         return false;
-    const int widest = M <= 1 ? 8 : M <= 2 ? 4 : 2;
-    return K <= kTmaWarps * 512 * widest;
+    if ((K + stage_bytes(M) - 1) / stage_bytes(M) > kTmaWarps)
+        return false;
+    if (fused && (long)M * K > kUnionBytes)
+        return false;
+    return true;
+}
+
+bool gemv_tma_supported(int M, int K)
+{
+    return gemv_group_job_ok(M, K, false);
+}
+
+// Splits `ctas` CTAs over the jobs in proportion to packed bytes (largest
+// remainder), at least one CTA per job and never more CTAs than rows x slices.
+static void split_ctas(const GroupArgs &g, int ctas, int *cta_begin)
+{
+    const int kStage = stage_bytes(g.M);
+    double total = 0.0;
+    double bytes[kMaxJobs];
+    int cap[kMaxJobs];
+    for (int j = 0; j < g.njobs; ++j) {
+        const long G = (g.jobs[j].N + 2) / 3;
+        const long T = (g.jobs[j].K + kStage - 1) / kStage;
+        bytes[j] = (double)G * g.jobs[j].K;
+        cap[j] = (int)(G * T < ctas ? G * T : ctas);
+        total += bytes[j];
+    }
+    int count[kMaxJobs];
+    double frac[kMaxJobs];
+    int used = 0;
+    for (int j = 0; j < g.njobs; ++j) {
+        const double want = total > 0 ? ctas * bytes[j] / total : 1.0;
+        count[j] = (int)want;
+        if (count[j] < 1)
+            count[j] = 1;
+        if (count[j] > cap[j])
+            count[j] = cap[j];
+        frac[j] = want - (int)want;
+        used += count[j];
+    }
+    while (used < ctas) {
+        int best = -1;
+        for (int j = 0; j < g.njobs; ++j)
+            if (count[j] < cap[j] && (best < 0 || frac[j] > frac[best]))
+                best = j;
+        if (best < 0)
+            break;
+        ++count[best];
+        frac[best] = -1.0;
+        ++used;
+    }
+    cta_begin[0] = 0;
+    for (int j = 0; j < g.njobs; ++j)
+        cta_begin[j + 1] = cta_begin[j] + count[j];
+}
+
+template <int MT>
+static cudaError_t launch_group_mt(const GroupArgs &g, int grid, cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(gemv_group_kernel<MT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaDynSmem);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = kTmaDynSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_group_kernel<MT>, g, (int)kTmaDynSmem);
+}
+
+cudaError_t launch_gemv_group(GroupArgs &g, cudaStream_t stream)
+{
+    if (g.njobs < 1 || g.njobs > kMaxJobs)
+        return cudaErrorInvalidValue;
+    const int sms = device_sm_count();
+    const int kStage = stage_bytes(g.M);
+    long items = 0;
+    for (int j = 0; j < g.njobs; ++j)
+        items += (long)((g.jobs[j].N + 2) / 3) * ((g.jobs[j].K + kStage - 1) / kStage);
+    int ctas = items < sms ? (int)items : sms;
+    if (ctas < g.njobs)
+        ctas = g.njobs;
+    split_ctas(g, ctas, g.cta_begin);
+    const int grid = g.cta_begin[g.njobs];
+    switch (tma_token_block(g.M)) {
+    case 1: return launch_group_mt<1>(g, grid, stream);
+    case 2: return launch_group_mt<2>(g, grid, stream);
+    default: return launch_group_mt<4>(g, grid, stream);
+    }
 }
 
 cudaError_t launch_gemv_tma(const LinearArgs &a, cudaStream_t stream)
 {
-    const int MT = tma_token_block(a.M);
-    const int G = (a.N + 2) / 3;
-    const int sms = device_sm_count();
-    const int cc = choose_cc(G, a.K, sms, MT);
-    if (cc == 0)
-        return cudaErrorInvalidValue;
-    const int T = (a.K + cc * 512 - 1) / (cc * 512);
-    if (T > kTmaWarps)
-        return cudaErrorInvalidValue;
-    // enough CTAs to cover the rows, at most one per SM
-    const int items = G * T;
-    int grid = (items + kTmaWarps - 1) / kTmaWarps;
-    grid = grid < 1 ? 1 : grid > sms ? sms : grid;
-#define S3D8_TMA_CASE(mt, c)                                                                      \
-    if (MT == mt && cc == c)                                                                      \
-        return launch_tma_mt_cc<mt, c>(a, T, grid, stream);
-    S3D8_TMA_CASE(1, 8)
-    S3D8_TMA_CASE(1, 7)
-    S3D8_TMA_CASE(1, 4)
-    S3D8_TMA_CASE(1, 2)
-    S3D8_TMA_CASE(1, 1)
-    S3D8_TMA_CASE(2, 4)
-    S3D8_TMA_CASE(2, 2)
-    S3D8_TMA_CASE(2, 1)
-    S3D8_TMA_CASE(4, 2)
-    S3D8_TMA_CASE(4, 1)
-#undef S3D8_TMA_CASE
-    return cudaErrorInvalidValue;
+    GroupArgs g = {};
+    g.njobs = 1;
+    g.M = a.M;
+    g.status = a.status;
+    GroupJob &j = g.jobs[0];
+    j.packed = a.packed;
+    j.C = a.C;
+    j.cs = a.cs;
+    j.x = nullptr;
+    j.xq = a.xq;
+    j.xscale = a.xscale;
+    j.xq_out = nullptr;
+    j.xscale_out = nullptr;
+    j.out = a.out;
+    j.acc = a.acc;
+    j.N = a.N;
+    j.K = a.K;
+    return launch_gemv_group(g, stream);
 }
 
 }  // namespace s3d8

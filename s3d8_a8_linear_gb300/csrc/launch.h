@@ -22,6 +22,31 @@ struct LinearArgs {
     int *status;                // device status word
 };
 
+// One linear of a grouped launch (see s3d8_linear_job in include/s3d8.h).
+struct GroupJob {
+    const uint8_t *packed;
+    const int8_t *C;
+    const __nv_bfloat16 *cs;
+    const __nv_bfloat16 *x;     // bf16 activations to quantise in-kernel, or nullptr
+    const int8_t *xq;           // pre-quantised codes (when x == nullptr)
+    const float *xscale;
+    int8_t *xq_out;             // optional copies of the in-kernel codes / scales
+    float *xscale_out;
+    __nv_bfloat16 *out;
+    int32_t *acc;
+    int N, K;
+};
+
+constexpr int kMaxJobs = 8;
+
+struct GroupArgs {
+    GroupJob jobs[kMaxJobs];
+    int njobs;
+    int M;
+    int cta_begin[kMaxJobs + 1];   // filled by the launcher
+    int *status;
+};
+
 int device_sm_count();
 
 cudaError_t launch_quantize_act(const __nv_bfloat16 *x, int M, int K, int8_t *xq, float *xscale,
@@ -30,6 +55,8 @@ cudaError_t launch_decode(const uint8_t *packed, const int8_t *C, int N, int K, 
                           cudaStream_t stream);
 cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t stream);
 bool gemv_tma_supported(int M, int K);
+bool gemv_group_job_ok(int M, int K, bool fused);
+cudaError_t launch_gemv_group(GroupArgs &g, cudaStream_t stream);
 cudaError_t launch_gemv_tma(const LinearArgs &a, cudaStream_t stream);
 
 }  // namespace s3d8

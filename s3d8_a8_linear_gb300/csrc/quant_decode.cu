@@ -8,7 +8,8 @@ namespace s3d8 {
 // Per-token absmax INT8 quantisation.  One CTA per row (grid-stride over rows),
 // 16-byte vector loads, two passes over the row (the second hits L1/L2).
 // xscale = absmax / 127 with IEEE division; q = rint(x / xscale), ties to even,
-// clamped to +-127; a zero row gives scale 0 and codes 0.
+// clamped to +-127 (quant_code: one multiply by RN(1/xscale), exact division
+// only near ties); a zero row gives scale 0 and codes 0.
 // ---------------------------------------------------------------------------
 constexpr int kQuantThreads = 256;
 
@@ -43,29 +44,13 @@ __global__ __launch_bounds__(kQuantThreads) void quantize_act_kernel(
             amax = fmaxf(amax, red[i]);
         __syncthreads();  // red is reused by the next row
         const float s = __fdiv_rn(amax, 127.0f);
+        const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
         if (threadIdx.x == 0)
             xscale[m] = s;
         uint2 *qrow = reinterpret_cast<uint2 *>(xq + (size_t)m * K);
         for (int c = threadIdx.x; c < chunks; c += kQuantThreads) {
             const uint4 v = __ldg(row + c);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t packed[2] = {0u, 0u};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
-                const float f[2] = {__low2float(h), __high2float(h)};
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    int q = 0;
-                    if (s != 0.0f) {
-                        q = __float2int_rn(__fdiv_rn(f[e], s));
-                        q = max(-127, min(127, q));
-                    }
-                    const int byte = 2 * j + e;
-                    packed[byte >> 2] |= ((uint32_t)(uint8_t)q) << (8 * (byte & 3));
-                }
-            }
-            qrow[c] = make_uint2(packed[0], packed[1]);
+            qrow[c] = quant_chunk8(v, s, r);
         }
     }
 }

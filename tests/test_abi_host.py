@@ -138,3 +138,25 @@ def test_binding_refuses_cpu_tensors(lib):
     C = torch.zeros((32, 3), dtype=torch.int8)
     with pytest.raises(ValueError):
         s3d8.decode(packed, C, 3)
+
+
+@no_device_only
+def test_batch_rejects(lib):
+    job = s3d8.LinearJob()
+    job.packed, job.centroids, job.chan_scale_bf16, job.xq = A16, A16B, A16C, A16
+    job.xscale, job.out_bf16, job.N, job.K = A16B, A16C, 3, 32
+    arr = (s3d8.LinearJob * 9)(*([job] * 9))
+    assert lib.s3d8_linear_batch(arr, 9, 1, None) == -1          # more than 8 jobs
+    assert lib.s3d8_linear_batch(None, 2, 1, None) == -1
+    assert lib.s3d8_linear_batch(arr, 2, 5, None) == -3          # M > 4
+    assert lib.s3d8_linear_batch(arr, 0, 1, None) == 0
+    assert lib.s3d8_linear_batch(arr, 2, 0, None) == 0
+    both = s3d8.LinearJob.from_buffer_copy(job)
+    both.x_bf16 = A16
+    assert lib.s3d8_linear_batch((s3d8.LinearJob * 1)(both), 1, 1, None) == -1   # x and xq
+    bad_k = s3d8.LinearJob.from_buffer_copy(job)
+    bad_k.K = 40
+    assert lib.s3d8_linear_batch((s3d8.LinearJob * 1)(bad_k), 1, 1, None) == -1
+    mis = s3d8.LinearJob.from_buffer_copy(job)
+    mis.packed = A16 + 4
+    assert lib.s3d8_linear_batch((s3d8.LinearJob * 1)(mis), 1, 1, None) == -2

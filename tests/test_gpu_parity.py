@@ -67,6 +67,45 @@ def test_quantize_act_bitexact(M, K, outliers):
     np.testing.assert_array_equal(to_np(xq), xq_o)
 
 
+def _all_bf16_up_to(amax_bits):
+    # every finite bf16 value with |x| <= bf16(amax), both signs, plus amax itself
+    pos = np.arange(0, 0x7F80, dtype=np.uint32).astype(np.uint16)
+    pos = pos[si.bf16_bits_to_f32(pos) <= si.bf16_bits_to_f32(np.array([amax_bits], np.uint16))[0]]
+    vals = np.concatenate([pos, pos | np.uint16(0x8000), np.array([amax_bits], np.uint16)])
+    pad = (-len(vals)) % 16
+    return np.concatenate([vals, np.zeros(pad, np.uint16)])
+
+
+@pytest.mark.parametrize("amax", [1.0, 3.7, 127.0, 0.0078125, 6.0e-31, 2.5e35, 1.0e-38])
+def test_quantize_exhaustive_bf16(amax):
+    """Every bf16 value below a row's absmax, through both GPU quantisers (the
+    standalone kernel and the one fused into the grouped linear launch)."""
+    a_bits = int(si.f32_to_bf16_bits(np.array([amax], np.float32))[0])
+    row = _all_bf16_up_to(a_bits)[None, :]
+    xq_o, xs_o = oracle.quantize_act(row)
+    xq, xs = s3d8.quantize_act(bf16_bits(row))
+    np.testing.assert_array_equal(to_np(xs), xs_o)
+    np.testing.assert_array_equal(to_np(xq), xq_o)
+    # fused path: slices of at most 28672 values that all contain the absmax
+    rng = np.random.default_rng(a_bits)
+    vals = row[0]
+    C = si.centroids(rng)
+    for start in range(0, vals.size, 28656):
+        part = np.concatenate([vals[start:start + 28656], np.array([a_bits], np.uint16)])
+        part = np.concatenate([part, np.zeros((-part.size) % 16, np.uint16)])[None, :]
+        K = part.shape[1]
+        pq_o, ps_o = oracle.quantize_act(part)
+        xq_out = torch.empty((1, K), dtype=torch.int8, device=dev())
+        xs_out = torch.empty((1,), dtype=torch.float32, device=dev())
+        N = 3
+        packed = si.packed_bytes(rng, 1, K)
+        s3d8.linear_batch([dict(packed=u8(packed), centroids=i8(C), chan_scale=bf16_bits(
+            si.chan_scale(rng, N)), N=N, x=bf16_bits(part), xq_out=xq_out, xscale_out=xs_out)], 1)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(to_np(xs_out), ps_o)
+        np.testing.assert_array_equal(to_np(xq_out), pq_o)
+
+
 def test_quantize_act_ties_and_guards():
     # absmax 127 gives a unit scale: halves round to even
     vals = [127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -0.5, 126.5, 0.0, -127.0, 64.0, 1.0, -1.0,
