@@ -455,13 +455,14 @@ def prefill_measure(torch, s3d8, dev, M=2048, reps=3):
         x = to_dev_bf16(si.acts(M, K, seed=3), dev)
         xq, xs = s3d8.quantize_act(x)
         out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        s3d8.linear(packed, C, cs, xq, xs, N, out=out)
+        ws = torch.empty((s3d8.workspace_size(M, N, K),), dtype=torch.uint8, device=dev)
+        s3d8.linear(packed, C, cs, xq, xs, N, out=out, workspace=ws)
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         for _ in range(reps):
-            s3d8.linear(packed, C, cs, xq, xs, N, out=out)
+            s3d8.linear(packed, C, cs, xq, xs, N, out=out, workspace=ws)
         t1.record()
         t1.synchronize()
         ms = t0.elapsed_time(t1) / reps

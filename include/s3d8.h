@@ -172,6 +172,15 @@ int s3d8_linear_batch(const s3d8_linear_job *jobs, int count, int64_t M, void *s
  * (S3D8_OK or S3D8_ERR_TIMEOUT), or S3D8_ERR_CUDA if the synchronisation fails. */
 int s3d8_device_status(void *stream);
 
+/*
+ * Failure-path self-test (no fault, no hang): launches one warp that waits on an
+ * mbarrier nothing completes, for `polls` polls (1..2^24), then records
+ * S3D8_ERR_TIMEOUT in the device status word exactly as the streaming kernels'
+ * bounded waits do.  s3d8_device_status then returns (and clears) the timeout.
+ * Covers the bounded-wait design of the kernels; the pages have no counterpart.
+ */
+int s3d8_selftest_wait_timeout(int64_t polls, void *stream);
+
 /* Static English text for a status code. */
 const char *s3d8_status_string(int status);
 

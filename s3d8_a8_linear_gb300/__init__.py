@@ -76,12 +76,14 @@ def load(build_if_missing: bool = False):
     L.s3d8_linear_ex.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, SZ, I, P]
     L.s3d8_linear_acc_i32.argtypes = [P, P, P, I64, I64, I64, P, P, SZ, I, P]
     L.s3d8_linear_batch.argtypes = [ctypes.POINTER(LinearJob), I, I64, P]
+    L.s3d8_selftest_wait_timeout.argtypes = [I64, P]
     L.s3d8_device_status.argtypes = [P]
     L.s3d8_status_string.argtypes = [I]
     L.s3d8_status_string.restype = ctypes.c_char_p
     L.s3d8_version.argtypes = []
     for fn in ("s3d8_quantize_act", "s3d8_decode", "s3d8_linear", "s3d8_linear_ex",
-               "s3d8_linear_acc_i32", "s3d8_linear_batch", "s3d8_device_status", "s3d8_version"):
+               "s3d8_linear_acc_i32", "s3d8_linear_batch", "s3d8_selftest_wait_timeout",
+               "s3d8_device_status", "s3d8_version"):
         getattr(L, fn).restype = I
     _lib = L
     return L
@@ -245,6 +247,11 @@ def linear_batch(jobs, M: int):
     st = load().s3d8_linear_batch(arr, len(jobs), M, _stream(device))
     _check("s3d8_linear_batch", st)
     return results
+
+
+def selftest_wait_timeout(polls: int = 1000) -> None:
+    """Run the bounded-wait failure path once (see include/s3d8.h)."""
+    _check("s3d8_selftest_wait_timeout", load().s3d8_selftest_wait_timeout(polls, _stream(None)))
 
 
 def device_status() -> int:

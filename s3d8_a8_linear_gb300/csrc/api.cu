@@ -124,13 +124,24 @@ int s3d8_decode(const uint8_t *packed, const int8_t *centroids, int64_t N, int64
                                      static_cast<cudaStream_t>(stream)));
 }
 
+// The algorithm AUTO runs: the bulk-copy GEMV up to 4 tokens, the tensor-core
+// GEMM from kTcMinM tokens, the plain GEMV in between.
+constexpr int64_t kTcMinM = 16;
+
+static int resolve_algo(int64_t M, int64_t K, int algo)
+{
+    (void)K;
+    if (algo != S3D8_ALGO_AUTO)
+        return algo;
+    return M >= kTcMinM ? S3D8_ALGO_TC : S3D8_ALGO_GEMV;
+}
+
 size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo)
 {
-    (void)M;
     (void)N;
-    (void)K;
-    (void)algo;
-    return 0;
+    if (M <= 0 || K <= 0 || M > S3D8_MAX_M || K > S3D8_MAX_K)
+        return 0;
+    return resolve_algo(M, K, algo) == S3D8_ALGO_TC ? prefill_workspace_bytes((int)M, (int)K) : 0;
 }
 
 static int linear_common(const uint8_t *packed, const int8_t *centroids, const void *chan_scale,
@@ -163,7 +174,8 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     const size_t need = s3d8_linear_workspace_size(M, N, K, algo);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return S3D8_ERR_WORKSPACE;
-    if (algo != S3D8_ALGO_AUTO && algo != S3D8_ALGO_GEMV)
+    algo = resolve_algo(M, K, algo);
+    if (algo != S3D8_ALGO_GEMV && algo != S3D8_ALGO_TC)
         return S3D8_ERR_UNSUPPORTED;
 
     LinearArgs a;
@@ -181,6 +193,8 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     a.ws_bytes = workspace_bytes;
     a.status = device_status_ptr();
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    if (algo == S3D8_ALGO_TC)
+        return cuda_status(launch_prefill_tc(a, strm));
     if (gemv_tma_supported(a.M, a.K))
         return cuda_status(launch_gemv_tma(a, strm));
     return cuda_status(launch_gemv(a, strm));
@@ -275,6 +289,16 @@ int s3d8_linear_batch(const s3d8_linear_job *jobs, int count, int64_t M, void *s
         return S3D8_OK;
     g.status = device_status_ptr();
     return cuda_status(launch_gemv_group(g, static_cast<cudaStream_t>(stream)));
+}
+
+int s3d8_selftest_wait_timeout(int64_t polls, void *stream)
+{
+    if (polls < 1 || polls > (1 << 24))
+        return S3D8_ERR_INVALID_ARG;
+    int *st = device_status_ptr();
+    if (!st)
+        return S3D8_ERR_CUDA;
+    return cuda_status(launch_wait_timeout((int)polls, st, static_cast<cudaStream_t>(stream)));
 }
 
 int s3d8_device_status(void *stream)

@@ -1,0 +1,472 @@
+// Prefill-regime S3D8 linear on the 5th-generation tensor cores (tcgen05).
+//
+// sm_103a has no tcgen05 integer MMA, and its legacy INT8 tensor rate is about a
+// thirteenth of bf16, so the product runs as bf16 x bf16 -> fp32 with an exact
+// integer result: int8 codes and int8 weights are exact in bf16, every product
+// is an integer below 2^14, and each K-chunk of at most 1024 columns keeps every
+// partial sum below 127 * 127 * 1024 < 2^24, where fp32 holds integers exactly.
+// After each chunk the fp32 accumulator is drained into int32 registers.
+//
+// Tile: 128 tokens (MMA M) x 240 output channels (MMA N; 80 whole packed groups)
+// per CTA, K in blocks of 64.  Sixteen warps in four warpgroups:
+//   warp 0      bulk tensor copies (TMA) of the bf16 activation tile (from the
+//               workspace) and of the 80 x 64 packed-byte tile;
+//   warp 1      TMEM allocation and the MMA issuer (one thread);
+//   warps 2-7   decode: packed bytes -> bf16 weights, written straight into the
+//               128-byte-swizzled K-major layout the MMA descriptor reads;
+//   warps 8-15  drain the fp32 accumulator per K-chunk into int32 registers and
+//               write the epilogue (x_s * acc) * W_s as bf16 (or the raw int32).
+// Warpgroups 0-1 give registers up (setmaxnreg 80) so that the drain warps can
+// hold 120 int32 sums each (setmaxnreg 176): 128 x (80+80+176+176) = 65536.
+// TMEM holds two accumulator buffers (columns 0 and 256) so that the MMA fills
+// one chunk while the other drains.  Every mbarrier wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tma.cuh"
+
+namespace s3d8 {
+
+namespace tc {
+
+constexpr int BM = 128;                  // tokens per tile
+constexpr int GROUPS = 80;               // packed rows per tile
+constexpr int BN = 3 * GROUPS;           // 240 channels per tile
+constexpr int BK = 64;                   // K per block (128 bytes of bf16)
+constexpr int STAGES = 3;
+constexpr int CHUNK_BLOCKS = 16;         // 16 x 64 = 1024 columns per exact chunk
+constexpr int A_BYTES = BM * BK * 2;     // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;     // 30 KiB
+constexpr int P_BYTES = GROUPS * BK;     // 5 KiB packed bytes
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + P_BYTES;
+constexpr int LUT_COPIES = 16;
+constexpr int LUT_BYTES = kLutEntries * LUT_COPIES * 8;   // 32 KiB
+constexpr int NBARS = 3 * STAGES + 4;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + LUT_BYTES + NBARS * 8 + 16;
+constexpr int THREADS = 16 * 32;
+constexpr int PRODUCERS = 192;   // warps 2-7
+constexpr int DRAIN_WARP0 = 8;
+constexpr int HALF = BN / 2;             // 120 columns per epilogue thread
+
+static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzled tiles must stay 1024-aligned");
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t a)
+{
+    // tcgen05 shared-memory descriptor: start >> 4, LBO 16 B (unused for swizzled
+    // K-major), SBO 1024 B between 8-row atoms, version 1, 128-byte swizzle.
+    return (uint64_t)((a & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+// bf16 bits of a small integer (exact: |v| <= 127 needs 7 significant bits).
+__device__ __forceinline__ uint32_t bf16_bits_of(int v)
+{
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((float)v));
+}
+
+struct Params {
+    int M, N, K;
+    const int8_t *C;
+    const __nv_bfloat16 *cs;
+    const float *xscale;
+    __nv_bfloat16 *out;
+    int32_t *acc;
+    int *status;
+    int vec_out;   // out / acc rows may be written with 16-byte stores
+};
+
+__global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_constant__ CUtensorMap tm_act,
+                                                             const __grid_constant__ CUtensorMap tm_pk,
+                                                             Params p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *smem = smem_raw + (base - raw);
+    const uint32_t lut = base + STAGES * STAGE_BYTES;
+    const uint32_t bars = lut + LUT_BYTES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + STAGES * STAGE_BYTES + LUT_BYTES + NBARS * 8);
+    // barriers: a_full[S] (TMA bytes), b_full[S] (decoded tile), empty[S] (MMA done),
+    //           acc_full[2] (chunk in TMEM), acc_empty[2] (chunk drained)
+    const uint32_t a_full = bars, b_full = bars + 8 * STAGES, empty = bars + 16 * STAGES;
+    const uint32_t acc_full = bars + 24 * STAGES, acc_empty = acc_full + 16;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mtiles = (p.M + BM - 1) / BM;
+    const int mt = (int)(blockIdx.x % (unsigned)mtiles), nt = (int)(blockIdx.x / (unsigned)mtiles);
+    const int m0 = mt * BM;
+    const int g0 = nt * GROUPS;
+    const int nk = (p.K + BK - 1) / BK;
+    const int nchunks = (nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(a_full + 8 * s, 1);
+            mbar_init(b_full + 8 * s, PRODUCERS / 32);
+            mbar_init(empty + 8 * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(acc_full + 8 * i, 1);
+            mbar_init(acc_empty + 8 * i, 8);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_addr(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // decode table: byte -> [bf16 w0 | bf16 w1 << 16, bf16 w2], 16 copies (one per
+    // half-warp lane) so that 8-byte lookups never conflict.
+    {
+        __shared__ int8_t Cs[96];
+        for (int i = threadIdx.x; i < 96; i += THREADS)
+            Cs[i] = p.C[i];
+        __syncthreads();
+        uint2 *t = reinterpret_cast<uint2 *>(smem + STAGES * STAGE_BYTES);
+        for (int i = threadIdx.x; i < kLutEntries * LUT_COPIES; i += THREADS) {
+            const uint32_t e = expanded_entry(Cs, (uint32_t)(i / LUT_COPIES));
+            const int w0 = (int8_t)(e & 0xFF), w1 = (int8_t)((e >> 8) & 0xFF), w2 = (int8_t)((e >> 16) & 0xFF);
+            t[i] = make_uint2(bf16_bits_of(w0) | (bf16_bits_of(w1) << 16), bf16_bits_of(w2));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool timed_out = false;
+
+    if (warp < DRAIN_WARP0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+    if (warp == 0) {
+        // ---- bulk tensor copies ------------------------------------------------
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % STAGES;
+                if (kb >= STAGES && !mbar_wait_bounded(empty + 8 * s, ((kb / STAGES) - 1) & 1)) {
+                    timed_out = true;
+                    break;
+                }
+                issued = kb + 1;
+                const uint32_t st = base + s * STAGE_BYTES;
+                mbar_arrive_expect_tx(a_full + 8 * s, A_BYTES + P_BYTES);
+                tma_2d(st, &tm_act, kb * BK, m0, a_full + 8 * s);
+                tma_2d(st + A_BYTES + B_BYTES, &tm_pk, kb * BK, g0, a_full + 8 * s);
+            }
+            // never leave with copies in flight: wait (bounded) for the last ones
+            for (int kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
+                if (!mbar_wait_bounded(a_full + 8 * (kb % STAGES), (kb / STAGES) & 1))
+                    timed_out = true;
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer ----------------------------------------------------------
+        if (lane == 0) {
+            int issued = 0;
+            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                   ((uint32_t)(BM >> 4) << 24);
+            for (int kb = 0; kb < nk && !timed_out; ++kb) {
+                const int s = kb % STAGES;
+                const int c = kb / CHUNK_BLOCKS, kin = kb % CHUNK_BLOCKS;
+                const uint32_t d = tmem + (uint32_t)((c & 1) * 256);
+                if (kin == 0 && c >= 2 && !mbar_wait_bounded(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
+                    timed_out = true;
+                    break;
+                }
+                if (!mbar_wait_bounded(a_full + 8 * s, (kb / STAGES) & 1) ||
+                    !mbar_wait_bounded(b_full + 8 * s, (kb / STAGES) & 1)) {
+                    timed_out = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = base + s * STAGE_BYTES, b = a + A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
+                             (kin | kk) ? 1u : 0u);
+                mma_commit(empty + 8 * s);
+                if (kin == CHUNK_BLOCKS - 1 || kb == nk - 1)
+                    mma_commit(acc_full + 8 * (c & 1));
+                issued = kb + 1;
+            }
+            // the tensor core must be done with TMEM and shared memory before exit
+            if (issued > 0 && !mbar_wait_bounded(empty + 8 * ((issued - 1) % STAGES), ((issued - 1) / STAGES) & 1))
+                timed_out = true;
+        }
+    } else {
+        // ---- decode packed bytes into the swizzled bf16 weight tile -------------
+        const int t = threadIdx.x - 64;
+        const uint32_t lut_lane = lut + (uint32_t)((lane & (LUT_COPIES - 1)) * 8);
+        for (int kb = 0; kb < nk && !timed_out; ++kb) {
+            const int s = kb % STAGES;
+            if (!mbar_wait_bounded(a_full + 8 * s, (kb / STAGES) & 1)) {
+                timed_out = true;
+                break;
+            }
+            const uint32_t st = base + s * STAGE_BYTES;
+            const uint32_t btile = st + A_BYTES, ptile = st + A_BYTES + B_BYTES;
+            for (int u = t; u < GROUPS * 8; u += PRODUCERS) {
+                const int gl = u >> 3, j = u & 7;   // group, 16-byte chunk (8 k)
+                uint32_t pk0, pk1;
+                asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(pk0), "=r"(pk1) : "r"(ptile + gl * 64 + j * 8));
+                uint2 e[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t byte = ((i < 4 ? pk0 : pk1) >> (8 * (i & 3))) & 0xFFu;
+                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                                 : "=r"(e[i].x), "=r"(e[i].y)
+                                 : "r"(lut_lane + byte * (LUT_COPIES * 8)));
+                }
+                uint32_t w[3][4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    w[0][q] = prmt(e[2 * q].x, e[2 * q + 1].x, 0x5410);
+                    w[1][q] = prmt(e[2 * q].x, e[2 * q + 1].x, 0x7632);
+                    w[2][q] = prmt(e[2 * q].y, e[2 * q + 1].y, 0x5410);
+                }
+#pragma unroll
+                for (int d = 0; d < 3; ++d) {
+                    const int n = 3 * gl + d;
+                    const uint32_t addr = btile + n * 128 + (((uint32_t)j ^ (uint32_t)(n & 7)) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[d][0]),
+                                 "r"(w[d][1]), "r"(w[d][2]), "r"(w[d][3])
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_smem();   // generic writes -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b_full + 8 * s);
+        }
+    }
+    } else {
+        // ---- drain chunks into int32, then the epilogue ---------------------------
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
+        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        const int h = (warp - DRAIN_WARP0) >> 2; // which half of the 240 columns
+        int32_t acc[HALF];
+#pragma unroll
+        for (int i = 0; i < HALF; ++i)
+            acc[i] = 0;
+        for (int c = 0; c < nchunks && !timed_out; ++c) {
+            if (!mbar_wait_bounded(acc_full + 8 * (c & 1), (c >> 1) & 1)) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((c & 1) * 256 + h * HALF);
+#pragma unroll
+            for (int g = 0; g < HALF / 24; ++g) {
+                float v[3][8];
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+                    tmem_ld8(ta + (g * 3 + i) * 8, v[i]);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        acc[(g * 3 + i) * 8 + j] += __float2int_rn(v[i][j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acc_empty + 8 * (c & 1));
+        }
+        const int row = m0 + 32 * q + lane;
+        if (!timed_out && row < p.M) {
+            const int nbase = nt * BN + h * HALF;
+            const bool full = nbase + HALF <= p.N;
+            if (p.acc) {
+                int32_t *dst = p.acc + (size_t)row * p.N + nbase;
+                if (full && p.vec_out) {
+#pragma unroll
+                    for (int i = 0; i < HALF; i += 4)
+                        *reinterpret_cast<int4 *>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < HALF; ++i)
+                        if (nbase + i < p.N)
+                            dst[i] = acc[i];
+                }
+            } else {
+                const float xs = p.xscale[row];
+                __nv_bfloat16 *dst = p.out + (size_t)row * p.N + nbase;
+                if (full && p.vec_out) {
+#pragma unroll
+                    for (int i = 0; i < HALF; i += 8) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const __nv_bfloat16 lo = epilogue_bf16(acc[i + 2 * j], xs, p.cs[nbase + i + 2 * j]);
+                            const __nv_bfloat16 hi =
+                                epilogue_bf16(acc[i + 2 * j + 1], xs, p.cs[nbase + i + 2 * j + 1]);
+                            o[j] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+                        }
+                        *reinterpret_cast<uint4 *>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < HALF; ++i)
+                        if (nbase + i < p.N)
+                            dst[i] = epilogue_bf16(acc[i], xs, p.cs[nbase + i]);
+                }
+            }
+        }
+    }
+    if (timed_out)
+        record_timeout(p.status);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+}
+
+// int8 codes -> bf16 (exact), the tensor-core A operand.
+__global__ void codes_to_bf16_kernel(const int8_t *__restrict__ xq, __nv_bfloat16 *__restrict__ a, long n16)
+{
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (long)gridDim.x * blockDim.x) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xq) + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b0 = (int8_t)(w[j] & 0xFF), b1 = (int8_t)((w[j] >> 8) & 0xFF);
+            const int b2 = (int8_t)((w[j] >> 16) & 0xFF), b3 = (int8_t)(w[j] >> 24);
+            o[2 * j] = bf16_bits_of(b0) | (bf16_bits_of(b1) << 16);
+            o[2 * j + 1] = bf16_bits_of(b2) | (bf16_bits_of(b3) << 16);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(a) + 2 * i;
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+}  // namespace tc
+
+size_t prefill_workspace_bytes(int M, int K)
+{
+    return (size_t)M * (size_t)K * 2 + 256;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream)
+{
+    using namespace tc;
+    if (!a.ws || a.ws_bytes < prefill_workspace_bytes(a.M, a.K))
+        return cudaErrorInvalidValue;
+    auto encode = tensor_map_encoder();
+    if (!encode)
+        return cudaErrorNotSupported;
+    __nv_bfloat16 *act = reinterpret_cast<__nv_bfloat16 *>(((uintptr_t)a.ws + 255) & ~(uintptr_t)255);
+    const long n16 = (long)a.M * a.K / 16;
+    const int sms = device_sm_count();
+    int cgrid = (int)((n16 + 255) / 256);
+    if (cgrid > sms * 8)
+        cgrid = sms * 8;
+    tc::codes_to_bf16_kernel<<<cgrid, 256, 0, stream>>>(a.xq, act, n16);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+
+    const int G = (a.N + 2) / 3;
+    CUtensorMap tm_act, tm_pk;
+    const cuuint64_t dA[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    const cuuint64_t sA[1] = {(cuuint64_t)a.K * 2};
+    const cuuint32_t boxA[2] = {BK, BM}, es[2] = {1, 1};
+    const cuuint64_t dP[2] = {(cuuint64_t)a.K, (cuuint64_t)G};
+    const cuuint64_t sP[1] = {(cuuint64_t)a.K};
+    const cuuint32_t boxP[2] = {BK, GROUPS};
+    if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, act, dA, sA, boxA, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), dP, sP, boxP, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    e = cudaFuncSetAttribute(tc::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    tc::Params p;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.C = a.C;
+    p.cs = a.cs;
+    p.xscale = a.xscale;
+    p.out = a.out;
+    p.acc = a.acc;
+    p.status = a.status;
+    p.vec_out = a.acc ? ((a.N & 3) == 0 && ((uintptr_t)a.acc & 15) == 0)
+                      : ((a.N & 7) == 0 && ((uintptr_t)a.out & 15) == 0);
+    const long tiles = (long)((a.M + BM - 1) / BM) * (long)((G + GROUPS - 1) / GROUPS);
+    if (tiles > 0x7FFFFFFFL)
+        return cudaErrorInvalidValue;
+    tc::prefill_kernel<<<(unsigned)tiles, THREADS, SMEM_BYTES, stream>>>(tm_act, tm_pk, p);
+    return cudaGetLastError();
+}
+
+}  // namespace s3d8

@@ -45,11 +45,11 @@ def assert_out_close(got, ref):
         raise AssertionError(f"out outside tolerance at {i}: got {got[i]}, ref {ref[i]}")
 
 
-def guarded(shape, dtype, fill):
-    """A tensor view with guard elements on both sides, and a checker that the
-    guards were left untouched."""
+def guarded(shape, dtype, fill, pad=64):
+    """A tensor view with `pad` guard elements on both sides, and a checker that
+    the guards were left untouched.  An odd pad gives a view that is not
+    16-byte aligned."""
     n = int(np.prod(shape))
-    pad = 64
     buf = torch.full((n + 2 * pad,), fill, dtype=dtype, device=dev())
     view = buf[pad:pad + n].view(*shape)
 

@@ -17,7 +17,7 @@ from gpu_util import (assert_out_close, bf16_bits, bf16_to_f64, dev, f32, guarde
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = [s3d8.ALGO_GEMV]
+ALGOS = [s3d8.ALGO_GEMV, s3d8.ALGO_TC]
 ALGO_IDS = {s3d8.ALGO_AUTO: "auto", s3d8.ALGO_GEMV: "gemv", s3d8.ALGO_SKINNY: "skinny",
             s3d8.ALGO_TC: "tc"}
 
@@ -257,6 +257,59 @@ def test_zero_activation_row_gives_zero(algo):
     assert (out[1] == 0).all()
 
 
+TC_TILES = [(128, 240, 64), (129, 241, 1040), (300, 722, 2112), (256, 480, 3072),
+            (1, 3, 16), (17, 1201, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", TC_TILES)
+def test_tc_tiles_and_tails(M, N, K):
+    """Tensor-core path in full against the oracle: whole and ragged 128-token and
+    240-channel tiles, K ragged against the 64-column block and the 1024-column
+    exact chunk."""
+    C, packed, cs, x = rand_case(M, N, K, seed=M * 7919 + N * 31 + K)
+    xq, xs = oracle.quantize_act(x)
+    ref, acc_o = oracle.linear(packed, C, cs, xq, xs, N)
+    np.testing.assert_array_equal(gpu_acc(C, packed, xq, N, s3d8.ALGO_TC), acc_o)
+    out, check = guarded((M, N), torch.bfloat16, 3.0)
+    s3d8.linear(u8(packed), i8(C), bf16_bits(cs), i8(xq), f32(xs), N, out=out, algo=s3d8.ALGO_TC)
+    torch.cuda.synchronize()
+    check()
+    assert_out_close(bf16_to_f64(out), ref)
+
+
+def test_tc_unaligned_outputs():
+    """Output views that are only 2- (bf16) or 4-byte (int32) aligned take the
+    scalar store path and still match."""
+    M, N, K = 130, 480, 256
+    C, packed, cs, x = rand_case(M, N, K, seed=5)
+    xq, xs = oracle.quantize_act(x)
+    ref, acc_o = oracle.linear(packed, C, cs, xq, xs, N)
+    out, check = guarded((M, N), torch.bfloat16, 3.0, pad=65)
+    s3d8.linear(u8(packed), i8(C), bf16_bits(cs), i8(xq), f32(xs), N, out=out, algo=s3d8.ALGO_TC)
+    acc, check_acc = guarded((M, N), torch.int32, 7, pad=33)
+    s3d8.linear_acc_i32(u8(packed), i8(C), i8(xq), N, algo=s3d8.ALGO_TC, acc=acc)
+    torch.cuda.synchronize()
+    check()
+    check_acc()
+    assert_out_close(bf16_to_f64(out), ref)
+    np.testing.assert_array_equal(to_np(acc).astype(np.int64), acc_o)
+
+
+def test_tc_adversarial_chunk_sums():
+    """Every product +16129 over 1024 columns is the largest partial sum an exact
+    fp32 chunk holds (16,516,096 < 2^24); two chunks in a row must still add
+    exactly in int32 (K = 2048 + 1024 + 16)."""
+    C = np.full((32, 3), 127, np.int8)
+    M, N, K = 200, 243, 3088
+    packed = np.full((si.groups(N), K), oracle.pack_byte(3, 0, 0, 0), np.uint8)
+    xq = np.full((M, K), 127, np.int8)
+    xq[1::2, 1024:2048] = -127        # odd rows: the middle chunk cancels the first
+    acc_o, bad = oracle.linear_acc(packed, C, xq, N)
+    assert bad == 0
+    np.testing.assert_array_equal(gpu_acc(C, packed, xq, N, s3d8.ALGO_TC), acc_o)
+    assert acc_o[0, 0] == 16129 * K
+
+
 def test_empty_and_rejected_calls():
     packed = torch.zeros((2, 32), dtype=torch.uint8, device=dev())
     C = torch.zeros((32, 3), dtype=torch.int8, device=dev())
@@ -278,4 +331,18 @@ def test_empty_and_rejected_calls():
         s3d8.linear(torch.zeros((2, 24), dtype=torch.uint8, device=dev()), C, cs,
                     torch.zeros((1, 24), dtype=torch.int8, device=dev()), xs1, 5)
     assert e.value.status == -1
+    assert s3d8.device_status() == 0
+
+
+def test_bounded_wait_reports_timeout_and_recovers():
+    """A wait that nothing completes ends with S3D8_ERR_TIMEOUT in the status
+    word (no fault, no hang); the status clears on read and work continues."""
+    assert s3d8.device_status() == 0
+    s3d8.selftest_wait_timeout(2000)
+    assert s3d8.device_status() == -5
+    assert s3d8.device_status() == 0
+    C, packed, cs, x = rand_case(2, 9, 64, seed=77)
+    xq, xs = oracle.quantize_act(x)
+    _, acc_o = oracle.linear(packed, C, cs, xq, xs, 9)
+    np.testing.assert_array_equal(gpu_acc(C, packed, xq, 9, s3d8.ALGO_GEMV), acc_o)
     assert s3d8.device_status() == 0
