@@ -181,6 +181,33 @@ int s3d8_device_status(void *stream);
  */
 int s3d8_selftest_wait_timeout(int64_t polls, void *stream);
 
+/* Size of the fixed device scratch behind s3d8_linear_tc_noalloc (32 MiB). */
+#define S3D8_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * The tensor-core linear (s3d8_linear_ex with S3D8_ALGO_TC: same kernels, same
+ * results, same argument layouts and alignment rules) for callers that cannot
+ * allocate device memory: code inside an allocator or memory-pool callback, a
+ * real-time loop that must never wait on the driver's allocator, or a host that
+ * owns all device memory itself.  It calls no cudaMalloc or cudaFree and no
+ * allocating library routine.  Instead of caller workspace it uses a fixed
+ * scratch array of S3D8_NOALLOC_SCRATCH_BYTES compiled into the library, which
+ * every GPU that loads the library holds until the process exits.  The paper
+ * has no counterpart; this is a deployment convenience.
+ *   - Shapes with 2 * M * K + 256 > S3D8_NOALLOC_SCRATCH_BYTES are rejected with
+ *     S3D8_ERR_WORKSPACE before any CUDA call (e.g. M <= 2047 at K = 4096).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (once per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - All calls on a device share the one array.  Calls that overlap on the GPU
+ *     (on different streams, or from several threads without ordering) race on
+ *     it and give wrong results; order them on one stream.
+ * Inputs and outputs are still the caller's device memory, as in s3d8_linear.
+ */
+int s3d8_linear_tc_noalloc(const uint8_t *packed, const int8_t *centroids,
+                           const void *chan_scale_bf16, const int8_t *xq, const float *xscale,
+                           int64_t M, int64_t N, int64_t K, void *out_bf16, void *stream);
+
 /* Static English text for a status code. */
 const char *s3d8_status_string(int status);
 

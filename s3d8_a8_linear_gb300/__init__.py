@@ -77,6 +77,7 @@ def load(build_if_missing: bool = False):
     L.s3d8_linear_acc_i32.argtypes = [P, P, P, I64, I64, I64, P, P, SZ, I, P]
     L.s3d8_linear_batch.argtypes = [ctypes.POINTER(LinearJob), I, I64, P]
     L.s3d8_selftest_wait_timeout.argtypes = [I64, P]
+    L.s3d8_linear_tc_noalloc.argtypes = [P, P, P, P, P, I64, I64, I64, P, P]
     L.s3d8_device_status.argtypes = [P]
     L.s3d8_status_string.argtypes = [I]
     L.s3d8_status_string.restype = ctypes.c_char_p
@@ -181,6 +182,30 @@ def linear(packed: torch.Tensor, centroids: torch.Tensor, chan_scale: torch.Tens
         _dev(out, "out", torch.bfloat16, (M, N)),
         None if ws is None else ws.data_ptr(), ws_bytes, algo, _stream(packed.device))
     _check("s3d8_linear_ex", st)
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def linear_tc_noalloc(packed: torch.Tensor, centroids: torch.Tensor, chan_scale: torch.Tensor,
+                      xq: torch.Tensor, xscale: torch.Tensor, N: int,
+                      out: torch.Tensor) -> torch.Tensor:
+    """The tensor-core linear into the caller's `out` without any device
+    allocation, neither here nor in the library: its scratch is a fixed array of
+    NOALLOC_SCRATCH_BYTES inside the library (2 M K + 256 bytes must fit).  For
+    callers that cannot allocate device memory.  Calls that overlap on the GPU
+    share that array and race; order them on one stream."""
+    G, K = packed.shape
+    if G != groups(N):
+        raise ValueError(f"packed has {G} rows, expected ceil(N/3) = {groups(N)}")
+    M = xq.shape[0]
+    st = load().s3d8_linear_tc_noalloc(
+        _dev(packed, "packed", torch.uint8), _dev(centroids, "centroids", torch.int8, (32, 3)),
+        _dev(chan_scale, "chan_scale", torch.bfloat16, (N,)), _dev(xq, "xq", torch.int8, (M, K)),
+        _dev(xscale, "xscale", torch.float32, (M,)), M, N, K,
+        _dev(out, "out", torch.bfloat16, (M, N)), _stream(packed.device))
+    _check("s3d8_linear_tc_noalloc", st)
     return out
 
 

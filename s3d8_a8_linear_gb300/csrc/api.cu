@@ -27,7 +27,7 @@ int device_sm_count()
     return cached[dev];
 }
 
-static int *device_status_ptr()
+int *device_status_ptr()
 {
     static int *cached[kMaxDevices] = {nullptr};
     int dev = 0;

@@ -48,6 +48,7 @@ struct GroupArgs {
 };
 
 int device_sm_count();
+int *device_status_ptr();   // this device's sticky status word, or nullptr
 
 cudaError_t launch_quantize_act(const __nv_bfloat16 *x, int M, int K, int8_t *xq, float *xscale,
                                 cudaStream_t stream);
