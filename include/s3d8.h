@@ -16,7 +16,8 @@
  * Conventions shared by every entry point
  *   - Every pointer is caller-owned DEVICE memory unless stated otherwise.  The
  *     library allocates nothing per call and keeps no state except one device
- *     status word (see s3d8_device_status).
+ *     status word (see s3d8_device_status) and the fixed scratch array of
+ *     s3d8_linear_tc_noalloc.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
  *     is the legacy default stream).  They neither synchronise nor read device
  *     memory from the host.
@@ -30,6 +31,13 @@
  *     accumulator is exact (127 * 127 * K < 2^31).
  *   - Not checked, for speed: centroid values must lie in 0..127 and the bf16
  *     inputs must be finite.
+ *   - The decode-regime kernels (s3d8_linear_batch, and s3d8_linear* for
+ *     M <= 4) use programmatic dependent launch: when the kernel before them on
+ *     the stream allows an early start (this library's kernels do), they read
+ *     the packed weights and centroid tables while that kernel is still
+ *     finishing, and everything else only after it has completed.  So packed
+ *     weights and centroids must not be outputs of the kernel launched
+ *     immediately before on the same stream; activations and scales may be.
  */
 #ifndef S3D8_H
 #define S3D8_H

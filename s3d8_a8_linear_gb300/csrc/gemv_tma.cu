@@ -14,18 +14,21 @@
 //     activations the CTA first quantises the whole row into shared memory
 //     (per-token absmax / 127 with IEEE division, round-half-even), so that no
 //     separate quantisation launch is needed.
-// Work inside a CTA: a contiguous range of packed rows of its job.  A row's K
-// is cut into T slices of 4 KiB (the last may be shorter); warp w always takes
-// slice w % T of rows r0 + w / T + i * (16 / T).  A warp covers 512 contiguous
+// Work inside a job: a contiguous range of packed rows per CTA.  A row's K is
+// cut into T slices of 4 KiB (the last may be shorter); warp w always takes
+// slice w % T of rows r0 + w / T + i * (16 / T).  (Dealing rows out in stripes
+// across CTAs, so that all warps of a job read one moving window of HBM, was
+// measured slower on GB300.)  A warp covers 512 contiguous
 // bytes per step (16 per lane), so each bulk copy is one contiguous row slice.
 // The channel sums of a row slice are reduced with a transposed butterfly; with
 // T > 1 the slices of a row meet in shared-memory atomics, written out after a
 // CTA barrier.  Output: bf16 epilogue (x_s * acc) * W_s, or raw int32 sums.
 //
-// Programmatic dependent launch: the kernel lets the next grid launch early and
-// reads no input before griddepcontrol.wait; after it, the 96-byte table and the
-// activations are requested before the bulk weight copies so that the prologue
-// (table build, quantisation) overlaps the first slices in flight.
+// Programmatic dependent launch: the kernel lets the next grid launch early.
+// Before griddepcontrol.wait it touches only weights (centroid table, the wide
+// decode table, the first bulk copies of packed rows), which are parameters and
+// never outputs of the preceding kernel; the activations (and everything
+// written) come after the wait.
 #include "common.cuh"
 #include "launch.h"
 #include "tma.cuh"
@@ -34,7 +37,9 @@ namespace s3d8 {
 
 constexpr int kTmaWarps = 16;
 constexpr int kTmaThreads = kTmaWarps * 32;
-constexpr int kDepth = 2;
+constexpr int kDepth = 2;    // row slices per warp ring
+constexpr int kHalves = 2;   // each slice arrives as two bulk copies with their own barriers
+constexpr int kBarsPerWarp = kDepth * kHalves;
 // 512-byte chunks per slice: 8 (4 KiB) for up to 2 tokens, 4 for 3..4 tokens so
 // that the activations of the slice still fit in registers.
 __host__ __device__ constexpr int chunks_for(int MT)
@@ -51,7 +56,7 @@ __host__ __device__ constexpr int pow2_at_least(int v)
 
 struct TmaLayout {
     uint32_t lut;    // wide table (64 KiB, window-aligned)
-    uint32_t bars;   // kTmaWarps * kDepth mbarriers
+    uint32_t bars;   // kTmaWarps * kBarsPerWarp mbarriers
     uint32_t uni;    // kUnionBytes: quantised activations, later the T > 1 sums
     uint32_t ring;   // this warp's ring
     bool ok;
@@ -68,7 +73,7 @@ __device__ __forceinline__ TmaLayout tma_layout(uint32_t base, uint32_t size, in
     const uint32_t ring_bytes = kDepth * stage;
     uint32_t lo = (base + 7) & ~7u;
     uint32_t hi = L.lut + kWideLutBytes;
-    const uint32_t small = kTmaWarps * kDepth * 8 + 16 + kUnionBytes;
+    const uint32_t small = kTmaWarps * kBarsPerWarp * 8 + 16 + kUnionBytes;
     uint32_t small_at;
     if (lo + small <= L.lut) {
         small_at = lo;
@@ -78,7 +83,7 @@ __device__ __forceinline__ TmaLayout tma_layout(uint32_t base, uint32_t size, in
         hi += small;
     }
     L.bars = small_at;
-    L.uni = (small_at + kTmaWarps * kDepth * 8 + 15) & ~15u;
+    L.uni = (small_at + kTmaWarps * kBarsPerWarp * 8 + 15) & ~15u;
     lo = (lo + 127) & ~127u;
     hi = (hi + 127) & ~127u;
     const uint32_t below = L.lut > lo ? (L.lut - lo) / ring_bytes : 0;
@@ -201,13 +206,14 @@ __device__ __forceinline__ void act_codes(const ActRegs &r, int M, int K, const 
 
 template <int MT, int CH>
 struct SliceCompute {
-    // Decodes `nch` 512-byte chunks of a staged slice and accumulates all tokens.
-    template <bool FULL>
+    // Decodes chunks [J0, J1) (512 bytes each, at st + 512 j) of a staged slice,
+    // only those below `nch` unless FULL, and accumulates all tokens.
+    template <bool FULL, int J0, int J1>
     __device__ __forceinline__ static void run(uint32_t st, int nch, uint32_t lane_base,
                                                const uint32_t (&xr)[MT][CH][4], int (&acc)[MT][3])
     {
 #pragma unroll
-        for (int j = 0; j < CH; ++j) {
+        for (int j = J0; j < J1; ++j) {
             if (FULL || j < nch) {
                 const uint4 p = lds_v4(st + j * 512);
                 const uint32_t pw[4] = {p.x, p.y, p.z, p.w};
@@ -235,7 +241,6 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
     constexpr int NV = 3 * MT;
     constexpr int P = pow2_at_least(NV);
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint32_t stage_tab[kLutEntries];
     __shared__ float red[kTmaWarps * MT];
     __shared__ float scale_s[MT];
 
@@ -258,8 +263,8 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
     const int slice_len = max(0, min(kStage, K - slice_off));
     const int nch = (slice_len + 511) / 512;
     const int per_cta = (G + nctas - 1) / nctas;
-    const int cta_beg = b * per_cta;
-    const int cta_end = min(G, cta_beg + per_cta);
+    const int row0 = b * per_cta;                       // first packed row of this CTA
+    const int nloc = max(0, min(G, row0 + per_cta) - row0);
 
     const uint32_t dyn = smem_addr(smem);
     const TmaLayout L = tma_layout(dyn, (uint32_t)smem_size, warp, kStage);
@@ -269,32 +274,73 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
         return;
     }
     const uint32_t ring = L.ring;
-    const uint32_t bar0 = L.bars + warp * kDepth * 8;
+    const uint32_t bar0 = L.bars + warp * kBarsPerWarp * 8;
     int8_t *xs = reinterpret_cast<int8_t *>(smem + (L.uni - dyn));
     int *sacc = reinterpret_cast<int *>(smem + (L.uni - dyn));
     const int range_rows = kUnionBytes / (4 * NV);
 
-    if (lane == 0)
-        for (int s = 0; s < kDepth; ++s)
-            mbar_init(bar0 + s * 8, 1);
-    fence_proxy_async_smem();
-    pdl_launch_dependents();
-    pdl_wait();   // inputs may come from the previous grid: read nothing before this
-
-    // ---- phase A: small inputs first (table bytes, activations), then the ring
-    // fill, so that the small loads are not queued behind the bulk copies -------
+    // ---- before the grid dependency: weights only (table, first bulk copies) --
+    // The packed bytes and the centroid table are parameters, never outputs of
+    // the preceding kernel, so they are read while that kernel drains.
     __shared__ int8_t Cv[96];
-    int8_t cval = 0;
+    if (lane == 0)
+        for (int s = 0; s < kBarsPerWarp; ++s)
+            mbar_init(bar0 + s * 8, 1);
     if (threadIdx.x < 96) {
         short t;
         asm volatile("ld.global.nc.s8 %0, [%1];" : "=h"(t) : "l"(job.C + threadIdx.x));
-        cval = (int8_t)t;
+        Cv[threadIdx.x] = (int8_t)t;
     }
+    fence_proxy_async_smem();
+    __syncthreads();
+    // A warp's ring holds kDepth row slices; slice u of this warp sits in slot
+    // u % kDepth and arrives as two halves (bytes [0, len0) and [len0, len)),
+    // each with its own barrier, so that the first half of a slot can be
+    // refilled while the second half is still being decoded.
+    constexpr int kHalfBytes = kStage / kHalves;
+    const int len0 = min(slice_len, kHalfBytes), len1 = slice_len - len0;
+    auto issue_slice = [&](int slot, int row) {
+        if (lane == 0) {
+            const uint8_t *src = job.packed + (size_t)row * K + slice_off;
+            const uint32_t dst = ring + slot * kStage;
+            const uint32_t b = bar0 + slot * kHalves * 8;
+            fence_proxy_async_smem();   // this warp's earlier reads of the slot precede the refill
+            mbar_arrive_expect_tx(b, (uint32_t)len0);
+            bulk_load(dst, src, (uint32_t)len0, b);
+            if (len1 > 0) {
+                mbar_arrive_expect_tx(b + 8, (uint32_t)len1);
+                bulk_load(dst + kHalfBytes, src + kHalfBytes, (uint32_t)len1, b + 8);
+            }
+        }
+    };
+    int issued = 0, consumed = 0;
+    const int nrow0 = min(range_rows, nloc);
+    const int nmine0 = active ? max(0, (nrow0 - rs + sets - 1) / sets) : 0;
+    for (int i = 0; i < kDepth && i < nmine0; ++i)
+        issue_slice(issued++ % kDepth, row0 + rs + i * sets);
+    // wide table: entry b's 32 lane copies are 128 contiguous bytes at lut + 256 b
+    {
+        const uint32_t lut = L.lut;
+#pragma unroll
+        for (int i = 0; i < kLutEntries * 8 / kTmaThreads; ++i) {
+            const int q = threadIdx.x + i * kTmaThreads;
+            const uint32_t e = expanded_entry(Cv, (uint32_t)(q >> 3));
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(lut + (uint32_t)(q >> 3) * 256u +
+                                                                           (uint32_t)(q & 7) * 16u),
+                         "r"(e)
+                         : "memory");
+        }
+    }
+    pdl_launch_dependents();
+    pdl_wait();   // activations may come from the previous grid: read them only now
+
+    // ---- activations -------------------------------------------------------------
     const bool fused = job.x != nullptr;
     ActRegs act;
     uint32_t xr[MT][CH][4];
     if (fused) {
         act_load(job.x, M, K, act);
+        act_amax_partial<MT>(act, M, K, red);
     } else {
 #pragma unroll
         for (int m = 0; m < MT; ++m)
@@ -309,43 +355,14 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
                 xr[m][j][2] = v.z;
                 xr[m][j][3] = v.w;
             }
+        if (threadIdx.x < MT)   // scales are read only for the bf16 output (none on the int32 path)
+            scale_s[threadIdx.x] =
+                ((int)threadIdx.x < M && job.xscale != nullptr) ? job.xscale[threadIdx.x] : 0.0f;
     }
-    int issued = 0, consumed = 0;
-    const int nrow0 = min(range_rows, cta_end - cta_beg);
-    const int nmine0 = active ? max(0, (nrow0 - rs + sets - 1) / sets) : 0;
-    for (int i = 0; i < kDepth && i < nmine0; ++i) {
-        if (lane == 0) {
-            const uint32_t bar = bar0 + (issued % kDepth) * 8;
-            mbar_arrive_expect_tx(bar, (uint32_t)slice_len);
-            bulk_load(ring + (issued % kDepth) * kStage,
-                      job.packed + (size_t)(cta_beg + rs + i * sets) * K + slice_off,
-                      (uint32_t)slice_len, bar);
-        }
-        ++issued;
-    }
-    if (threadIdx.x < 96)
-        Cv[threadIdx.x] = cval;
-    if (fused)
-        act_amax_partial<MT>(act, M, K, red);
-    __syncthreads();
-
-    // ---- phase B: table entries, scales and activation codes ------------------
-    if (threadIdx.x < kLutEntries)
-        stage_tab[threadIdx.x] = expanded_entry(Cv, threadIdx.x);
-    if (fused)
-        act_codes<MT>(act, M, K, red, xs, scale_s);
-    else if (threadIdx.x < MT)   // scales are read only for the bf16 output (none on the int32 path)
-        scale_s[threadIdx.x] =
-            ((int)threadIdx.x < M && job.xscale != nullptr) ? job.xscale[threadIdx.x] : 0.0f;
-    __syncthreads();
-
-    // ---- phase C: replicate the table, take the activation slice ---------------
-    {
-        uint32_t *wt = reinterpret_cast<uint32_t *>(smem + (L.lut - dyn));
-        for (int e = threadIdx.x; e < kLutEntries * 32; e += kTmaThreads)
-            wt[(e >> 5) * 64 + (e & 31)] = stage_tab[e >> 5];
-    }
+    __syncthreads();   // table written; warp maxima (fused) or scales published
     if (fused) {
+        act_codes<MT>(act, M, K, red, xs, scale_s);
+        __syncthreads();
         if (b == 0) {   // optional copies of the codes and scales for the caller
             if (job.xq_out)
                 for (int c = threadIdx.x; c < M * K / 16; c += kTmaThreads)
@@ -367,8 +384,9 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
                 xr[m][j][3] = v.w;
             }
     }
-    __syncthreads();   // table complete; the union buffer is free for the T > 1 sums
     if (T > 1) {
+        if (fused)
+            __syncthreads();   // every warp holds its codes: the union buffer is free
         for (int i = threadIdx.x; i < nrow0 * NV; i += kTmaThreads)
             sacc[i] = 0;
         __syncthreads();
@@ -381,50 +399,61 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
     // ---- stream ---------------------------------------------------------------
     const uint32_t lane_base = L.lut | (uint32_t)(lane << 2);
     bool timed_out = false;
-    for (int r0 = cta_beg; r0 < cta_end; r0 += range_rows) {
-        const int nrow = min(range_rows, cta_end - r0);
+    bool pending0 = false;   // a first-half refill issued for a slice not yet counted in `issued`
+    for (int r0 = 0; r0 < nloc; r0 += range_rows) {
+        const int nrow = min(range_rows, nloc - r0);
         const int nmine = (active && !timed_out) ? max(0, (nrow - rs + sets - 1) / sets) : 0;
-        if (r0 != cta_beg) {   // the first range's copies were issued above
-            for (int i = 0; i < kDepth && i < nmine; ++i) {
-                if (lane == 0) {
-                    const uint32_t bar = bar0 + (issued % kDepth) * 8;
-                    mbar_arrive_expect_tx(bar, (uint32_t)slice_len);
-                    bulk_load(ring + (issued % kDepth) * kStage,
-                              job.packed + (size_t)(r0 + rs + i * sets) * K + slice_off,
-                              (uint32_t)slice_len, bar);
-                }
-                ++issued;
-            }
-        }
+        if (r0 != 0)   // the first range's copies were issued above
+            for (int i = 0; i < kDepth && i < nmine; ++i)
+                issue_slice(issued++ % kDepth, row0 + r0 + rs + i * sets);
         for (int i = 0; i < nmine; ++i) {
             const int u = consumed;
             const int s = u % kDepth;
-            const uint32_t bar = bar0 + s * 8;
-            if (!mbar_wait_bounded(bar, (uint32_t)((u / kDepth) & 1))) {
-                timed_out = true;
-                break;
-            }
-            ++consumed;
+            const uint32_t par = (uint32_t)((u / kDepth) & 1);
+            const uint32_t b = bar0 + s * kHalves * 8;
+            const bool refill = i + kDepth < nmine;
+            const int next_row = row0 + r0 + rs + (i + kDepth) * sets;
             int acc[MT][3];
 #pragma unroll
             for (int m = 0; m < MT; ++m)
                 acc[m][0] = acc[m][1] = acc[m][2] = 0;
             const uint32_t st = ring + s * kStage + lane * 16;
-            if (slice_len == kStage)
-                SliceCompute<MT, CH>::template run<true>(st, nch, lane_base, xr, acc);
-            else
-                SliceCompute<MT, CH>::template run<false>(st, nch, lane_base, xr, acc);
-            __syncwarp();
-            if (i + kDepth < nmine) {
-                if (lane == 0) {
-                    fence_proxy_async_smem();   // this warp's reads of stage s precede the refill
-                    mbar_arrive_expect_tx(bar, (uint32_t)slice_len);
-                    bulk_load(ring + s * kStage,
-                              job.packed + (size_t)(r0 + rs + (i + kDepth) * sets) * K + slice_off,
-                              (uint32_t)slice_len, bar);
-                }
-                ++issued;
+            if (!mbar_wait_bounded(b, par)) {
+                timed_out = true;
+                break;
             }
+            if (slice_len == kStage)
+                SliceCompute<MT, CH>::template run<true, 0, CH / 2>(st, nch, lane_base, xr, acc);
+            else
+                SliceCompute<MT, CH>::template run<false, 0, CH / 2>(st, nch, lane_base, xr, acc);
+            __syncwarp();
+            if (refill && lane == 0) {   // first half of the slot is free: refill it
+                const uint8_t *src = job.packed + (size_t)next_row * K + slice_off;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(b, (uint32_t)len0);
+                bulk_load(ring + s * kStage, src, (uint32_t)len0, b);
+            }
+            if (len1 > 0) {
+                if (!mbar_wait_bounded(b + 8, par)) {
+                    timed_out = true;
+                    pending0 = refill;
+                    break;
+                }
+                if (slice_len == kStage)
+                    SliceCompute<MT, CH>::template run<true, CH / 2, CH>(st, nch, lane_base, xr, acc);
+                else
+                    SliceCompute<MT, CH>::template run<false, CH / 2, CH>(st, nch, lane_base, xr, acc);
+                __syncwarp();
+                if (refill && lane == 0) {
+                    const uint8_t *src = job.packed + (size_t)next_row * K + slice_off + kHalfBytes;
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(b + 8, (uint32_t)len1);
+                    bulk_load(ring + s * kStage + kHalfBytes, src, (uint32_t)len1, b + 8);
+                }
+            }
+            ++consumed;
+            if (refill)
+                ++issued;
             int v[P];
 #pragma unroll
             for (int e = 0; e < P; ++e)
@@ -432,7 +461,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
             const int sum = warp_reduce_transposed<P>(v, lane);
             const int idx = lane / (32 / P);
             const bool leader = (lane & (32 / P - 1)) == 0;
-            const int row = r0 + rs + i * sets;
+            const int lrow = r0 + rs + i * sets, row = row0 + lrow;
             if (leader && idx < NV) {
                 const int m = idx / 3, n = 3 * row + (idx - 3 * m);
                 if (T == 1) {
@@ -443,7 +472,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
                             job.out[(size_t)m * N + n] = epilogue_bf16(sum, xsc[m], job.cs[n]);
                     }
                 } else {
-                    atomicAdd(&sacc[(row - r0) * NV + idx], sum);
+                    atomicAdd(&sacc[(lrow - r0) * NV + idx], sum);
                 }
             }
         }
@@ -451,7 +480,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
             __syncthreads();
             for (int e = threadIdx.x; e < nrow * NV; e += kTmaThreads) {
                 const int rl = e / NV, idx = e - rl * NV;
-                const int m = idx / 3, n = 3 * (r0 + rl) + (idx - 3 * m);
+                const int m = idx / 3, n = 3 * (row0 + r0 + rl) + (idx - 3 * m);
                 if (m < M && n < N) {
                     if (job.acc)
                         job.acc[(size_t)m * N + n] = sacc[e];
@@ -464,8 +493,16 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
         }
     }
     if (timed_out) {
-        for (int u = consumed + 1; u < issued; ++u)   // drain this warp's copies in flight
-            mbar_wait_bounded(bar0 + (u % kDepth) * 8, (uint32_t)((u / kDepth) & 1));
+        // never leave with copies in flight: wait (bounded) for both halves of
+        // every issued slice not yet consumed, and for an early first-half refill
+        for (int v = consumed; v < issued; ++v) {
+            const uint32_t b = bar0 + (v % kDepth) * kHalves * 8;
+            mbar_wait_bounded(b, (uint32_t)((v / kDepth) & 1));
+            if (len1 > 0)
+                mbar_wait_bounded(b + 8, (uint32_t)((v / kDepth) & 1));
+        }
+        if (pending0)
+            mbar_wait_bounded(bar0 + (issued % kDepth) * kHalves * 8, (uint32_t)((issued / kDepth) & 1));
         if (lane == 0)
             record_timeout(g.status);
     }
@@ -501,18 +538,29 @@ bool gemv_tma_supported(int M, int K)
     return gemv_group_job_ok(M, K, false);
 }
 
-// Splits `ctas` CTAs over the jobs in proportion to packed bytes (largest
+// Splits `ctas` CTAs over the jobs in proportion to their cost (largest
 // remainder), at least one CTA per job and never more CTAs than rows x slices.
+// Cost = packed bytes, plus for jobs that quantise their activations in-kernel
+// the longer prologue of a long row, in bytes a CTA would have streamed in that
+// time (measured on GB300: about 1.2 us more at K = 14336 than at K = 4096, at
+// about 32 KB per microsecond per SM).
 static void split_ctas(const GroupArgs &g, int ctas, int *cta_begin)
 {
     const int kStage = stage_bytes(g.M);
     double total = 0.0;
     double bytes[kMaxJobs];
     int cap[kMaxJobs];
+    double raw = 0.0;
+    for (int j = 0; j < g.njobs; ++j)
+        raw += (double)((g.jobs[j].N + 2) / 3) * g.jobs[j].K;
     for (int j = 0; j < g.njobs; ++j) {
         const long G = (g.jobs[j].N + 2) / 3;
         const long T = (g.jobs[j].K + kStage - 1) / kStage;
         bytes[j] = (double)G * g.jobs[j].K;
+        if (g.jobs[j].x && g.jobs[j].K > 4096 && raw > 0) {
+            const double est_ctas = ctas * bytes[j] / raw;
+            bytes[j] += est_ctas * 1.2 * (g.jobs[j].K - 4096) / 10240.0 * 32768.0;
+        }
         cap[j] = (int)(G * T < ctas ? G * T : ctas);
         total += bytes[j];
     }
@@ -571,6 +619,14 @@ cudaError_t launch_gemv_group(GroupArgs &g, cudaStream_t stream)
         return cudaErrorInvalidValue;
     const int sms = device_sm_count();
     const int kStage = stage_bytes(g.M);
+    // jobs with the longest rows first: their CTAs take the SMs that free up
+    // first while the preceding grid drains, since their prologue is longest
+    for (int a = 1; a < g.njobs; ++a)
+        for (int c = a; c > 0 && g.jobs[c].K > g.jobs[c - 1].K; --c) {
+            const GroupJob tmp = g.jobs[c];
+            g.jobs[c] = g.jobs[c - 1];
+            g.jobs[c - 1] = tmp;
+        }
     long items = 0;
     for (int j = 0; j < g.njobs; ++j)
         items += (long)((g.jobs[j].N + 2) / 3) * ((g.jobs[j].K + kStage - 1) / kStage);
