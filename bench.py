@@ -374,6 +374,8 @@ def gpu_arm(args):
     e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 4000))
     prefill = prefill_measure(torch, s3d8, dev) if not args.skip_prefill else None
     unpack = unpack_measure(torch, s3d8, dev)
+    sweep = decode_sweep_measure(torch, s3d8, dev)
+    stack = stack_measure(torch, s3d8, dev)
 
     if rank != 0:
         return
@@ -395,6 +397,7 @@ def gpu_arm(args):
         "gpu_launches": args.steps * n_launches("group1"),
         "device_status": status,
         "roofline": roofline, "variants": variants, "e2e": e2e, "prefill": prefill,
+        "decode_sweep": sweep, "text_stack": stack,
         "unpack": unpack, "clocks": clocks, "cpu_baseline": cpu,
     }
     print(json.dumps(line))
@@ -403,27 +406,38 @@ def gpu_arm(args):
 def e2e_measure(torch, s3d8, copies, dev, steps):
     """Same metric through the Python binding, with the four activations copied
     in from pinned host memory and the seven outputs copied back every step
-    (the step itself is the captured grouped launch)."""
+    (the step itself is the captured grouped launch).  Inputs and outputs each
+    live in one contiguous buffer, so a step is one host->device copy, the
+    launch, and one device->host copy."""
     step = Step(1, dev)
-    host_x = {k: torch.from_numpy(si.acts(1, K, seed=5, index=i).view(np.int16)).view(
-        torch.bfloat16).pin_memory() for i, (k, K) in enumerate(ACT_K.items())}
-    host_out = {n: torch.empty((1, N), dtype=torch.bfloat16).pin_memory()
-                for n, _, N in si.LLAMA_11B_LAYER}
+    xk = list(ACT_K.items())
+    x_all = torch.empty((sum(K for _, K in xk),), dtype=torch.bfloat16, device=dev)
+    host_x = torch.empty_like(x_all, device="cpu").pin_memory()
+    off = 0
+    for i, (k, K) in enumerate(xk):
+        step.x[k] = x_all[off:off + K].view(1, K)
+        host_x[off:off + K] = torch.from_numpy(si.acts(1, K, seed=5, index=i).view(np.int16)).view(
+            torch.bfloat16)[0]
+        off += K
+    o_all = torch.empty((sum(N for _, _, N in si.LLAMA_11B_LAYER),), dtype=torch.bfloat16, device=dev)
+    host_out = torch.empty_like(o_all, device="cpu").pin_memory()
+    off = 0
+    for n, _, N in si.LLAMA_11B_LAYER:
+        step.out[n] = o_all[off:off + N].view(1, N)
+        off += N
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
         step.run(s3d8, copies[0], "group1")
     stream.synchronize()
     graphs = [capture(torch, stream, lambda r=r: step.run(s3d8, copies[r], "group1"))
               for r in range(COPIES)]
-    h2d = sum(t.numel() * 2 for t in host_x.values())
-    d2h = sum(t.numel() * 2 for t in host_out.values())
+    h2d = host_x.numel() * 2
+    d2h = host_out.numel() * 2
 
     def one(i):
-        for k in ACT_K:
-            step.x[k].copy_(host_x[k], non_blocking=True)
+        x_all.copy_(host_x, non_blocking=True)
         graphs[i % COPIES].replay()
-        for n in host_out:
-            host_out[n].copy_(step.out[n], non_blocking=True)
+        host_out.copy_(o_all, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for i in range(20):
@@ -440,8 +454,9 @@ def e2e_measure(torch, s3d8, copies, dev, steps):
     ms = t0.elapsed_time(t1) / steps
     return {"value": round(LAYER_WEIGHT_BYTES / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
-            "steps": steps, "path": "Python binding (grouped launch) captured in a CUDA graph, "
-                                    "pinned host copies in and out every step"}
+            "steps": steps, "path": "Python binding (grouped launch) captured in a CUDA graph; per step one "
+                                    "pinned host->device copy of the four activations and one "
+                                    "device->host copy of the seven outputs"}
 
 
 def prefill_measure(torch, s3d8, dev, M=2048, reps=3):
@@ -474,6 +489,96 @@ def prefill_measure(torch, s3d8, dev, M=2048, reps=3):
     res["tops"] = round(tot_ops / (tot_ms * 1e-3) / 1e12, 2)
     res["unit"] = "TOPS (int8 multiply-adds x2)"
     return res
+
+
+def device_matrix(torch, dev, gen, K, N):
+    """Random S3D8 fields of the recipe's distribution, drawn on the device with a
+    seeded generator (uniform bytes, table entries 1..127, |N(0, 0.02)|/127
+    channel scales): for timing copies whose values nothing checks."""
+    G = si.groups(N)
+    return dict(K=K, N=N,
+                packed=torch.randint(0, 256, (G, K), dtype=torch.uint8, device=dev, generator=gen),
+                C=torch.randint(1, 128, (32, 3), dtype=torch.int8, device=dev, generator=gen),
+                cs=(torch.randn((N,), device=dev, generator=gen).abs() * (0.02 / 127)).to(
+                    torch.bfloat16))
+
+
+def decode_sweep_measure(torch, s3d8, dev, copies=8, reps=40):
+    """Batched decode (M = 8..64) on the gate/up and down shapes through
+    s3d8_linear (automatic algorithm choice), rotating `copies` weight copies."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    res = {}
+    for name, K, N in si.SWEEP_SHAPES:
+        mats = [device_matrix(torch, dev, gen, K, N) for _ in range(copies)]
+        for M in si.DECODE_SWEEP_M:
+            x = to_dev_bf16(si.acts(M, K, seed=7, outliers=True), dev)
+            xq, xs = s3d8.quantize_act(x)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty((max(1, s3d8.workspace_size(M, N, K)),), dtype=torch.uint8, device=dev)
+            for m in mats:
+                s3d8.linear(m["packed"], m["C"], m["cs"], xq, xs, N, out=out, workspace=ws)
+            torch.cuda.synchronize()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for i in range(reps):
+                m = mats[i % copies]
+                s3d8.linear(m["packed"], m["C"], m["cs"], xq, xs, N, out=out, workspace=ws)
+            t1.record()
+            t1.synchronize()
+            ms = t0.elapsed_time(t1) / reps
+            res[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2),
+                                   "weight_gbs": round(weight_bytes(K, N) / (ms * 1e-3) / 1e9, 1),
+                                   "tops": round(2 * M * N * K / (ms * 1e-3) / 1e12, 2)}
+        del mats
+    return res
+
+
+def stack_measure(torch, s3d8, dev, reps=5):
+    """The whole 40-layer text stack plus the LM head at M = 1 (3.08 GB of
+    packed weights): one grouped launch per layer with fused quantisation and
+    one for the head, captured as one graph of 41 launches."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    layers = [[dict(name=n, **device_matrix(torch, dev, gen, K, N)) for n, K, N in si.LLAMA_11B_LAYER]
+              for _ in range(si.LLAMA_11B_LAYERS)]
+    _, hK, hN = si.LLAMA_11B_HEAD
+    head = device_matrix(torch, dev, gen, hK, hN)
+    x = {k: to_dev_bf16(si.acts(1, K, seed=11, index=i), dev) for i, (k, K) in enumerate(ACT_K.items())}
+    outs = {n: torch.empty((1, N), dtype=torch.bfloat16, device=dev) for n, _, N in si.LLAMA_11B_LAYER}
+    hout = torch.empty((1, hN), dtype=torch.bfloat16, device=dev)
+    total = sum(weight_bytes(m["K"], m["N"]) for L in layers for m in L) + weight_bytes(hK, hN)
+
+    def run():
+        for L in layers:
+            s3d8.linear_batch([dict(packed=m["packed"], centroids=m["C"], chan_scale=m["cs"],
+                                    N=m["N"], x=x[si.LLAMA_11B_INPUT_OF[m["name"]]],
+                                    out=outs[m["name"]]) for m in L], 1)
+        s3d8.linear_batch([dict(packed=head["packed"], centroids=head["C"], chan_scale=head["cs"],
+                                N=hN, x=x["attn"], out=hout)], 1)
+
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        run()
+    stream.synchronize()
+    g = capture(torch, stream, run)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        t1.record(stream)
+    t1.synchronize()
+    ms = t0.elapsed_time(t1) / reps
+    del layers, head
+    return {"workload": "40 decoder layers x 7 S3D8 linears + LM head 4096->128256, M=1",
+            "weight_bytes": total, "launches": si.LLAMA_11B_LAYERS + 1, "ms": round(ms, 4),
+            "value": round(total / (ms * 1e-3) / 1e9, 1), "unit": UNIT}
 
 
 def unpack_measure(torch, s3d8, dev, reps=20):

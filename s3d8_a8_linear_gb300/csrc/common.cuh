@@ -150,10 +150,22 @@ __device__ __forceinline__ int quant_code(float x, float s, float r)
 }
 
 // Eight bf16 values (one 16-byte chunk) -> eight codes (8 bytes).  The common
-// path is branch-free over the eight values (one multiply, floor, compare and
-// convert each, all independent); the rare near-tie values are redone exactly
-// afterwards.  Out of line so that unrolled prologue loops share one copy.
-static __device__ __noinline__ uint2 quant_chunk8(uint4 v, float s, float r)
+// path is branch-free over the eight values and uses only full-rate FP32 adds,
+// multiplies and min/max: t = RN(x * r) is clamped to +-127 and rounded to the
+// nearest integer (ties to even) by adding 1.5 * 2^23, whose float encoding
+// then holds the two's-complement code in its low byte.  Clamping before
+// rounding gives the same code as rounding before clamping, because +-127 are
+// integers.  t - rint(t), exact in fp32, flags the rare near-ties, which are
+// redone with the exact quotient afterwards.  Out of line so that unrolled
+// prologue loops share one copy.
+constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
+
+#ifdef S3D8_QUANT_NOINLINE
+static __device__ __noinline__
+#else
+static __device__ __forceinline__
+#endif
+uint2 quant_chunk8(uint4 v, float s, float r)
 {
     if (s == 0.0f)
         return make_uint2(0u, 0u);
@@ -161,30 +173,26 @@ static __device__ __noinline__ uint2 quant_chunk8(uint4 v, float s, float r)
     float x[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
-        x[2 * j] = __low2float(h);
-        x[2 * j + 1] = __high2float(h);
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
     }
-    int q[8];
+    uint32_t b[8];
     bool redo = s < kTinyScale;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        const float t = __fmul_rn(x[e], r);
-        const float f = t - floorf(t);
-        redo |= fabsf(f - 0.5f) < kTieMargin;
-        q[e] = max(-127, min(127, __float2int_rn(t)));
+        const float t = fminf(fmaxf(__fmul_rn(x[e], r), -127.0f), 127.0f);
+        const float y = __fadd_rn(t, kRoundMagic);
+        const float d = __fsub_rn(t, __fsub_rn(y, kRoundMagic));   // t - rint(t)
+        redo |= fabsf(fabsf(d) - 0.5f) < kTieMargin;
+        b[e] = __float_as_uint(y);
     }
     if (redo) {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            q[e] = quant_code(x[e], s, r);
+            b[e] = (uint32_t)quant_code(x[e], s, r);
     }
-    uint32_t lo = 0u, hi = 0u;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        lo |= ((uint32_t)(uint8_t)q[e]) << (8 * e);
-        hi |= ((uint32_t)(uint8_t)q[e + 4]) << (8 * e);
-    }
+    const uint32_t lo = prmt(prmt(b[0], b[1], 0x0040), prmt(b[2], b[3], 0x0040), 0x5410);
+    const uint32_t hi = prmt(prmt(b[4], b[5], 0x0040), prmt(b[6], b[7], 0x0040), 0x5410);
     return make_uint2(lo, hi);
 }
 

@@ -40,6 +40,13 @@ constexpr int kTmaThreads = kTmaWarps * 32;
 constexpr int kDepth = 2;    // row slices per warp ring
 constexpr int kHalves = 2;   // each slice arrives as two bulk copies with their own barriers
 constexpr int kBarsPerWarp = kDepth * kHalves;
+#ifndef S3D8_PREWAIT_SLICES
+#define S3D8_PREWAIT_SLICES 1
+#endif
+// Row slices a warp requests before the grid dependency wait; the rest of the
+// ring is filled after the activation loads have been issued, so that their
+// replies do not queue behind a whole ring of weight bytes.
+constexpr int kPrewaitSlices = S3D8_PREWAIT_SLICES;
 // 512-byte chunks per slice: 8 (4 KiB) for up to 2 tokens, 4 for 3..4 tokens so
 // that the activations of the slice still fit in registers.
 __host__ __device__ constexpr int chunks_for(int MT)
@@ -113,6 +120,18 @@ struct ActRegs {
     uint4 v[kActChunksPerThread];
 };
 
+// Token (row of x) that 16-byte chunk c belongs to, for rows of per_row chunks:
+// compares instead of an integer division.
+template <int MT>
+__device__ __forceinline__ int chunk_token(int c, int per_row)
+{
+    int m = 0;
+#pragma unroll
+    for (int t = 1; t < MT; ++t)
+        m += c >= t * per_row ? 1 : 0;
+    return m;
+}
+
 // Volatile loads: all chunks leave at once, here, instead of being sunk one by
 // one to their first use (which would serialise their latencies).
 __device__ __forceinline__ void act_load(const __nv_bfloat16 *__restrict__ x, int M, int K, ActRegs &r)
@@ -142,7 +161,7 @@ __device__ __forceinline__ void act_amax_partial(const ActRegs &r, int M, int K,
     for (int i = 0; i < kActChunksPerThread; ++i) {
         const int c = threadIdx.x + i * kTmaThreads;
         if (c < chunks) {
-            const int m = c / per_row;
+            const int m = chunk_token<MT>(c, per_row);
             const uint32_t w[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
             float a = 0.0f;
 #pragma unroll
@@ -176,12 +195,14 @@ __device__ __forceinline__ void act_codes(const ActRegs &r, int M, int K, const 
     const int chunks = M * K / 8;
     const int per_row = K / 8;
     float sc[MT], rcp[MT];
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        float a = 0.0f;
+        // fold the kTmaWarps warp maxima across the lanes: one load, five shuffles
+        float a = lane < kTmaWarps ? red[lane * MT + m] : 0.0f;
 #pragma unroll
-        for (int w = 0; w < kTmaWarps; ++w)
-            a = fmaxf(a, red[w * MT + m]);
+        for (int o = 16; o > 0; o >>= 1)
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
         sc[m] = __fdiv_rn(a, 127.0f);
         rcp[m] = sc[m] > 0.0f ? __frcp_rn(sc[m]) : 0.0f;
         if (threadIdx.x == 0)
@@ -191,7 +212,7 @@ __device__ __forceinline__ void act_codes(const ActRegs &r, int M, int K, const 
     for (int i = 0; i < kActChunksPerThread; ++i) {
         const int c = threadIdx.x + i * kTmaThreads;
         if (c < chunks) {
-            const int m = c / per_row;
+            const int m = chunk_token<MT>(c, per_row);
             float s = 0.0f, inv = 0.0f;
 #pragma unroll
             for (int mm = 0; mm < MT; ++mm)
@@ -316,7 +337,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
     int issued = 0, consumed = 0;
     const int nrow0 = min(range_rows, nloc);
     const int nmine0 = active ? max(0, (nrow0 - rs + sets - 1) / sets) : 0;
-    for (int i = 0; i < kDepth && i < nmine0; ++i)
+    for (int i = 0; i < kPrewaitSlices && i < nmine0; ++i)
         issue_slice(issued++ % kDepth, row0 + rs + i * sets);
     // wide table: entry b's 32 lane copies are 128 contiguous bytes at lut + 256 b
     {
@@ -340,6 +361,8 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
     uint32_t xr[MT][CH][4];
     if (fused) {
         act_load(job.x, M, K, act);
+        for (int i = kPrewaitSlices; i < kDepth && i < nmine0; ++i)   // rest of the ring, behind x
+            issue_slice(issued++ % kDepth, row0 + rs + i * sets);
         act_amax_partial<MT>(act, M, K, red);
     } else {
 #pragma unroll
@@ -355,6 +378,8 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
                 xr[m][j][2] = v.z;
                 xr[m][j][3] = v.w;
             }
+        for (int i = kPrewaitSlices; i < kDepth && i < nmine0; ++i)   // rest of the ring, behind x
+            issue_slice(issued++ % kDepth, row0 + rs + i * sets);
         if (threadIdx.x < MT)   // scales are read only for the bf16 output (none on the int32 path)
             scale_s[threadIdx.x] =
                 ((int)threadIdx.x < M && job.xscale != nullptr) ? job.xscale[threadIdx.x] : 0.0f;
