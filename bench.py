@@ -327,7 +327,7 @@ def gpu_arm(args):
 
     # ---- other launch structures (same weights, same rotation) --------------
     variants = {}
-    for mode in ("group4", "separate"):
+    for mode in (() if args.layer_only else ("group4", "separate")):
         n = max(COPIES, (args.steps // 4) // COPIES * COPIES)
         replay_steps(mode, COPIES * 4)
         ms = replay_steps(mode, n)
@@ -371,11 +371,13 @@ def gpu_arm(args):
                     "bytes_per_launch": launch_bytes[0], "avg_launch_us": round(avg_ms * 1e3, 3),
                     "launches_timed": len(launch_ms), "peak_kind": peak_kind}
 
-    e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 4000))
-    prefill = prefill_measure(torch, s3d8, dev) if not args.skip_prefill else None
-    unpack = unpack_measure(torch, s3d8, dev)
-    sweep = decode_sweep_measure(torch, s3d8, dev)
-    stack = stack_measure(torch, s3d8, dev)
+    e2e = prefill = unpack = sweep = stack = None
+    if not args.layer_only:
+        e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 4000))
+        prefill = prefill_measure(torch, s3d8, dev) if not args.skip_prefill else None
+        unpack = unpack_measure(torch, s3d8, dev)
+        sweep = decode_sweep_measure(torch, s3d8, dev)
+        stack = stack_measure(torch, s3d8, dev)
 
     if rank != 0:
         return
@@ -674,11 +676,22 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--layer-only", action="store_true",
+                    help="time the headline step only (no variants, e2e, sweeps); for profiling")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the M = 2048 tensor-core measurement and print it; for profiling")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = 10 if args.steps is None else args.steps
         args.warmup = 3 if args.warmup is None else args.warmup
         reference_arm(args)
+        return
+    if args.prefill_only:
+        import torch
+
+        import s3d8_a8_linear_gb300 as s3d8
+        s3d8.load(build_if_missing=True)
+        print(json.dumps(prefill_measure(torch, s3d8, torch.device("cuda:0"))))
         return
     args.steps = 40000 if args.steps is None else args.steps
     args.warmup = 400 if args.warmup is None else args.warmup

@@ -96,7 +96,8 @@ int s3d8_decode(const uint8_t *packed, const int8_t *centroids, int64_t N, int64
                 void *stream);
 
 /* Bytes of device workspace s3d8_linear_ex needs for this shape and algorithm
- * (0 when none).  Pure host function. */
+ * (0 when none).  Host function; the tensor-core algorithm's size depends on
+ * the current device's SM count (how far a small M splits K). */
 size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo);
 
 /*
@@ -202,8 +203,11 @@ int s3d8_selftest_wait_timeout(int64_t polls, void *stream);
  * scratch array of S3D8_NOALLOC_SCRATCH_BYTES compiled into the library, which
  * every GPU that loads the library holds until the process exits.  The paper
  * has no counterpart; this is a deployment convenience.
- *   - Shapes with 2 * M * K + 256 > S3D8_NOALLOC_SCRATCH_BYTES are rejected with
- *     S3D8_ERR_WORKSPACE before any CUDA call (e.g. M <= 2047 at K = 4096).
+ *   - Shapes whose tensor-core workspace (s3d8_linear_workspace_size with
+ *     S3D8_ALGO_TC) exceeds S3D8_NOALLOC_SCRATCH_BYTES are rejected with
+ *     S3D8_ERR_WORKSPACE before any launch: the bf16 activation copy needs
+ *     2 * M * K + 256 bytes (so M <= 2047 at K = 4096), plus the int32 partial
+ *     sums when a small M splits K.
  *   - The first call on a device looks up the scratch array's device address
  *     (once per device, with that device current); make that first call before
  *     any stream capture.

@@ -193,7 +193,8 @@ def linear_tc_noalloc(packed: torch.Tensor, centroids: torch.Tensor, chan_scale:
                       out: torch.Tensor) -> torch.Tensor:
     """The tensor-core linear into the caller's `out` without any device
     allocation, neither here nor in the library: its scratch is a fixed array of
-    NOALLOC_SCRATCH_BYTES inside the library (2 M K + 256 bytes must fit).  For
+    NOALLOC_SCRATCH_BYTES inside the library (the tensor-core workspace of the
+    shape must fit).  For
     callers that cannot allocate device memory.  Calls that overlap on the GPU
     share that array and race; order them on one stream."""
     G, K = packed.shape

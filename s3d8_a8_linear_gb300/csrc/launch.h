@@ -60,7 +60,7 @@ cudaError_t launch_wait_timeout(int polls, int *status, cudaStream_t stream);
 bool gemv_group_job_ok(int M, int K, bool fused);
 cudaError_t launch_gemv_group(GroupArgs &g, cudaStream_t stream);
 cudaError_t launch_gemv_tma(const LinearArgs &a, cudaStream_t stream);
-size_t prefill_workspace_bytes(int M, int K);
+size_t prefill_workspace_bytes(int M, int N, int K);
 cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream);
 
 }  // namespace s3d8

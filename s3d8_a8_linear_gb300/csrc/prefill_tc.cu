@@ -35,22 +35,30 @@ constexpr int BM = 128;                  // tokens per tile
 constexpr int GROUPS = 80;               // packed rows per tile
 constexpr int BN = 3 * GROUPS;           // 240 channels per tile
 constexpr int BK = 64;                   // K per block (128 bytes of bf16)
-constexpr int STAGES = 3;
+constexpr int LSTAGES = 6;               // ring of loaded tiles (A + packed bytes)
+constexpr int BSTAGES = 2;               // ring of decoded weight tiles
 constexpr int CHUNK_BLOCKS = 16;         // 16 x 64 = 1024 columns per exact chunk
 constexpr int A_BYTES = BM * BK * 2;     // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;     // 30 KiB
 constexpr int P_BYTES = GROUPS * BK;     // 5 KiB packed bytes
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + P_BYTES;
 constexpr int LUT_COPIES = 16;
 constexpr int LUT_BYTES = kLutEntries * LUT_COPIES * 8;   // 32 KiB
-constexpr int NBARS = 3 * STAGES + 4;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + LUT_BYTES + NBARS * 8 + 16;
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + LSTAGES * A_BYTES;
+constexpr int OFF_P = OFF_B + BSTAGES * B_BYTES;
+constexpr int OFF_LUT = OFF_P + LSTAGES * P_BYTES;
+constexpr int OFF_BARS = OFF_LUT + LUT_BYTES;
+constexpr int NBARS = 2 * LSTAGES + 2 * BSTAGES + 4;
+constexpr int SMEM_BYTES = 1024 + OFF_BARS + NBARS * 8 + 16;
 constexpr int THREADS = 16 * 32;
 constexpr int PRODUCERS = 192;   // warps 2-7
 constexpr int DRAIN_WARP0 = 8;
 constexpr int HALF = BN / 2;             // 120 columns per epilogue thread
 
-static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzled tiles must stay 1024-aligned");
+static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0,
+              "swizzled tiles must stay 1024-aligned");
+static_assert(OFF_P % 128 == 0 && P_BYTES % 128 == 0, "packed tiles 128-byte aligned");
+static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory budget");
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t a)
 {
@@ -118,7 +126,11 @@ struct Params {
     __nv_bfloat16 *out;
     int32_t *acc;
     int *status;
-    int vec_out;   // out / acc rows may be written with 16-byte stores
+    int vec_out;        // out / acc rows may be written with 16-byte stores
+    int nsplit;         // K is split into nsplit ranges of kb_per_split 64-column blocks
+    int kb_per_split;
+    int32_t *part;      // with nsplit > 1: int32 partial sums [nsplit][M][N]
+    int vec_part;       // partial rows may be written with 16-byte stores
 };
 
 __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_constant__ CUtensorMap tm_act,
@@ -129,27 +141,38 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *smem = smem_raw + (base - raw);
-    const uint32_t lut = base + STAGES * STAGE_BYTES;
-    const uint32_t bars = lut + LUT_BYTES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + STAGES * STAGE_BYTES + LUT_BYTES + NBARS * 8);
-    // barriers: a_full[S] (TMA bytes), b_full[S] (decoded tile), empty[S] (MMA done),
-    //           acc_full[2] (chunk in TMEM), acc_empty[2] (chunk drained)
-    const uint32_t a_full = bars, b_full = bars + 8 * STAGES, empty = bars + 16 * STAGES;
-    const uint32_t acc_full = bars + 24 * STAGES, acc_empty = acc_full + 16;
+    const uint32_t lut = base + OFF_LUT;
+    const uint32_t bars = base + OFF_BARS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BARS + NBARS * 8);
+    // barriers: l_full[L] (TMA bytes of A and packed), l_empty[L] (MMA done with
+    //           the slot), b_full[B] (decoded tile written), b_empty[B] (MMA done
+    //           with the decoded tile), acc_full[2] (chunk in TMEM), acc_empty[2]
+    const uint32_t l_full = bars, l_empty = l_full + 8 * LSTAGES;
+    const uint32_t b_full = l_empty + 8 * LSTAGES, b_empty = b_full + 8 * BSTAGES;
+    const uint32_t acc_full = b_empty + 8 * BSTAGES, acc_empty = acc_full + 16;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mtiles = (p.M + BM - 1) / BM;
-    const int mt = (int)(blockIdx.x % (unsigned)mtiles), nt = (int)(blockIdx.x / (unsigned)mtiles);
+    const int ntiles = ((p.N + 2) / 3 + GROUPS - 1) / GROUPS;
+    const int mt = (int)(blockIdx.x % (unsigned)mtiles);
+    const int rest = (int)(blockIdx.x / (unsigned)mtiles);
+    const int nt = rest % ntiles, split = rest / ntiles;
     const int m0 = mt * BM;
     const int g0 = nt * GROUPS;
-    const int nk = (p.K + BK - 1) / BK;
+    // this CTA's K range: 64-column blocks [kbase, kbase + nk)
+    const int nk_all = (p.K + BK - 1) / BK;
+    const int kbase = split * p.kb_per_split;
+    const int nk = min(p.kb_per_split, nk_all - kbase);
     const int nchunks = (nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(a_full + 8 * s, 1);
+        for (int s = 0; s < LSTAGES; ++s) {
+            mbar_init(l_full + 8 * s, 1);
+            mbar_init(l_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < BSTAGES; ++s) {
             mbar_init(b_full + 8 * s, PRODUCERS / 32);
-            mbar_init(empty + 8 * s, 1);
+            mbar_init(b_empty + 8 * s, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full + 8 * i, 1);
@@ -170,7 +193,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         for (int i = threadIdx.x; i < 96; i += THREADS)
             Cs[i] = p.C[i];
         __syncthreads();
-        uint2 *t = reinterpret_cast<uint2 *>(smem + STAGES * STAGE_BYTES);
+        uint2 *t = reinterpret_cast<uint2 *>(smem + OFF_LUT);
         for (int i = threadIdx.x; i < kLutEntries * LUT_COPIES; i += THREADS) {
             const uint32_t e = expanded_entry(Cs, (uint32_t)(i / LUT_COPIES));
             const int w0 = (int8_t)(e & 0xFF), w1 = (int8_t)((e >> 8) & 0xFF), w2 = (int8_t)((e >> 16) & 0xFF);
@@ -190,20 +213,19 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         if (lane == 0) {
             int issued = 0;
             for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % STAGES;
-                if (kb >= STAGES && !mbar_wait_bounded(empty + 8 * s, ((kb / STAGES) - 1) & 1)) {
+                const int s = kb % LSTAGES;
+                if (kb >= LSTAGES && !mbar_wait_bounded(l_empty + 8 * s, ((kb / LSTAGES) - 1) & 1)) {
                     timed_out = true;
                     break;
                 }
                 issued = kb + 1;
-                const uint32_t st = base + s * STAGE_BYTES;
-                mbar_arrive_expect_tx(a_full + 8 * s, A_BYTES + P_BYTES);
-                tma_2d(st, &tm_act, kb * BK, m0, a_full + 8 * s);
-                tma_2d(st + A_BYTES + B_BYTES, &tm_pk, kb * BK, g0, a_full + 8 * s);
+                mbar_arrive_expect_tx(l_full + 8 * s, A_BYTES + P_BYTES);
+                tma_2d(base + OFF_A + s * A_BYTES, &tm_act, (kbase + kb) * BK, m0, l_full + 8 * s);
+                tma_2d(base + OFF_P + s * P_BYTES, &tm_pk, (kbase + kb) * BK, g0, l_full + 8 * s);
             }
             // never leave with copies in flight: wait (bounded) for the last ones
-            for (int kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
-                if (!mbar_wait_bounded(a_full + 8 * (kb % STAGES), (kb / STAGES) & 1))
+            for (int kb = issued - LSTAGES < 0 ? 0 : issued - LSTAGES; kb < issued; ++kb)
+                if (!mbar_wait_bounded(l_full + 8 * (kb % LSTAGES), (kb / LSTAGES) & 1))
                     timed_out = true;
         }
     } else if (warp == 1) {
@@ -213,31 +235,33 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
             const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                                    ((uint32_t)(BM >> 4) << 24);
             for (int kb = 0; kb < nk && !timed_out; ++kb) {
-                const int s = kb % STAGES;
+                const int s = kb % LSTAGES, bs = kb % BSTAGES;
                 const int c = kb / CHUNK_BLOCKS, kin = kb % CHUNK_BLOCKS;
                 const uint32_t d = tmem + (uint32_t)((c & 1) * 256);
                 if (kin == 0 && c >= 2 && !mbar_wait_bounded(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
                     timed_out = true;
                     break;
                 }
-                if (!mbar_wait_bounded(a_full + 8 * s, (kb / STAGES) & 1) ||
-                    !mbar_wait_bounded(b_full + 8 * s, (kb / STAGES) & 1)) {
+                if (!mbar_wait_bounded(l_full + 8 * s, (kb / LSTAGES) & 1) ||
+                    !mbar_wait_bounded(b_full + 8 * bs, (kb / BSTAGES) & 1)) {
                     timed_out = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a = base + s * STAGE_BYTES, b = a + A_BYTES;
+                const uint32_t a = base + OFF_A + s * A_BYTES, b = base + OFF_B + bs * B_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     mma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
                              (kin | kk) ? 1u : 0u);
-                mma_commit(empty + 8 * s);
+                mma_commit(l_empty + 8 * s);
+                mma_commit(b_empty + 8 * bs);
                 if (kin == CHUNK_BLOCKS - 1 || kb == nk - 1)
                     mma_commit(acc_full + 8 * (c & 1));
                 issued = kb + 1;
             }
             // the tensor core must be done with TMEM and shared memory before exit
-            if (issued > 0 && !mbar_wait_bounded(empty + 8 * ((issued - 1) % STAGES), ((issued - 1) / STAGES) & 1))
+            if (issued > 0 &&
+                !mbar_wait_bounded(l_empty + 8 * ((issued - 1) % LSTAGES), ((issued - 1) / LSTAGES) & 1))
                 timed_out = true;
         }
     } else {
@@ -245,13 +269,13 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         const int t = threadIdx.x - 64;
         const uint32_t lut_lane = lut + (uint32_t)((lane & (LUT_COPIES - 1)) * 8);
         for (int kb = 0; kb < nk && !timed_out; ++kb) {
-            const int s = kb % STAGES;
-            if (!mbar_wait_bounded(a_full + 8 * s, (kb / STAGES) & 1)) {
+            const int s = kb % LSTAGES, bs = kb % BSTAGES;
+            if (!mbar_wait_bounded(l_full + 8 * s, (kb / LSTAGES) & 1) ||
+                (kb >= BSTAGES && !mbar_wait_bounded(b_empty + 8 * bs, ((kb / BSTAGES) - 1) & 1))) {
                 timed_out = true;
                 break;
             }
-            const uint32_t st = base + s * STAGE_BYTES;
-            const uint32_t btile = st + A_BYTES, ptile = st + A_BYTES + B_BYTES;
+            const uint32_t btile = base + OFF_B + bs * B_BYTES, ptile = base + OFF_P + s * P_BYTES;
             for (int u = t; u < GROUPS * 8; u += PRODUCERS) {
                 const int gl = u >> 3, j = u & 7;   // group, 16-byte chunk (8 k)
                 uint32_t pk0, pk1;
@@ -283,7 +307,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
             fence_proxy_async_smem();   // generic writes -> visible to the tensor core
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(b_full + 8 * s);
+                mbar_arrive(b_full + 8 * bs);
         }
     }
     } else {
@@ -324,9 +348,11 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         if (!timed_out && row < p.M) {
             const int nbase = nt * BN + h * HALF;
             const bool full = nbase + HALF <= p.N;
-            if (p.acc) {
-                int32_t *dst = p.acc + (size_t)row * p.N + nbase;
-                if (full && p.vec_out) {
+            int32_t *accp = p.part ? p.part + (size_t)split * p.M * p.N : p.acc;
+            const bool vec_acc = p.part ? p.vec_part : p.vec_out;
+            if (accp) {
+                int32_t *dst = accp + (size_t)row * p.N + nbase;
+                if (full && vec_acc) {
 #pragma unroll
                     for (int i = 0; i < HALF; i += 4)
                         *reinterpret_cast<int4 *>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
@@ -390,11 +416,66 @@ __global__ void codes_to_bf16_kernel(const int8_t *__restrict__ xq, __nv_bfloat1
     }
 }
 
+// Split-K finish: out[m, n] (or acc) from the sum of the nsplit int32 partials.
+// Integer sums, so the order of the splits does not matter.
+__global__ void finalize_kernel(const int32_t *__restrict__ part, int nsplit, int M, int N,
+                                const float *__restrict__ xscale, const __nv_bfloat16 *__restrict__ cs,
+                                __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc)
+{
+    const size_t plane = (size_t)M * N;
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < plane; e += (size_t)gridDim.x * blockDim.x) {
+        int32_t v = 0;
+        for (int sp = 0; sp < nsplit; ++sp)
+            v += __ldg(part + (size_t)sp * plane + e);
+        if (acc) {
+            acc[e] = v;
+        } else {
+            const int m = (int)(e / (size_t)N), n = (int)(e - (size_t)m * N);
+            out[e] = epilogue_bf16(v, __ldg(xscale + m), cs[n]);
+        }
+    }
+}
+
 }  // namespace tc
 
-size_t prefill_workspace_bytes(int M, int K)
+// K split of the tensor-core GEMM when its output tiles alone cannot fill the
+// GPU: the number of 64-column blocks per split that minimises
+// waves x (blocks per CTA + a per-CTA fixed cost of about 4 blocks).
+static void tc_plan(int M, int N, int K, int sms, int &nsplit, int &kb_per_split)
 {
-    return (size_t)M * (size_t)K * 2 + 256;
+    const long tiles = (long)((M + tc::BM - 1) / tc::BM) * (((N + 2) / 3 + tc::GROUPS - 1) / tc::GROUPS);
+    const int nk = (K + tc::BK - 1) / tc::BK;
+    nsplit = 1;
+    kb_per_split = nk;
+    if (tiles >= sms)
+        return;
+    double best = 1e30;
+    for (int s = 1; s <= 16 && s <= nk; ++s) {
+        const int kbps = (nk + s - 1) / s;
+        const int real = (nk + kbps - 1) / kbps;   // no empty splits
+        const long ctas = tiles * real;
+        const double cost = (double)((ctas + sms - 1) / sms) * (kbps + 4);
+        if (cost < best - 1e-9) {
+            best = cost;
+            nsplit = real;
+            kb_per_split = kbps;
+        }
+    }
+}
+
+static size_t align256(size_t v)
+{
+    return (v + 255) & ~(size_t)255;
+}
+
+size_t prefill_workspace_bytes(int M, int N, int K)
+{
+    int nsplit, kbps;
+    tc_plan(M, N, K, device_sm_count(), nsplit, kbps);
+    size_t bytes = align256((size_t)M * K * 2) + 256;
+    if (nsplit > 1)
+        bytes += align256((size_t)nsplit * M * N * 4);
+    return bytes;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -414,12 +495,17 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream)
 {
     using namespace tc;
-    if (!a.ws || a.ws_bytes < prefill_workspace_bytes(a.M, a.K))
+    if (!a.ws || a.ws_bytes < prefill_workspace_bytes(a.M, a.N, a.K))
         return cudaErrorInvalidValue;
+    int nsplit, kbps;
+    tc_plan(a.M, a.N, a.K, device_sm_count(), nsplit, kbps);
     auto encode = tensor_map_encoder();
     if (!encode)
         return cudaErrorNotSupported;
     __nv_bfloat16 *act = reinterpret_cast<__nv_bfloat16 *>(((uintptr_t)a.ws + 255) & ~(uintptr_t)255);
+    int32_t *part = nsplit > 1 ? reinterpret_cast<int32_t *>(reinterpret_cast<unsigned char *>(act) +
+                                                             align256((size_t)a.M * a.K * 2))
+                               : nullptr;
     const long n16 = (long)a.M * a.K / 16;
     const int sms = device_sm_count();
     int cgrid = (int)((n16 + 255) / 256);
@@ -462,10 +548,23 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream)
     p.status = a.status;
     p.vec_out = a.acc ? ((a.N & 3) == 0 && ((uintptr_t)a.acc & 15) == 0)
                       : ((a.N & 7) == 0 && ((uintptr_t)a.out & 15) == 0);
-    const long tiles = (long)((a.M + BM - 1) / BM) * (long)((G + GROUPS - 1) / GROUPS);
-    if (tiles > 0x7FFFFFFFL)
+    p.nsplit = nsplit;
+    p.kb_per_split = kbps;
+    p.part = part;
+    p.vec_part = (a.N & 3) == 0;
+    const long ctas = (long)((a.M + BM - 1) / BM) * (long)((G + GROUPS - 1) / GROUPS) * nsplit;
+    if (ctas > 0x7FFFFFFFL)
         return cudaErrorInvalidValue;
-    tc::prefill_kernel<<<(unsigned)tiles, THREADS, SMEM_BYTES, stream>>>(tm_act, tm_pk, p);
+    tc::prefill_kernel<<<(unsigned)ctas, THREADS, SMEM_BYTES, stream>>>(tm_act, tm_pk, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || nsplit == 1)
+        return e;
+    const size_t plane = (size_t)a.M * a.N;
+    long fgrid = (long)((plane + 255) / 256);
+    if (fgrid > (long)sms * 16)
+        fgrid = (long)sms * 16;
+    tc::finalize_kernel<<<(unsigned)fgrid, 256, 0, stream>>>(part, nsplit, a.M, a.N, a.xscale, a.cs, a.out,
+                                                             a.acc);
     return cudaGetLastError();
 }
 
