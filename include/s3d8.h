@@ -32,7 +32,7 @@
  *   - Not checked, for speed: centroid values must lie in 0..127 and the bf16
  *     inputs must be finite.
  *   - The decode-regime kernels (s3d8_linear_batch, and s3d8_linear* for
- *     M <= 4) use programmatic dependent launch: when the kernel before them on
+ *     M <= 8) use programmatic dependent launch: when the kernel before them on
  *     the stream allows an early start (this library's kernels do), they read
  *     the packed weights and centroid tables while that kernel is still
  *     finishing, and everything else only after it has completed.  So packed
@@ -165,7 +165,7 @@ typedef struct {
 #define S3D8_MAX_BATCH 8
 
 /*
- * Several independent S3D8 linears (the same token count M, 1 <= M <= 4) in one
+ * Several independent S3D8 linears (the same token count M, 1 <= M <= 8) in one
  * launch: the GPU's SMs are divided among the jobs in proportion to their
  * packed bytes and every job streams its weights concurrently.  With x_bf16 the
  * activation quantisation is fused into the launch (each CTA quantises the
@@ -173,7 +173,7 @@ typedef struct {
  * example the q, k and v projections of one token, or the seven projections of
  * a decoder layer when their inputs are available together.
  * Up to S3D8_MAX_BATCH jobs; each job's K must satisfy the s3d8_linear rules and
- * K <= 65536.  Returns S3D8_ERR_UNSUPPORTED for M > 4.
+ * K <= 65536.  Returns S3D8_ERR_UNSUPPORTED for M > 8.
  */
 int s3d8_linear_batch(const s3d8_linear_job *jobs, int count, int64_t M, void *stream);
 

@@ -230,7 +230,7 @@ def linear_acc_i32(packed: torch.Tensor, centroids: torch.Tensor, xq: torch.Tens
 
 
 def linear_batch(jobs, M: int):
-    """Several independent S3D8 linears with the same token count M (1..4) in one
+    """Several independent S3D8 linears with the same token count M (1..8) in one
     launch.  Each job is a dict with keys packed, centroids, chan_scale, N and
     either x (bf16 [M, K], quantised inside the launch) or xq + xscale; optional
     out (bf16 [M, N]), acc (int32 [M, N], replaces out), xq_out, xscale_out.

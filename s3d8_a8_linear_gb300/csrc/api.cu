@@ -124,9 +124,9 @@ int s3d8_decode(const uint8_t *packed, const int8_t *centroids, int64_t N, int64
                                      static_cast<cudaStream_t>(stream)));
 }
 
-// The algorithm AUTO runs: the bulk-copy GEMV up to 4 tokens, the tensor-core
-// GEMM from kTcMinM tokens, the plain GEMV in between.
-constexpr int64_t kTcMinM = 16;
+// The algorithm AUTO runs: the bulk-copy GEMV up to 8 tokens, the tensor-core
+// GEMM from kTcMinM tokens.
+constexpr int64_t kTcMinM = 9;
 
 static int resolve_algo(int64_t M, int64_t K, int algo)
 {
@@ -240,7 +240,7 @@ int s3d8_linear_batch(const s3d8_linear_job *jobs, int count, int64_t M, void *s
         return S3D8_OK;
     if (!jobs)
         return S3D8_ERR_INVALID_ARG;
-    if (M > 4)
+    if (M > 8)
         return S3D8_ERR_UNSUPPORTED;
     GroupArgs g = {};
     g.M = (int)M;

@@ -1,4 +1,4 @@
-// Streaming S3D8 GEMV for the decode regime (M <= 4 tokens), grouped form.
+// Streaming S3D8 GEMV for the decode regime (M <= 8 tokens), grouped form.
 //
 // One launch runs up to kMaxJobs independent linears.  The CTAs (one per SM,
 // 16 warps) are divided among the jobs in proportion to their packed bytes, so
@@ -47,11 +47,11 @@ constexpr int kBarsPerWarp = kDepth * kHalves;
 // ring is filled after the activation loads have been issued, so that their
 // replies do not queue behind a whole ring of weight bytes.
 constexpr int kPrewaitSlices = S3D8_PREWAIT_SLICES;
-// 512-byte chunks per slice: 8 (4 KiB) for up to 2 tokens, 4 for 3..4 tokens so
-// that the activations of the slice still fit in registers.
+// 512-byte chunks per slice: 8 (4 KiB) for up to 2 tokens, 4 for 3..4 tokens and
+// 2 for 5..8 tokens, so that the activations of the slice still fit in registers.
 __host__ __device__ constexpr int chunks_for(int MT)
 {
-    return MT <= 2 ? 8 : 4;
+    return MT <= 2 ? 8 : MT <= 4 ? 4 : 2;
 }
 constexpr int kUnionBytes = 28672;               // fused activations, then T > 1 sums
 constexpr int kTmaDynSmem = 232448 - 4096;
@@ -539,7 +539,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
 
 static int tma_token_block(int M)
 {
-    return M <= 1 ? 1 : M <= 2 ? 2 : 4;
+    return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
 }
 
 static int stage_bytes(int M)
@@ -549,7 +549,7 @@ static int stage_bytes(int M)
 
 bool gemv_group_job_ok(int M, int K, bool fused)
 {
-    if (M < 1 || M > 4)
+    if (M < 1 || M > 8)
         return false;
     if ((K + stage_bytes(M) - 1) / stage_bytes(M) > kTmaWarps)
         return false;
@@ -663,7 +663,8 @@ cudaError_t launch_gemv_group(GroupArgs &g, cudaStream_t stream)
     switch (tma_token_block(g.M)) {
     case 1: return launch_group_mt<1>(g, grid, stream);
     case 2: return launch_group_mt<2>(g, grid, stream);
-    default: return launch_group_mt<4>(g, grid, stream);
+    case 4: return launch_group_mt<4>(g, grid, stream);
+    default: return launch_group_mt<8>(g, grid, stream);
     }
 }
 

@@ -12,10 +12,11 @@
 //   warp 0      bulk tensor copies (TMA) of the bf16 activation tile (from the
 //               workspace) and of the 80 x 64 packed-byte tile;
 //   warp 1      TMEM allocation and the MMA issuer (one thread);
-//   warps 2-7   decode: packed bytes -> bf16 weights, written straight into the
+//   warps 2-15  decode: packed bytes -> bf16 weights, written straight into the
 //               128-byte-swizzled K-major layout the MMA descriptor reads;
-//   warps 8-15  drain the fp32 accumulator per K-chunk into int32 registers and
-//               write the epilogue (x_s * acc) * W_s as bf16 (or the raw int32).
+//   warps 8-15  also drain the fp32 accumulator per K-chunk into int32 registers
+//               (between decode steps) and write the epilogue (x_s * acc) * W_s
+//               as bf16 (or the raw int32).
 // Warpgroups 0-1 give registers up (setmaxnreg 80) so that the drain warps can
 // hold 120 int32 sums each (setmaxnreg 176): 128 x (80+80+176+176) = 65536.
 // TMEM holds two accumulator buffers (columns 0 and 256) so that the MMA fills
@@ -51,7 +52,7 @@ constexpr int OFF_BARS = OFF_LUT + LUT_BYTES;
 constexpr int NBARS = 2 * LSTAGES + 2 * BSTAGES + 4;
 constexpr int SMEM_BYTES = 1024 + OFF_BARS + NBARS * 8 + 16;
 constexpr int THREADS = 16 * 32;
-constexpr int PRODUCERS = 192;   // warps 2-7
+constexpr int DECODERS = 14 * 32;   // warps 2-15 all decode (8-15 also drain)
 constexpr int DRAIN_WARP0 = 8;
 constexpr int HALF = BN / 2;             // 120 columns per epilogue thread
 
@@ -118,6 +119,55 @@ __device__ __forceinline__ uint32_t bf16_bits_of(int v)
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((float)v));
 }
 
+// Expands this thread's share of a 80 x 64 packed tile (units u = t, t + nthr, ...;
+// one unit = one group's 8 bytes at one 16-byte column chunk) into the
+// 128-byte-swizzled K-major bf16 tile: element (n, k) at n * 128 +
+// ((k / 8) ^ (n % 8)) * 16 + (k % 8) * 2.
+__device__ __forceinline__ void decode_tile(uint32_t ptile, uint32_t btile, uint32_t lut_lane, int t, int nthr)
+{
+    for (int u = t; u < GROUPS * 8; u += nthr) {
+        const int gl = u >> 3, j = u & 7;   // group, 16-byte chunk (8 k)
+        uint32_t pk0, pk1;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(pk0), "=r"(pk1) : "r"(ptile + gl * 64 + j * 8));
+        uint2 e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t byte = ((i < 4 ? pk0 : pk1) >> (8 * (i & 3))) & 0xFFu;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(e[i].x), "=r"(e[i].y)
+                         : "r"(lut_lane + byte * (LUT_COPIES * 8)));
+        }
+        uint32_t w[3][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            w[0][q] = prmt(e[2 * q].x, e[2 * q + 1].x, 0x5410);
+            w[1][q] = prmt(e[2 * q].x, e[2 * q + 1].x, 0x7632);
+            w[2][q] = prmt(e[2 * q].y, e[2 * q + 1].y, 0x5410);
+        }
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const int n = 3 * gl + d;
+            const uint32_t addr = btile + n * 128 + (((uint32_t)j ^ (uint32_t)(n & 7)) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[d][0]), "r"(w[d][1]),
+                         "r"(w[d][2]), "r"(w[d][3])
+                         : "memory");
+        }
+    }
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 struct Params {
     int M, N, K;
     const int8_t *C;
@@ -171,7 +221,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
             mbar_init(l_empty + 8 * s, 1);
         }
         for (int s = 0; s < BSTAGES; ++s) {
-            mbar_init(b_full + 8 * s, PRODUCERS / 32);
+            mbar_init(b_full + 8 * s, DECODERS / 32);
             mbar_init(b_empty + 8 * s, 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -275,35 +325,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
                 timed_out = true;
                 break;
             }
-            const uint32_t btile = base + OFF_B + bs * B_BYTES, ptile = base + OFF_P + s * P_BYTES;
-            for (int u = t; u < GROUPS * 8; u += PRODUCERS) {
-                const int gl = u >> 3, j = u & 7;   // group, 16-byte chunk (8 k)
-                uint32_t pk0, pk1;
-                asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(pk0), "=r"(pk1) : "r"(ptile + gl * 64 + j * 8));
-                uint2 e[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t byte = ((i < 4 ? pk0 : pk1) >> (8 * (i & 3))) & 0xFFu;
-                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                                 : "=r"(e[i].x), "=r"(e[i].y)
-                                 : "r"(lut_lane + byte * (LUT_COPIES * 8)));
-                }
-                uint32_t w[3][4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    w[0][q] = prmt(e[2 * q].x, e[2 * q + 1].x, 0x5410);
-                    w[1][q] = prmt(e[2 * q].x, e[2 * q + 1].x, 0x7632);
-                    w[2][q] = prmt(e[2 * q].y, e[2 * q + 1].y, 0x5410);
-                }
-#pragma unroll
-                for (int d = 0; d < 3; ++d) {
-                    const int n = 3 * gl + d;
-                    const uint32_t addr = btile + n * 128 + (((uint32_t)j ^ (uint32_t)(n & 7)) << 4);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[d][0]),
-                                 "r"(w[d][1]), "r"(w[d][2]), "r"(w[d][3])
-                                 : "memory");
-                }
-            }
+            decode_tile(base + OFF_P + s * P_BYTES, base + OFF_B + bs * B_BYTES, lut_lane, t, DECODERS);
             fence_proxy_async_smem();   // generic writes -> visible to the tensor core
             __syncwarp();
             if (lane == 0)
@@ -319,11 +341,8 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < HALF; ++i)
             acc[i] = 0;
-        for (int c = 0; c < nchunks && !timed_out; ++c) {
-            if (!mbar_wait_bounded(acc_full + 8 * (c & 1), (c >> 1) & 1)) {
-                timed_out = true;
-                break;
-            }
+        // fp32 chunk c in TMEM -> int32 registers; then release its buffer
+        auto drain = [&](int c) {
             tc_fence_after();
             const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((c & 1) * 256 + h * HALF);
 #pragma unroll
@@ -343,6 +362,38 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(acc_empty + 8 * (c & 1));
+        };
+        // Between chunk drains these warps decode too.  A finished chunk is
+        // drained before the next K block is decoded, so the MMA never waits on
+        // a buffer these warps have not released while they wait on the MMA.
+        const int t = threadIdx.x - 64;
+        const uint32_t lut_lane = lut + (uint32_t)((lane & (LUT_COPIES - 1)) * 8);
+        int cn = 0;   // next chunk to drain
+        for (int kb = 0; kb < nk && !timed_out; ++kb) {
+            while (cn < nchunks) {
+                const bool ready = __shfl_sync(0xffffffffu, (int)mbar_test(acc_full + 8 * (cn & 1), (cn >> 1) & 1), 0) != 0;
+                if (!ready)
+                    break;
+                drain(cn++);
+            }
+            const int s = kb % LSTAGES, bs = kb % BSTAGES;
+            if (!mbar_wait_bounded(l_full + 8 * s, (kb / LSTAGES) & 1) ||
+                (kb >= BSTAGES && !mbar_wait_bounded(b_empty + 8 * bs, ((kb / BSTAGES) - 1) & 1))) {
+                timed_out = true;
+                break;
+            }
+            decode_tile(base + OFF_P + s * P_BYTES, base + OFF_B + bs * B_BYTES, lut_lane, t, DECODERS);
+            fence_proxy_async_smem();   // generic writes -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b_full + 8 * bs);
+        }
+        for (; cn < nchunks && !timed_out; ++cn) {
+            if (!mbar_wait_bounded(acc_full + 8 * (cn & 1), (cn >> 1) & 1)) {
+                timed_out = true;
+                break;
+            }
+            drain(cn);
         }
         const int row = m0 + 32 * q + lane;
         if (!timed_out && row < p.M) {

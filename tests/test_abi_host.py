@@ -148,7 +148,7 @@ def test_batch_rejects(lib):
     arr = (s3d8.LinearJob * 9)(*([job] * 9))
     assert lib.s3d8_linear_batch(arr, 9, 1, None) == -1          # more than 8 jobs
     assert lib.s3d8_linear_batch(None, 2, 1, None) == -1
-    assert lib.s3d8_linear_batch(arr, 2, 5, None) == -3          # M > 4
+    assert lib.s3d8_linear_batch(arr, 2, 9, None) == -3          # M > 8
     assert lib.s3d8_linear_batch(arr, 0, 1, None) == 0
     assert lib.s3d8_linear_batch(arr, 2, 0, None) == 0
     both = s3d8.LinearJob.from_buffer_copy(job)

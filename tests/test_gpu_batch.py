@@ -2,7 +2,7 @@
 
 Covers fused activation quantisation (codes and scales bit-exact, optional
 copies returned), pre-quantised jobs, int32 accumulators, partial K slices,
-N not a multiple of 3, M = 1..4, and the rejection of unsupported sizes.
+N not a multiple of 3, M = 1..8, and the rejection of unsupported sizes.
 """
 import numpy as np
 import pytest
@@ -57,7 +57,7 @@ def test_layer_fused_m1():
         np.testing.assert_array_equal(to_np(j["xscale_out"]), qref[a][1], err_msg=name)
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])
 def test_mixed_jobs_exact(M):
     rng = np.random.default_rng(40 + M)
     shapes = [(96, 256), (7, 16), (1000, 5008), (50, 4096 + 16), (4096, 2048)]
