@@ -141,7 +141,7 @@ size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo)
     (void)N;
     if (M <= 0 || K <= 0 || M > S3D8_MAX_M || K > S3D8_MAX_K)
         return 0;
-    return resolve_algo(M, K, algo) == S3D8_ALGO_TC ? prefill_workspace_bytes((int)M, (int)N, (int)K) : 0;
+    return resolve_algo(M, K, algo) == S3D8_ALGO_TC ? prefill_workspace_bytes((int)M, (int)N, (int)K, prefill_predecode((int)M)) : 0;
 }
 
 static int linear_common(const uint8_t *packed, const int8_t *centroids, const void *chan_scale,
@@ -194,7 +194,7 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     a.status = device_status_ptr();
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     if (algo == S3D8_ALGO_TC)
-        return cuda_status(launch_prefill_tc(a, strm));
+        return cuda_status(launch_prefill_tc(a, prefill_predecode(a.M), strm));
     if (gemv_tma_supported(a.M, a.K))
         return cuda_status(launch_gemv_tma(a, strm));
     return cuda_status(launch_gemv(a, strm));

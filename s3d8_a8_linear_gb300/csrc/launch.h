@@ -60,7 +60,11 @@ cudaError_t launch_wait_timeout(int polls, int *status, cudaStream_t stream);
 bool gemv_group_job_ok(int M, int K, bool fused);
 cudaError_t launch_gemv_group(GroupArgs &g, cudaStream_t stream);
 cudaError_t launch_gemv_tma(const LinearArgs &a, cudaStream_t stream);
-size_t prefill_workspace_bytes(int M, int N, int K);
-cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream);
+// Tensor-core path; `pre` expands the weights to bf16 in the workspace first and
+// feeds both operands by bulk tensor copy (large M), otherwise the weight tile
+// is decoded from packed bytes inside the GEMM.
+bool prefill_predecode(int M);
+size_t prefill_workspace_bytes(int M, int N, int K, bool pre);
+cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream);
 
 }  // namespace s3d8

@@ -56,6 +56,15 @@ constexpr int DECODERS = 14 * 32;   // warps 2-15 all decode (8-15 also drain)
 constexpr int DRAIN_WARP0 = 8;
 constexpr int HALF = BN / 2;             // 120 columns per epilogue thread
 
+// Variant with pre-decoded bf16 weights (both operands by bulk tensor copy): a
+// ring of PSTAGES (activation tile + weight tile), no packed tiles, no table.
+constexpr int PSTAGES = 4;
+constexpr int P_OFF_B = PSTAGES * A_BYTES;
+constexpr int P_OFF_BARS = P_OFF_B + PSTAGES * B_BYTES;
+constexpr int P_NBARS = 2 * PSTAGES + 4;
+constexpr int P_SMEM_BYTES = 1024 + P_OFF_BARS + P_NBARS * 8 + 16;
+static_assert(P_OFF_B % 1024 == 0 && P_SMEM_BYTES + 1024 <= 232448, "pre-decoded layout");
+
 static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0,
               "swizzled tiles must stay 1024-aligned");
 static_assert(OFF_P % 128 == 0 && P_BYTES % 128 == 0, "packed tiles 128-byte aligned");
@@ -183,23 +192,33 @@ struct Params {
     int vec_part;       // partial rows may be written with 16-byte stores
 };
 
+// PRE = false: the weight tile is decoded from packed bytes in shared memory by
+// warps 2-15.  PRE = true: the weights were expanded to bf16 [N, K] in global
+// memory beforehand and arrive by bulk tensor copy like the activations; warps
+// 2-7 idle and 8-15 only drain.
+template <bool PRE>
 __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_constant__ CUtensorMap tm_act,
                                                              const __grid_constant__ CUtensorMap tm_pk,
                                                              Params p)
 {
+    constexpr int LST = PRE ? PSTAGES : LSTAGES;
+    constexpr int BST = PRE ? 0 : BSTAGES;
+    constexpr int O_B = PRE ? P_OFF_B : OFF_B;
+    constexpr int O_BARS = PRE ? P_OFF_BARS : OFF_BARS;
+    constexpr int NB = PRE ? P_NBARS : NBARS;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *smem = smem_raw + (base - raw);
     const uint32_t lut = base + OFF_LUT;
-    const uint32_t bars = base + OFF_BARS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BARS + NBARS * 8);
-    // barriers: l_full[L] (TMA bytes of A and packed), l_empty[L] (MMA done with
-    //           the slot), b_full[B] (decoded tile written), b_empty[B] (MMA done
-    //           with the decoded tile), acc_full[2] (chunk in TMEM), acc_empty[2]
-    const uint32_t l_full = bars, l_empty = l_full + 8 * LSTAGES;
-    const uint32_t b_full = l_empty + 8 * LSTAGES, b_empty = b_full + 8 * BSTAGES;
-    const uint32_t acc_full = b_empty + 8 * BSTAGES, acc_empty = acc_full + 16;
+    const uint32_t bars = base + O_BARS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + O_BARS + NB * 8);
+    // barriers: l_full[L] (TMA bytes of the slot), l_empty[L] (MMA done with the
+    //           slot), b_full[B] (decoded tile written), b_empty[B] (MMA done with
+    //           the decoded tile), acc_full[2] (chunk in TMEM), acc_empty[2]
+    const uint32_t l_full = bars, l_empty = l_full + 8 * LST;
+    const uint32_t b_full = l_empty + 8 * LST, b_empty = b_full + 8 * BST;
+    const uint32_t acc_full = b_empty + 8 * BST, acc_empty = acc_full + 16;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mtiles = (p.M + BM - 1) / BM;
@@ -216,11 +235,11 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
     const int nchunks = (nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < LSTAGES; ++s) {
+        for (int s = 0; s < LST; ++s) {
             mbar_init(l_full + 8 * s, 1);
             mbar_init(l_empty + 8 * s, 1);
         }
-        for (int s = 0; s < BSTAGES; ++s) {
+        for (int s = 0; s < BST; ++s) {
             mbar_init(b_full + 8 * s, DECODERS / 32);
             mbar_init(b_empty + 8 * s, 1);
         }
@@ -238,7 +257,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
     }
     // decode table: byte -> [bf16 w0 | bf16 w1 << 16, bf16 w2], 16 copies (one per
     // half-warp lane) so that 8-byte lookups never conflict.
-    {
+    if (!PRE) {
         __shared__ int8_t Cs[96];
         for (int i = threadIdx.x; i < 96; i += THREADS)
             Cs[i] = p.C[i];
@@ -263,19 +282,22 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         if (lane == 0) {
             int issued = 0;
             for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % LSTAGES;
-                if (kb >= LSTAGES && !mbar_wait_bounded(l_empty + 8 * s, ((kb / LSTAGES) - 1) & 1)) {
+                const int s = kb % LST;
+                if (kb >= LST && !mbar_wait_bounded(l_empty + 8 * s, ((kb / LST) - 1) & 1)) {
                     timed_out = true;
                     break;
                 }
                 issued = kb + 1;
-                mbar_arrive_expect_tx(l_full + 8 * s, A_BYTES + P_BYTES);
+                mbar_arrive_expect_tx(l_full + 8 * s, A_BYTES + (PRE ? B_BYTES : P_BYTES));
                 tma_2d(base + OFF_A + s * A_BYTES, &tm_act, (kbase + kb) * BK, m0, l_full + 8 * s);
-                tma_2d(base + OFF_P + s * P_BYTES, &tm_pk, (kbase + kb) * BK, g0, l_full + 8 * s);
+                if (PRE)
+                    tma_2d(base + O_B + s * B_BYTES, &tm_pk, (kbase + kb) * BK, nt * BN, l_full + 8 * s);
+                else
+                    tma_2d(base + OFF_P + s * P_BYTES, &tm_pk, (kbase + kb) * BK, g0, l_full + 8 * s);
             }
             // never leave with copies in flight: wait (bounded) for the last ones
-            for (int kb = issued - LSTAGES < 0 ? 0 : issued - LSTAGES; kb < issued; ++kb)
-                if (!mbar_wait_bounded(l_full + 8 * (kb % LSTAGES), (kb / LSTAGES) & 1))
+            for (int kb = issued - LST < 0 ? 0 : issued - LST; kb < issued; ++kb)
+                if (!mbar_wait_bounded(l_full + 8 * (kb % LST), (kb / LST) & 1))
                     timed_out = true;
         }
     } else if (warp == 1) {
@@ -285,40 +307,40 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
             const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                                    ((uint32_t)(BM >> 4) << 24);
             for (int kb = 0; kb < nk && !timed_out; ++kb) {
-                const int s = kb % LSTAGES, bs = kb % BSTAGES;
+                const int s = kb % LST, bs = PRE ? s : kb % BSTAGES;
                 const int c = kb / CHUNK_BLOCKS, kin = kb % CHUNK_BLOCKS;
                 const uint32_t d = tmem + (uint32_t)((c & 1) * 256);
                 if (kin == 0 && c >= 2 && !mbar_wait_bounded(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
                     timed_out = true;
                     break;
                 }
-                if (!mbar_wait_bounded(l_full + 8 * s, (kb / LSTAGES) & 1) ||
-                    !mbar_wait_bounded(b_full + 8 * bs, (kb / BSTAGES) & 1)) {
+                if (!mbar_wait_bounded(l_full + 8 * s, (kb / LST) & 1) ||
+                    (!PRE && !mbar_wait_bounded(b_full + 8 * bs, (kb / BSTAGES) & 1))) {
                     timed_out = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a = base + OFF_A + s * A_BYTES, b = base + OFF_B + bs * B_BYTES;
+                const uint32_t a = base + OFF_A + s * A_BYTES, b = base + O_B + bs * B_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     mma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
                              (kin | kk) ? 1u : 0u);
                 mma_commit(l_empty + 8 * s);
-                mma_commit(b_empty + 8 * bs);
+                if (!PRE)
+                    mma_commit(b_empty + 8 * bs);
                 if (kin == CHUNK_BLOCKS - 1 || kb == nk - 1)
                     mma_commit(acc_full + 8 * (c & 1));
                 issued = kb + 1;
             }
             // the tensor core must be done with TMEM and shared memory before exit
-            if (issued > 0 &&
-                !mbar_wait_bounded(l_empty + 8 * ((issued - 1) % LSTAGES), ((issued - 1) / LSTAGES) & 1))
+            if (issued > 0 && !mbar_wait_bounded(l_empty + 8 * ((issued - 1) % LST), ((issued - 1) / LST) & 1))
                 timed_out = true;
         }
     } else {
         // ---- decode packed bytes into the swizzled bf16 weight tile -------------
         const int t = threadIdx.x - 64;
         const uint32_t lut_lane = lut + (uint32_t)((lane & (LUT_COPIES - 1)) * 8);
-        for (int kb = 0; kb < nk && !timed_out; ++kb) {
+        for (int kb = 0; kb < (PRE ? 0 : nk) && !timed_out; ++kb) {
             const int s = kb % LSTAGES, bs = kb % BSTAGES;
             if (!mbar_wait_bounded(l_full + 8 * s, (kb / LSTAGES) & 1) ||
                 (kb >= BSTAGES && !mbar_wait_bounded(b_empty + 8 * bs, ((kb / BSTAGES) - 1) & 1))) {
@@ -369,7 +391,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         const int t = threadIdx.x - 64;
         const uint32_t lut_lane = lut + (uint32_t)((lane & (LUT_COPIES - 1)) * 8);
         int cn = 0;   // next chunk to drain
-        for (int kb = 0; kb < nk && !timed_out; ++kb) {
+        for (int kb = 0; kb < (PRE ? 0 : nk) && !timed_out; ++kb) {
             while (cn < nchunks) {
                 const bool ready = __shfl_sync(0xffffffffu, (int)mbar_test(acc_full + 8 * (cn & 1), (cn >> 1) & 1), 0) != 0;
                 if (!ready)
@@ -467,6 +489,56 @@ __global__ void codes_to_bf16_kernel(const int8_t *__restrict__ xq, __nv_bfloat1
     }
 }
 
+// Weights expanded to bf16 [N, K] (row n = component n % 3 of packed row n / 3),
+// for the pre-decoded variant.  One thread per 16 packed bytes; the 16-copy
+// table of bf16 triples is the kernel's own.
+__global__ __launch_bounds__(256) void decode_bf16_kernel(const uint8_t *__restrict__ packed,
+                                                          const int8_t *__restrict__ C, int N, int K,
+                                                          __nv_bfloat16 *__restrict__ w)
+{
+    __shared__ int8_t Cs[96];
+    __shared__ uint2 lut[kLutEntries * LUT_COPIES];
+    for (int i = threadIdx.x; i < 96; i += blockDim.x)
+        Cs[i] = C[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < kLutEntries * LUT_COPIES; i += blockDim.x) {
+        const uint32_t e = expanded_entry(Cs, (uint32_t)(i / LUT_COPIES));
+        const int w0 = (int8_t)(e & 0xFF), w1 = (int8_t)((e >> 8) & 0xFF), w2 = (int8_t)((e >> 16) & 0xFF);
+        lut[i] = make_uint2(bf16_bits_of(w0) | (bf16_bits_of(w1) << 16), bf16_bits_of(w2));
+    }
+    __syncthreads();
+    const int G = (N + 2) / 3, kc = K / 16;
+    const uint2 *mylut = lut + (threadIdx.x & (LUT_COPIES - 1));
+    for (long u = (long)blockIdx.x * blockDim.x + threadIdx.x; u < (long)G * kc; u += (long)gridDim.x * blockDim.x) {
+        const int g = (int)(u / kc), c = (int)(u - (long)g * kc);
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(packed + (size_t)g * K) + c);
+        const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[3][8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint2 e[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                e[i] = mylut[((pw[q] >> (8 * i)) & 0xFFu) * LUT_COPIES];
+            o[0][2 * q] = prmt(e[0].x, e[1].x, 0x5410);
+            o[0][2 * q + 1] = prmt(e[2].x, e[3].x, 0x5410);
+            o[1][2 * q] = prmt(e[0].x, e[1].x, 0x7632);
+            o[1][2 * q + 1] = prmt(e[2].x, e[3].x, 0x7632);
+            o[2][2 * q] = prmt(e[0].y, e[1].y, 0x5410);
+            o[2][2 * q + 1] = prmt(e[2].y, e[3].y, 0x5410);
+        }
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const int n = 3 * g + d;
+            if (n < N) {
+                uint4 *dst = reinterpret_cast<uint4 *>(w + (size_t)n * K + (size_t)c * 16);
+                dst[0] = make_uint4(o[d][0], o[d][1], o[d][2], o[d][3]);
+                dst[1] = make_uint4(o[d][4], o[d][5], o[d][6], o[d][7]);
+            }
+        }
+    }
+}
+
 // Split-K finish: out[m, n] (or acc) from the sum of the nsplit int32 partials.
 // Integer sums, so the order of the splits does not matter.
 __global__ void finalize_kernel(const int32_t *__restrict__ part, int nsplit, int M, int N,
@@ -519,13 +591,25 @@ static size_t align256(size_t v)
     return (v + 255) & ~(size_t)255;
 }
 
-size_t prefill_workspace_bytes(int M, int N, int K)
+// From this many tokens the weights are expanded to bf16 once per call and the
+// GEMM reads them by bulk tensor copy: the expansion then costs less than
+// re-decoding every weight tile once per 128-token tile inside the GEMM.
+constexpr int kPredecodeMinM = 384;
+
+bool prefill_predecode(int M)
+{
+    return M >= kPredecodeMinM;
+}
+
+size_t prefill_workspace_bytes(int M, int N, int K, bool pre)
 {
     int nsplit, kbps;
     tc_plan(M, N, K, device_sm_count(), nsplit, kbps);
     size_t bytes = align256((size_t)M * K * 2) + 256;
     if (nsplit > 1)
         bytes += align256((size_t)nsplit * M * N * 4);
+    if (pre)
+        bytes += align256((size_t)N * K * 2);
     return bytes;
 }
 
@@ -543,10 +627,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream)
+cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream)
 {
     using namespace tc;
-    if (!a.ws || a.ws_bytes < prefill_workspace_bytes(a.M, a.N, a.K))
+    if (!a.ws || a.ws_bytes < prefill_workspace_bytes(a.M, a.N, a.K, pre))
         return cudaErrorInvalidValue;
     int nsplit, kbps;
     tc_plan(a.M, a.N, a.K, device_sm_count(), nsplit, kbps);
@@ -554,9 +638,10 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream)
     if (!encode)
         return cudaErrorNotSupported;
     __nv_bfloat16 *act = reinterpret_cast<__nv_bfloat16 *>(((uintptr_t)a.ws + 255) & ~(uintptr_t)255);
-    int32_t *part = nsplit > 1 ? reinterpret_cast<int32_t *>(reinterpret_cast<unsigned char *>(act) +
-                                                             align256((size_t)a.M * a.K * 2))
-                               : nullptr;
+    unsigned char *after_act = reinterpret_cast<unsigned char *>(act) + align256((size_t)a.M * a.K * 2);
+    int32_t *part = nsplit > 1 ? reinterpret_cast<int32_t *>(after_act) : nullptr;
+    __nv_bfloat16 *wdec = reinterpret_cast<__nv_bfloat16 *>(
+        after_act + (nsplit > 1 ? align256((size_t)nsplit * a.M * a.N * 4) : 0));
     const long n16 = (long)a.M * a.K / 16;
     const int sms = device_sm_count();
     int cgrid = (int)((n16 + 255) / 256);
@@ -566,6 +651,16 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
+    if (pre) {
+        const long units = (long)((a.N + 2) / 3) * (a.K / 16);
+        long dgrid = (units + 255) / 256;
+        if (dgrid > (long)sms * 8)
+            dgrid = (long)sms * 8;
+        tc::decode_bf16_kernel<<<(unsigned)dgrid, 256, 0, stream>>>(a.packed, a.C, a.N, a.K, wdec);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
 
     const int G = (a.N + 2) / 3;
     CUtensorMap tm_act, tm_pk;
@@ -579,12 +674,24 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream)
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    if (encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), dP, sP, boxP, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (pre) {
+        // bf16 weights [N, K]: 64-column x 240-row boxes, 128-byte swizzle like the activations
+        const cuuint64_t dW[2] = {(cuuint64_t)a.K, (cuuint64_t)a.N};
+        const cuuint64_t sW[1] = {(cuuint64_t)a.K * 2};
+        const cuuint32_t boxW[2] = {BK, BN};
+        if (encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wdec, dW, sW, boxW, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else if (encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), dP, sP, boxP, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
         return cudaErrorInvalidValue;
+    }
 
-    e = cudaFuncSetAttribute(tc::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const int smem_bytes = pre ? P_SMEM_BYTES : SMEM_BYTES;
+    e = pre ? cudaFuncSetAttribute(tc::prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)
+            : cudaFuncSetAttribute(tc::prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess)
         return e;
     tc::Params p;
@@ -606,7 +713,10 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, cudaStream_t stream)
     const long ctas = (long)((a.M + BM - 1) / BM) * (long)((G + GROUPS - 1) / GROUPS) * nsplit;
     if (ctas > 0x7FFFFFFFL)
         return cudaErrorInvalidValue;
-    tc::prefill_kernel<<<(unsigned)ctas, THREADS, SMEM_BYTES, stream>>>(tm_act, tm_pk, p);
+    if (pre)
+        tc::prefill_kernel<true><<<(unsigned)ctas, THREADS, smem_bytes, stream>>>(tm_act, tm_pk, p);
+    else
+        tc::prefill_kernel<false><<<(unsigned)ctas, THREADS, smem_bytes, stream>>>(tm_act, tm_pk, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || nsplit == 1)
         return e;

@@ -258,14 +258,17 @@ def test_zero_activation_row_gives_zero(algo):
 
 
 TC_TILES = [(128, 240, 64), (129, 241, 1040), (300, 722, 2112), (256, 480, 3072),
-            (1, 3, 16), (17, 1201, 1024)]
+            (1, 3, 16), (17, 1201, 1024),
+            # from 384 tokens the weights are expanded to bf16 first (both operands by TMA)
+            (384, 241, 1040), (520, 722, 2112)]
 
 
 @pytest.mark.parametrize("M,N,K", TC_TILES)
 def test_tc_tiles_and_tails(M, N, K):
     """Tensor-core path in full against the oracle: whole and ragged 128-token and
     240-channel tiles, K ragged against the 64-column block and the 1024-column
-    exact chunk."""
+    exact chunk, with the weight tiles decoded inside the GEMM (small M) and
+    pre-expanded to bf16 (M >= 384)."""
     C, packed, cs, x = rand_case(M, N, K, seed=M * 7919 + N * 31 + K)
     xq, xs = oracle.quantize_act(x)
     ref, acc_o = oracle.linear(packed, C, cs, xq, xs, N)
