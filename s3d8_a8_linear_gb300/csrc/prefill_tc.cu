@@ -221,18 +221,26 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
     const uint32_t acc_full = b_empty + 8 * BST, acc_empty = acc_full + 16;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Persistent: CTA b takes output tiles b, b + gridDim.x, ...  A tile is
+    // (128 tokens, 240 channels, one K split); consecutive tile indices share the
+    // channel tile, so the CTAs working at one time reuse its weights from L2.
     const int mtiles = (p.M + BM - 1) / BM;
     const int ntiles = ((p.N + 2) / 3 + GROUPS - 1) / GROUPS;
-    const int mt = (int)(blockIdx.x % (unsigned)mtiles);
-    const int rest = (int)(blockIdx.x / (unsigned)mtiles);
-    const int nt = rest % ntiles, split = rest / ntiles;
-    const int m0 = mt * BM;
-    const int g0 = nt * GROUPS;
-    // this CTA's K range: 64-column blocks [kbase, kbase + nk)
     const int nk_all = (p.K + BK - 1) / BK;
-    const int kbase = split * p.kb_per_split;
-    const int nk = min(p.kb_per_split, nk_all - kbase);
-    const int nchunks = (nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
+    const int total = mtiles * ntiles * p.nsplit;
+    struct Tile {
+        int m0, nt, split, kbase, nk;
+    };
+    auto tile_of = [&](int t) {
+        Tile T;
+        const int mt = t % mtiles, rest = t / mtiles;
+        T.nt = rest % ntiles;
+        T.split = rest / ntiles;
+        T.m0 = mt * BM;
+        T.kbase = T.split * p.kb_per_split;
+        T.nk = min(p.kb_per_split, nk_all - T.kbase);
+        return T;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < LST; ++s) {
@@ -280,78 +288,91 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
     if (warp == 0) {
         // ---- bulk tensor copies ------------------------------------------------
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % LST;
-                if (kb >= LST && !mbar_wait_bounded(l_empty + 8 * s, ((kb / LST) - 1) & 1)) {
-                    timed_out = true;
-                    break;
+            int issued = 0;   // k-blocks issued by this CTA over all its tiles
+            for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+                const Tile T = tile_of(t);
+                for (int kb = 0; kb < T.nk; ++kb) {
+                    const int s = issued % LST;
+                    if (issued >= LST && !mbar_wait_bounded(l_empty + 8 * s, ((issued / LST) - 1) & 1)) {
+                        timed_out = true;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(l_full + 8 * s, A_BYTES + (PRE ? B_BYTES : P_BYTES));
+                    tma_2d(base + OFF_A + s * A_BYTES, &tm_act, (T.kbase + kb) * BK, T.m0, l_full + 8 * s);
+                    if (PRE)
+                        tma_2d(base + O_B + s * B_BYTES, &tm_pk, (T.kbase + kb) * BK, T.nt * BN, l_full + 8 * s);
+                    else
+                        tma_2d(base + OFF_P + s * P_BYTES, &tm_pk, (T.kbase + kb) * BK, T.nt * GROUPS,
+                               l_full + 8 * s);
+                    ++issued;
                 }
-                issued = kb + 1;
-                mbar_arrive_expect_tx(l_full + 8 * s, A_BYTES + (PRE ? B_BYTES : P_BYTES));
-                tma_2d(base + OFF_A + s * A_BYTES, &tm_act, (kbase + kb) * BK, m0, l_full + 8 * s);
-                if (PRE)
-                    tma_2d(base + O_B + s * B_BYTES, &tm_pk, (kbase + kb) * BK, nt * BN, l_full + 8 * s);
-                else
-                    tma_2d(base + OFF_P + s * P_BYTES, &tm_pk, (kbase + kb) * BK, g0, l_full + 8 * s);
             }
             // never leave with copies in flight: wait (bounded) for the last ones
-            for (int kb = issued - LST < 0 ? 0 : issued - LST; kb < issued; ++kb)
-                if (!mbar_wait_bounded(l_full + 8 * (kb % LST), (kb / LST) & 1))
+            for (int v = issued - LST < 0 ? 0 : issued - LST; v < issued; ++v)
+                if (!mbar_wait_bounded(l_full + 8 * (v % LST), (v / LST) & 1))
                     timed_out = true;
         }
     } else if (warp == 1) {
         // ---- MMA issuer ----------------------------------------------------------
         if (lane == 0) {
-            int issued = 0;
+            int g = 0;    // k-blocks consumed by this CTA over all its tiles
+            int gc = 0;   // chunks started by this CTA over all its tiles
             const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                                    ((uint32_t)(BM >> 4) << 24);
-            for (int kb = 0; kb < nk && !timed_out; ++kb) {
-                const int s = kb % LST, bs = PRE ? s : kb % BSTAGES;
-                const int c = kb / CHUNK_BLOCKS, kin = kb % CHUNK_BLOCKS;
-                const uint32_t d = tmem + (uint32_t)((c & 1) * 256);
-                if (kin == 0 && c >= 2 && !mbar_wait_bounded(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
-                    timed_out = true;
-                    break;
-                }
-                if (!mbar_wait_bounded(l_full + 8 * s, (kb / LST) & 1) ||
-                    (!PRE && !mbar_wait_bounded(b_full + 8 * bs, (kb / BSTAGES) & 1))) {
-                    timed_out = true;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a = base + OFF_A + s * A_BYTES, b = base + O_B + bs * B_BYTES;
+            for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+                const Tile T = tile_of(t);
+                for (int kb = 0; kb < T.nk; ++kb) {
+                    const int s = g % LST, bs = PRE ? s : g % BSTAGES;
+                    const int c = gc + kb / CHUNK_BLOCKS, kin = kb % CHUNK_BLOCKS;
+                    const uint32_t d = tmem + (uint32_t)((c & 1) * 256);
+                    if (kin == 0 && c >= 2 && !mbar_wait_bounded(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
+                        timed_out = true;
+                        break;
+                    }
+                    if (!mbar_wait_bounded(l_full + 8 * s, (g / LST) & 1) ||
+                        (!PRE && !mbar_wait_bounded(b_full + 8 * bs, (g / BSTAGES) & 1))) {
+                        timed_out = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = base + OFF_A + s * A_BYTES, b = base + O_B + bs * B_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
-                             (kin | kk) ? 1u : 0u);
-                mma_commit(l_empty + 8 * s);
-                if (!PRE)
-                    mma_commit(b_empty + 8 * bs);
-                if (kin == CHUNK_BLOCKS - 1 || kb == nk - 1)
-                    mma_commit(acc_full + 8 * (c & 1));
-                issued = kb + 1;
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
+                                 (kin | kk) ? 1u : 0u);
+                    mma_commit(l_empty + 8 * s);
+                    if (!PRE)
+                        mma_commit(b_empty + 8 * bs);
+                    if (kin == CHUNK_BLOCKS - 1 || kb == T.nk - 1)
+                        mma_commit(acc_full + 8 * (c & 1));
+                    ++g;
+                }
+                gc += (T.nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
             }
             // the tensor core must be done with TMEM and shared memory before exit
-            if (issued > 0 && !mbar_wait_bounded(l_empty + 8 * ((issued - 1) % LST), ((issued - 1) / LST) & 1))
+            if (g > 0 && !mbar_wait_bounded(l_empty + 8 * ((g - 1) % LST), ((g - 1) / LST) & 1))
                 timed_out = true;
         }
     } else {
         // ---- decode packed bytes into the swizzled bf16 weight tile -------------
-        const int t = threadIdx.x - 64;
+        const int tid = threadIdx.x - 64;
         const uint32_t lut_lane = lut + (uint32_t)((lane & (LUT_COPIES - 1)) * 8);
-        for (int kb = 0; kb < (PRE ? 0 : nk) && !timed_out; ++kb) {
-            const int s = kb % LSTAGES, bs = kb % BSTAGES;
-            if (!mbar_wait_bounded(l_full + 8 * s, (kb / LSTAGES) & 1) ||
-                (kb >= BSTAGES && !mbar_wait_bounded(b_empty + 8 * bs, ((kb / BSTAGES) - 1) & 1))) {
-                timed_out = true;
-                break;
+        int g = 0;
+        for (int t = blockIdx.x; t < (PRE ? 0 : total) && !timed_out; t += gridDim.x) {
+            const Tile T = tile_of(t);
+            for (int kb = 0; kb < T.nk; ++kb, ++g) {
+                const int s = g % LSTAGES, bs = g % BSTAGES;
+                if (!mbar_wait_bounded(l_full + 8 * s, (g / LSTAGES) & 1) ||
+                    (g >= BSTAGES && !mbar_wait_bounded(b_empty + 8 * bs, ((g / BSTAGES) - 1) & 1))) {
+                    timed_out = true;
+                    break;
+                }
+                decode_tile(base + OFF_P + s * P_BYTES, base + OFF_B + bs * B_BYTES, lut_lane, tid, DECODERS);
+                fence_proxy_async_smem();   // generic writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(b_full + 8 * bs);
             }
-            decode_tile(base + OFF_P + s * P_BYTES, base + OFF_B + bs * B_BYTES, lut_lane, t, DECODERS);
-            fence_proxy_async_smem();   // generic writes -> visible to the tensor core
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(b_full + 8 * bs);
         }
     }
     } else {
@@ -360,102 +381,110 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int h = (warp - DRAIN_WARP0) >> 2; // which half of the 240 columns
         int32_t acc[HALF];
-#pragma unroll
-        for (int i = 0; i < HALF; ++i)
-            acc[i] = 0;
         // fp32 chunk c in TMEM -> int32 registers; then release its buffer
         auto drain = [&](int c) {
             tc_fence_after();
             const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((c & 1) * 256 + h * HALF);
 #pragma unroll
-            for (int g = 0; g < HALF / 24; ++g) {
+            for (int gg = 0; gg < HALF / 24; ++gg) {
                 float v[3][8];
 #pragma unroll
                 for (int i = 0; i < 3; ++i)
-                    tmem_ld8(ta + (g * 3 + i) * 8, v[i]);
+                    tmem_ld8(ta + (gg * 3 + i) * 8, v[i]);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                 for (int i = 0; i < 3; ++i)
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        acc[(g * 3 + i) * 8 + j] += __float2int_rn(v[i][j]);
+                        acc[(gg * 3 + i) * 8 + j] += __float2int_rn(v[i][j]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(acc_empty + 8 * (c & 1));
         };
-        // Between chunk drains these warps decode too.  A finished chunk is
-        // drained before the next K block is decoded, so the MMA never waits on
-        // a buffer these warps have not released while they wait on the MMA.
-        const int t = threadIdx.x - 64;
+        // Between chunk drains these warps decode too (packed variant).  A finished
+        // chunk is drained before the next K block is decoded, so the MMA never
+        // waits on a buffer these warps have not released while they wait on it.
+        const int tid = threadIdx.x - 64;
         const uint32_t lut_lane = lut + (uint32_t)((lane & (LUT_COPIES - 1)) * 8);
-        int cn = 0;   // next chunk to drain
-        for (int kb = 0; kb < (PRE ? 0 : nk) && !timed_out; ++kb) {
-            while (cn < nchunks) {
-                const bool ready = __shfl_sync(0xffffffffu, (int)mbar_test(acc_full + 8 * (cn & 1), (cn >> 1) & 1), 0) != 0;
-                if (!ready)
-                    break;
-                drain(cn++);
-            }
-            const int s = kb % LSTAGES, bs = kb % BSTAGES;
-            if (!mbar_wait_bounded(l_full + 8 * s, (kb / LSTAGES) & 1) ||
-                (kb >= BSTAGES && !mbar_wait_bounded(b_empty + 8 * bs, ((kb / BSTAGES) - 1) & 1))) {
-                timed_out = true;
-                break;
-            }
-            decode_tile(base + OFF_P + s * P_BYTES, base + OFF_B + bs * B_BYTES, lut_lane, t, DECODERS);
-            fence_proxy_async_smem();   // generic writes -> visible to the tensor core
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(b_full + 8 * bs);
-        }
-        for (; cn < nchunks && !timed_out; ++cn) {
-            if (!mbar_wait_bounded(acc_full + 8 * (cn & 1), (cn >> 1) & 1)) {
-                timed_out = true;
-                break;
-            }
-            drain(cn);
-        }
-        const int row = m0 + 32 * q + lane;
-        if (!timed_out && row < p.M) {
-            const int nbase = nt * BN + h * HALF;
-            const bool full = nbase + HALF <= p.N;
-            int32_t *accp = p.part ? p.part + (size_t)split * p.M * p.N : p.acc;
-            const bool vec_acc = p.part ? p.vec_part : p.vec_out;
-            if (accp) {
-                int32_t *dst = accp + (size_t)row * p.N + nbase;
-                if (full && vec_acc) {
+        int g = 0;    // decoded k-blocks over all tiles
+        int gc = 0;   // first chunk of the current tile
+        for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
+            const Tile T = tile_of(t);
+            const int nch = (T.nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
 #pragma unroll
-                    for (int i = 0; i < HALF; i += 4)
-                        *reinterpret_cast<int4 *>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < HALF; ++i)
-                        if (nbase + i < p.N)
-                            dst[i] = acc[i];
+            for (int i = 0; i < HALF; ++i)
+                acc[i] = 0;
+            int cn = gc;   // next chunk to drain
+            for (int kb = 0; kb < (PRE ? 0 : T.nk) && !timed_out; ++kb, ++g) {
+                while (cn < gc + nch) {
+                    const bool ready =
+                        __shfl_sync(0xffffffffu, (int)mbar_test(acc_full + 8 * (cn & 1), (cn >> 1) & 1), 0) != 0;
+                    if (!ready)
+                        break;
+                    drain(cn++);
                 }
-            } else {
-                const float xs = p.xscale[row];
-                __nv_bfloat16 *dst = p.out + (size_t)row * p.N + nbase;
-                if (full && p.vec_out) {
+                const int s = g % LSTAGES, bs = g % BSTAGES;
+                if (!mbar_wait_bounded(l_full + 8 * s, (g / LSTAGES) & 1) ||
+                    (g >= BSTAGES && !mbar_wait_bounded(b_empty + 8 * bs, ((g / BSTAGES) - 1) & 1))) {
+                    timed_out = true;
+                    break;
+                }
+                decode_tile(base + OFF_P + s * P_BYTES, base + OFF_B + bs * B_BYTES, lut_lane, tid, DECODERS);
+                fence_proxy_async_smem();   // generic writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(b_full + 8 * bs);
+            }
+            for (; cn < gc + nch && !timed_out; ++cn) {
+                if (!mbar_wait_bounded(acc_full + 8 * (cn & 1), (cn >> 1) & 1)) {
+                    timed_out = true;
+                    break;
+                }
+                drain(cn);
+            }
+            gc += nch;
+            const int row = T.m0 + 32 * q + lane;
+            if (!timed_out && row < p.M) {
+                const int nbase = T.nt * BN + h * HALF;
+                const bool full = nbase + HALF <= p.N;
+                int32_t *accp = p.part ? p.part + (size_t)T.split * p.M * p.N : p.acc;
+                const bool vec_acc = p.part ? p.vec_part : p.vec_out;
+                if (accp) {
+                    int32_t *dst = accp + (size_t)row * p.N + nbase;
+                    if (full && vec_acc) {
 #pragma unroll
-                    for (int i = 0; i < HALF; i += 8) {
-                        uint32_t o[4];
+                        for (int i = 0; i < HALF; i += 4)
+                            *reinterpret_cast<int4 *>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                    } else {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const __nv_bfloat16 lo = epilogue_bf16(acc[i + 2 * j], xs, p.cs[nbase + i + 2 * j]);
-                            const __nv_bfloat16 hi =
-                                epilogue_bf16(acc[i + 2 * j + 1], xs, p.cs[nbase + i + 2 * j + 1]);
-                            o[j] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
+                        for (int i = 0; i < HALF; ++i)
+                            if (nbase + i < p.N)
+                                dst[i] = acc[i];
                     }
                 } else {
+                    const float xs = p.xscale[row];
+                    __nv_bfloat16 *dst = p.out + (size_t)row * p.N + nbase;
+                    if (full && p.vec_out) {
 #pragma unroll
-                    for (int i = 0; i < HALF; ++i)
-                        if (nbase + i < p.N)
-                            dst[i] = epilogue_bf16(acc[i], xs, p.cs[nbase + i]);
+                        for (int i = 0; i < HALF; i += 8) {
+                            uint32_t o[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const __nv_bfloat16 lo = epilogue_bf16(acc[i + 2 * j], xs, p.cs[nbase + i + 2 * j]);
+                                const __nv_bfloat16 hi =
+                                    epilogue_bf16(acc[i + 2 * j + 1], xs, p.cs[nbase + i + 2 * j + 1]);
+                                o[j] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+                            }
+                            *reinterpret_cast<uint4 *>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < HALF; ++i)
+                            if (nbase + i < p.N)
+                                dst[i] = epilogue_bf16(acc[i], xs, p.cs[nbase + i]);
+                    }
                 }
             }
         }
@@ -469,23 +498,35 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
 }
 
-// int8 codes -> bf16 (exact), the tensor-core A operand.
+// int8 codes -> bf16 (exact), the tensor-core A operand.  Two 16-byte loads in
+// flight per thread and iteration.
+__device__ __forceinline__ void codes16_to_bf16(uint4 v, uint4 *dst)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int b0 = (int8_t)(w[j] & 0xFF), b1 = (int8_t)((w[j] >> 8) & 0xFF);
+        const int b2 = (int8_t)((w[j] >> 16) & 0xFF), b3 = (int8_t)(w[j] >> 24);
+        o[2 * j] = bf16_bits_of(b0) | (bf16_bits_of(b1) << 16);
+        o[2 * j + 1] = bf16_bits_of(b2) | (bf16_bits_of(b3) << 16);
+    }
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 __global__ void codes_to_bf16_kernel(const int8_t *__restrict__ xq, __nv_bfloat16 *__restrict__ a, long n16)
 {
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (long)gridDim.x * blockDim.x) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xq) + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int b0 = (int8_t)(w[j] & 0xFF), b1 = (int8_t)((w[j] >> 8) & 0xFF);
-            const int b2 = (int8_t)((w[j] >> 16) & 0xFF), b3 = (int8_t)(w[j] >> 24);
-            o[2 * j] = bf16_bits_of(b0) | (bf16_bits_of(b1) << 16);
-            o[2 * j + 1] = bf16_bits_of(b2) | (bf16_bits_of(b3) << 16);
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(a) + 2 * i;
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    const uint4 *src = reinterpret_cast<const uint4 *>(xq);
+    uint4 *dst = reinterpret_cast<uint4 *>(a);
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += 2 * stride) {
+        const uint4 v0 = __ldg(src + i);
+        const bool two = i + stride < n16;
+        const uint4 v1 = two ? __ldg(src + i + stride) : make_uint4(0u, 0u, 0u, 0u);
+        codes16_to_bf16(v0, dst + 2 * i);
+        if (two)
+            codes16_to_bf16(v1, dst + 2 * (i + stride));
     }
 }
 
@@ -644,9 +685,9 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream
         after_act + (nsplit > 1 ? align256((size_t)nsplit * a.M * a.N * 4) : 0));
     const long n16 = (long)a.M * a.K / 16;
     const int sms = device_sm_count();
-    int cgrid = (int)((n16 + 255) / 256);
-    if (cgrid > sms * 8)
-        cgrid = sms * 8;
+    int cgrid = (int)((n16 + 511) / 512);
+    if (cgrid > sms * 16)
+        cgrid = sms * 16;
     tc::codes_to_bf16_kernel<<<cgrid, 256, 0, stream>>>(a.xq, act, n16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -710,9 +751,10 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream
     p.kb_per_split = kbps;
     p.part = part;
     p.vec_part = (a.N & 3) == 0;
-    const long ctas = (long)((a.M + BM - 1) / BM) * (long)((G + GROUPS - 1) / GROUPS) * nsplit;
-    if (ctas > 0x7FFFFFFFL)
+    const long tiles = (long)((a.M + BM - 1) / BM) * (long)((G + GROUPS - 1) / GROUPS) * nsplit;
+    if (tiles > 0x7FFFFFFFL)
         return cudaErrorInvalidValue;
+    const long ctas = tiles < sms ? tiles : sms;   // persistent CTAs walk the tiles
     if (pre)
         tc::prefill_kernel<true><<<(unsigned)ctas, THREADS, smem_bytes, stream>>>(tm_act, tm_pk, p);
     else
