@@ -243,6 +243,29 @@ def group_bytes(names, M=1):
     return total + sum(2 * M * ACT_K[a] + 4 * M for a in acts)
 
 
+def rank_env():
+    """(world, rank, local rank) from the torchrun environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(torch, value, device, world):
+    """The largest per-rank step time: every rank runs its own replica of the
+    step (no exchange on the data path), so the job is as slow as its slowest
+    rank.  Collective only when more than one rank runs."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, ms_step, bytes_per_step=LAYER_WEIGHT_BYTES):
+    """Whole-job weight GB/s: every rank streams its own copy of the layer per
+    step (weak scaling), over the slowest rank's step time."""
+    return world * bytes_per_step / (ms_step * 1e-3) / 1e9
+
+
 def capture(torch, stream, fn):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -263,9 +286,7 @@ def gpu_arm(args):
 
     import s3d8_a8_linear_gb300 as s3d8
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
@@ -353,12 +374,8 @@ def gpu_arm(args):
         launch_bytes = [group_bytes([n for n, _, _ in si.LLAMA_11B_LAYER])] * len(launch_ms)
     status = s3d8.device_status()
 
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-
-    value = world * LAYER_WEIGHT_BYTES / (ms_step * 1e-3) / 1e9
+    ms_step = max_over_ranks(torch, ms_step, dev, world)
+    value = job_value(world, ms_step)
     hbm_peak, _, peak_kind = load_peaks()
     # The timed region runs nothing but the grouped kernel, one launch per step, so
     # its average launch duration there is the region's event time / launches.

@@ -63,12 +63,13 @@ typedef enum {
     S3D8_ERR_WORKSPACE = -6    /* workspace missing or smaller than required      */
 } s3d8_status;
 
-/* Algorithm choice for s3d8_linear_ex.  AUTO picks by M. */
+/* Algorithm choice for s3d8_linear_ex.  AUTO picks by M: GEMV up to 8 tokens,
+ * SKINNY for 9..16, TC from 17. */
 typedef enum {
     S3D8_ALGO_AUTO = 0,
-    S3D8_ALGO_GEMV = 1,    /* CUDA-core decode + dp4a GEMV, weights streamed once per 8 tokens */
-    S3D8_ALGO_SKINNY = 2,  /* decode in registers + mma.sync s8 (M up to a few hundred)       */
-    S3D8_ALGO_TC = 3       /* tcgen05 bf16 tensor-core GEMM with exact chunked int32 sums      */
+    S3D8_ALGO_GEMV = 1,    /* CUDA-core table decode + dp4a; bulk-copy rings up to 8 tokens      */
+    S3D8_ALGO_SKINNY = 2,  /* table decode into mma.sync bf16 register fragments, 1..32 tokens   */
+    S3D8_ALGO_TC = 3       /* tcgen05 bf16 tensor-core GEMM with exact chunked int32 sums       */
 } s3d8_algo;
 
 /*

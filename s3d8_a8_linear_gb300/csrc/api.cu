@@ -124,16 +124,20 @@ int s3d8_decode(const uint8_t *packed, const int8_t *centroids, int64_t N, int64
                                      static_cast<cudaStream_t>(stream)));
 }
 
-// The algorithm AUTO runs: the bulk-copy GEMV up to 8 tokens, the tensor-core
-// GEMM from kTcMinM tokens.
-constexpr int64_t kTcMinM = 9;
+// The algorithm AUTO runs (measured on GB300 on the 11B gate/up and down shapes):
+// the bulk-copy dp4a GEMV up to 8 tokens, the register-fragment mma.sync path
+// from 9 to 16 tokens, the tcgen05 GEMM from 17 tokens.
+constexpr int64_t kSkinnyMinM = 9;
+constexpr int64_t kTcMinM = 17;
 
 static int resolve_algo(int64_t M, int64_t K, int algo)
 {
     (void)K;
     if (algo != S3D8_ALGO_AUTO)
         return algo;
-    return M >= kTcMinM ? S3D8_ALGO_TC : S3D8_ALGO_GEMV;
+    if (M >= kTcMinM)
+        return S3D8_ALGO_TC;
+    return M >= kSkinnyMinM ? S3D8_ALGO_SKINNY : S3D8_ALGO_GEMV;
 }
 
 size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo)
@@ -141,7 +145,12 @@ size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo)
     (void)N;
     if (M <= 0 || K <= 0 || M > S3D8_MAX_M || K > S3D8_MAX_K)
         return 0;
-    return resolve_algo(M, K, algo) == S3D8_ALGO_TC ? prefill_workspace_bytes((int)M, (int)N, (int)K, prefill_predecode((int)M)) : 0;
+    const int r = resolve_algo(M, K, algo);
+    if (r == S3D8_ALGO_TC)
+        return prefill_workspace_bytes((int)M, (int)N, (int)K, prefill_predecode((int)M));
+    if (r == S3D8_ALGO_SKINNY && skinny_supported((int)M))
+        return skinny_workspace_bytes((int)M, (int)N, (int)K);
+    return 0;
 }
 
 static int linear_common(const uint8_t *packed, const int8_t *centroids, const void *chan_scale,
@@ -175,7 +184,7 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     if (need > 0 && (!workspace || workspace_bytes < need))
         return S3D8_ERR_WORKSPACE;
     algo = resolve_algo(M, K, algo);
-    if (algo != S3D8_ALGO_GEMV && algo != S3D8_ALGO_TC)
+    if (algo == S3D8_ALGO_SKINNY && !skinny_supported((int)M))
         return S3D8_ERR_UNSUPPORTED;
 
     LinearArgs a;
@@ -195,6 +204,8 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     if (algo == S3D8_ALGO_TC)
         return cuda_status(launch_prefill_tc(a, prefill_predecode(a.M), strm));
+    if (algo == S3D8_ALGO_SKINNY)
+        return cuda_status(launch_skinny(a, strm));
     if (gemv_tma_supported(a.M, a.K))
         return cuda_status(launch_gemv_tma(a, strm));
     return cuda_status(launch_gemv(a, strm));

@@ -48,6 +48,7 @@ struct GroupArgs {
 };
 
 int device_sm_count();
+void *tensor_map_encoder_fn();   // cuTensorMapEncodeTiled, or nullptr
 int *device_status_ptr();   // this device's sticky status word, or nullptr
 
 cudaError_t launch_quantize_act(const __nv_bfloat16 *x, int M, int K, int8_t *xq, float *xscale,
@@ -66,5 +67,12 @@ cudaError_t launch_gemv_tma(const LinearArgs &a, cudaStream_t stream);
 bool prefill_predecode(int M);
 size_t prefill_workspace_bytes(int M, int N, int K, bool pre);
 cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream);
+// Split-K finish shared by the tensor-core and skinny paths: sums int32 partials
+// [nsplit][M][N] into a.out (epilogue) or a.acc.
+cudaError_t launch_splitk_finalize(const int32_t *part, int nsplit, const LinearArgs &a, cudaStream_t stream);
+// mma.sync path for a few tokens (1..32), weights decoded into register fragments.
+bool skinny_supported(int M);
+size_t skinny_workspace_bytes(int M, int N, int K);
+cudaError_t launch_skinny(const LinearArgs &a, cudaStream_t stream);
 
 }  // namespace s3d8

@@ -654,16 +654,34 @@ size_t prefill_workspace_bytes(int M, int N, int K, bool pre)
     return bytes;
 }
 
+cudaError_t launch_splitk_finalize(const int32_t *part, int nsplit, const LinearArgs &a, cudaStream_t stream)
+{
+    const size_t plane = (size_t)a.M * a.N;
+    long fgrid = (long)((plane + 255) / 256);
+    if (fgrid > (long)device_sm_count() * 16)
+        fgrid = (long)device_sm_count() * 16;
+    tc::finalize_kernel<<<(unsigned)fgrid, 256, 0, stream>>>(part, nsplit, a.M, a.N, a.xscale, a.cs, a.out, a.acc);
+    return cudaGetLastError();
+}
+
+void *tensor_map_encoder_fn();
+
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder_fn());
+}
+
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime.
+void *tensor_map_encoder_fn()
+{
+    static void *fn = nullptr;
     if (!fn) {
         cudaDriverEntryPointQueryResult q;
         void *f = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+            fn = f;
     }
     return fn;
 }
@@ -762,13 +780,7 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream
     e = cudaGetLastError();
     if (e != cudaSuccess || nsplit == 1)
         return e;
-    const size_t plane = (size_t)a.M * a.N;
-    long fgrid = (long)((plane + 255) / 256);
-    if (fgrid > (long)sms * 16)
-        fgrid = (long)sms * 16;
-    tc::finalize_kernel<<<(unsigned)fgrid, 256, 0, stream>>>(part, nsplit, a.M, a.N, a.xscale, a.cs, a.out,
-                                                             a.acc);
-    return cudaGetLastError();
+    return launch_splitk_finalize(part, nsplit, a, stream);
 }
 
 }  // namespace s3d8
