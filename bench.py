@@ -50,6 +50,7 @@ import s3d8_inputs as si  # noqa: E402
 METRIC = "S3D8 linear weight GB/s (M=1) & INT8 TOPS (prefill), % of roofline"
 UNIT = "GB/s"
 COPIES = 8
+GRAPH_ROUNDS = 8
 WORKLOAD = ("Llama-3.2-11B text decoder layer, decode M=1: S3D8 linears q 4096->4096, "
             "k/v 4096->1024, o 4096->4096, gate/up 4096->14336, down 14336->4096")
 
@@ -308,18 +309,22 @@ def gpu_arm(args):
     # One graph holds the COPIES consecutive steps (one per weight copy), the way a
     # decode loop captures its layers; consecutive launches inside it overlap
     # through programmatic dependent launch.  Single-step graphs cover the rest.
-    def run_all(mode):
-        for r in range(COPIES):
-            step.run(s3d8, copies[r], mode)
+    def run_all(mode, rounds):
+        for _ in range(rounds):
+            for r in range(COPIES):
+                step.run(s3d8, copies[r], mode)
 
-    multi = {mode: capture(torch, stream, lambda mode=mode: run_all(mode))
+    # The headline graph holds GRAPH_ROUNDS passes over the copies (64 steps), so
+    # that graph boundaries (where consecutive launches cannot overlap) are rare.
+    multi = {mode: capture(torch, stream, lambda mode=mode: run_all(mode, GRAPH_ROUNDS if mode == "group1" else 1))
              for mode in ("group1", "group4", "separate")}
+    per_graph = {mode: COPIES * (GRAPH_ROUNDS if mode == "group1" else 1) for mode in multi}
     single = [capture(torch, stream, lambda r=r: step.run(s3d8, copies[r], "group1"))
               for r in range(COPIES)]
     torch.cuda.synchronize()
 
     def replay_steps(mode, steps):
-        full, rest = divmod(steps, COPIES)
+        full, rest = divmod(steps, per_graph[mode])
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -327,7 +332,7 @@ def gpu_arm(args):
             for _ in range(full):
                 multi[mode].replay()
             for r in range(rest):
-                single[r].replay()
+                single[r % COPIES].replay()
             t1.record(stream)
         t1.synchronize()
         return t0.elapsed_time(t1) / steps
@@ -416,9 +421,9 @@ def gpu_arm(args):
                    "l2": f"inputs larger than L2: {COPIES} rotating layer copies "
                          f"({COPIES * LAYER_WEIGHT_BYTES / 1e6:.0f} MB of weights)",
                    "launch": "one grouped launch per step (7 projections, activation "
-                             "quantisation fused); the 8 rotating steps captured in one CUDA "
-                             "graph, consecutive launches overlapping by programmatic "
-                             "dependent launch",
+                             "quantisation fused); 64 consecutive steps (8 passes over the 8 "
+                             "rotating copies) captured in one CUDA graph, consecutive launches "
+                             "overlapping by programmatic dependent launch",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": args.steps * n_launches("group1"),
         "device_status": status,
