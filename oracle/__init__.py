@@ -66,6 +66,8 @@ def lib():
         L.s3d8o_linear_acc_at.argtypes = [P, P, P, I64, I64, I64, P, P, I64, P]
         L.s3d8o_linear_acc_at.restype = None
         L.s3d8o_linear_out.argtypes = [P, P, P, I64, I64, P]
+        L.s3d8o_encode.argtypes = [P, P, I64, I64, P, P]
+        L.s3d8o_encode.restype = I32
         L.s3d8o_linear_out.restype = None
     return _lib
 
@@ -183,3 +185,17 @@ def linear(packed, C, chan_scale_bits, xq, xscale, N: int):
     acc, bad = linear_acc(packed, C, xq, N)
     assert bad == 0, "accumulator outside int32"
     return linear_out(acc, xscale, chan_scale_bits), acc
+
+
+def encode(w_bf16_bits: np.ndarray, C: np.ndarray):
+    """Direct-cast encoder: bf16 weights [N, K] and a 32x3 table -> (packed
+    [ceil(N/3), K] uint8, chan_scale [N] bf16 bits).  Paper section 3.4,
+    "Quantization" (forward pass with frozen centroids)."""
+    w = _as(w_bf16_bits, np.uint16)
+    N, K = w.shape
+    C = _as(C, np.int8, (32, 3))
+    packed = np.empty((groups(N), K), np.uint8)
+    cs = np.empty((N,), np.uint16)
+    if lib().s3d8o_encode(_ptr(w), _ptr(C), N, K, _ptr(packed), _ptr(cs)) != 0:
+        raise MemoryError("oracle encoder scratch")
+    return packed, cs

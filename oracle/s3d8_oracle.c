@@ -29,7 +29,12 @@
  *     round-half-even(x / s) clamped to [-127, 127]; an all-zero row gives
  *     s = 0 and q = 0;
  *   - output: out[m,n] = xscale[m] * acc[m,n] * chan_scale[n], evaluated here
- *     in fp64 (the GPU evaluates it in fp32 and rounds once to bf16).
+ *     in fp64 (the GPU evaluates it in fp32 and rounds once to bf16);
+ *   - direct-cast encoder ([P] section 3.4 "Quantization", the forward-pass
+ *     assignment with frozen centroids): alpha is rounded to bf16 (the stored
+ *     scale) and the scaled magnitudes divide by that stored value; the
+ *     squared distances are fp32 sums in the order d = 0, 1, 2, so that the
+ *     GPU can take every argmin decision in the same arithmetic.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math, no
  * FMA contraction, so that the fp32 activation quantiser is plain IEEE
@@ -37,6 +42,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* bfloat16 is the upper half of an IEEE binary32; widening is exact. */
@@ -195,4 +201,85 @@ void s3d8o_linear_out(const int64_t *acc, const float *xscale, const uint16_t *c
         for (int64_t n = 0; n < N; ++n)
             out[m * N + n] = (double)xscale[m] * (double)acc[m * N + n] *
                              (double)bf16_bits_to_float(chan_scale[n]);
+}
+
+
+/* ---------------------------------------------------------------------------
+ * Direct-cast encoder, [P] section 3.4 "Quantization" (forward pass with the
+ * centroids frozen).  w is bf16 bit patterns [N, K], row-major.
+ *   alpha_n = max_k |W_nk| / 127 (fp32 division), stored as bf16 (round to
+ *             nearest even): chan_scale[n];
+ *   W'_{g,k,d} = |W_{3g+d,k}| / alpha_{3g+d}, with the stored alpha, in fp32;
+ *             0 when that alpha is 0 and for the padded channels 3g+d >= N;
+ *   s = +1 for W >= 0 (selector 0), -1 otherwise (selector 1); padded: 0;
+ *   q = argmin over l of ((C[l][0] - W'_0)^2 + (C[l][1] - W'_1)^2)
+ *       + (C[l][2] - W'_2)^2, each operation rounded in fp32, the lowest
+ *       index winning a tie.
+ * packed is [ceil(N/3), K]; the byte follows [B] "Bit layout".
+ * ------------------------------------------------------------------------- */
+static uint16_t float_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+static float centroid_dist2(const int8_t *Crow, const float *wp)
+{
+    float t0 = (float)Crow[0] - wp[0];
+    float t1 = (float)Crow[1] - wp[1];
+    float t2 = (float)Crow[2] - wp[2];
+    float s = t0 * t0;
+    s = s + t1 * t1;
+    s = s + t2 * t2;
+    return s;
+}
+
+/* Returns 0, or -1 when the scratch for the scales cannot be allocated. */
+int32_t s3d8o_encode(const uint16_t *w, const int8_t *C, int64_t N, int64_t K, uint8_t *packed,
+                     uint16_t *chan_scale)
+{
+    float *alpha = (float *)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+    if (!alpha)
+        return -1;
+    for (int64_t n = 0; n < N; ++n) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(bf16_bits_to_float(w[n * K + k]));
+            if (a > amax)
+                amax = a;
+        }
+        chan_scale[n] = float_to_bf16_rne(amax / 127.0f);
+        alpha[n] = bf16_bits_to_float(chan_scale[n]);
+    }
+    const int64_t G = (N + 2) / 3;
+    for (int64_t g = 0; g < G; ++g)
+        for (int64_t k = 0; k < K; ++k) {
+            float wp[3];
+            int32_t sel[3];
+            for (int d = 0; d < 3; ++d) {
+                const int64_t n = 3 * g + d;
+                wp[d] = 0.0f;
+                sel[d] = 0;
+                if (n < N) {
+                    const float v = bf16_bits_to_float(w[n * K + k]);
+                    sel[d] = (v >= 0.0f) ? 0 : 1;
+                    if (alpha[n] != 0.0f)
+                        wp[d] = fabsf(v) / alpha[n];
+                }
+            }
+            int32_t best = 0;
+            float bestd = centroid_dist2(C, wp);
+            for (int32_t l = 1; l < 32; ++l) {
+                const float dl = centroid_dist2(C + 3 * l, wp);
+                if (dl < bestd) {
+                    bestd = dl;
+                    best = l;
+                }
+            }
+            packed[g * K + k] = s3d8o_pack_byte(best, sel[0], sel[1], sel[2]);
+        }
+    free(alpha);
+    return 0;
 }

@@ -347,3 +347,162 @@ def test_input_bf16_conversion_matches_torch():
     f = (rng.standard_normal(4096) * np.exp(rng.uniform(-30, 30, 4096))).astype(np.float32)
     want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(si.f32_to_bf16_bits(f), want)
+
+
+# --------------------------------------------------------------------------
+# Direct-cast encoder (Llama-Mobile paper, section 3.4 "Quantization":
+# alpha = absmax / 127, s = sign with W >= 0 positive, q = nearest centroid of
+# |W| / alpha in L2, the lowest index winning a tie)
+# --------------------------------------------------------------------------
+
+def _bf16_exact(vals):
+    """float -> bf16 bits for values that bf16 holds exactly."""
+    a = np.asarray(vals, np.float32)
+    b = si.f32_to_bf16_bits(a)
+    assert np.array_equal(si.bf16_bits_to_f32(b), a)
+    return b
+
+
+def test_encode_hand_worked_case():
+    # Hand table: C[q] = (4q+1, 4q+2, 4q+3).  Both columns scaled by 1/64, and
+    # every row holds a +-127/64, so alpha = 1/64 exactly for the three rows.
+    #  column 0: (125, -126, 127) is centroid 31 itself, signs (+, -, +);
+    #  column 1: (127, 127, 1) in magnitude, signs (-, +, -).  With
+    #    f(q) = (4q - 126)^2 + (4q - 125)^2 + (4q + 2)^2:
+    #    f(20) = 2116 + 2025 + 6724 = 10865, f(21) = 1764 + 1681 + 7396 = 10841,
+    #    f(22) = 1444 + 1369 + 8100 = 10913, and f is a parabola in q: q = 21.
+    C = hand_table()
+    w = _bf16_exact(np.array([[125, -127], [-126, 127], [127, -1]], np.float32) / 64)
+    packed, cs = oracle.encode(w, C)
+    assert np.array_equal(si.bf16_bits_to_f32(cs), np.full(3, 1 / 64, np.float32))
+    # fields by the pages' layout: S0 is w0's sign, S1 w1's sign, S2 w2's sign
+    assert oracle.byte_fields(int(packed[0, 0])) == (31, 0, 1, 0)
+    assert oracle.byte_fields(int(packed[0, 1])) == (21, 1, 0, 1)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_encode_roundtrips_exactly_representable_weights(seed):
+    # W = s * C[q] * alpha with alpha a power of two and one column that holds
+    # 127 * alpha in every row, so |W| / alpha is C[q] exactly: distance 0 and,
+    # with all-distinct table rows, the only nearest centroid.
+    rng = np.random.default_rng(seed)
+    C = rng.permutation(np.arange(1, 97)).reshape(32, 3).astype(np.int8)
+    C[31] = 127                                   # centroid 31 = (127, 127, 127)
+    N, K = 3 * 5, 40
+    Q = rng.integers(0, 32, size=(N // 3, K))
+    Q[:, 0] = 31
+    S = rng.integers(0, 2, size=(N, K))
+    alpha = 2.0 ** rng.integers(-12, -4, size=N)
+    W = np.zeros((N, K))
+    for n in range(N):
+        W[n] = (1 - 2 * S[n]) * C[Q[n // 3], n % 3] * alpha[n]
+    packed, cs = oracle.encode(_bf16_exact(W), C)
+    assert np.array_equal(si.bf16_bits_to_f32(cs).astype(np.float64), alpha)
+    # decode by the pages' own signed-table construction, independent of the oracle
+    assert np.array_equal(dense_by_pages_lut(packed, C, N), (1 - 2 * S) * C[Q.repeat(3, 0), np.tile([0, 1, 2], N // 3)[:, None]])
+
+
+def test_encode_tie_goes_to_lowest_index():
+    C = hand_table()
+    C[9] = C[4]                                   # a duplicate row later in the table
+    C[20] = C[4]
+    w = _bf16_exact(np.array([[17, 127], [18, 127], [19, 127]], np.float32))   # alpha = 1, C[4]
+    packed, _ = oracle.encode(w, C)
+    assert oracle.byte_fields(int(packed[0, 0]))[0] == 4
+    # a point exactly halfway between two centroids on one axis
+    C = np.zeros((32, 3), np.int8)
+    C[:, 0] = np.arange(32) * 4
+    w = _bf16_exact(np.array([[42, 127], [0, 0], [0, 0]], np.float32))     # 42: midway 40 / 44
+    packed, _ = oracle.encode(w, C)
+    assert oracle.byte_fields(int(packed[0, 0]))[0] == 10
+
+
+def test_encode_signs_zeros_and_zero_channels():
+    C = hand_table()
+    pz, nz = 0x0000, 0x8000                        # +0 and -0 in bf16
+    w = np.array([[pz, nz, 0x3F80], [nz, pz, 0xBF80], [0, 0, 0]], np.uint16)   # row 2 all zero
+    packed, cs = oracle.encode(w, C)
+    assert cs[2] == 0                              # alpha of an all-zero channel is 0
+    for k in range(3):
+        Q, S0, S1, S2 = oracle.byte_fields(int(packed[0, k]))
+        assert S2 == 0                             # zero channel: positive
+        # -0 >= 0, so both zero forms take the positive selector
+        if k < 2:
+            assert (S0, S1) == (0, 0)
+    assert oracle.byte_fields(int(packed[0, 2]))[1:3] == (0, 1)
+    # a zero group is (0, 0, 0): nearest is the row of least norm, centroid 0 here
+    assert oracle.byte_fields(int(packed[0, 0]))[0] == 0
+
+
+def test_encode_pads_missing_channels_positive_and_zero():
+    C = hand_table()
+    rng = np.random.default_rng(7)
+    for N in (1, 2, 4, 5):
+        W = si.f32_to_bf16_bits(rng.standard_normal((N, 16)).astype(np.float32))
+        packed, cs = oracle.encode(W, C)
+        assert packed.shape == (si.groups(N), 16) and cs.shape == (N,)
+        g = (N - 1) // 3
+        for k in range(16):
+            f = oracle.byte_fields(int(packed[g, k]))
+            for d in range(N - 3 * g, 3):
+                assert f[1 + d] == 0
+        # the padded components enter the distance as 0
+        Cf = C.astype(np.float64)
+        csf = si.bf16_bits_to_f32(cs).astype(np.float64)
+        Wf = si.bf16_bits_to_f32(W).astype(np.float64)
+        for k in range(16):
+            wp = np.zeros(3)
+            for d in range(N - 3 * g):
+                wp[d] = abs(Wf[3 * g + d, k]) / csf[3 * g + d]
+            dist = ((Cf - wp) ** 2).sum(1)
+            q = oracle.byte_fields(int(packed[g, k]))[0]
+            assert dist[q] <= dist.min() * (1 + 1e-5) + 1e-3
+
+
+@pytest.mark.parametrize("N,K,seed", [(12, 64, 0), (7, 33, 1), (30, 16, 2)])
+def test_encode_picks_a_nearest_centroid_and_the_right_scales(N, K, seed):
+    rng = np.random.default_rng(seed)
+    C = si.centroids(rng)
+    Wf32 = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    Wf32[0, 3] = 0.25                              # an outlier channel
+    W = si.f32_to_bf16_bits(Wf32)
+    Wf = si.bf16_bits_to_f32(W).astype(np.float64)
+    packed, cs = oracle.encode(W, C)
+    alpha = si.bf16_bits_to_f32(cs).astype(np.float64)
+    amax = np.abs(Wf).max(1)
+    # alpha is absmax / 127 to bf16 precision (8 significant bits)
+    assert np.all(np.abs(127 * alpha - amax) <= amax * 2.0 ** -8)
+    # decoded signs follow the weights' signs; magnitudes are the chosen centroid
+    dense = dense_by_pages_lut(packed, C, N)
+    G = si.groups(N)
+    Cf = C.astype(np.float64)
+    for g in range(G):
+        ch = [3 * g + d for d in range(3) if 3 * g + d < N]
+        for k in range(K):
+            q = oracle.byte_fields(int(packed[g, k]))[0]
+            wp = np.zeros(3)
+            for d, n in enumerate(ch):
+                wp[d] = abs(Wf[n, k]) / alpha[n]
+                assert dense[n, k] == (C[q, d] if Wf[n, k] >= 0 else -int(C[q, d]))
+            dist = ((Cf - wp) ** 2).sum(1)
+            # the fp32 decision may differ from exact arithmetic only within rounding
+            assert dist[q] <= dist.min() * (1 + 1e-5) + 1e-3
+            # and no centroid before q is strictly nearer by more than rounding
+            assert np.all(dist[:q] >= dist[q] - (dist[q] * 1e-5 + 1e-3))
+
+
+def test_encode_then_decode_is_a_fixed_point():
+    # Encoding the decoded weights s * alpha * C[q] (exactly representable when
+    # alpha is a power of two and a channel holds 127) gives the same bytes back.
+    rng = np.random.default_rng(3)
+    C = si.centroids(rng)
+    C[0] = 127
+    N, K = 9, 24
+    packed = si.packed_bytes(rng, si.groups(N), K)
+    packed[:, 0] = oracle.pack_byte(0, 0, 0, 0)
+    dense = dense_by_pages_lut(packed, C, N).astype(np.float64)
+    assert len({tuple(r) for r in C.tolist()}) == 32     # the nearest centroid is unique
+    W = _bf16_exact(dense * 2.0 ** -9)
+    again, cs = oracle.encode(W, C)
+    assert np.all(si.bf16_bits_to_f32(cs) == np.float32(2.0 ** -9))
+    assert np.array_equal(again, packed)
