@@ -400,13 +400,14 @@ def gpu_arm(args):
         roofline["isolated_launch_us"] = round(iso_ms * 1e3, 3)
         roofline["isolated_achieved"] = round(step_bytes / (iso_ms * 1e-3) / 1e9, 1)
 
-    e2e = prefill = unpack = sweep = stack = None
+    e2e = prefill = unpack = sweep = stack = encode = None
     if not args.layer_only:
         e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 4000))
         prefill = prefill_measure(torch, s3d8, dev) if not args.skip_prefill else None
         unpack = unpack_measure(torch, s3d8, dev)
         sweep = decode_sweep_measure(torch, s3d8, dev)
         stack = stack_measure(torch, s3d8, dev)
+        encode = encode_measure(torch, s3d8, dev)
 
     if rank != 0:
         return
@@ -429,7 +430,7 @@ def gpu_arm(args):
         "device_status": status,
         "roofline": roofline, "variants": variants, "e2e": e2e, "prefill": prefill,
         "decode_sweep": sweep, "text_stack": stack,
-        "unpack": unpack, "clocks": clocks, "cpu_baseline": cpu,
+        "unpack": unpack, "encode": encode, "clocks": clocks, "cpu_baseline": cpu,
     }
     print(json.dumps(line))
 
@@ -632,6 +633,46 @@ def unpack_measure(torch, s3d8, dev, reps=20):
     return {"shape": "4096x14336 (gate)", "us": round(ms * 1e3, 2),
             "read_gbs": round(rd / (ms * 1e-3) / 1e9, 1),
             "total_gbs": round((rd + N * K) / (ms * 1e-3) / 1e9, 1)}
+
+
+def encode_measure(torch, s3d8, dev, reps=3):
+    """Direct-cast encoder over the seven matrices of one 11B decoder layer
+    (218 M bf16 weights, 436 MB, larger than L2), weights N(0, 0.02) drawn on
+    the device.  Algorithmic traffic: the bf16 weights once, the packed bytes
+    and the scales written once; the fp32 work is 32 three-component squared
+    distances (8 operations each) per packed byte."""
+    gen = torch.Generator(device=dev).manual_seed(9)
+    mats = []
+    for name, K, N in si.LLAMA_11B_LAYER:
+        w = (torch.randn((N, K), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        C = torch.randint(1, 128, (32, 3), dtype=torch.int8, device=dev, generator=gen)
+        p = torch.empty((si.groups(N), K), dtype=torch.uint8, device=dev)
+        cs = torch.empty((N,), dtype=torch.bfloat16, device=dev)
+        mats.append((w, C, p, cs))
+    ws = torch.empty((s3d8.ENCODE_WORKSPACE_BYTES,), dtype=torch.uint8, device=dev)
+
+    def run():
+        for w, C, p, cs in mats:
+            s3d8.encode(w, C, p, cs, ws)
+
+    run()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        run()
+    t1.record()
+    t1.synchronize()
+    ms = t0.elapsed_time(t1) / reps
+    params = sum(N * K for _, K, N in si.LLAMA_11B_LAYER)
+    codes = sum(si.groups(N) * K for _, K, N in si.LLAMA_11B_LAYER)
+    nbytes = 2 * params + codes + 2 * sum(N for _, _, N in si.LLAMA_11B_LAYER)
+    return {"workload": "one 11B decoder layer's 7 bf16 matrices -> S3D8", "params": params,
+            "ms": round(ms, 3), "gparams_s": round(params / (ms * 1e-3) / 1e9, 2),
+            "algorithmic_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "fp32_tflops": round(codes * 32 * 8 / (ms * 1e-3) / 1e12, 2),
+            "launches": 2 * len(mats) * reps}
 
 
 # ---------------------------------------------------------------------------

@@ -96,6 +96,42 @@ int s3d8_quantize_act(const void *x_bf16, int64_t M, int64_t K, int8_t *xq, floa
 int s3d8_decode(const uint8_t *packed, const int8_t *centroids, int64_t N, int64_t K, int8_t *w,
                 void *stream);
 
+/*
+ * Direct-cast encoder: bf16 weights -> channel scales and packed S3D8 bytes,
+ * with the centroid table held fixed (paper section 3.4, "Quantization": the
+ * forward assignment; the byte layout of blog section "Bit layout").
+ *   w_bf16     : [N, K] bfloat16, row-major, 16-byte aligned
+ *   centroids  : [32 * 3] int8, row-major C[q][d], values 0..127 (any alignment)
+ *   packed     : [G, K] uint8 output, row-major, 8-byte aligned
+ *   chan_scale : [N] bfloat16 output, 2-byte aligned
+ *   workspace  : device scratch of S3D8_ENCODE_WORKSPACE_BYTES, 16-byte
+ *                aligned, caller-owned, not shared by calls that overlap on
+ *                the GPU (S3D8_ERR_WORKSPACE when missing or smaller)
+ * chan_scale[n] = bf16_rn(max_k |W[n,k]| / 127) (fp32 IEEE division).  For
+ * packed row g and column k, with alpha the stored scale of each channel:
+ * W'_d = |W[3g+d,k]| / alpha (IEEE fp32; 0 when alpha is 0 and for the padded
+ * channels 3g+d >= N); the selector of channel d is 0 (+) where W >= 0,
+ * including -0, and 1 elsewhere (0 for padded channels); Q is the first index
+ * l minimising ((C_l0 - W'_0)^2 + (C_l1 - W'_1)^2) + (C_l2 - W'_2)^2 evaluated
+ * in fp32, every operation rounded to nearest.  Two launches: scales and a
+ * per-call candidate table (in the workspace), then the assignment.
+ */
+#define S3D8_ENCODE_WORKSPACE_BYTES 16384u
+int s3d8_encode(const void *w_bf16, const int8_t *centroids, int64_t N, int64_t K,
+                uint8_t *packed, void *chan_scale_bf16, void *workspace, size_t workspace_bytes,
+                void *stream);
+
+/*
+ * Self-test of the encoder's scaled magnitude: out[i] = |x[i]| / alpha[i]
+ * through the same device code the encoder uses (a correction step on a
+ * per-channel reciprocal, IEEE division outside its range).  Must equal the
+ * IEEE fp32 quotient for every finite x and alpha > 0 with |x| <= 2^20 alpha
+ * (the encoder only meets |x| <= 128 alpha); alpha = 0 gives 0.  x, alpha:
+ * [n] bfloat16; out: [n] fp32.
+ */
+int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t n, float *out,
+                             void *stream);
+
 /* Bytes of device workspace s3d8_linear_ex needs for this shape and algorithm
  * (0 when none).  Host function; the tensor-core algorithm's size depends on
  * the current device's SM count (how far a small M splits K). */

@@ -70,6 +70,8 @@ def load(build_if_missing: bool = False):
     P, I64, SZ, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
     L.s3d8_quantize_act.argtypes = [P, I64, I64, P, P, P]
     L.s3d8_decode.argtypes = [P, P, I64, I64, P, P]
+    L.s3d8_encode.argtypes = [P, P, I64, I64, P, P, P, SZ, P]
+    L.s3d8_selftest_scaled_abs.argtypes = [P, P, I64, P, P]
     L.s3d8_linear_workspace_size.argtypes = [I64, I64, I64, I]
     L.s3d8_linear_workspace_size.restype = SZ
     L.s3d8_linear.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, SZ, P]
@@ -82,7 +84,8 @@ def load(build_if_missing: bool = False):
     L.s3d8_status_string.argtypes = [I]
     L.s3d8_status_string.restype = ctypes.c_char_p
     L.s3d8_version.argtypes = []
-    for fn in ("s3d8_quantize_act", "s3d8_decode", "s3d8_linear", "s3d8_linear_ex",
+    for fn in ("s3d8_quantize_act", "s3d8_decode", "s3d8_encode", "s3d8_selftest_scaled_abs",
+               "s3d8_linear", "s3d8_linear_ex",
                "s3d8_linear_acc_i32", "s3d8_linear_batch", "s3d8_selftest_wait_timeout",
                "s3d8_device_status", "s3d8_version"):
         getattr(L, fn).restype = I
@@ -147,6 +150,44 @@ def decode(packed: torch.Tensor, centroids: torch.Tensor, N: int,
                             _dev(w, "w", torch.int8, (N, K)), _stream(packed.device))
     _check("s3d8_decode", st)
     return w
+
+
+ENCODE_WORKSPACE_BYTES = 16384
+
+
+def encode(w: torch.Tensor, centroids: torch.Tensor, packed: torch.Tensor | None = None,
+           chan_scale: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Direct-cast encoder: bf16 W[N, K] + int8 C[32, 3] -> (packed uint8
+    [ceil(N/3), K], chan_scale bf16 [N])."""
+    if w.dim() != 2:
+        raise ValueError("w must be 2-D [N, K]")
+    N, K = w.shape
+    if packed is None:
+        packed = torch.empty((groups(N), K), dtype=torch.uint8, device=w.device)
+    if chan_scale is None:
+        chan_scale = torch.empty((N,), dtype=torch.bfloat16, device=w.device)
+    if workspace is None:
+        workspace = torch.empty((ENCODE_WORKSPACE_BYTES,), dtype=torch.uint8, device=w.device)
+    st = load().s3d8_encode(_dev(w, "w", torch.bfloat16),
+                            _dev(centroids, "centroids", torch.int8, (32, 3)), N, K,
+                            _dev(packed, "packed", torch.uint8, (groups(N), K)),
+                            _dev(chan_scale, "chan_scale", torch.bfloat16, (N,)),
+                            _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                            _stream(w.device))
+    _check("s3d8_encode", st)
+    return packed, chan_scale
+
+
+def selftest_scaled_abs(x: torch.Tensor, alpha: torch.Tensor) -> torch.Tensor:
+    """|x| / alpha elementwise (bf16 inputs, fp32 result) through the encoder's
+    device code; for checking it against IEEE division."""
+    n = x.numel()
+    out = torch.empty((n,), dtype=torch.float32, device=x.device)
+    st = load().s3d8_selftest_scaled_abs(_dev(x, "x", torch.bfloat16),
+                                         _dev(alpha, "alpha", torch.bfloat16, tuple(x.shape)), n,
+                                         _dev(out, "out", torch.float32), _stream(x.device))
+    _check("s3d8_selftest_scaled_abs", st)
+    return out
 
 
 def workspace_size(M: int, N: int, K: int, algo: int = ALGO_AUTO) -> int:

@@ -124,6 +124,46 @@ int s3d8_decode(const uint8_t *packed, const int8_t *centroids, int64_t N, int64
                                      static_cast<cudaStream_t>(stream)));
 }
 
+int s3d8_encode(const void *w_bf16, const int8_t *centroids, int64_t N, int64_t K,
+                uint8_t *packed, void *chan_scale_bf16, void *workspace, size_t workspace_bytes,
+                void *stream)
+{
+    int st = check_k(K);
+    if (st == S3D8_OK)
+        st = check_mn(0, N);
+    if (st != S3D8_OK)
+        return st;
+    if (N == 0)
+        return S3D8_OK;
+    if (!w_bf16 || !centroids || !packed || !chan_scale_bf16)
+        return S3D8_ERR_INVALID_ARG;
+    if (!aligned(w_bf16, 16) || !aligned(packed, 8) || !aligned(chan_scale_bf16, 2))
+        return S3D8_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < S3D8_ENCODE_WORKSPACE_BYTES)
+        return S3D8_ERR_WORKSPACE;
+    if (!aligned(workspace, 16))
+        return S3D8_ERR_ALIGNMENT;
+    return cuda_status(launch_encode(static_cast<const __nv_bfloat16 *>(w_bf16), centroids, (int)N,
+                                     (int)K, packed, static_cast<__nv_bfloat16 *>(chan_scale_bf16),
+                                     workspace, static_cast<cudaStream_t>(stream)));
+}
+
+int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t n, float *out,
+                             void *stream)
+{
+    if (n < 0)
+        return S3D8_ERR_INVALID_ARG;
+    if (n == 0)
+        return S3D8_OK;
+    if (!x_bf16 || !alpha_bf16 || !out)
+        return S3D8_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 2) || !aligned(alpha_bf16, 2) || !aligned(out, 4))
+        return S3D8_ERR_ALIGNMENT;
+    return cuda_status(launch_selftest_scaled_abs(static_cast<const __nv_bfloat16 *>(x_bf16),
+                                                  static_cast<const __nv_bfloat16 *>(alpha_bf16),
+                                                  n, out, static_cast<cudaStream_t>(stream)));
+}
+
 // The algorithm AUTO runs (measured on GB300 on the 11B gate/up and down shapes):
 // the bulk-copy dp4a GEMV up to 8 tokens, the register-fragment mma.sync path
 // from 9 to 16 tokens, the tcgen05 GEMM from 17 tokens.

@@ -1,0 +1,356 @@
+// Direct-cast encoder: bf16 weights W[N, K] and a fixed 32 x 3 centroid table
+// -> per-channel bf16 scales and packed S3D8 bytes [ceil(N/3), K].
+//
+// Llama-Mobile: Efficient 2.7-Bit Quantization of VLMs, section 3.4
+// "Quantization" (the forward assignment with frozen centroids):
+//   alpha_n = max_k |W[n,k]| / 127                      -> stored as bf16
+//   W'      = |W| / alpha (the stored alpha), per 3-vector of channels 3g..3g+2
+//   s       = + where W >= 0, - elsewhere
+//   q       = the nearest centroid to W' in L2, the lowest index on a tie.
+// The byte follows "11 billion parameters on a phone" (Graphcore Research
+// blog), section "Bit layout": bit 0 = S0, bits 1..5 = Q, bit 6 = S1,
+// bit 7 = S2 xor S0.
+//
+// Every decision is taken in fp32 with IEEE rounding and no contraction: the
+// division, then t_d = C_d - W'_d, then ((t0 t0 + t1 t1) + t2 t2), compared
+// with "<" in index order.  Padded channels (3g + d >= N) enter as W'_d = 0
+// with a + selector; a channel whose alpha is 0 gives W' = 0.
+#include "common.cuh"
+#include "launch.h"
+
+namespace s3d8 {
+
+// ---------------------------------------------------------------------------
+// Channel scales.  One warp per row (stride over the row CTAs), 16-byte loads, four in
+// flight per lane.  For finite bf16 values |a| <= |b| exactly when the low
+// 15 bits compare that way, so the row maximum is a packed 16-bit integer max
+// of the masked words; it is converted back to fp32 once per row.
+// ---------------------------------------------------------------------------
+constexpr int kScaleThreads = 256;
+
+// Packed per-half maximum of |x| (as 15-bit magnitudes) over 8 bf16 values.
+__device__ __forceinline__ uint32_t absmax_word(const uint4 v)
+{
+    const uint32_t a = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+    const uint32_t b = __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
+    return __vmaxu2(a, b);
+}
+constexpr int kScaleRowsPerCta = kScaleThreads / 32;
+
+__device__ __forceinline__ void scale_rows(const __nv_bfloat16 *__restrict__ w, int N, int K,
+                                           int ctas, __nv_bfloat16 *__restrict__ chan_scale)
+{
+    const int lane = threadIdx.x & 31;
+    const int chunks = K / 8;
+    for (int n = blockIdx.x * kScaleRowsPerCta + (threadIdx.x >> 5); n < N;
+         n += ctas * kScaleRowsPerCta) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(w + (size_t)n * K);
+        uint32_t m = 0;
+        int c = lane;
+        for (; c + 96 < chunks; c += 128) {
+            const uint4 v0 = __ldg(row + c), v1 = __ldg(row + c + 32);
+            const uint4 v2 = __ldg(row + c + 64), v3 = __ldg(row + c + 96);
+            m = __vmaxu2(m, absmax_word(v0));
+            m = __vmaxu2(m, absmax_word(v1));
+            m = __vmaxu2(m, absmax_word(v2));
+            m = __vmaxu2(m, absmax_word(v3));
+        }
+        for (; c < chunks; c += 32)
+            m = __vmaxu2(m, absmax_word(__ldg(row + c)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) {
+            const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+            const float amax = __uint_as_float((hi > lo ? hi : lo) << 16);
+            chan_scale[n] = __float2bfloat16_rn(__fdiv_rn(amax, 127.0f));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Candidate masks.  The cube [0, 128)^3 of scaled magnitudes W' is cut into
+// 16^3 cells of side 8.  For each cell, bit l of its mask is set when
+// centroid l can be the nearest (in the fp32 arithmetic above) to some point
+// of the closed cell: its smallest squared distance to the cell is at most
+// the smallest, over all centroids, of the largest squared distance to the
+// cell, plus a margin of 1.  Box distances of integer centroids to integer
+// corners are integers below 2^24, so they are exact in fp32; the fp32 value
+// of a point's squared distance differs from the real one by less than 0.025
+// (relative error below 6 units of 2^-24 on values below 2^16), so the margin
+// keeps every centroid that can win, ties included.  Cells are indexed
+// i0 + 16 i1 + 256 i2 with i_d = floor(W'_d / 8).
+// ---------------------------------------------------------------------------
+constexpr int kCellBits = 4;
+constexpr int kCells = 1 << (3 * kCellBits);   // 4096
+constexpr float kCellSide = 8.0f;
+
+__device__ uint32_t cell_mask(const int8_t *__restrict__ C, int cell)
+{
+    float lo[3], hi[3];
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        lo[d] = kCellSide * (float)((cell >> (kCellBits * d)) & ((1 << kCellBits) - 1));
+        hi[d] = lo[d] + kCellSide;
+    }
+    float thr = 3.0e38f;
+    for (int l = 0; l < 32; ++l) {
+        float far = 0.0f;
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const float c = (float)C[3 * l + d];
+            const float a = c - lo[d], b = c - hi[d];
+            far += fmaxf(a * a, b * b);
+        }
+        thr = fminf(thr, far);
+    }
+    thr += 1.0f;
+    uint32_t mask = 0;
+    for (int l = 0; l < 32; ++l) {
+        float near = 0.0f;
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const float c = (float)C[3 * l + d];
+            const float e = fmaxf(0.0f, fmaxf(lo[d] - c, c - hi[d]));
+            near += e * e;
+        }
+        mask |= (near <= thr ? 1u : 0u) << l;
+    }
+    return mask;
+}
+
+// The channel-scale kernel's trailing CTAs build the masks, one cell per thread.
+constexpr int kMaskCtas = kCells / kScaleThreads;
+
+__global__ __launch_bounds__(kScaleThreads) void encode_prepare_kernel(
+    const __nv_bfloat16 *__restrict__ w, const int8_t *__restrict__ C, int N, int K,
+    int row_ctas, __nv_bfloat16 *__restrict__ chan_scale, uint32_t *__restrict__ masks)
+{
+    if ((int)blockIdx.x >= row_ctas) {
+        const int cell = ((int)blockIdx.x - row_ctas) * kScaleThreads + threadIdx.x;
+        masks[cell] = cell_mask(C, cell);
+        return;
+    }
+    scale_rows(w, N, K, row_ctas, chan_scale);
+}
+
+// ---------------------------------------------------------------------------
+// Scaled magnitude q = RN(a / alpha) for a = |x| >= 0.  With r = RN(1/alpha)
+// computed once per channel, q0 = RN(a r) is within one unit in the last place
+// of a / alpha, the remainder a - alpha q0 is then exact in one fused
+// multiply-add, and RN(q0 + rem r) is the correctly rounded quotient
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990, the division theorem).
+// The argument needs every intermediate far from underflow and overflow: the
+// fast path runs for alpha in [2^-50, 2^50] and a = 0 or a >= alpha 2^-30,
+// with a <= 2^20 alpha (the encoder meets a <= 128 alpha: alpha is the row's
+// absmax / 127 rounded to bf16).  A nonzero a below alpha 2^-30, or any
+// nonzero a when alpha is outside the range, takes the IEEE division.
+// alpha = 0 gives 0.  The test "a is 0 or a >= lo" is one unsigned compare
+// of (bits(a) - 1) against lo_m1 = bits(lo) - 1.
+// ---------------------------------------------------------------------------
+struct ChanDiv {
+    float alpha, r;
+    uint32_t lo_m1;
+};
+
+__device__ __forceinline__ ChanDiv chan_div(float alpha)
+{
+    ChanDiv c;
+    c.alpha = alpha;
+    if (alpha == 0.0f) {
+        c.r = 0.0f;                  // q0 = 0, rem = a, q = 0 for every finite a
+        c.lo_m1 = 0u;
+    } else if (alpha >= 0x1p-50f && alpha <= 0x1p50f) {
+        c.r = __frcp_rn(alpha);
+        c.lo_m1 = __float_as_uint(alpha * 0x1p-30f) - 1u;   // exact power-of-two scaling
+    } else {
+        c.r = 0.0f;                  // a = 0 still gives 0 on the fast path
+        c.lo_m1 = 0xFFFFFFFFu;
+    }
+    return c;
+}
+
+__device__ __forceinline__ float scaled_abs(float a, const ChanDiv &c)
+{
+    const float q0 = __fmul_rn(a, c.r);
+    const float rem = __fmaf_rn(-q0, c.alpha, a);
+    float q = __fmaf_rn(rem, c.r, q0);
+    if (__float_as_uint(a) - 1u < c.lo_m1)
+        q = __fdiv_rn(a, c.alpha);
+    return q;
+}
+
+__global__ void selftest_scaled_abs_kernel(const __nv_bfloat16 *__restrict__ x,
+                                           const __nv_bfloat16 *__restrict__ alpha, int64_t n,
+                                           float *__restrict__ out)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = scaled_abs(fabsf(__bfloat162float(x[i])), chan_div(__bfloat162float(alpha[i])));
+}
+
+cudaError_t launch_selftest_scaled_abs(const __nv_bfloat16 *x, const __nv_bfloat16 *alpha,
+                                       int64_t n, float *out, cudaStream_t stream)
+{
+    const int64_t want = (n + 255) / 256;
+    const int grid = (int)(want < 4096 ? want : 4096);
+    selftest_scaled_abs_kernel<<<grid, 256, 0, stream>>>(x, alpha, n, out);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Assignment.  Persistent CTAs; a thread takes one packed row g and 8
+// consecutive k per item: three 16-byte loads (rows 3g, 3g+1, 3g+2), 8 output
+// bytes.  Per code, the cell's mask from shared memory lists the candidates.
+// The warp walks them in lockstep for as many steps as its largest candidate
+// count: at each step a lane takes its highest remaining index l (as
+// c = clz(mask) = 31 - l) and clears it; a lane with none left gets c = 32.
+// The table is stored by c (entry c = centroid 31 - c) with a far-away dummy
+// at c = 32, so that lane's distance is +inf and never wins.  A centroid
+// whose distance is <= the best so far replaces it; walking indices downward,
+// that leaves the lowest index among equal distances, the answer of a 0..31
+// scan with a strict "<".
+// The table is stored eight times, entry c of copy j at float4 8 c + j, and
+// lane t reads copy t mod 8: the eight lanes of a 128-bit access phase then
+// touch distinct bank groups whatever entries they want.
+// Finite inputs give W' <= 127.25 (alpha >= absmax/127 (1 - 2^-9)), inside the
+// cell grid; the cell index is masked to 12 bits in any case.
+// ---------------------------------------------------------------------------
+constexpr int kEncodeThreads = 256;
+constexpr int kEncodeCtasPerSm = 5;
+constexpr int kTabEntries = 33;
+
+__device__ __forceinline__ float dist2(const float4 c, float w0, float w1, float w2)
+{
+    const float t0 = __fsub_rn(c.x, w0);
+    const float t1 = __fsub_rn(c.y, w1);
+    const float t2 = __fsub_rn(c.z, w2);
+    return __fadd_rn(__fadd_rn(__fmul_rn(t0, t0), __fmul_rn(t1, t1)), __fmul_rn(t2, t2));
+}
+
+// floor(v / 8) + 2^23 for 0 <= v < 2^26, rounded toward -inf in one fused
+// multiply-add (v / 8 is exact); the low 4 bits are the cell coordinate.
+__device__ __forceinline__ uint32_t cell_coord(float v)
+{
+    return __float_as_uint(__fmaf_rd(v, 0.125f, 8388608.0f)) & 15u;
+}
+
+// Negative-selector flags of the two bf16 in a word, at bits 15 and 31: the
+// sign bit, unless the magnitude is 0 (-0 takes the + selector).
+__device__ __forceinline__ uint32_t neg_flags(uint32_t u)
+{
+    const uint32_t nz = (u & 0x7FFF7FFFu) + 0x7FFF7FFFu;  // bit 15 / 31 set iff magnitude != 0
+    return u & nz & 0x80008000u;
+}
+
+__global__ __launch_bounds__(kEncodeThreads, kEncodeCtasPerSm) void encode_assign_kernel(
+    const __nv_bfloat16 *__restrict__ w, const int8_t *__restrict__ C,
+    const __nv_bfloat16 *__restrict__ chan_scale, const uint32_t *__restrict__ masks_g, int N,
+    int K, int G, uint8_t *__restrict__ packed)
+{
+    __shared__ __align__(16) uint32_t masks[kCells];
+    __shared__ float4 tab[kTabEntries * 8];
+    for (int i = threadIdx.x; i < kCells / 4; i += kEncodeThreads)
+        reinterpret_cast<uint4 *>(masks)[i] = __ldg(reinterpret_cast<const uint4 *>(masks_g) + i);
+    for (int i = threadIdx.x; i < kTabEntries * 8; i += kEncodeThreads) {
+        const int c = i >> 3;
+        tab[i] = c < 32 ? make_float4((float)C[3 * (31 - c)], (float)C[3 * (31 - c) + 1],
+                                      (float)C[3 * (31 - c) + 2], 0.0f)
+                        : make_float4(1.0e30f, 1.0e30f, 1.0e30f, 0.0f);
+    }
+    __syncthreads();
+    const float4 *mytab = tab + (threadIdx.x & 7);
+
+    const int chunks = K / 8;
+    const int64_t items = (int64_t)G * chunks;
+    // The loop runs per warp (the walk below is a warp collective); lanes past
+    // the end work on zeros and store nothing.
+    for (int64_t base = (int64_t)blockIdx.x * kEncodeThreads + (threadIdx.x & ~31); base < items;
+         base += (int64_t)gridDim.x * kEncodeThreads) {
+        const int64_t it = base + (threadIdx.x & 31);
+        const bool live = it < items;
+        const int g = live ? (int)(it / chunks) : 0;
+        const int c = live ? (int)(it - (int64_t)g * chunks) : 0;
+        uint32_t u[3][4];
+        ChanDiv dv[3];
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const int n = 3 * g + d;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            float alpha = 0.0f;
+            if (live && n < N) {
+                v = __ldg(reinterpret_cast<const uint4 *>(w + (size_t)n * K) + c);
+                alpha = __bfloat162float(chan_scale[n]);
+            }
+            u[d][0] = v.x;
+            u[d][1] = v.y;
+            u[d][2] = v.z;
+            u[d][3] = v.w;
+            dv[d] = chan_div(alpha);
+        }
+        // selectors: byte e of out[e / 4] gets S0 at bit 0, S1 at bit 6 and
+        // S2 xor S0 at bit 7; the flags of codes 4o..4o+3 sit at bits 15 and 31
+        // of words 2o and 2o+1, gathered to bit 7 of each byte by one permute
+        uint32_t out[2];
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+            const uint32_t f0 = __byte_perm(neg_flags(u[0][2 * o]), neg_flags(u[0][2 * o + 1]), 0x7531);
+            const uint32_t f1 = __byte_perm(neg_flags(u[1][2 * o]), neg_flags(u[1][2 * o + 1]), 0x7531);
+            const uint32_t f2 = __byte_perm(neg_flags(u[2][2 * o]), neg_flags(u[2][2 * o + 1]), 0x7531);
+            out[o] = (f0 >> 7) | (f1 >> 1) | (f2 ^ f0);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float wp[3];
+#pragma unroll
+            for (int d = 0; d < 3; ++d) {
+                const uint32_t word = u[d][e >> 1];
+                const float x = __uint_as_float((e & 1) ? (word & 0xFFFF0000u) : (word << 16));
+                wp[d] = scaled_abs(fabsf(x), dv[d]);
+            }
+            const uint32_t cell = cell_coord(wp[0]) + 16u * cell_coord(wp[1]) +
+                                  256u * cell_coord(wp[2]);
+            uint32_t cand = masks[cell];
+            const uint32_t steps = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)__popc(cand));
+            float bestd = 3.0e38f;
+            uint32_t best = 31;   // centroid 0 if nothing compares (only NaN inputs)
+            for (uint32_t i = 0; i < steps; ++i) {
+                const uint32_t k = __clz(cand);                  // 32 when none is left
+                cand ^= __funnelshift_rc(0x80000000u, 0u, k);    // clears that bit; 0 for k = 32
+                const float dl = dist2(mytab[8 * k], wp[0], wp[1], wp[2]);
+                if (dl <= bestd) {
+                    bestd = dl;
+                    best = k;
+                }
+            }
+            out[e >> 2] += (31u - best) << (1 + 8 * (e & 3));
+        }
+        if (live)
+            reinterpret_cast<uint2 *>(packed + (size_t)g * K)[c] = make_uint2(out[0], out[1]);
+    }
+}
+
+cudaError_t launch_encode(const __nv_bfloat16 *w, const int8_t *C, int N, int K, uint8_t *packed,
+                          __nv_bfloat16 *chan_scale, void *workspace, cudaStream_t stream)
+{
+    const int sms = device_sm_count();
+    uint32_t *masks = static_cast<uint32_t *>(workspace);
+    const int rows_ctas = (N + kScaleRowsPerCta - 1) / kScaleRowsPerCta;
+    const int g1 = rows_ctas < sms * 8 ? rows_ctas : sms * 8;
+    encode_prepare_kernel<<<g1 + kMaskCtas, kScaleThreads, 0, stream>>>(w, C, N, K, g1, chan_scale,
+                                                                         masks);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const int G = (N + 2) / 3;
+    const int64_t items = (int64_t)G * (K / 8);
+    const int64_t want = (items + kEncodeThreads - 1) / kEncodeThreads;
+    const int64_t cap = (int64_t)sms * kEncodeCtasPerSm;
+    const int g2 = (int)(want < cap ? want : cap);
+    encode_assign_kernel<<<g2, kEncodeThreads, 0, stream>>>(w, C, chan_scale, masks, N, K, G,
+                                                           packed);
+    return cudaGetLastError();
+}
+
+}  // namespace s3d8

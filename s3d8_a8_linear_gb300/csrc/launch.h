@@ -53,6 +53,10 @@ int *device_status_ptr();   // this device's sticky status word, or nullptr
 
 cudaError_t launch_quantize_act(const __nv_bfloat16 *x, int M, int K, int8_t *xq, float *xscale,
                                 cudaStream_t stream);
+cudaError_t launch_encode(const __nv_bfloat16 *w, const int8_t *C, int N, int K, uint8_t *packed,
+                          __nv_bfloat16 *chan_scale, void *workspace, cudaStream_t stream);
+cudaError_t launch_selftest_scaled_abs(const __nv_bfloat16 *x, const __nv_bfloat16 *alpha,
+                                       int64_t n, float *out, cudaStream_t stream);
 cudaError_t launch_decode(const uint8_t *packed, const int8_t *C, int N, int K, int8_t *w,
                           cudaStream_t stream);
 cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t stream);

@@ -49,7 +49,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for fn in ("s3d8_quantize_act", "s3d8_linear", "s3d8_decode", "s3d8_linear_ex",
                "s3d8_linear_acc_i32", "s3d8_linear_workspace_size", "s3d8_device_status",
-               "s3d8_status_string", "s3d8_version"):
+               "s3d8_status_string", "s3d8_version", "s3d8_encode"):
         assert fn in names
 
 
@@ -115,6 +115,8 @@ def test_empty_calls_are_no_ops(lib):
     assert lib.s3d8_quantize_act(None, 0, 32, None, None, None) == 0
     assert lib.s3d8_decode(None, None, 0, 32, None, None) == 0
     assert lib.s3d8_linear_acc_i32(None, None, None, 0, 5, 32, None, None, 0, 0, None) == 0
+    assert lib.s3d8_encode(None, None, 0, 32, None, None, None, 0, None) == 0
+    assert lib.s3d8_selftest_scaled_abs(None, None, 0, None, None) == 0
 
 
 @no_device_only
@@ -129,6 +131,18 @@ def test_other_entry_points_reject(lib):
     assert lib.s3d8_linear_acc_i32(A16, A16B, A16C, 2, 5, 32, A16 + 2, None, 0, 0, None) == -2
     assert lib.s3d8_linear_ex(A16, A16B, A16C, A16, A16B, 2, 3, 32, A16C, None, 0, 7, None) == -1
     assert lib.s3d8_linear_ex(A16, A16B, A16C, A16, A16B, 2, 3, 32, A16C, None, 0, -1, None) == -1
+    enc = lib.s3d8_encode
+    WS = 16384
+    assert enc(A16, A16B, 6, 24, A16C, A16, A16B, WS, None) == -1            # K % 16
+    assert enc(A16, None, 6, 32, A16C, A16, A16B, WS, None) == -1
+    assert enc(A16 + 8, A16B, 6, 32, A16C, A16, A16B, WS, None) == -2        # w alignment
+    assert enc(A16, A16B, 6, 32, A16C + 4, A16, A16B, WS, None) == -2        # packed
+    assert enc(A16, A16B, 6, 32, A16C, A16 + 1, A16B, WS, None) == -2        # scales
+    assert enc(A16, A16B, 6, 32, A16C, A16, None, WS, None) == -6            # no workspace
+    assert enc(A16, A16B, 6, 32, A16C, A16, A16B, WS - 1, None) == -6        # too small
+    assert enc(A16, A16B, 6, 32, A16C, A16, A16B + 8, WS, None) == -2        # ws alignment
+    assert lib.s3d8_selftest_scaled_abs(A16, A16B, -1, A16C, None) == -1
+    assert lib.s3d8_selftest_scaled_abs(A16 + 1, A16B, 4, A16C, None) == -2
 
 
 def test_binding_refuses_cpu_tensors(lib):
