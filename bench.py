@@ -750,6 +750,9 @@ def main():
                     help="time the headline step only (no variants, e2e, sweeps); for profiling")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the M = 2048 tensor-core measurement and print it; for profiling")
+    ap.add_argument("--encode-only", action="store_true",
+                    help="run only the encoder measurement (one 11B layer) and print it; for "
+                         "profiling")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = 10 if args.steps is None else args.steps
@@ -762,6 +765,14 @@ def main():
         import s3d8_a8_linear_gb300 as s3d8
         s3d8.load(build_if_missing=True)
         print(json.dumps(prefill_measure(torch, s3d8, torch.device("cuda:0"))))
+        return
+    if args.encode_only:
+        import torch
+
+        import s3d8_a8_linear_gb300 as s3d8
+        s3d8.load(build_if_missing=True)
+        print(json.dumps(encode_measure(torch, s3d8, torch.device("cuda:0"),
+                                        reps=3 if args.steps is None else args.steps)))
         return
     args.steps = 40000 if args.steps is None else args.steps
     args.warmup = 400 if args.warmup is None else args.warmup

@@ -70,22 +70,26 @@ __device__ __forceinline__ void scale_rows(const __nv_bfloat16 *__restrict__ w, 
 
 // ---------------------------------------------------------------------------
 // Candidate masks.  The cube [0, 128)^3 of scaled magnitudes W' is cut into
-// 16^3 cells of side 8.  For each cell, bit l of its mask is set when
-// centroid l can be the nearest (in the fp32 arithmetic above) to some point
-// of the closed cell: its smallest squared distance to the cell is at most
-// the smallest, over all centroids, of the largest squared distance to the
-// cell, plus a margin of 1.  Box distances of integer centroids to integer
-// corners are integers below 2^24, so they are exact in fp32; the fp32 value
+// 16^3 cells of side 8, indexed i0 + 16 i1 + 256 i2 with i_d = floor(W'_d / 8).
+// Bit l of a cell's mask is cleared when some centroid j is nearer than l by
+// more than a margin of 1 everywhere in the closed cell.  D_l(x) - D_j(x) =
+// |C_l|^2 - |C_j|^2 - 2 x.(C_l - C_j) is linear in x, so its minimum over the
+// box is at a corner: each axis takes lo or hi, whichever gives the larger
+// x_d (C_l - C_j)_d.  All of these are integers below 2^24 (corners are
+// multiples of 8 up to 128, centroids 0..127), exact in fp32.  The fp32 value
 // of a point's squared distance differs from the real one by less than 0.025
-// (relative error below 6 units of 2^-24 on values below 2^16), so the margin
-// keeps every centroid that can win, ties included.  Cells are indexed
-// i0 + 16 i1 + 256 i2 with i_d = floor(W'_d / 8).
+// (relative error below 6 units of 2^-24 on values below 2^16), so a centroid
+// that can be the fp32 minimum anywhere in the cell, ties included, keeps its
+// bit; the centroid nearest to any point of the cell always does.
+// One warp per cell, lane l testing centroid l against all j; a ballot forms
+// the mask.
 // ---------------------------------------------------------------------------
 constexpr int kCellBits = 4;
 constexpr int kCells = 1 << (3 * kCellBits);   // 4096
 constexpr float kCellSide = 8.0f;
 
-__device__ uint32_t cell_mask(const int8_t *__restrict__ C, int cell)
+// ctab[l] = (C_l0, C_l1, C_l2, |C_l|^2)
+__device__ __forceinline__ uint32_t cell_mask(const float4 *ctab, int cell, int lane)
 {
     float lo[3], hi[3];
 #pragma unroll
@@ -93,42 +97,38 @@ __device__ uint32_t cell_mask(const int8_t *__restrict__ C, int cell)
         lo[d] = kCellSide * (float)((cell >> (kCellBits * d)) & ((1 << kCellBits) - 1));
         hi[d] = lo[d] + kCellSide;
     }
-    float thr = 3.0e38f;
-    for (int l = 0; l < 32; ++l) {
-        float far = 0.0f;
-#pragma unroll
-        for (int d = 0; d < 3; ++d) {
-            const float c = (float)C[3 * l + d];
-            const float a = c - lo[d], b = c - hi[d];
-            far += fmaxf(a * a, b * b);
-        }
-        thr = fminf(thr, far);
+    const float4 me = ctab[lane];
+    bool keep = true;
+    for (int j = 0; j < 32; ++j) {
+        const float4 o = ctab[j];
+        const float d0 = me.x - o.x, d1 = me.y - o.y, d2 = me.z - o.z;
+        const float mx = fmaxf(lo[0] * d0, hi[0] * d0) + fmaxf(lo[1] * d1, hi[1] * d1) +
+                         fmaxf(lo[2] * d2, hi[2] * d2);
+        const float mn = (me.w - o.w) - 2.0f * mx;
+        keep = keep && !(mn > 1.0f);
     }
-    thr += 1.0f;
-    uint32_t mask = 0;
-    for (int l = 0; l < 32; ++l) {
-        float near = 0.0f;
-#pragma unroll
-        for (int d = 0; d < 3; ++d) {
-            const float c = (float)C[3 * l + d];
-            const float e = fmaxf(0.0f, fmaxf(lo[d] - c, c - hi[d]));
-            near += e * e;
-        }
-        mask |= (near <= thr ? 1u : 0u) << l;
-    }
-    return mask;
+    return __ballot_sync(0xFFFFFFFFu, keep);
 }
 
-// The channel-scale kernel's trailing CTAs build the masks, one cell per thread.
-constexpr int kMaskCtas = kCells / kScaleThreads;
+// The channel-scale kernel's trailing CTAs build the masks, one cell per warp.
+constexpr int kMaskCtas = kCells / (kScaleThreads / 32);
 
 __global__ __launch_bounds__(kScaleThreads) void encode_prepare_kernel(
     const __nv_bfloat16 *__restrict__ w, const int8_t *__restrict__ C, int N, int K,
     int row_ctas, __nv_bfloat16 *__restrict__ chan_scale, uint32_t *__restrict__ masks)
 {
     if ((int)blockIdx.x >= row_ctas) {
-        const int cell = ((int)blockIdx.x - row_ctas) * kScaleThreads + threadIdx.x;
-        masks[cell] = cell_mask(C, cell);
+        __shared__ float4 ctab[32];
+        if (threadIdx.x < 32) {
+            const float c0 = (float)C[3 * threadIdx.x], c1 = (float)C[3 * threadIdx.x + 1];
+            const float c2 = (float)C[3 * threadIdx.x + 2];
+            ctab[threadIdx.x] = make_float4(c0, c1, c2, c0 * c0 + c1 * c1 + c2 * c2);
+        }
+        __syncthreads();
+        const int cell = ((int)blockIdx.x - row_ctas) * (kScaleThreads / 32) + (threadIdx.x >> 5);
+        const uint32_t m = cell_mask(ctab, cell, threadIdx.x & 31);
+        if ((threadIdx.x & 31) == 0)
+            masks[cell] = m;
         return;
     }
     scale_rows(w, N, K, row_ctas, chan_scale);
@@ -171,14 +171,21 @@ __device__ __forceinline__ ChanDiv chan_div(float alpha)
     return c;
 }
 
-__device__ __forceinline__ float scaled_abs(float a, const ChanDiv &c)
+__device__ __forceinline__ float scaled_abs_fast(float a, const ChanDiv &c)
 {
     const float q0 = __fmul_rn(a, c.r);
     const float rem = __fmaf_rn(-q0, c.alpha, a);
-    float q = __fmaf_rn(rem, c.r, q0);
-    if (__float_as_uint(a) - 1u < c.lo_m1)
-        q = __fdiv_rn(a, c.alpha);
-    return q;
+    return __fmaf_rn(rem, c.r, q0);
+}
+
+__device__ __forceinline__ bool needs_ieee_div(float a, const ChanDiv &c)
+{
+    return __float_as_uint(a) - 1u < c.lo_m1;
+}
+
+__device__ __forceinline__ float scaled_abs(float a, const ChanDiv &c)
+{
+    return needs_ieee_div(a, c) ? __fdiv_rn(a, c.alpha) : scaled_abs_fast(a, c);
 }
 
 __global__ void selftest_scaled_abs_kernel(const __nv_bfloat16 *__restrict__ x,
@@ -218,7 +225,7 @@ cudaError_t launch_selftest_scaled_abs(const __nv_bfloat16 *x, const __nv_bfloat
 // cell grid; the cell index is masked to 12 bits in any case.
 // ---------------------------------------------------------------------------
 constexpr int kEncodeThreads = 256;
-constexpr int kEncodeCtasPerSm = 5;
+constexpr int kEncodeCtasPerSm = 4;
 constexpr int kTabEntries = 33;
 
 __device__ __forceinline__ float dist2(const float4 c, float w0, float w1, float w2)
@@ -234,6 +241,13 @@ __device__ __forceinline__ float dist2(const float4 c, float w0, float w1, float
 __device__ __forceinline__ uint32_t cell_coord(float v)
 {
     return __float_as_uint(__fmaf_rd(v, 0.125f, 8388608.0f)) & 15u;
+}
+
+// |x| of element e (0..7) of an 8-element bf16 chunk held as 4 words, in fp32.
+__device__ __forceinline__ float elem_abs(const uint32_t (&u)[4], int e)
+{
+    const uint32_t word = u[e >> 1];
+    return __uint_as_float(((e & 1) ? (word & 0xFFFF0000u) : (word << 16)) & 0x7FFFFFFFu);
 }
 
 // Negative-selector flags of the two bf16 in a word, at bits 15 and 31: the
@@ -300,31 +314,58 @@ __global__ __launch_bounds__(kEncodeThreads, kEncodeCtasPerSm) void encode_assig
             const uint32_t f2 = __byte_perm(neg_flags(u[2][2 * o]), neg_flags(u[2][2 * o + 1]), 0x7531);
             out[o] = (f0 >> 7) | (f1 >> 1) | (f2 ^ f0);
         }
+        // Two halves of 4 codes: the 12 scaled magnitudes of a half, then its
+        // walks.  One branch per half sends the (never seen in practice)
+        // elements outside the fast division's range to the IEEE division.
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float wp[3];
+        for (int h = 0; h < 2; ++h) {
+            float wp[3][4];
+            bool slow = false;
 #pragma unroll
-            for (int d = 0; d < 3; ++d) {
-                const uint32_t word = u[d][e >> 1];
-                const float x = __uint_as_float((e & 1) ? (word & 0xFFFF0000u) : (word << 16));
-                wp[d] = scaled_abs(fabsf(x), dv[d]);
+            for (int d = 0; d < 3; ++d)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    slow |= needs_ieee_div(elem_abs(u[d], 4 * h + e), dv[d]);
+            if (slow) {
+#pragma unroll
+                for (int d = 0; d < 3; ++d)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        wp[d][e] = scaled_abs(elem_abs(u[d], 4 * h + e), dv[d]);
+            } else {
+#pragma unroll
+                for (int d = 0; d < 3; ++d)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        wp[d][e] = scaled_abs_fast(elem_abs(u[d], 4 * h + e), dv[d]);
             }
-            const uint32_t cell = cell_coord(wp[0]) + 16u * cell_coord(wp[1]) +
-                                  256u * cell_coord(wp[2]);
-            uint32_t cand = masks[cell];
-            const uint32_t steps = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)__popc(cand));
-            float bestd = 3.0e38f;
-            uint32_t best = 31;   // centroid 0 if nothing compares (only NaN inputs)
-            for (uint32_t i = 0; i < steps; ++i) {
-                const uint32_t k = __clz(cand);                  // 32 when none is left
-                cand ^= __funnelshift_rc(0x80000000u, 0u, k);    // clears that bit; 0 for k = 32
-                const float dl = dist2(mytab[8 * k], wp[0], wp[1], wp[2]);
-                if (dl <= bestd) {
-                    bestd = dl;
-                    best = k;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float w0 = wp[0][e], w1 = wp[1][e], w2 = wp[2][e];
+                const uint32_t cell = cell_coord(w0) + 16u * cell_coord(w1) + 256u * cell_coord(w2);
+                uint32_t cand = masks[cell];
+                const uint32_t steps = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)__popc(cand));
+                float bestd = 3.0e38f;
+                uint32_t best = 31;   // centroid 0 if nothing compares (only NaN inputs)
+                // two candidates per trip; a lane with none left reads the dummy
+                for (uint32_t i = 0; i < steps; i += 2) {
+                    const uint32_t k0 = __clz(cand);                 // 32 when none is left
+                    cand ^= __funnelshift_rc(0x80000000u, 0u, k0);   // clears it; 0 for k = 32
+                    const uint32_t k1 = __clz(cand);
+                    cand ^= __funnelshift_rc(0x80000000u, 0u, k1);
+                    const float d0 = dist2(mytab[8 * k0], w0, w1, w2);
+                    const float d1 = dist2(mytab[8 * k1], w0, w1, w2);
+                    if (d0 <= bestd) {
+                        bestd = d0;
+                        best = k0;
+                    }
+                    if (d1 <= bestd) {
+                        bestd = d1;
+                        best = k1;
+                    }
                 }
+                out[h] += (31u - best) << (1 + 8 * e);
             }
-            out[e >> 2] += (31u - best) << (1 + 8 * (e & 3));
         }
         if (live)
             reinterpret_cast<uint2 *>(packed + (size_t)g * K)[c] = make_uint2(out[0], out[1]);
