@@ -520,7 +520,51 @@ def prefill_measure(torch, s3d8, dev, M=2048, reps=3):
         tot_ms += ms
     res["tops"] = round(tot_ops / (tot_ms * 1e-3) / 1e12, 2)
     res["unit"] = "TOPS (int8 multiply-adds x2)"
+    res["two_step"] = two_step_measure(torch, s3d8, dev, M, reps)
     return res
+
+
+def two_step_measure(torch, s3d8, dev, M, reps):
+    """The pages' prefill method, for comparison: a standalone unpack to dense
+    int8 weights (s3d8_decode), then a library GEMM on the dense weights, either
+    INT8 x INT8 -> int32 (torch._int_mm, cuBLASLt) or the same codes as bf16
+    (torch.matmul, cuBLAS).  The epilogue is left out, so these times are lower
+    bounds for the two-step layer."""
+    out = {}
+    for name, K, N in si.SWEEP_SHAPES:
+        mat = si.matrix(name, K, N, seed=3)
+        packed = torch.from_numpy(mat.packed).to(dev)
+        C = torch.from_numpy(mat.C).to(dev)
+        xq = torch.randint(-127, 128, (M, K), dtype=torch.int8, device=dev)
+        w = torch.empty((N, K), dtype=torch.int8, device=dev)
+        xb = xq.to(torch.bfloat16)
+        wb = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+
+        def timed(fn):
+            fn()
+            torch.cuda.synchronize()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for _ in range(reps):
+                fn()
+            t1.record()
+            t1.synchronize()
+            return t0.elapsed_time(t1) / reps
+
+        dec_ms = timed(lambda: s3d8.decode(packed, C, N, w))
+        i8_ms = timed(lambda: torch._int_mm(xq, w.t()))
+        cvt_ms = timed(lambda: wb.copy_(w))
+        bf_ms = timed(lambda: torch.matmul(xb, wb.t()))
+        ops = 2 * M * N * K
+        out[name] = {"decode_us": round(dec_ms * 1e3, 1),
+                     "int8_gemm_us": round(i8_ms * 1e3, 1),
+                     "int8_two_step_tops": round(ops / ((dec_ms + i8_ms) * 1e-3) / 1e12, 1),
+                     "to_bf16_us": round(cvt_ms * 1e3, 1),
+                     "bf16_gemm_us": round(bf_ms * 1e3, 1),
+                     "bf16_two_step_tops": round(
+                         ops / ((dec_ms + cvt_ms + bf_ms) * 1e-3) / 1e12, 1)}
+    return out
 
 
 def device_matrix(torch, dev, gen, K, N):

@@ -68,6 +68,8 @@ def lib():
         L.s3d8o_linear_out.argtypes = [P, P, P, I64, I64, P]
         L.s3d8o_encode.argtypes = [P, P, I64, I64, P, P]
         L.s3d8o_encode.restype = I32
+        L.s3d8o_fit_centroids.argtypes = [P, I64, I64, P, I32, P, P]
+        L.s3d8o_fit_centroids.restype = I32
         L.s3d8o_linear_out.restype = None
     return _lib
 
@@ -199,3 +201,17 @@ def encode(w_bf16_bits: np.ndarray, C: np.ndarray):
     if lib().s3d8o_encode(_ptr(w), _ptr(C), N, K, _ptr(packed), _ptr(cs)) != 0:
         raise MemoryError("oracle encoder scratch")
     return packed, cs
+
+
+def fit_centroids(w_bf16_bits: np.ndarray, r: np.ndarray, iters: int):
+    """Lloyd-Max centroid fit from k-means++ (paper section 3.4,
+    "Quantization"): bf16 weights [N, K], 32 uint32 draws -> (fp32 centroids
+    [32, 3], int8 table [32, 3])."""
+    w = _as(w_bf16_bits, np.uint16)
+    N, K = w.shape
+    r = _as(r, np.uint32, (32,))
+    cf = np.empty((32, 3), np.float32)
+    C = np.empty((32, 3), np.int8)
+    if lib().s3d8o_fit_centroids(_ptr(w), N, K, _ptr(r), int(iters), _ptr(cf), _ptr(C)) != 0:
+        raise MemoryError("oracle fit scratch")
+    return cf, C

@@ -34,7 +34,16 @@
  *     assignment with frozen centroids): alpha is rounded to bf16 (the stored
  *     scale) and the scaled magnitudes divide by that stored value; the
  *     squared distances are fp32 sums in the order d = 0, 1, 2, so that the
- *     GPU can take every argmin decision in the same arithmetic.
+ *     GPU can take every argmin decision in the same arithmetic;
+ *   - centroid fit ([P] section 3.4 "Quantization": Lloyd-Max with k-means++
+ *     initialisation on the zero-padded |W|/alpha 3-vectors, then Round):
+ *     the random draws are 32 caller-supplied 32-bit integers; D^2 weights
+ *     and cluster sums are taken on a fixed-point grid of 2^-20 (floor), so
+ *     that every sum is an exact integer and any summation order gives the
+ *     same result; a mean is RN(RN(sum / count) * 2^-20) in fp64, then
+ *     rounded to fp32; an empty cluster keeps its centroid; the iteration
+ *     count is fixed by the caller; Round is to nearest, ties to even,
+ *     clamped to 0..127.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math, no
  * FMA contraction, so that the fp32 activation quantiser is plain IEEE
@@ -281,5 +290,160 @@ int32_t s3d8o_encode(const uint16_t *w, const int8_t *C, int64_t N, int64_t K, u
             packed[g * K + k] = s3d8o_pack_byte(best, sel[0], sel[1], sel[2]);
         }
     free(alpha);
+    return 0;
+}
+
+
+/* ---------------------------------------------------------------------------
+ * Centroid fit, [P] section 3.4 "Quantization": C = Round(Lloyd-Max({W'})),
+ * Lloyd-Max started from k-means++ (Arthur and Vassilvitskii, "k-means++: the
+ * advantages of careful seeding", SODA 2007).
+ *
+ * Points: p = g K + k for packed row g and column k, W'_p = (|W[3g+d,k]| /
+ * alpha_{3g+d})_{d=0,1,2} exactly as in the encoder (alpha stored as bf16;
+ * padded channels and alpha = 0 give 0).  Np = ceil(N/3) K points.
+ *
+ * k-means++: centre 0 is point floor(r[0] Np / 2^32).  For t = 1..31, with
+ * D2_p the fp32 squared distance from p to its nearest chosen centre and
+ * w_p = floor(D2_p 2^20), S = sum w_p: centre t is the first point whose
+ * inclusive prefix sum of w exceeds floor(r[t] S / 2^32), i.e. point p with
+ * probability w_p / S; if S = 0 it is point floor(r[t] Np / 2^32).
+ *
+ * Lloyd: `iters` times, assign every point to its nearest centroid (fp32
+ * distance as in the encoder, lowest index on a tie), then move each centroid
+ * with a nonempty cluster to the mean of its points: per component,
+ * float(RN(RN(sum_p floor(W'_pd 2^20) / n) 2^-20)) with the division in fp64.
+ *
+ * Outputs the fp32 centroids (cf, 32 x 3) and C = clamp(rint(cf), 0, 127).
+ * Returns 0, or -1 when scratch cannot be allocated.
+ * ------------------------------------------------------------------------- */
+static float fdist2(const float *c, const float *w)
+{
+    float t0 = c[0] - w[0];
+    float t1 = c[1] - w[1];
+    float t2 = c[2] - w[2];
+    float s = t0 * t0;
+    s = s + t1 * t1;
+    s = s + t2 * t2;
+    return s;
+}
+
+/* floor(r x / 2^32) for r < 2^32, x < 2^62, in 64-bit integers */
+static uint64_t scale_draw(uint32_t r, uint64_t x)
+{
+    const uint64_t hi = x >> 32, lo = x & 0xFFFFFFFFu;
+    return (uint64_t)r * hi + (((uint64_t)r * lo) >> 32);
+}
+
+static void scaled_points(const uint16_t *w, int64_t N, int64_t K, float *P)
+{
+    const int64_t G = (N + 2) / 3;
+    float alpha[3];
+    for (int64_t g = 0; g < G; ++g) {
+        for (int d = 0; d < 3; ++d) {
+            const int64_t n = 3 * g + d;
+            alpha[d] = 0.0f;
+            if (n < N) {
+                float amax = 0.0f;
+                for (int64_t k = 0; k < K; ++k) {
+                    float a = fabsf(bf16_bits_to_float(w[n * K + k]));
+                    if (a > amax)
+                        amax = a;
+                }
+                alpha[d] = bf16_bits_to_float(float_to_bf16_rne(amax / 127.0f));
+            }
+        }
+        for (int64_t k = 0; k < K; ++k)
+            for (int d = 0; d < 3; ++d) {
+                const int64_t n = 3 * g + d;
+                float v = 0.0f;
+                if (n < N && alpha[d] != 0.0f)
+                    v = fabsf(bf16_bits_to_float(w[n * K + k])) / alpha[d];
+                P[3 * (g * K + k) + d] = v;
+            }
+    }
+}
+
+int32_t s3d8o_fit_centroids(const uint16_t *w, int64_t N, int64_t K, const uint32_t *r,
+                            int32_t iters, float *cf, int8_t *C)
+{
+    const int64_t Np = ((N + 2) / 3) * K;
+    float *P = (float *)malloc((size_t)Np * 3 * sizeof(float));
+    float *D2 = (float *)malloc((size_t)Np * sizeof(float));
+    if (!P || !D2) {
+        free(P);
+        free(D2);
+        return -1;
+    }
+    scaled_points(w, N, K, P);
+
+    /* k-means++ */
+    int64_t idx = (int64_t)scale_draw(r[0], (uint64_t)Np);
+    memcpy(cf, P + 3 * idx, 3 * sizeof(float));
+    for (int64_t p = 0; p < Np; ++p)
+        D2[p] = fdist2(cf, P + 3 * p);
+    for (int t = 1; t < 32; ++t) {
+        uint64_t S = 0;
+        for (int64_t p = 0; p < Np; ++p)
+            S += (uint64_t)(D2[p] * 1048576.0f);
+        if (S == 0) {
+            idx = (int64_t)scale_draw(r[t], (uint64_t)Np);
+        } else {
+            const uint64_t target = scale_draw(r[t], S);
+            uint64_t run = 0;
+            idx = Np - 1;
+            for (int64_t p = 0; p < Np; ++p) {
+                run += (uint64_t)(D2[p] * 1048576.0f);
+                if (run > target) {
+                    idx = p;
+                    break;
+                }
+            }
+        }
+        memcpy(cf + 3 * t, P + 3 * idx, 3 * sizeof(float));
+        for (int64_t p = 0; p < Np; ++p) {
+            const float d = fdist2(cf + 3 * t, P + 3 * p);
+            if (d < D2[p])
+                D2[p] = d;
+        }
+    }
+
+    /* Lloyd-Max */
+    for (int32_t it = 0; it < iters; ++it) {
+        uint64_t sum[32][3];
+        uint64_t cnt[32];
+        memset(sum, 0, sizeof sum);
+        memset(cnt, 0, sizeof cnt);
+        for (int64_t p = 0; p < Np; ++p) {
+            int best = 0;
+            float bestd = fdist2(cf, P + 3 * p);
+            for (int l = 1; l < 32; ++l) {
+                const float d = fdist2(cf + 3 * l, P + 3 * p);
+                if (d < bestd) {
+                    bestd = d;
+                    best = l;
+                }
+            }
+            cnt[best] += 1;
+            for (int d = 0; d < 3; ++d)
+                sum[best][d] += (uint64_t)(P[3 * p + d] * 1048576.0f);
+        }
+        for (int l = 0; l < 32; ++l)
+            if (cnt[l] > 0)
+                for (int d = 0; d < 3; ++d) {
+                    const double mean = (double)sum[l][d] / (double)cnt[l];
+                    cf[3 * l + d] = (float)(mean * 0x1p-20);
+                }
+    }
+    for (int i = 0; i < 96; ++i) {
+        float v = rintf(cf[i]);
+        if (v < 0.0f)
+            v = 0.0f;
+        if (v > 127.0f)
+            v = 127.0f;
+        C[i] = (int8_t)v;
+    }
+    free(P);
+    free(D2);
     return 0;
 }

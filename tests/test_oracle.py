@@ -506,3 +506,167 @@ def test_encode_then_decode_is_a_fixed_point():
     again, cs = oracle.encode(W, C)
     assert np.all(si.bf16_bits_to_f32(cs) == np.float32(2.0 ** -9))
     assert np.array_equal(again, packed)
+
+
+# --------------------------------------------------------------------------
+# Centroid fit (Llama-Mobile paper, section 3.4 "Quantization": Lloyd-Max
+# with k-means++ initialisation on the zero-padded |W| / alpha 3-vectors, then
+# Round).  Draws are 32 caller-supplied 32-bit integers.
+# --------------------------------------------------------------------------
+
+GRID_X = (13, 40, 68, 96)
+GRID_Z = (12, 60)
+
+
+def cluster_centres():
+    """31 grid centres 28+ apart, plus (127, 127, 127)."""
+    cs = [(x, y, z) for x in GRID_X for y in GRID_X for z in GRID_Z]
+    cs.remove((96, 96, 60))
+    cs.append((127, 127, 127))
+    return np.array(cs, np.float64)
+
+
+def weights_from_points(Wp, alpha_exp=-8, seed=0):
+    """bf16 weights whose scaled magnitudes are the given points [G, K, 3]:
+    W = s * W' * 2^alpha_exp with random signs; every channel must hold 127."""
+    rng = np.random.default_rng(seed)
+    G, K, _ = Wp.shape
+    W = np.zeros((3 * G, K))
+    for d in range(3):
+        W[d::3] = Wp[:, :, d] * (2.0 ** alpha_exp)
+    W *= 1 - 2 * rng.integers(0, 2, size=W.shape)
+    return _bf16_exact(W)
+
+
+def draws(seed):
+    return np.random.default_rng(seed).integers(0, 2 ** 32, 32, dtype=np.uint64).astype(np.uint32)
+
+
+def clustered_points(G=16, K=256, seed=0, half_up=()):
+    """Each point is a cluster centre plus an offset of +-0.5 on one axis
+    (means within 0.5 / count of the centre), or {0, +1} in x for the centres in
+    half_up (mean x.5 when the count is even)."""
+    rng = np.random.default_rng(seed)
+    cs = cluster_centres()
+    Wp = np.zeros((G, K, 3))
+    lab = rng.permutation(np.arange(G * K) % 32).reshape(G, K)
+    lab[:, 0] = 31                                   # every row holds (127, 127, 127)
+    counts = {}
+    for g in range(G):
+        for k in range(K):
+            c = lab[g, k]
+            i = counts.get(c, 0)
+            counts[c] = i + 1
+            off = np.zeros(3)
+            if c != 31:
+                if c in half_up:
+                    off[0] = i % 2
+                else:
+                    off[i % 3] = 0.5 if (i // 3) % 2 == 0 else -0.5
+            Wp[g, k] = cs[c] + off
+    return Wp, lab, counts
+
+
+def sorted_rows(a):
+    a = np.asarray(a)
+    return a[np.lexsort(a.T[::-1])]
+
+
+def test_fit_recovers_well_separated_clusters():
+    Wp, lab, counts = clustered_points()
+    W = weights_from_points(Wp)
+    cf, C = oracle.fit_centroids(W, draws(1), iters=8)
+    assert np.array_equal(sorted_rows(C.astype(np.int64)), sorted_rows(cluster_centres().astype(np.int64)))
+    # the fp32 centroids are the cluster means, within the 2^-20 grid of the sums
+    means = np.array([Wp[lab == c].mean(0) for c in range(32)])
+    assert np.allclose(sorted_rows(cf.astype(np.float64)), sorted_rows(means), atol=2e-6)
+
+
+def test_fit_rounds_half_to_even():
+    # clusters (13, y, z) and (40, y, z) take x in {c, c+1} equally: mean c + 0.5
+    half = [i for i, c in enumerate(cluster_centres()) if c[0] in (13.0, 40.0)
+            and c[1] == 13.0 and c[2] == 12.0]
+    Wp, lab, counts = clustered_points(seed=3, half_up=half)
+    assert all(counts[c] % 2 == 0 for c in half)
+    W = weights_from_points(Wp, seed=3)
+    cf, C = oracle.fit_centroids(W, draws(4), iters=8)
+    got = {tuple(r) for r in C.astype(np.int64).tolist()}
+    assert (14, 13, 12) in got and (13, 13, 12) not in got    # 13.5 -> 14
+    assert (40, 13, 12) in got and (41, 13, 12) not in got    # 40.5 -> 40
+    assert np.isclose(cf.astype(np.float64), 13.5).any() and np.isclose(cf.astype(np.float64), 40.5).any()
+
+
+def test_fit_with_fewer_distinct_points_than_centroids():
+    # one packed row, 16 distinct points on a line (rows 1, 2 all zero): k-means++
+    # never draws a point already covered while any weight is left, so all 16
+    # become centroids; every point then sits on its own centroid
+    xs = np.array([0, 3, 8, 10, 20, 33, 47, 51, 64, 70, 80, 90, 100, 110, 120, 127], np.float64)
+    Wp = np.zeros((1, 16, 3))
+    Wp[0, :, 0] = xs
+    W = np.zeros((3, 16), np.uint16)
+    W[0] = _bf16_exact(xs)                          # alpha = 1 exactly
+    cf, C = oracle.fit_centroids(W, draws(5), iters=3)
+    assert set(cf[:, 0].tolist()) == set(xs.tolist())
+    assert np.all(cf[:, 1:] == 0)
+    assert set(C[:, 0].astype(np.int64).tolist()) == set(xs.astype(np.int64).tolist())
+
+
+def test_kmeanspp_second_centre_follows_d2_weights():
+    # first centre fixed at point 0 (x = 0) by r[0] = 0; over a fine grid of r[1]
+    # the second centre must be point p with frequency D2_p / sum D2 = x_p^2 / sum x^2
+    xs = np.array([0, 3, 8, 10, 20, 33, 47, 51, 64, 70, 80, 90, 100, 110, 120, 127], np.float64)
+    W = np.zeros((3, 16), np.uint16)
+    W[0] = _bf16_exact(xs)
+    T = 2048
+    hits = dict.fromkeys(xs.tolist(), 0)
+    for j in range(T):
+        r = np.zeros(32, np.uint32)
+        r[1] = int((j + 0.5) / T * 2 ** 32)
+        cf, _ = oracle.fit_centroids(W, r, iters=0)
+        assert cf[0, 0] == 0.0
+        hits[float(cf[1, 0])] += 1
+    p = xs ** 2 / (xs ** 2).sum()
+    freq = np.array([hits[x] for x in xs.tolist()]) / T
+    assert np.all(np.abs(freq - p) <= 2.0 / T), np.abs(freq - p).max()
+
+
+def _points_f64(W):
+    Wf = si.bf16_bits_to_f32(W).astype(np.float64)
+    N, K = Wf.shape
+    G = si.groups(N)
+    amax = np.abs(Wf).max(1)
+    alpha = si.bf16_bits_to_f32(si.f32_to_bf16_bits((amax / 127).astype(np.float32))).astype(np.float64)
+    P = np.zeros((G, K, 3))
+    for n in range(N):
+        if alpha[n] > 0:
+            P[n // 3, :, n % 3] = np.abs(Wf[n]) / alpha[n]
+    return P.reshape(-1, 3)
+
+
+def test_lloyd_step_moves_centroids_to_the_means_of_their_points():
+    rng = np.random.default_rng(8)
+    W = si.f32_to_bf16_bits((rng.standard_normal((31, 128)) * 0.02).astype(np.float32))
+    r = draws(9)
+    c0, _ = oracle.fit_centroids(W, r, iters=0)
+    c1, _ = oracle.fit_centroids(W, r, iters=1)
+    P = _points_f64(W)
+    d = ((P[:, None, :] - c0.astype(np.float64)[None]) ** 2).sum(2)
+    lab = d.argmin(1)
+    for l in range(32):
+        if (lab == l).any():
+            assert np.allclose(c1[l], P[lab == l].mean(0), atol=2e-6, rtol=1e-6), l
+        else:
+            assert np.array_equal(c1[l], c0[l])          # an empty cluster stays put
+
+
+def test_lloyd_objective_never_increases():
+    rng = np.random.default_rng(10)
+    W = si.f32_to_bf16_bits((rng.standard_normal((45, 96)) * 0.02).astype(np.float32))
+    P = _points_f64(W)
+    r = draws(11)
+    prev = np.inf
+    for it in range(7):
+        c, _ = oracle.fit_centroids(W, r, iters=it)
+        sse = ((P[:, None, :] - c.astype(np.float64)[None]) ** 2).sum(2).min(1).sum()
+        assert sse <= prev * (1 + 1e-9) + 1e-6, (it, sse, prev)
+        prev = sse
