@@ -400,7 +400,7 @@ def gpu_arm(args):
         roofline["isolated_launch_us"] = round(iso_ms * 1e3, 3)
         roofline["isolated_achieved"] = round(step_bytes / (iso_ms * 1e-3) / 1e9, 1)
 
-    e2e = prefill = unpack = sweep = stack = encode = None
+    e2e = prefill = unpack = sweep = stack = encode = fit = None
     if not args.layer_only:
         e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 4000))
         prefill = prefill_measure(torch, s3d8, dev) if not args.skip_prefill else None
@@ -408,6 +408,7 @@ def gpu_arm(args):
         sweep = decode_sweep_measure(torch, s3d8, dev)
         stack = stack_measure(torch, s3d8, dev)
         encode = encode_measure(torch, s3d8, dev)
+        fit = fit_measure(torch, s3d8, dev)
 
     if rank != 0:
         return
@@ -430,7 +431,7 @@ def gpu_arm(args):
         "device_status": status,
         "roofline": roofline, "variants": variants, "e2e": e2e, "prefill": prefill,
         "decode_sweep": sweep, "text_stack": stack,
-        "unpack": unpack, "encode": encode, "clocks": clocks, "cpu_baseline": cpu,
+        "unpack": unpack, "encode": encode, "fit": fit, "clocks": clocks, "cpu_baseline": cpu,
     }
     print(json.dumps(line))
 
@@ -719,6 +720,38 @@ def encode_measure(torch, s3d8, dev, reps=3):
             "launches": 2 * len(mats) * reps}
 
 
+def fit_measure(torch, s3d8, dev, iters=25, reps=2):
+    """Centroid fit (k-means++ then `iters` Lloyd iterations) on the gate
+    matrix (4096 -> 14336, 19.6 M points), weights N(0, 0.02) drawn on the
+    device.  The Lloyd assignment is the dominant cost: 32 squared distances
+    (8 fp32 operations each) per point and iteration."""
+    gen = torch.Generator(device=dev).manual_seed(11)
+    N, K = 14336, 4096
+    w = (torch.randn((N, K), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    draws = torch.randint(-2 ** 31, 2 ** 31 - 1, (32,), dtype=torch.int32, device=dev,
+                          generator=gen)
+    ws = torch.empty((s3d8.fit_workspace_size(N, K),), dtype=torch.uint8, device=dev)
+    s3d8.fit_centroids(w, draws, iters, ws)
+    torch.cuda.synchronize()
+    res = {}
+    for it in (0, iters):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            s3d8.fit_centroids(w, draws, it, ws)
+        t1.record()
+        t1.synchronize()
+        res[it] = t0.elapsed_time(t1) / reps
+    points = si.groups(N) * K
+    per_iter = (res[iters] - res[0]) / iters
+    return {"workload": "gate matrix 4096 -> 14336, 19.6 M points, 32 centroids",
+            "iters": iters, "ms": round(res[iters], 3), "kmeanspp_ms": round(res[0], 3),
+            "lloyd_ms_per_iter": round(per_iter, 4),
+            "lloyd_gpoints_s": round(points / (per_iter * 1e-3) / 1e9, 1),
+            "lloyd_fp32_tflops": round(points * 32 * 8 / (per_iter * 1e-3) / 1e12, 2)}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 # ---------------------------------------------------------------------------
@@ -795,8 +828,8 @@ def main():
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the M = 2048 tensor-core measurement and print it; for profiling")
     ap.add_argument("--encode-only", action="store_true",
-                    help="run only the encoder measurement (one 11B layer) and print it; for "
-                         "profiling")
+                    help="run only the encoder and centroid-fit measurements and print them; "
+                         "for profiling")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = 10 if args.steps is None else args.steps
@@ -817,6 +850,7 @@ def main():
         s3d8.load(build_if_missing=True)
         print(json.dumps(encode_measure(torch, s3d8, torch.device("cuda:0"),
                                         reps=3 if args.steps is None else args.steps)))
+        print(json.dumps(fit_measure(torch, s3d8, torch.device("cuda:0"))))
         return
     args.steps = 40000 if args.steps is None else args.steps
     args.warmup = 400 if args.warmup is None else args.warmup

@@ -122,6 +122,36 @@ int s3d8_encode(const void *w_bf16, const int8_t *centroids, int64_t N, int64_t 
                 void *stream);
 
 /*
+ * Centroid fit (paper section 3.4, "Quantization": C = Round(Lloyd-Max(W'))
+ * with k-means++ initialisation, Arthur and Vassilvitskii, SODA 2007), on the
+ * ceil(N/3) K points W'_p = (|W[3g+d,k]| / alpha_{3g+d})_{d=0..2}, with
+ * alpha and W' exactly as in s3d8_encode (padded channels are 0).
+ *   w_bf16        : [N, K] bfloat16, row-major, 16-byte aligned
+ *   draws         : [32] uint32 random draws (device), 4-byte aligned
+ *   iters         : Lloyd iterations, 0..S3D8_FIT_MAX_ITERS (0: k-means++ only)
+ *   centroids_f32 : [32 * 3] fp32 output, the fitted centroids before Round
+ *   centroids     : [32 * 3] int8 output, the table: rint (ties to even) of
+ *                   centroids_f32 clamped to 0..127
+ *   workspace     : s3d8_fit_workspace_size(N, K) bytes, 256-byte aligned,
+ *                   caller-owned, not shared by calls that overlap on the GPU
+ *                   (about 16 bytes per point)
+ * k-means++: centre 0 is point floor(draws[0] Np / 2^32); centre t >= 1 is
+ * the first point whose inclusive prefix sum of w_p = floor(D2_p 2^20) exceeds
+ * floor(draws[t] S / 2^32), S = sum w_p, D2_p the fp32 squared distance to the
+ * nearest chosen centre (point floor(draws[t] Np / 2^32) when S = 0).
+ * Lloyd: nearest centroid per point in fp32 (lowest index on a tie); each
+ * nonempty cluster's centroid becomes float(RN(sum_p floor(W'_p 2^20) / n)
+ * 2^-20) per component (fp64 division); empty clusters stay.  All sums are
+ * exact integers, so the result does not depend on the order of summation.
+ * 2 + 63 + 2 iters + 1 launches; N == 0 is rejected (no points).
+ */
+#define S3D8_FIT_MAX_ITERS 10000
+size_t s3d8_fit_workspace_size(int64_t N, int64_t K);
+int s3d8_fit_centroids(const void *w_bf16, int64_t N, int64_t K, const uint32_t *draws,
+                       int32_t iters, float *centroids_f32, int8_t *centroids, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
  * Self-test of the encoder's scaled magnitude: out[i] = |x[i]| / alpha[i]
  * through the same device code the encoder uses (a correction step on a
  * per-channel reciprocal, IEEE division outside its range).  Must equal the

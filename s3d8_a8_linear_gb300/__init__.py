@@ -72,6 +72,9 @@ def load(build_if_missing: bool = False):
     L.s3d8_decode.argtypes = [P, P, I64, I64, P, P]
     L.s3d8_encode.argtypes = [P, P, I64, I64, P, P, P, SZ, P]
     L.s3d8_selftest_scaled_abs.argtypes = [P, P, I64, P, P]
+    L.s3d8_fit_workspace_size.argtypes = [I64, I64]
+    L.s3d8_fit_workspace_size.restype = SZ
+    L.s3d8_fit_centroids.argtypes = [P, I64, I64, P, ctypes.c_int32, P, P, P, SZ, P]
     L.s3d8_linear_workspace_size.argtypes = [I64, I64, I64, I]
     L.s3d8_linear_workspace_size.restype = SZ
     L.s3d8_linear.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, SZ, P]
@@ -85,6 +88,7 @@ def load(build_if_missing: bool = False):
     L.s3d8_status_string.restype = ctypes.c_char_p
     L.s3d8_version.argtypes = []
     for fn in ("s3d8_quantize_act", "s3d8_decode", "s3d8_encode", "s3d8_selftest_scaled_abs",
+               "s3d8_fit_centroids",
                "s3d8_linear", "s3d8_linear_ex",
                "s3d8_linear_acc_i32", "s3d8_linear_batch", "s3d8_selftest_wait_timeout",
                "s3d8_device_status", "s3d8_version"):
@@ -176,6 +180,32 @@ def encode(w: torch.Tensor, centroids: torch.Tensor, packed: torch.Tensor | None
                             _stream(w.device))
     _check("s3d8_encode", st)
     return packed, chan_scale
+
+
+def fit_workspace_size(N: int, K: int) -> int:
+    return int(load().s3d8_fit_workspace_size(N, K))
+
+
+def fit_centroids(w: torch.Tensor, draws: torch.Tensor, iters: int,
+                  workspace: torch.Tensor | None = None):
+    """Lloyd-Max centroid fit from k-means++ on the scaled 3-vectors of bf16
+    W[N, K]; draws: 32 int32 (read as uint32) on the device.  Returns (fp32
+    centroids [32, 3], int8 table [32, 3])."""
+    if w.dim() != 2:
+        raise ValueError("w must be 2-D [N, K]")
+    N, K = w.shape
+    cf = torch.empty((32, 3), dtype=torch.float32, device=w.device)
+    C = torch.empty((32, 3), dtype=torch.int8, device=w.device)
+    if workspace is None:
+        workspace = torch.empty((max(fit_workspace_size(N, K), 1),), dtype=torch.uint8,
+                                device=w.device)
+    st = load().s3d8_fit_centroids(_dev(w, "w", torch.bfloat16), N, K,
+                                   _dev(draws, "draws", torch.int32, (32,)), int(iters),
+                                   _dev(cf, "cf", torch.float32), _dev(C, "C", torch.int8),
+                                   _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                                   _stream(w.device))
+    _check("s3d8_fit_centroids", st)
+    return cf, C
 
 
 def selftest_scaled_abs(x: torch.Tensor, alpha: torch.Tensor) -> torch.Tensor:

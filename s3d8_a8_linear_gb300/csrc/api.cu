@@ -148,6 +148,37 @@ int s3d8_encode(const void *w_bf16, const int8_t *centroids, int64_t N, int64_t 
                                      workspace, static_cast<cudaStream_t>(stream)));
 }
 
+size_t s3d8_fit_workspace_size(int64_t N, int64_t K)
+{
+    if (N <= 0 || K <= 0 || N > S3D8_MAX_N || K > S3D8_MAX_K || K % 16 != 0)
+        return 0;
+    return fit_workspace_bytes(N, K);
+}
+
+int s3d8_fit_centroids(const void *w_bf16, int64_t N, int64_t K, const uint32_t *draws,
+                       int32_t iters, float *centroids_f32, int8_t *centroids, void *workspace,
+                       size_t workspace_bytes, void *stream)
+{
+    int st = check_k(K);
+    if (st == S3D8_OK)
+        st = check_mn(0, N);
+    if (st != S3D8_OK)
+        return st;
+    if (N == 0 || iters < 0 || iters > S3D8_FIT_MAX_ITERS)
+        return S3D8_ERR_INVALID_ARG;
+    if (!w_bf16 || !draws || !centroids_f32 || !centroids)
+        return S3D8_ERR_INVALID_ARG;
+    if (!aligned(w_bf16, 16) || !aligned(draws, 4) || !aligned(centroids_f32, 4))
+        return S3D8_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < fit_workspace_bytes(N, K))
+        return S3D8_ERR_WORKSPACE;
+    if (!aligned(workspace, 256))
+        return S3D8_ERR_ALIGNMENT;
+    return cuda_status(launch_fit(static_cast<const __nv_bfloat16 *>(w_bf16), (int)N, (int)K, draws,
+                                  iters, centroids_f32, centroids, workspace,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
 int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t n, float *out,
                              void *stream)
 {

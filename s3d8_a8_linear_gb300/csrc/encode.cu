@@ -394,4 +394,399 @@ cudaError_t launch_encode(const __nv_bfloat16 *w, const int8_t *C, int N, int K,
     return cudaGetLastError();
 }
 
+// ===========================================================================
+// Centroid fit (paper section 3.4, "Quantization": C = Round(Lloyd-Max(W'))
+// with k-means++ initialisation, Arthur and Vassilvitskii, SODA 2007).
+//
+// Points: p = g K + k, W'_p = (|W[3g+d,k]| / alpha_{3g+d})_d exactly as in the
+// encoder, stored as three fp32 arrays (structure of arrays).  Draws are 32
+// caller-supplied 32-bit integers r[t].  Every sum is an exact integer on a
+// 2^-20 grid (floor), so the order in which the GPU adds is immaterial:
+//   k-means++: centre 0 = point floor(r[0] Np / 2^32); for t >= 1, with
+//     w_p = floor(D2_p 2^20) (D2_p the fp32 squared distance to the nearest
+//     chosen centre) and S = sum w_p, centre t = the first point whose
+//     inclusive prefix sum of w exceeds floor(r[t] S / 2^32) (point
+//     floor(r[t] Np / 2^32) when S = 0);
+//   Lloyd: `iters` times, nearest centroid per point (fp32, lowest index on a
+//     tie), then each nonempty cluster's centroid becomes, per component,
+//     float(RN(sum floor(W' 2^20) / n) 2^-20) with the division in fp64; an
+//     empty cluster keeps its centroid;
+//   Round: to nearest, ties to even, clamped to 0..127.
+// ===========================================================================
+constexpr int kFitThreads = 256;
+constexpr int kKppSelectThreads = 1024;
+
+struct FitSpace {
+    __nv_bfloat16 *alpha;   // [N]
+    float *P[3];            // [Np] each
+    float *D2;              // [Np]
+    unsigned long long *bsum;  // [blocks] k-means++ block sums of w
+    unsigned long long *acc;   // [32][4] Lloyd sums (x, y, z) and counts
+};
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// k-means++ point blocks: 4 per SM, at most one per thread of the select kernel.
+static int fit_blocks()
+{
+    const int b = device_sm_count() * 4;
+    return b < kKppSelectThreads ? b : kKppSelectThreads;
+}
+
+// Byte offsets of the workspace parts; total returned.
+static size_t fit_layout(int64_t N, int64_t K, int blocks, size_t off[6])
+{
+    const int64_t Np = (N + 2) / 3 * K;
+    size_t o = 0;
+    off[0] = o;  o = align_up(o + (size_t)N * 2, 256);
+    for (int d = 0; d < 3; ++d) {
+        off[1 + d] = o;
+        o = align_up(o + (size_t)Np * 4, 256);
+    }
+    off[4] = o;  o = align_up(o + (size_t)Np * 4, 256);
+    off[5] = o;  o = align_up(o + (size_t)blocks * 8 + 32 * 4 * 8, 256);
+    return o;
+}
+
+size_t fit_workspace_bytes(int64_t N, int64_t K)
+{
+    size_t off[6];
+    return fit_layout(N, K, fit_blocks(), off);
+}
+
+static FitSpace fit_space(void *ws, int64_t N, int64_t K, int blocks)
+{
+    size_t off[6];
+    fit_layout(N, K, blocks, off);
+    char *b = static_cast<char *>(ws);
+    FitSpace f;
+    f.alpha = reinterpret_cast<__nv_bfloat16 *>(b + off[0]);
+    for (int d = 0; d < 3; ++d)
+        f.P[d] = reinterpret_cast<float *>(b + off[1 + d]);
+    f.D2 = reinterpret_cast<float *>(b + off[4]);
+    f.bsum = reinterpret_cast<unsigned long long *>(b + off[5]);
+    f.acc = f.bsum + blocks;
+    return f;
+}
+
+// Scaled magnitudes of all points, 8 consecutive k of one packed row per thread.
+__global__ __launch_bounds__(kFitThreads) void fit_points_kernel(
+    const __nv_bfloat16 *__restrict__ w, const __nv_bfloat16 *__restrict__ alpha, int N, int K,
+    int G, float *__restrict__ P0, float *__restrict__ P1, float *__restrict__ P2)
+{
+    const int chunks = K / 8;
+    const int64_t items = (int64_t)G * chunks;
+    float *const P[3] = {P0, P1, P2};
+    for (int64_t it = (int64_t)blockIdx.x * kFitThreads + threadIdx.x; it < items;
+         it += (int64_t)gridDim.x * kFitThreads) {
+        const int g = (int)(it / chunks);
+        const int c = (int)(it - (int64_t)g * chunks);
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const int n = 3 * g + d;
+            uint32_t u[4] = {0u, 0u, 0u, 0u};
+            float a = 0.0f;
+            if (n < N) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(w + (size_t)n * K) + c);
+                u[0] = v.x;
+                u[1] = v.y;
+                u[2] = v.z;
+                u[3] = v.w;
+                a = __bfloat162float(alpha[n]);
+            }
+            const ChanDiv dv = chan_div(a);
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                q[e] = scaled_abs(elem_abs(u, e), dv);
+            float4 *dst = reinterpret_cast<float4 *>(P[d] + (size_t)it * 8);
+            dst[0] = make_float4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_float4(q[4], q[5], q[6], q[7]);
+        }
+    }
+}
+
+// floor(r x / 2^32) for r < 2^32 and x < 2^62.
+__device__ __forceinline__ unsigned long long scale_draw(uint32_t r, unsigned long long x)
+{
+    return (unsigned long long)r * (x >> 32) + (((unsigned long long)r * (x & 0xFFFFFFFFull)) >> 32);
+}
+
+__device__ __forceinline__ unsigned long long d2_weight(float d2)
+{
+    return __float2ull_rz(d2 * 1048576.0f);   // d2 < 2^17: the product is exact
+}
+
+// Block b of `blocks` covers points [b per, min((b + 1) per, Np)).
+__device__ __forceinline__ void block_range(int64_t Np, int blocks, int b, int64_t &lo, int64_t &hi)
+{
+    const int64_t per = (Np + blocks - 1) / blocks;
+    lo = (int64_t)b * per;
+    hi = lo + per < Np ? lo + per : Np;
+    if (lo > Np)
+        lo = Np;
+}
+
+// D2 update against centre t, and per-block sums of the weights.
+__global__ __launch_bounds__(kFitThreads) void kpp_update_kernel(
+    const float *__restrict__ P0, const float *__restrict__ P1, const float *__restrict__ P2,
+    float *__restrict__ D2, int64_t Np, const float *__restrict__ cf, int t,
+    unsigned long long *__restrict__ bsum)
+{
+    __shared__ unsigned long long red[kFitThreads / 32];
+    int64_t lo, hi;
+    block_range(Np, gridDim.x, blockIdx.x, lo, hi);
+    const float4 c = make_float4(cf[3 * t], cf[3 * t + 1], cf[3 * t + 2], 0.0f);
+    unsigned long long sum = 0;
+    for (int64_t p = lo + threadIdx.x; p < hi; p += kFitThreads) {
+        float d = dist2(c, P0[p], P1[p], P2[p]);
+        if (t > 0)
+            d = fminf(d, D2[p]);
+        D2[p] = d;
+        sum += d2_weight(d);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long s2 = 0;
+        for (int i = 0; i < kFitThreads / 32; ++i)
+            s2 += red[i];
+        bsum[blockIdx.x] = s2;
+    }
+}
+
+// Inclusive prefix sum over the CTA (blockDim.x a multiple of 32, at most 1024).
+__device__ unsigned long long block_inclusive_scan(unsigned long long v,
+                                                   unsigned long long *warp_tot)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o)
+            v += n;
+    }
+    if (lane == 31)
+        warp_tot[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+        const int nw = blockDim.x >> 5;
+        unsigned long long t = lane < nw ? warp_tot[lane] : 0ull;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, t, o);
+            if (lane >= o)
+                t += n;
+        }
+        if (lane < nw)
+            warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const unsigned long long before = wid > 0 ? warp_tot[wid - 1] : 0ull;
+    __syncthreads();   // warp_tot may be reused by the caller's next scan
+    return v + before;
+}
+
+// Choose centre t (one CTA): uniform for t = 0 or when every weight is 0,
+// otherwise the D^2 draw by a two-level prefix search (block sums, then the
+// chosen block's points in per-thread chunks).
+__global__ __launch_bounds__(kKppSelectThreads) void kpp_select_kernel(
+    const float *__restrict__ P0, const float *__restrict__ P1, const float *__restrict__ P2,
+    const float *__restrict__ D2, int64_t Np, const unsigned long long *__restrict__ bsum,
+    int blocks, const uint32_t *__restrict__ r, int t, float *__restrict__ cf)
+{
+    __shared__ unsigned long long warp_tot[32];
+    __shared__ unsigned long long sh_target, sh_excl;
+    __shared__ int sh_block;
+    __shared__ long long sh_idx;
+    const uint32_t draw = r[t];
+    if (threadIdx.x == 0) {
+        sh_idx = -1;
+        sh_block = -1;
+    }
+    unsigned long long incl = 0, mine = 0;
+    if (t > 0) {
+        mine = (int)threadIdx.x < blocks ? bsum[threadIdx.x] : 0ull;
+        incl = block_inclusive_scan(mine, warp_tot);
+        // the total is the last thread's inclusive sum
+        if (threadIdx.x == blockDim.x - 1)
+            sh_target = incl;
+        __syncthreads();
+        const unsigned long long S = sh_target;
+        __syncthreads();
+        if (S != 0) {
+            const unsigned long long target = scale_draw(draw, S);
+            if (incl > target && incl - mine <= target) {
+                sh_block = (int)threadIdx.x;
+                sh_target = target;
+                sh_excl = incl - mine;
+            }
+        }
+    }
+    __syncthreads();
+    if (sh_block < 0) {
+        if (threadIdx.x == 0)
+            sh_idx = (long long)scale_draw(draw, (unsigned long long)Np);
+    } else {
+        int64_t lo, hi;
+        block_range(Np, blocks, sh_block, lo, hi);
+        const int64_t n = hi - lo;
+        const int64_t per = (n + kKppSelectThreads - 1) / kKppSelectThreads;
+        const int64_t c0 = lo + (int64_t)threadIdx.x * per;
+        const int64_t c1 = c0 + per < hi ? c0 + per : hi;
+        unsigned long long s = 0;
+        for (int64_t p = c0; p < c1; ++p)
+            s += d2_weight(D2[p]);
+        const unsigned long long cincl = block_inclusive_scan(s, warp_tot);
+        const unsigned long long want = sh_target - sh_excl;   // residual within the block
+        if (cincl > want && cincl - s <= want) {
+            unsigned long long run = cincl - s;
+            for (int64_t p = c0; p < c1; ++p) {
+                run += d2_weight(D2[p]);
+                if (run > want) {
+                    sh_idx = p;
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // the block and point sums come from the same D2 values, so a point is
+        // always found; the guard only keeps the read in bounds
+        const long long i = sh_idx >= 0 && sh_idx < Np ? sh_idx : 0;
+        cf[3 * t] = P0[i];
+        cf[3 * t + 1] = P1[i];
+        cf[3 * t + 2] = P2[i];
+    }
+}
+
+// Lloyd assignment: nearest centroid per point, sums into per-warp shared bins,
+// then one global add per bin and CTA.  Np is a multiple of 16 (K is), so every
+// thread takes 4 whole points.
+__global__ __launch_bounds__(kFitThreads) void lloyd_assign_kernel(
+    const float *__restrict__ P0, const float *__restrict__ P1, const float *__restrict__ P2,
+    int64_t Np, const float *__restrict__ cf, unsigned long long *__restrict__ acc)
+{
+    __shared__ float4 cen[32];
+    __shared__ unsigned long long bins[kFitThreads / 32][32][4];
+    if (threadIdx.x < 32)
+        cen[threadIdx.x] = make_float4(cf[3 * threadIdx.x], cf[3 * threadIdx.x + 1],
+                                       cf[3 * threadIdx.x + 2], 0.0f);
+    for (int i = threadIdx.x; i < (kFitThreads / 32) * 32 * 4; i += kFitThreads)
+        (&bins[0][0][0])[i] = 0ull;
+    __syncthreads();
+    unsigned long long(*mybins)[4] = bins[threadIdx.x >> 5];
+    const int64_t quads = Np / 4;
+    for (int64_t q = (int64_t)blockIdx.x * kFitThreads + threadIdx.x; q < quads;
+         q += (int64_t)gridDim.x * kFitThreads) {
+        const float4 x = reinterpret_cast<const float4 *>(P0)[q];
+        const float4 y = reinterpret_cast<const float4 *>(P1)[q];
+        const float4 z = reinterpret_cast<const float4 *>(P2)[q];
+        const float px[4] = {x.x, x.y, x.z, x.w}, py[4] = {y.x, y.y, y.z, y.w},
+                    pz[4] = {z.x, z.y, z.z, z.w};
+        float bestd[4];
+        int best[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            bestd[j] = dist2(cen[0], px[j], py[j], pz[j]);
+            best[j] = 0;
+        }
+#pragma unroll 4
+        for (int l = 1; l < 32; ++l) {
+            const float4 c = cen[l];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float d = dist2(c, px[j], py[j], pz[j]);
+                if (d < bestd[j]) {
+                    bestd[j] = d;
+                    best[j] = l;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            atomicAdd(&mybins[best[j]][0], d2_weight(px[j]));
+            atomicAdd(&mybins[best[j]][1], d2_weight(py[j]));
+            atomicAdd(&mybins[best[j]][2], d2_weight(pz[j]));
+            atomicAdd(&mybins[best[j]][3], 1ull);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        const int l = threadIdx.x >> 2, j = threadIdx.x & 3;
+        unsigned long long s = 0;
+        for (int wi = 0; wi < kFitThreads / 32; ++wi)
+            s += bins[wi][l][j];
+        if (s)
+            atomicAdd(&acc[4 * l + j], s);
+    }
+}
+
+// New centroids from the sums (empty clusters stay), then the sums are cleared.
+__global__ void lloyd_update_kernel(unsigned long long *__restrict__ acc, float *__restrict__ cf)
+{
+    const int i = threadIdx.x;
+    if (i < 96) {
+        const int l = i / 3, d = i - 3 * (i / 3);
+        const unsigned long long n = acc[4 * l + 3];
+        if (n != 0)
+            cf[i] = (float)(((double)acc[4 * l + d] / (double)n) * 0x1p-20);
+    }
+    __syncthreads();
+    if (i < 128)
+        acc[i] = 0ull;
+}
+
+__global__ void fit_round_kernel(const float *__restrict__ cf, int8_t *__restrict__ C)
+{
+    const int i = threadIdx.x;
+    if (i < 96) {
+        int v = __float2int_rn(cf[i]);
+        v = v < 0 ? 0 : (v > 127 ? 127 : v);
+        C[i] = (int8_t)v;
+    }
+}
+
+cudaError_t launch_fit(const __nv_bfloat16 *w, int N, int K, const uint32_t *r, int iters,
+                       float *cf, int8_t *C, void *workspace, cudaStream_t stream)
+{
+    const int sms = device_sm_count();
+    const int blocks = fit_blocks();
+    const FitSpace f = fit_space(workspace, N, K, blocks);
+    const int G = (N + 2) / 3;
+    const int64_t Np = (int64_t)G * K;
+    const int rows_ctas = (N + kScaleRowsPerCta - 1) / kScaleRowsPerCta;
+    const int g1 = rows_ctas < sms * 8 ? rows_ctas : sms * 8;
+    encode_prepare_kernel<<<g1, kScaleThreads, 0, stream>>>(w, nullptr, N, K, g1, f.alpha, nullptr);
+    const int64_t items = (int64_t)G * (K / 8);
+    const int64_t want = (items + kFitThreads - 1) / kFitThreads;
+    const int gp = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+    fit_points_kernel<<<gp, kFitThreads, 0, stream>>>(w, f.alpha, N, K, G, f.P[0], f.P[1], f.P[2]);
+    kpp_select_kernel<<<1, kKppSelectThreads, 0, stream>>>(f.P[0], f.P[1], f.P[2], f.D2, Np, f.bsum,
+                                                          blocks, r, 0, cf);
+    for (int t = 1; t < 32; ++t) {
+        kpp_update_kernel<<<blocks, kFitThreads, 0, stream>>>(f.P[0], f.P[1], f.P[2], f.D2, Np, cf,
+                                                              t - 1, f.bsum);
+        kpp_select_kernel<<<1, kKppSelectThreads, 0, stream>>>(f.P[0], f.P[1], f.P[2], f.D2, Np,
+                                                              f.bsum, blocks, r, t, cf);
+    }
+    cudaError_t e = cudaMemsetAsync(f.acc, 0, 32 * 4 * sizeof(unsigned long long), stream);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t quads = Np / 4;
+    const int64_t wantq = (quads + kFitThreads - 1) / kFitThreads;
+    const int ga = (int)(wantq < (int64_t)sms * 4 ? wantq : (int64_t)sms * 4);
+    for (int it = 0; it < iters; ++it) {
+        lloyd_assign_kernel<<<ga, kFitThreads, 0, stream>>>(f.P[0], f.P[1], f.P[2], Np, cf, f.acc);
+        lloyd_update_kernel<<<1, 128, 0, stream>>>(f.acc, cf);
+    }
+    fit_round_kernel<<<1, 128, 0, stream>>>(cf, C);
+    return cudaGetLastError();
+}
+
 }  // namespace s3d8

@@ -141,6 +141,15 @@ def test_other_entry_points_reject(lib):
     assert enc(A16, A16B, 6, 32, A16C, A16, None, WS, None) == -6            # no workspace
     assert enc(A16, A16B, 6, 32, A16C, A16, A16B, WS - 1, None) == -6        # too small
     assert enc(A16, A16B, 6, 32, A16C, A16, A16B + 8, WS, None) == -2        # ws alignment
+    fit = lib.s3d8_fit_centroids
+    assert fit(A16, 6, 32, A16B, 1, A16C, A16, A16B, 16, None) == -6             # ws too small
+    assert fit(A16, 0, 32, A16B, 1, A16C, A16, A16B, 1 << 30, None) == -1        # no points
+    assert fit(A16, 6, 24, A16B, 1, A16C, A16, A16B, 1 << 30, None) == -1        # K % 16
+    assert fit(A16, 6, 32, A16B, -1, A16C, A16, A16B, 1 << 30, None) == -1       # iters
+    assert fit(A16, 6, 32, None, 1, A16C, A16, A16B, 1 << 30, None) == -1
+    assert fit(A16 + 8, 6, 32, A16B, 1, A16C, A16, A16B, 1 << 30, None) == -2
+    assert fit(A16, 6, 32, A16B, 1, A16C, A16, A16B + 16, 1 << 30, None) == -2   # ws alignment
+    assert lib.s3d8_fit_workspace_size(6, 24) == 0
     assert lib.s3d8_selftest_scaled_abs(A16, A16B, -1, A16C, None) == -1
     assert lib.s3d8_selftest_scaled_abs(A16 + 1, A16B, 4, A16C, None) == -2
 
