@@ -512,15 +512,28 @@ __device__ __forceinline__ unsigned long long scale_draw(uint32_t r, unsigned lo
     return (unsigned long long)r * (x >> 32) + (((unsigned long long)r * (x & 0xFFFFFFFFull)) >> 32);
 }
 
-__device__ __forceinline__ unsigned long long d2_weight(float d2)
+// floor(x 2^20) for 0 <= x < 2^23 without a float-to-integer conversion (those
+// run on the FP64 pipe here): ip = floor(x) and floor(frac(x) 2^20) each come
+// from the low bits of an add of 2^23 rounded toward zero; x - ip is exact.
+__device__ __forceinline__ unsigned long long fixed20(float x)
 {
-    return __float2ull_rz(d2 * 1048576.0f);   // d2 < 2^17: the product is exact
+    const float t = __fadd_rz(x, 8388608.0f);                 // 2^23 + floor(x)
+    const float fr = __fsub_rn(x, __fsub_rn(t, 8388608.0f));  // x - floor(x), exact
+    const float u = __fadd_rz(__fmul_rn(fr, 1048576.0f), 8388608.0f);
+    return ((unsigned long long)(__float_as_uint(t) & 0x7FFFFFu) << 20) |
+           (__float_as_uint(u) & 0xFFFFFu);
 }
 
-// Block b of `blocks` covers points [b per, min((b + 1) per, Np)).
+__device__ __forceinline__ unsigned long long d2_weight(float d2)
+{
+    return fixed20(d2);   // d2 < 2^17
+}
+
+// Block b of `blocks` covers points [b per, min((b + 1) per, Np)), per a
+// multiple of 4 (Np is a multiple of 16), so that blocks start on whole quads.
 __device__ __forceinline__ void block_range(int64_t Np, int blocks, int b, int64_t &lo, int64_t &hi)
 {
-    const int64_t per = (Np + blocks - 1) / blocks;
+    const int64_t per = ((Np + blocks - 1) / blocks + 3) / 4 * 4;
     lo = (int64_t)b * per;
     hi = lo + per < Np ? lo + per : Np;
     if (lo > Np)
@@ -538,12 +551,18 @@ __global__ __launch_bounds__(kFitThreads) void kpp_update_kernel(
     block_range(Np, gridDim.x, blockIdx.x, lo, hi);
     const float4 c = make_float4(cf[3 * t], cf[3 * t + 1], cf[3 * t + 2], 0.0f);
     unsigned long long sum = 0;
-    for (int64_t p = lo + threadIdx.x; p < hi; p += kFitThreads) {
-        float d = dist2(c, P0[p], P1[p], P2[p]);
-        if (t > 0)
-            d = fminf(d, D2[p]);
-        D2[p] = d;
-        sum += d2_weight(d);
+    for (int64_t q = lo / 4 + threadIdx.x; q < hi / 4; q += kFitThreads) {
+        const float4 x = reinterpret_cast<const float4 *>(P0)[q];
+        const float4 y = reinterpret_cast<const float4 *>(P1)[q];
+        const float4 z = reinterpret_cast<const float4 *>(P2)[q];
+        float4 d = make_float4(dist2(c, x.x, y.x, z.x), dist2(c, x.y, y.y, z.y),
+                               dist2(c, x.z, y.z, z.z), dist2(c, x.w, y.w, z.w));
+        if (t > 0) {
+            const float4 o = reinterpret_cast<const float4 *>(D2)[q];
+            d = make_float4(fminf(d.x, o.x), fminf(d.y, o.y), fminf(d.z, o.z), fminf(d.w, o.w));
+        }
+        reinterpret_cast<float4 *>(D2)[q] = d;
+        sum += d2_weight(d.x) + d2_weight(d.y) + d2_weight(d.z) + d2_weight(d.w);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
@@ -667,20 +686,26 @@ __global__ __launch_bounds__(kKppSelectThreads) void kpp_select_kernel(
 
 // Lloyd assignment: nearest centroid per point, sums into per-warp shared bins,
 // then one global add per bin and CTA.  Np is a multiple of 16 (K is), so every
-// thread takes 4 whole points.
+// thread takes 4 whole points.  A point's fixed-point coordinate v < 2^27 goes
+// into a warp bin as two 32-bit atomic adds, v mod 2^16 and v / 2^16; the
+// launch keeps every warp at no more than 2^16 points (kLloydMaxWarpPoints),
+// so neither part can wrap, and the CTA recombines them exactly in 64 bits.
+constexpr int kLloydMaxWarpPoints = 1 << 16;
+constexpr int kBinWords = 8;   // x lo, x hi, y lo, y hi, z lo, z hi, count, unused
+
 __global__ __launch_bounds__(kFitThreads) void lloyd_assign_kernel(
     const float *__restrict__ P0, const float *__restrict__ P1, const float *__restrict__ P2,
     int64_t Np, const float *__restrict__ cf, unsigned long long *__restrict__ acc)
 {
     __shared__ float4 cen[32];
-    __shared__ unsigned long long bins[kFitThreads / 32][32][4];
+    __shared__ uint32_t bins[kFitThreads / 32][32][kBinWords];
     if (threadIdx.x < 32)
         cen[threadIdx.x] = make_float4(cf[3 * threadIdx.x], cf[3 * threadIdx.x + 1],
                                        cf[3 * threadIdx.x + 2], 0.0f);
-    for (int i = threadIdx.x; i < (kFitThreads / 32) * 32 * 4; i += kFitThreads)
-        (&bins[0][0][0])[i] = 0ull;
+    for (int i = threadIdx.x; i < (kFitThreads / 32) * 32 * kBinWords; i += kFitThreads)
+        (&bins[0][0][0])[i] = 0u;
     __syncthreads();
-    unsigned long long(*mybins)[4] = bins[threadIdx.x >> 5];
+    uint32_t(*mybins)[kBinWords] = bins[threadIdx.x >> 5];
     const int64_t quads = Np / 4;
     for (int64_t q = (int64_t)blockIdx.x * kFitThreads + threadIdx.x; q < quads;
          q += (int64_t)gridDim.x * kFitThreads) {
@@ -710,18 +735,29 @@ __global__ __launch_bounds__(kFitThreads) void lloyd_assign_kernel(
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            atomicAdd(&mybins[best[j]][0], d2_weight(px[j]));
-            atomicAdd(&mybins[best[j]][1], d2_weight(py[j]));
-            atomicAdd(&mybins[best[j]][2], d2_weight(pz[j]));
-            atomicAdd(&mybins[best[j]][3], 1ull);
+            uint32_t *bin = mybins[best[j]];
+            const uint32_t vx = (uint32_t)fixed20(px[j]), vy = (uint32_t)fixed20(py[j]),
+                           vz = (uint32_t)fixed20(pz[j]);
+            atomicAdd(bin + 0, vx & 0xFFFFu);
+            atomicAdd(bin + 1, vx >> 16);
+            atomicAdd(bin + 2, vy & 0xFFFFu);
+            atomicAdd(bin + 3, vy >> 16);
+            atomicAdd(bin + 4, vz & 0xFFFFu);
+            atomicAdd(bin + 5, vz >> 16);
+            atomicAdd(bin + 6, 1u);
         }
     }
     __syncthreads();
     if (threadIdx.x < 128) {
         const int l = threadIdx.x >> 2, j = threadIdx.x & 3;
         unsigned long long s = 0;
-        for (int wi = 0; wi < kFitThreads / 32; ++wi)
-            s += bins[wi][l][j];
+        for (int wi = 0; wi < kFitThreads / 32; ++wi) {
+            if (j < 3)
+                s += (unsigned long long)bins[wi][l][2 * j] +
+                     ((unsigned long long)bins[wi][l][2 * j + 1] << 16);
+            else
+                s += bins[wi][l][6];
+        }
         if (s)
             atomicAdd(&acc[4 * l + j], s);
     }
@@ -780,7 +816,14 @@ cudaError_t launch_fit(const __nv_bfloat16 *w, int N, int K, const uint32_t *r, 
         return e;
     const int64_t quads = Np / 4;
     const int64_t wantq = (quads + kFitThreads - 1) / kFitThreads;
-    const int ga = (int)(wantq < (int64_t)sms * 4 ? wantq : (int64_t)sms * 4);
+    // at least enough CTAs that no warp takes more than kLloydMaxWarpPoints points:
+    // a warp's lanes take quads q, q + grid * 256, ..., 4 points each
+    const int64_t min_grid = (quads + (int64_t)kFitThreads * (kLloydMaxWarpPoints / 4 / 32) - 1) /
+                             ((int64_t)kFitThreads * (kLloydMaxWarpPoints / 4 / 32));
+    int64_t ga64 = wantq < (int64_t)sms * 4 ? wantq : (int64_t)sms * 4;
+    if (ga64 < min_grid)
+        ga64 = min_grid;
+    const int ga = (int)ga64;
     for (int it = 0; it < iters; ++it) {
         lloyd_assign_kernel<<<ga, kFitThreads, 0, stream>>>(f.P[0], f.P[1], f.P[2], Np, cf, f.acc);
         lloyd_update_kernel<<<1, 128, 0, stream>>>(f.acc, cf);
