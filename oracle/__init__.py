@@ -70,6 +70,8 @@ def lib():
         L.s3d8o_encode.restype = I32
         L.s3d8o_fit_centroids.argtypes = [P, I64, I64, P, I32, P, P]
         L.s3d8o_fit_centroids.restype = I32
+        L.s3d8o_fake_quant.argtypes = [P, P, I64, I64, P]
+        L.s3d8o_fake_quant.restype = I32
         L.s3d8o_linear_out.restype = None
     return _lib
 
@@ -215,3 +217,15 @@ def fit_centroids(w_bf16_bits: np.ndarray, r: np.ndarray, iters: int):
     if lib().s3d8o_fit_centroids(_ptr(w), N, K, _ptr(r), int(iters), _ptr(cf), _ptr(C)) != 0:
         raise MemoryError("oracle fit scratch")
     return cf, C
+
+
+def fake_quant(w_bf16_bits: np.ndarray, C: np.ndarray) -> np.ndarray:
+    """QAT fake-quant forward: bf16 W [N, K] -> bf16 bits of s alpha C[q][n mod 3]
+    (paper section 3.4, Eq. 1 applied to the direct cast)."""
+    w = _as(w_bf16_bits, np.uint16)
+    N, K = w.shape
+    C = _as(C, np.int8, (32, 3))
+    out = np.empty((N, K), np.uint16)
+    if lib().s3d8o_fake_quant(_ptr(w), _ptr(C), N, K, _ptr(out)) != 0:
+        raise MemoryError("oracle fake-quant scratch")
+    return out

@@ -43,7 +43,13 @@
  *     same result; a mean is RN(RN(sum / count) * 2^-20) in fp64, then
  *     rounded to fp32; an empty cluster keeps its centroid; the iteration
  *     count is fixed by the caller; Round is to nearest, ties to even,
- *     clamped to 0..127.
+ *     clamped to 0..127;
+ *   - fake-quant forward ([P] section 3.4, QAT: the weight is quantised in
+ *     the forward pass and reconstructed by Eq. 1): W_hat = s alpha C[q][n mod
+ *     3] from the direct cast, the product alpha C formed in fp32 (exact: at
+ *     most 15 significant bits) and rounded once to bf16 (the training
+ *     matmul's dtype); the straight-through backward passes the gradient of
+ *     W_hat to the weights unchanged, so it needs no code here.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math, no
  * FMA contraction, so that the fp32 activation quantiser is plain IEEE
@@ -445,5 +451,35 @@ int32_t s3d8o_fit_centroids(const uint16_t *w, int64_t N, int64_t K, const uint3
     }
     free(P);
     free(D2);
+    return 0;
+}
+
+
+/* ---------------------------------------------------------------------------
+ * Fake-quant forward, [P] section 3.4 "Quantization" (QAT phase: quantise in
+ * the forward pass with the centroids frozen, reconstruct by Eq. 1):
+ * w_hat[n,k] = bf16_rn(s * alpha_n * C[q][n mod 3]) with (alpha, s, q) from
+ * s3d8o_encode.  Returns 0, or -1 when scratch cannot be allocated.
+ * ------------------------------------------------------------------------- */
+int32_t s3d8o_fake_quant(const uint16_t *w, const int8_t *C, int64_t N, int64_t K,
+                         uint16_t *w_hat)
+{
+    const int64_t G = (N + 2) / 3;
+    uint8_t *packed = (uint8_t *)malloc((size_t)(G > 0 ? G : 1) * (size_t)K);
+    uint16_t *cs = (uint16_t *)malloc((size_t)(N > 0 ? N : 1) * sizeof(uint16_t));
+    if (!packed || !cs || s3d8o_encode(w, C, N, K, packed, cs) != 0) {
+        free(packed);
+        free(cs);
+        return -1;
+    }
+    for (int64_t n = 0; n < N; ++n) {
+        const float alpha = bf16_bits_to_float(cs[n]);
+        for (int64_t k = 0; k < K; ++k) {
+            const int32_t wq = s3d8o_decode_component(packed[(n / 3) * K + k], C, (int32_t)(n % 3));
+            w_hat[n * K + k] = float_to_bf16_rne(alpha * (float)wq);
+        }
+    }
+    free(packed);
+    free(cs);
     return 0;
 }

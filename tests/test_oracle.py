@@ -670,3 +670,71 @@ def test_lloyd_objective_never_increases():
         sse = ((P[:, None, :] - c.astype(np.float64)[None]) ** 2).sum(2).min(1).sum()
         assert sse <= prev * (1 + 1e-9) + 1e-6, (it, sse, prev)
         prev = sse
+
+
+# --------------------------------------------------------------------------
+# Fake-quant forward (paper section 3.4: in QAT the weight is quantised in the
+# forward pass with the centroids frozen and rebuilt by Eq. 1)
+# --------------------------------------------------------------------------
+
+def test_fake_quant_keeps_exactly_representable_weights():
+    # s * alpha * C[q] with alpha a power of two and 127 in every channel is its
+    # own quantisation: the forward pass returns the weights bit for bit
+    rng = np.random.default_rng(12)
+    C = rng.permutation(np.arange(1, 97)).reshape(32, 3).astype(np.int8)
+    C[31] = 127
+    N, K = 12, 48
+    Q = rng.integers(0, 32, size=(N // 3, K))
+    Q[:, 0] = 31
+    S = rng.integers(0, 2, size=(N, K))
+    alpha = 2.0 ** rng.integers(-12, -4, size=N)
+    W = np.zeros((N, K))
+    for n in range(N):
+        W[n] = (1 - 2 * S[n]) * C[Q[n // 3], n % 3] * alpha[n]
+    Wb = _bf16_exact(W)
+    assert np.array_equal(oracle.fake_quant(Wb, C), Wb)
+
+
+def test_fake_quant_is_scale_times_signed_centroid():
+    # every output is +-alpha_n times an entry of column n mod 3 of the table,
+    # with the weight's sign (0 for a zero channel), within one bf16 rounding
+    rng = np.random.default_rng(13)
+    C = si.centroids(rng)
+    N, K = 14, 64
+    W = si.f32_to_bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    W[5] = 0
+    out = si.bf16_bits_to_f32(oracle.fake_quant(W, C)).astype(np.float64)
+    Wf = si.bf16_bits_to_f32(W).astype(np.float64)
+    alpha = np.abs(Wf).max(1) / 127
+    assert np.all(out[5] == 0)
+    for n in range(N):
+        if n == 5:
+            continue
+        ratio = np.abs(out[n]) / alpha[n]
+        col = C[:, n % 3].astype(np.float64)
+        near = np.abs(ratio[:, None] - col[None, :]).min(1)
+        assert np.all(near <= col.max() * 2.0 ** -7), n     # bf16 alpha and bf16 rounding
+        assert np.all(np.sign(out[n]) == np.sign(Wf[n]) * (out[n] != 0))
+
+
+def test_fake_quant_error_is_the_nearest_centroid_error():
+    # per 3-vector, the reconstruction error in units of alpha is the distance to
+    # the nearest centroid, so no other table row reconstructs the vector better
+    rng = np.random.default_rng(14)
+    C = si.centroids(rng)
+    N, K = 9, 40
+    W = si.f32_to_bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    out = si.bf16_bits_to_f32(oracle.fake_quant(W, C)).astype(np.float64)
+    Wf = si.bf16_bits_to_f32(W).astype(np.float64)
+    _, cs = oracle.encode(W, C)
+    a = si.bf16_bits_to_f32(cs).astype(np.float64)
+    Cf = C.astype(np.float64)
+    for g in range(N // 3):
+        for k in range(K):
+            wp = np.array([abs(Wf[3 * g + d, k]) / a[3 * g + d] for d in range(3)])
+            got = np.array([abs(out[3 * g + d, k]) / a[3 * g + d] for d in range(3)])
+            err = np.sqrt(((got - wp) ** 2).sum())
+            best = np.sqrt(((Cf - wp) ** 2).sum(1).min())
+            # the bf16 rounding of alpha C moves each component by at most
+            # 127 * 2^-9 (in units of alpha): sqrt(3) * 0.25 < 0.5 in total
+            assert err <= best + 0.5
