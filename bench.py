@@ -713,11 +713,26 @@ def encode_measure(torch, s3d8, dev, reps=3):
     params = sum(N * K for _, K, N in si.LLAMA_11B_LAYER)
     codes = sum(si.groups(N) * K for _, K, N in si.LLAMA_11B_LAYER)
     nbytes = 2 * params + codes + 2 * sum(N for _, _, N in si.LLAMA_11B_LAYER)
+    # the QAT fake-quant forward on the same matrices (bf16 in, bf16 out)
+    hats = [torch.empty_like(w) for w, _, _, _ in mats]
+    for (w, C, _, cs), h in zip(mats, hats):
+        s3d8.fake_quant(w, C, h, cs, ws)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(reps):
+        for (w, C, _, cs), h in zip(mats, hats):
+            s3d8.fake_quant(w, C, h, cs, ws)
+    t1.record()
+    t1.synchronize()
+    fq_ms = t0.elapsed_time(t1) / reps
     return {"workload": "one 11B decoder layer's 7 bf16 matrices -> S3D8", "params": params,
             "ms": round(ms, 3), "gparams_s": round(params / (ms * 1e-3) / 1e9, 2),
             "algorithmic_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
             "fp32_tflops": round(codes * 32 * 8 / (ms * 1e-3) / 1e12, 2),
-            "launches": 2 * len(mats) * reps}
+            "launches": 2 * len(mats) * reps,
+            "fake_quant_ms": round(fq_ms, 3),
+            "fake_quant_algorithmic_gbs": round((4 * params + 2 * sum(
+                N for _, _, N in si.LLAMA_11B_LAYER)) / (fq_ms * 1e-3) / 1e9, 1)}
 
 
 def fit_measure(torch, s3d8, dev, iters=25, reps=2):

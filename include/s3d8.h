@@ -122,6 +122,23 @@ int s3d8_encode(const void *w_bf16, const int8_t *centroids, int64_t N, int64_t 
                 void *stream);
 
 /*
+ * QAT fake-quant forward (paper section 3.4, "Quantization": in QAT the weight
+ * is quantised in the forward pass with the centroids frozen and rebuilt by
+ * Eq. 1): w_hat[n,k] = bf16_rn(s * alpha_n * C[q][n mod 3]) with alpha, s and q
+ * exactly as s3d8_encode chooses them (the product alpha C is exact in fp32).
+ * The straight-through backward passes the gradient of w_hat to w unchanged
+ * (no clipping: every weight is inside the absmax range), so it needs no call.
+ *   w_bf16     : [N, K] bfloat16, row-major, 16-byte aligned
+ *   centroids  : [32 * 3] int8, row-major C[q][d], values 0..127
+ *   w_hat_bf16 : [N, K] bfloat16 output, row-major, 16-byte aligned
+ *   chan_scale : [N] bfloat16 output (alpha), 2-byte aligned
+ *   workspace  : as for s3d8_encode (S3D8_ENCODE_WORKSPACE_BYTES, 16-byte aligned)
+ */
+int s3d8_fake_quant(const void *w_bf16, const int8_t *centroids, int64_t N, int64_t K,
+                    void *w_hat_bf16, void *chan_scale_bf16, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/*
  * Centroid fit (paper section 3.4, "Quantization": C = Round(Lloyd-Max(W'))
  * with k-means++ initialisation, Arthur and Vassilvitskii, SODA 2007), on the
  * ceil(N/3) K points W'_p = (|W[3g+d,k]| / alpha_{3g+d})_{d=0..2}, with

@@ -72,6 +72,7 @@ def load(build_if_missing: bool = False):
     L.s3d8_decode.argtypes = [P, P, I64, I64, P, P]
     L.s3d8_encode.argtypes = [P, P, I64, I64, P, P, P, SZ, P]
     L.s3d8_selftest_scaled_abs.argtypes = [P, P, I64, P, P]
+    L.s3d8_fake_quant.argtypes = [P, P, I64, I64, P, P, P, SZ, P]
     L.s3d8_fit_workspace_size.argtypes = [I64, I64]
     L.s3d8_fit_workspace_size.restype = SZ
     L.s3d8_fit_centroids.argtypes = [P, I64, I64, P, ctypes.c_int32, P, P, P, SZ, P]
@@ -88,7 +89,7 @@ def load(build_if_missing: bool = False):
     L.s3d8_status_string.restype = ctypes.c_char_p
     L.s3d8_version.argtypes = []
     for fn in ("s3d8_quantize_act", "s3d8_decode", "s3d8_encode", "s3d8_selftest_scaled_abs",
-               "s3d8_fit_centroids",
+               "s3d8_fit_centroids", "s3d8_fake_quant",
                "s3d8_linear", "s3d8_linear_ex",
                "s3d8_linear_acc_i32", "s3d8_linear_batch", "s3d8_selftest_wait_timeout",
                "s3d8_device_status", "s3d8_version"):
@@ -180,6 +181,43 @@ def encode(w: torch.Tensor, centroids: torch.Tensor, packed: torch.Tensor | None
                             _stream(w.device))
     _check("s3d8_encode", st)
     return packed, chan_scale
+
+
+def fake_quant(w: torch.Tensor, centroids: torch.Tensor, w_hat: torch.Tensor | None = None,
+               chan_scale: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """QAT fake-quant forward: bf16 W[N, K] -> (w_hat bf16 [N, K] = s alpha
+    C[q][n mod 3], chan_scale bf16 [N])."""
+    if w.dim() != 2:
+        raise ValueError("w must be 2-D [N, K]")
+    N, K = w.shape
+    if w_hat is None:
+        w_hat = torch.empty((N, K), dtype=torch.bfloat16, device=w.device)
+    if chan_scale is None:
+        chan_scale = torch.empty((N,), dtype=torch.bfloat16, device=w.device)
+    if workspace is None:
+        workspace = torch.empty((ENCODE_WORKSPACE_BYTES,), dtype=torch.uint8, device=w.device)
+    st = load().s3d8_fake_quant(_dev(w, "w", torch.bfloat16),
+                                _dev(centroids, "centroids", torch.int8, (32, 3)), N, K,
+                                _dev(w_hat, "w_hat", torch.bfloat16, (N, K)),
+                                _dev(chan_scale, "chan_scale", torch.bfloat16, (N,)),
+                                _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                                _stream(w.device))
+    _check("s3d8_fake_quant", st)
+    return w_hat, chan_scale
+
+
+class FakeQuantSTE(torch.autograd.Function):
+    """Q(theta) in the forward pass (s3d8_fake_quant), identity in the
+    backward pass (straight-through estimator): the QAT weight path."""
+
+    @staticmethod
+    def forward(ctx, w, centroids):
+        w_hat, _ = fake_quant(w.detach(), centroids)
+        return w_hat
+
+    @staticmethod
+    def backward(ctx, grad):
+        return grad, None
 
 
 def fit_workspace_size(N: int, K: int) -> int:

@@ -179,6 +179,31 @@ int s3d8_fit_centroids(const void *w_bf16, int64_t N, int64_t K, const uint32_t 
                                   static_cast<cudaStream_t>(stream)));
 }
 
+int s3d8_fake_quant(const void *w_bf16, const int8_t *centroids, int64_t N, int64_t K,
+                    void *w_hat_bf16, void *chan_scale_bf16, void *workspace,
+                    size_t workspace_bytes, void *stream)
+{
+    int st = check_k(K);
+    if (st == S3D8_OK)
+        st = check_mn(0, N);
+    if (st != S3D8_OK)
+        return st;
+    if (N == 0)
+        return S3D8_OK;
+    if (!w_bf16 || !centroids || !w_hat_bf16 || !chan_scale_bf16)
+        return S3D8_ERR_INVALID_ARG;
+    if (!aligned(w_bf16, 16) || !aligned(w_hat_bf16, 16) || !aligned(chan_scale_bf16, 2))
+        return S3D8_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < S3D8_ENCODE_WORKSPACE_BYTES)
+        return S3D8_ERR_WORKSPACE;
+    if (!aligned(workspace, 16))
+        return S3D8_ERR_ALIGNMENT;
+    return cuda_status(launch_fake_quant(static_cast<const __nv_bfloat16 *>(w_bf16), centroids,
+                                         (int)N, (int)K, static_cast<__nv_bfloat16 *>(w_hat_bf16),
+                                         static_cast<__nv_bfloat16 *>(chan_scale_bf16), workspace,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t n, float *out,
                              void *stream)
 {

@@ -258,10 +258,15 @@ __device__ __forceinline__ uint32_t neg_flags(uint32_t u)
     return u & nz & 0x80008000u;
 }
 
-__global__ __launch_bounds__(kEncodeThreads, kEncodeCtasPerSm) void encode_assign_kernel(
+// DENSE = false writes the packed bytes; DENSE = true writes the fake-quant
+// reconstruction w_hat[n, k] = bf16_rn(s alpha_n C[q][n mod 3]) instead (the
+// product of a bf16 alpha and an integer below 128 is exact in fp32).
+template <bool DENSE>
+__global__ __launch_bounds__(kEncodeThreads, DENSE ? kEncodeCtasPerSm - 1 : kEncodeCtasPerSm) void
+encode_assign_kernel(
     const __nv_bfloat16 *__restrict__ w, const int8_t *__restrict__ C,
     const __nv_bfloat16 *__restrict__ chan_scale, const uint32_t *__restrict__ masks_g, int N,
-    int K, int G, uint8_t *__restrict__ packed)
+    int K, int G, uint8_t *__restrict__ packed, __nv_bfloat16 *__restrict__ w_hat)
 {
     __shared__ __align__(16) uint32_t masks[kCells];
     __shared__ float4 tab[kTabEntries * 8];
@@ -307,6 +312,7 @@ __global__ __launch_bounds__(kEncodeThreads, kEncodeCtasPerSm) void encode_assig
         // S2 xor S0 at bit 7; the flags of codes 4o..4o+3 sit at bits 15 and 31
         // of words 2o and 2o+1, gathered to bit 7 of each byte by one permute
         uint32_t out[2];
+        uint32_t hat[3][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
 #pragma unroll
         for (int o = 0; o < 2; ++o) {
             const uint32_t f0 = __byte_perm(neg_flags(u[0][2 * o]), neg_flags(u[0][2 * o + 1]), 0x7531);
@@ -365,15 +371,39 @@ __global__ __launch_bounds__(kEncodeThreads, kEncodeCtasPerSm) void encode_assig
                     }
                 }
                 out[h] += (31u - best) << (1 + 8 * e);
+                if (DENSE) {
+                    const float4 cq = mytab[8 * best];
+                    const float cd[3] = {cq.x, cq.y, cq.z};
+#pragma unroll
+                    for (int d = 0; d < 3; ++d) {
+                        const uint32_t word = u[d][(4 * h + e) >> 1];
+                        const bool neg = neg_flags(word) & (((4 * h + e) & 1) ? 0x80000000u : 0x8000u);
+                        // the decoded weight is an integer: a zero table entry is
+                        // +0 whatever the selector (-0 + 0 = +0)
+                        const float wq = __fadd_rn(neg ? -cd[d] : cd[d], 0.0f);
+                        const float v = __fmul_rn(dv[d].alpha, wq);
+                        const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                        hat[d][(4 * h + e) >> 1] |= ((4 * h + e) & 1) ? (b << 16) : b;
+                    }
+                }
             }
         }
-        if (live)
+        if (!DENSE && live)
             reinterpret_cast<uint2 *>(packed + (size_t)g * K)[c] = make_uint2(out[0], out[1]);
+        if (DENSE && live) {
+#pragma unroll
+            for (int d = 0; d < 3; ++d)
+                if (3 * g + d < N)
+                    reinterpret_cast<uint4 *>(w_hat + (size_t)(3 * g + d) * K)[c] =
+                        make_uint4(hat[d][0], hat[d][1], hat[d][2], hat[d][3]);
+        }
     }
 }
 
-cudaError_t launch_encode(const __nv_bfloat16 *w, const int8_t *C, int N, int K, uint8_t *packed,
-                          __nv_bfloat16 *chan_scale, void *workspace, cudaStream_t stream)
+static cudaError_t launch_encode_impl(const __nv_bfloat16 *w, const int8_t *C, int N, int K,
+                                      uint8_t *packed, __nv_bfloat16 *w_hat,
+                                      __nv_bfloat16 *chan_scale, void *workspace,
+                                      cudaStream_t stream)
 {
     const int sms = device_sm_count();
     uint32_t *masks = static_cast<uint32_t *>(workspace);
@@ -387,11 +417,28 @@ cudaError_t launch_encode(const __nv_bfloat16 *w, const int8_t *C, int N, int K,
     const int G = (N + 2) / 3;
     const int64_t items = (int64_t)G * (K / 8);
     const int64_t want = (items + kEncodeThreads - 1) / kEncodeThreads;
-    const int64_t cap = (int64_t)sms * kEncodeCtasPerSm;
+    const int64_t cap = (int64_t)sms * (w_hat ? kEncodeCtasPerSm - 1 : kEncodeCtasPerSm);
     const int g2 = (int)(want < cap ? want : cap);
-    encode_assign_kernel<<<g2, kEncodeThreads, 0, stream>>>(w, C, chan_scale, masks, N, K, G,
-                                                           packed);
+    if (w_hat)
+        encode_assign_kernel<true><<<g2, kEncodeThreads, 0, stream>>>(w, C, chan_scale, masks, N, K,
+                                                                      G, nullptr, w_hat);
+    else
+        encode_assign_kernel<false><<<g2, kEncodeThreads, 0, stream>>>(w, C, chan_scale, masks, N,
+                                                                       K, G, packed, nullptr);
     return cudaGetLastError();
+}
+
+cudaError_t launch_encode(const __nv_bfloat16 *w, const int8_t *C, int N, int K, uint8_t *packed,
+                          __nv_bfloat16 *chan_scale, void *workspace, cudaStream_t stream)
+{
+    return launch_encode_impl(w, C, N, K, packed, nullptr, chan_scale, workspace, stream);
+}
+
+cudaError_t launch_fake_quant(const __nv_bfloat16 *w, const int8_t *C, int N, int K,
+                              __nv_bfloat16 *w_hat, __nv_bfloat16 *chan_scale, void *workspace,
+                              cudaStream_t stream)
+{
+    return launch_encode_impl(w, C, N, K, nullptr, w_hat, chan_scale, workspace, stream);
 }
 
 // ===========================================================================

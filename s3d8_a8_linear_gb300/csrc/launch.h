@@ -55,6 +55,9 @@ cudaError_t launch_quantize_act(const __nv_bfloat16 *x, int M, int K, int8_t *xq
                                 cudaStream_t stream);
 cudaError_t launch_encode(const __nv_bfloat16 *w, const int8_t *C, int N, int K, uint8_t *packed,
                           __nv_bfloat16 *chan_scale, void *workspace, cudaStream_t stream);
+cudaError_t launch_fake_quant(const __nv_bfloat16 *w, const int8_t *C, int N, int K,
+                              __nv_bfloat16 *w_hat, __nv_bfloat16 *chan_scale, void *workspace,
+                              cudaStream_t stream);
 size_t fit_workspace_bytes(int64_t N, int64_t K);
 cudaError_t launch_fit(const __nv_bfloat16 *w, int N, int K, const uint32_t *r, int iters,
                        float *cf, int8_t *C, void *workspace, cudaStream_t stream);

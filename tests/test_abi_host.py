@@ -117,6 +117,7 @@ def test_empty_calls_are_no_ops(lib):
     assert lib.s3d8_linear_acc_i32(None, None, None, 0, 5, 32, None, None, 0, 0, None) == 0
     assert lib.s3d8_encode(None, None, 0, 32, None, None, None, 0, None) == 0
     assert lib.s3d8_selftest_scaled_abs(None, None, 0, None, None) == 0
+    assert lib.s3d8_fake_quant(None, None, 0, 32, None, None, None, 0, None) == 0
 
 
 @no_device_only
@@ -150,6 +151,10 @@ def test_other_entry_points_reject(lib):
     assert fit(A16 + 8, 6, 32, A16B, 1, A16C, A16, A16B, 1 << 30, None) == -2
     assert fit(A16, 6, 32, A16B, 1, A16C, A16, A16B + 16, 1 << 30, None) == -2   # ws alignment
     assert lib.s3d8_fit_workspace_size(6, 24) == 0
+    fq = lib.s3d8_fake_quant
+    assert fq(A16, A16B, 6, 24, A16C, A16, A16B, WS, None) == -1                # K % 16
+    assert fq(A16, A16B, 6, 32, A16C + 8, A16, A16B, WS, None) == -2            # w_hat alignment
+    assert fq(A16, A16B, 6, 32, A16C, A16, None, WS, None) == -6
     assert lib.s3d8_selftest_scaled_abs(A16, A16B, -1, A16C, None) == -1
     assert lib.s3d8_selftest_scaled_abs(A16 + 1, A16B, 4, A16C, None) == -2
 

@@ -185,3 +185,69 @@ def test_scaled_magnitude_is_the_ieee_quotient():
     assert bad.size == 0, (bad.size, X[bad[:4]], A[bad[:4]], got[bad[:4]], want[bad[:4]])
     zero = to_np(s3d8.selftest_scaled_abs(bf16_bits(xs[:1000]), bf16_bits(np.zeros(1000, np.uint16))))
     assert np.all(zero == 0)
+
+
+# --------------------------------------------------------------------------
+# QAT fake-quant forward (s3d8_fake_quant) and its straight-through backward
+# --------------------------------------------------------------------------
+
+def run_fake_quant(w_bits, C):
+    w_hat, cs = s3d8.fake_quant(bf16_bits(w_bits), i8(C))
+    torch.cuda.synchronize()
+    return (to_np(w_hat.view(torch.int16)).view(np.uint16),
+            to_np(cs.view(torch.int16)).view(np.uint16))
+
+
+@pytest.mark.parametrize("N,K,seed", [(3, 16, 0), (1, 16, 1), (2, 32, 2), (5, 4096, 4),
+                                      (241, 1040, 6), (1024, 4096, 8)])
+def test_fake_quant_matches_oracle(N, K, seed):
+    rng = np.random.default_rng(50 + seed)
+    w = weights(rng, N, K)
+    C = si.centroids(rng)
+    got_w, got_s = run_fake_quant(w, C)
+    want_s = oracle.encode(w, C)[1]
+    assert np.array_equal(got_s, want_s)
+    want_w = oracle.fake_quant(w, C)
+    bad = np.argwhere(got_w != want_w)
+    assert bad.size == 0, bad[:4]
+
+
+def test_fake_quant_zero_channels_and_negative_zero():
+    rng = np.random.default_rng(60)
+    w = weights(rng, 12, 64)
+    w[4] = 0
+    w[7] = 0x8000                     # a whole channel of -0
+    w[9, 3] = 0x8000
+    C = si.centroids(rng)
+    C[5] = 0
+    got_w, _ = run_fake_quant(w, C)
+    assert np.array_equal(got_w, oracle.fake_quant(w, C))
+
+
+def test_fake_quant_straight_through_gradient():
+    # forward uses Q(theta); the gradient reaching theta is the gradient with
+    # respect to Q(theta), unchanged
+    rng = np.random.default_rng(61)
+    N, K, M = 48, 256, 8
+    theta = bf16_bits(weights(rng, N, K)).requires_grad_(True)
+    C = i8(si.centroids(rng))
+    x = torch.randn((M, K), device=dev()).to(torch.bfloat16)
+    r = torch.randn((M, N), device=dev()).to(torch.bfloat16)
+    w_hat = s3d8.FakeQuantSTE.apply(theta, C)
+    (x @ w_hat.t() * r).float().sum().backward()
+    leaf = s3d8.fake_quant(theta.detach(), C)[0].requires_grad_(True)
+    (x @ leaf.t() * r).float().sum().backward()
+    assert torch.equal(theta.grad, leaf.grad)
+    assert torch.equal(w_hat.detach(), leaf.detach())
+
+
+def test_fake_quant_argument_checks():
+    C = torch.zeros((32, 3), dtype=torch.int8, device=dev())
+    w = torch.zeros((6, 24), dtype=torch.bfloat16, device=dev())
+    with pytest.raises(s3d8.S3D8Error) as e:
+        s3d8.fake_quant(w, C)
+    assert e.value.status == -1
+    w = torch.zeros((6, 32), dtype=torch.bfloat16, device=dev())
+    with pytest.raises(s3d8.S3D8Error) as e:
+        s3d8.fake_quant(w, C, workspace=torch.zeros((64,), dtype=torch.uint8, device=dev()))
+    assert e.value.status == -6
