@@ -351,6 +351,23 @@ def gpu_arm(args):
         torch.distributed.barrier()
     clocks = sampler.stop()
 
+    # ---- spread: 64-step graph replays timed one by one, median and a 95 %
+    # bootstrap interval of the per-step time (outside the timed region) ------
+    spread = None
+    if not args.layer_only:
+        blocks = []
+        with torch.cuda.stream(stream):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(60)]
+            for a, b in evs:
+                a.record(stream)
+                multi["group1"].replay()
+                b.record(stream)
+            stream.synchronize()
+            blocks = [a.elapsed_time(b) / per_graph["group1"] for a, b in evs]
+        spread = bootstrap_median(blocks)
+        spread["block_steps"] = per_graph["group1"]
+
     # ---- other launch structures (same weights, same rotation) --------------
     variants = {}
     for mode in (() if args.layer_only else ("group4", "separate")):
@@ -390,6 +407,7 @@ def gpu_arm(args):
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
                 "traffic": traffic_per_launch(),
                 "kernel": "gemv_group_kernel<1>: one launch, 7 projections, fused quantisation",
                 "bytes_per_launch": step_bytes, "avg_launch_us": round(ms_step * 1e3, 3),
@@ -430,7 +448,7 @@ def gpu_arm(args):
         "gpu_launches": args.steps * n_launches("group1"),
         "device_status": status,
         "roofline": roofline, "variants": variants, "e2e": e2e, "prefill": prefill,
-        "decode_sweep": sweep, "text_stack": stack,
+        "decode_sweep": sweep, "text_stack": stack, "spread": spread,
         "unpack": unpack, "encode": encode, "fit": fit, "clocks": clocks, "cpu_baseline": cpu,
     }
     print(json.dumps(line))
@@ -778,6 +796,37 @@ def oracle_layer_step(oracle, mats, xs_bits):
         oracle.linear(m.packed, m.C, m.chan_scale, xq, xsc, m.N)
 
 
+def bootstrap_median(samples, draws=2000, seed=0):
+    """Median of per-step times (ms) with a 95 % percentile-bootstrap interval."""
+    import numpy as np
+    a = np.asarray(samples, np.float64)
+    rng = np.random.default_rng(seed)
+    meds = np.median(a[rng.integers(0, len(a), size=(draws, len(a)))], axis=1)
+    return {"median_ms_per_step": round(float(np.median(a)), 6),
+            "ci95_ms_per_step": [round(float(np.percentile(meds, 2.5)), 6),
+                                 round(float(np.percentile(meds, 97.5)), 6)],
+            "samples": len(a)}
+
+
+def oracle_layer_step_threads(oracle, mats, xs_bits, pool, slices):
+    """The same layer step with the unmodified oracle called concurrently on
+    packed-row slices of every matrix (the C calls run outside the interpreter
+    lock)."""
+    q = {k: oracle.quantize_act(xs_bits[k]) for k in ACT_K}
+    futs = []
+    for m in mats:
+        xq, xsc = q[si.LLAMA_11B_INPUT_OF[m.name]]
+        G = m.packed.shape[0]
+        step = (G + slices - 1) // slices
+        for g0 in range(0, G, step):
+            g1 = min(G, g0 + step)
+            n1 = min(3 * g1, m.N)
+            futs.append(pool.submit(oracle.linear, m.packed[g0:g1], m.C,
+                                    m.chan_scale[3 * g0:n1], xq, xsc, n1 - 3 * g0))
+    for f in futs:
+        f.result()
+
+
 def cpu_baseline(seconds, max_steps=None):
     import oracle
     mats = si.layer_matrices(layer=0, seed=0)
@@ -791,10 +840,29 @@ def cpu_baseline(seconds, max_steps=None):
         el = time.perf_counter() - t0
         if el >= seconds or (max_steps and n >= max_steps):
             break
-    return {"value": round(n * LAYER_WEIGHT_BYTES / el / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle", "seconds": round(el, 2),
-            "sample": f"{n} full layer steps at M=1 (4 activation quantisations + 7 linears), "
-                      "single-threaded plain C oracle"}
+    single = n * LAYER_WEIGHT_BYTES / el / 1e9
+    # all host cores: the same oracle calls spread over a thread pool
+    import concurrent.futures as cf
+    import platform
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        oracle_layer_step_threads(oracle, mats, xs_bits, pool, cores)
+        m = 0
+        t1 = time.perf_counter()
+        while True:
+            oracle_layer_step_threads(oracle, mats, xs_bits, pool, cores)
+            m += 1
+            el2 = time.perf_counter() - t1
+            if el2 >= seconds / 2 or (max_steps and m >= max_steps):
+                break
+    multi = m * LAYER_WEIGHT_BYTES / el2 / 1e9
+    return {"value": round(multi, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "seconds": round(el + el2, 2),
+            "single_thread_value": round(single, 4),
+            "host": f"{platform.machine()}, {cores} cores",
+            "sample": f"{m} full layer steps at M=1 (4 activation quantisations + 7 linears) with "
+                      f"the plain C oracle on {cores} threads (each linear split into {cores} "
+                      f"packed-row slices); single-threaded: {n} steps"}
 
 
 def reference_arm(args):
@@ -805,12 +873,15 @@ def reference_arm(args):
     mats = si.layer_matrices(layer=0, seed=0)
     xs_bits = {k: si.acts(1, K, seed=0, index=i) for i, (k, K) in enumerate(ACT_K.items())}
     oracle.lib()
-    for _ in range(args.warmup):
-        oracle_layer_step(oracle, mats, xs_bits)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_layer_step(oracle, mats, xs_bits)
-    el = time.perf_counter() - t0
+    import concurrent.futures as cf
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        for _ in range(args.warmup):
+            oracle_layer_step_threads(oracle, mats, xs_bits, pool, cores)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_layer_step_threads(oracle, mats, xs_bits, pool, cores)
+        el = time.perf_counter() - t0
     ms = el * 1e3 / args.steps
     value = LAYER_WEIGHT_BYTES / (ms * 1e-3) / 1e9
     line = {
@@ -820,9 +891,10 @@ def reference_arm(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic (seeded S3D8 fields, bf16 N(0,1) activations)",
         "config": {"workload": WORKLOAD, "M": 1, "weight_bytes_per_step": LAYER_WEIGHT_BYTES},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} full layer steps at M=1, single-threaded "
-                                   "plain C oracle"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} full layer steps at M=1, the plain C oracle "
+                                   f"on {cores} threads (each linear split into {cores} "
+                                   "packed-row slices)"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
