@@ -698,25 +698,44 @@ __global__ __launch_bounds__(kKppSelectThreads) void kpp_select_kernel(
         if (threadIdx.x == 0)
             sh_idx = (long long)scale_draw(draw, (unsigned long long)Np);
     } else {
+        // Within the chosen block: each warp sums a contiguous run of the block's
+        // points in coalesced rows of 32; a scan of the 32 warp sums finds the
+        // warp holding the crossing, which walks its rows with a warp scan.
         int64_t lo, hi;
         block_range(Np, blocks, sh_block, lo, hi);
-        const int64_t n = hi - lo;
-        const int64_t per = (n + kKppSelectThreads - 1) / kKppSelectThreads;
-        const int64_t c0 = lo + (int64_t)threadIdx.x * per;
-        const int64_t c1 = c0 + per < hi ? c0 + per : hi;
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        const int nw = kKppSelectThreads / 32;
+        const int64_t per_w = ((hi - lo + nw - 1) / nw + 31) / 32 * 32;
+        const int64_t w0 = lo + (int64_t)wid * per_w;
+        const int64_t w1 = w0 + per_w < hi ? w0 + per_w : hi;
         unsigned long long s = 0;
-        for (int64_t p = c0; p < c1; ++p)
+        for (int64_t p = w0 + lane; p < w1; p += 32)
             s += d2_weight(D2[p]);
-        const unsigned long long cincl = block_inclusive_scan(s, warp_tot);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+        const unsigned long long wincl = block_inclusive_scan(lane == 0 ? s : 0ull, warp_tot);
+        // wincl of lane 0 of warp w is the inclusive sum up to warp w
+        const unsigned long long incl_w = __shfl_sync(0xFFFFFFFFu, wincl, 0);
         const unsigned long long want = sh_target - sh_excl;   // residual within the block
-        if (cincl > want && cincl - s <= want) {
-            unsigned long long run = cincl - s;
-            for (int64_t p = c0; p < c1; ++p) {
-                run += d2_weight(D2[p]);
-                if (run > want) {
-                    sh_idx = p;
+        if (incl_w > want && incl_w - s <= want) {
+            unsigned long long run = incl_w - s;
+            for (int64_t r0 = w0; r0 < w1; r0 += 32) {
+                const int64_t p = r0 + lane;
+                unsigned long long v = p < w1 ? d2_weight(D2[p]) : 0ull;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+                    if (lane >= o)
+                        v += n;
+                }
+                const uint32_t hit = __ballot_sync(0xFFFFFFFFu, run + v > want);
+                if (hit) {
+                    if (lane == 0)
+                        sh_idx = r0 + (__ffs(hit) - 1);
                     break;
                 }
+                run += __shfl_sync(0xFFFFFFFFu, v, 31);
             }
         }
     }
@@ -738,7 +757,9 @@ __global__ __launch_bounds__(kKppSelectThreads) void kpp_select_kernel(
 // launch keeps every warp at no more than 2^16 points (kLloydMaxWarpPoints),
 // so neither part can wrap, and the CTA recombines them exactly in 64 bits.
 constexpr int kLloydMaxWarpPoints = 1 << 16;
-constexpr int kBinWords = 8;   // x lo, x hi, y lo, y hi, z lo, z hi, count, unused
+// x lo, x hi, y lo, y hi, z lo, z hi, count, and 2 unused words: a stride of 9
+// words puts the 32 bins of a warp on 32 different banks
+constexpr int kBinWords = 9;
 
 __global__ __launch_bounds__(kFitThreads) void lloyd_assign_kernel(
     const float *__restrict__ P0, const float *__restrict__ P1, const float *__restrict__ P2,
