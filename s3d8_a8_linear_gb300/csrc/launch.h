@@ -79,6 +79,8 @@ size_t prefill_workspace_bytes(int M, int N, int K, bool pre);
 cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream);
 // Split-K finish shared by the tensor-core and skinny paths: sums int32 partials
 // [nsplit][M][N] into a.out (epilogue) or a.acc.
+cudaError_t launch_prefill_pair(const LinearArgs &a, const __nv_bfloat16 *act, const __nv_bfloat16 *wdec,
+                                int32_t *part, int nsplit, int kbps, cudaStream_t stream);
 cudaError_t launch_splitk_finalize(const int32_t *part, int nsplit, const LinearArgs &a, cudaStream_t stream);
 // mma.sync path for a few tokens (1..32), weights decoded into register fragments.
 bool skinny_supported(int M);

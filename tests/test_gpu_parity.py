@@ -262,8 +262,11 @@ def test_zero_activation_row_gives_zero(algo):
 
 TC_TILES = [(128, 240, 64), (129, 241, 1040), (300, 722, 2112), (256, 480, 3072),
             (1, 3, 16), (17, 1201, 1024),
-            # from 384 tokens the weights are expanded to bf16 first (both operands by TMA)
-            (384, 241, 1040), (520, 722, 2112)]
+            # from 384 tokens the weights are expanded to bf16 first (both operands by
+            # TMA) and two SMs share each 256-token tile: the odd SM's rows past M,
+            # partial pair tiles, one K block, split and unsplit K
+            (384, 241, 1040), (520, 722, 2112), (768, 480, 3072), (400, 3, 16),
+            (1000, 1201, 4096), (2048, 96, 14336)]
 
 
 @pytest.mark.parametrize("M,N,K", TC_TILES)
@@ -311,10 +314,11 @@ def test_skinny_rejects_more_than_32_tokens():
     assert e.value.status == -3
 
 
-def test_tc_unaligned_outputs():
+@pytest.mark.parametrize("M", [130, 390])
+def test_tc_unaligned_outputs(M):
     """Output views that are only 2- (bf16) or 4-byte (int32) aligned take the
-    scalar store path and still match."""
-    M, N, K = 130, 480, 256
+    scalar store path and still match (one-SM and SM-pair kernels)."""
+    N, K = 480, 256
     C, packed, cs, x = rand_case(M, N, K, seed=5)
     xq, xs = oracle.quantize_act(x)
     ref, acc_o = oracle.linear(packed, C, cs, xq, xs, N)
@@ -329,12 +333,14 @@ def test_tc_unaligned_outputs():
     np.testing.assert_array_equal(to_np(acc).astype(np.int64), acc_o)
 
 
-def test_tc_adversarial_chunk_sums():
+@pytest.mark.parametrize("M", [200, 400])
+def test_tc_adversarial_chunk_sums(M):
     """Every product +16129 over 1024 columns is the largest partial sum an exact
     fp32 chunk holds (16,516,096 < 2^24); two chunks in a row must still add
-    exactly in int32 (K = 2048 + 1024 + 16)."""
+    exactly in int32 (K = 2048 + 1024 + 16).  One SM per tile (200 tokens) and
+    SM pairs on pre-expanded weights (400)."""
     C = np.full((32, 3), 127, np.int8)
-    M, N, K = 200, 243, 3088
+    N, K = 243, 3088
     packed = np.full((si.groups(N), K), oracle.pack_byte(3, 0, 0, 0), np.uint8)
     xq = np.full((M, K), 127, np.int8)
     xq[1::2, 1024:2048] = -127        # odd rows: the middle chunk cancels the first
