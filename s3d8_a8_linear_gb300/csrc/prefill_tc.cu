@@ -7,6 +7,10 @@
 // partial sum below 127 * 127 * 1024 < 2^24, where fp32 holds integers exactly.
 // After each chunk the fp32 accumulator is drained into int32 registers.
 //
+// This file holds the one-SM kernel that decodes packed weight tiles itself
+// (below 384 tokens) and the host side of both tensor-core paths; from 384
+// tokens the weights are expanded to bf16 first and prefill_pair.cu runs.
+//
 // Tile: 128 tokens (MMA M) x 240 output channels (MMA N; 80 whole packed groups)
 // per CTA, K in blocks of 64.  Sixteen warps in four warpgroups:
 //   warp 0      bulk tensor copies (TMA) of the bf16 activation tile (from the
@@ -27,20 +31,16 @@ namespace s3d8 {
 
 namespace tc {
 
-// PRE = false: the weight tile is decoded from packed bytes in shared memory by
-// warps 2-15.  PRE = true: the weights were expanded to bf16 [N, K] in global
-// memory beforehand and arrive by bulk tensor copy like the activations; warps
-// 2-7 idle and 8-15 only drain.
-template <bool PRE>
+// The weight tile is decoded from packed bytes in shared memory by warps 2-15.
 __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_constant__ CUtensorMap tm_act,
                                                              const __grid_constant__ CUtensorMap tm_pk,
                                                              Params p)
 {
-    constexpr int LST = PRE ? PSTAGES : LSTAGES;
-    constexpr int BST = PRE ? 0 : BSTAGES;
-    constexpr int O_B = PRE ? P_OFF_B : OFF_B;
-    constexpr int O_BARS = PRE ? P_OFF_BARS : OFF_BARS;
-    constexpr int NB = PRE ? P_NBARS : NBARS;
+    constexpr int LST = LSTAGES;
+    constexpr int BST = BSTAGES;
+    constexpr int O_B = OFF_B;
+    constexpr int O_BARS = OFF_BARS;
+    constexpr int NB = NBARS;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -100,7 +100,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
     }
     // decode table: byte -> [bf16 w0 | bf16 w1 << 16, bf16 w2], 16 copies (one per
     // half-warp lane) so that 8-byte lookups never conflict.
-    if (!PRE) {
+    {
         __shared__ int8_t Cs[96];
         for (int i = threadIdx.x; i < 96; i += THREADS)
             Cs[i] = p.C[i];
@@ -132,13 +132,10 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
                         timed_out = true;
                         break;
                     }
-                    mbar_arrive_expect_tx(l_full + 8 * s, A_BYTES + (PRE ? B_BYTES : P_BYTES));
+                    mbar_arrive_expect_tx(l_full + 8 * s, A_BYTES + P_BYTES);
                     tma_2d(base + OFF_A + s * A_BYTES, &tm_act, (T.kbase + kb) * BK, T.m0, l_full + 8 * s);
-                    if (PRE)
-                        tma_2d(base + O_B + s * B_BYTES, &tm_pk, (T.kbase + kb) * BK, T.nt * BN, l_full + 8 * s);
-                    else
-                        tma_2d(base + OFF_P + s * P_BYTES, &tm_pk, (T.kbase + kb) * BK, T.nt * GROUPS,
-                               l_full + 8 * s);
+                    tma_2d(base + OFF_P + s * P_BYTES, &tm_pk, (T.kbase + kb) * BK, T.nt * GROUPS,
+                           l_full + 8 * s);
                     ++issued;
                 }
             }
@@ -157,7 +154,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
             for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
                 const Tile T = tile_of(t);
                 for (int kb = 0; kb < T.nk; ++kb) {
-                    const int s = g % LST, bs = PRE ? s : g % BSTAGES;
+                    const int s = g % LST, bs = g % BSTAGES;
                     const int c = gc + kb / CHUNK_BLOCKS, kin = kb % CHUNK_BLOCKS;
                     const uint32_t d = tmem + (uint32_t)((c & 1) * 256);
                     if (kin == 0 && c >= 2 && !mbar_wait_bounded(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
@@ -165,7 +162,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
                         break;
                     }
                     if (!mbar_wait_bounded(l_full + 8 * s, (g / LST) & 1) ||
-                        (!PRE && !mbar_wait_bounded(b_full + 8 * bs, (g / BSTAGES) & 1))) {
+                        !mbar_wait_bounded(b_full + 8 * bs, (g / BSTAGES) & 1)) {
                         timed_out = true;
                         break;
                     }
@@ -176,8 +173,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
                         mma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
                                  (kin | kk) ? 1u : 0u);
                     mma_commit(l_empty + 8 * s);
-                    if (!PRE)
-                        mma_commit(b_empty + 8 * bs);
+                    mma_commit(b_empty + 8 * bs);
                     if (kin == CHUNK_BLOCKS - 1 || kb == T.nk - 1)
                         mma_commit(acc_full + 8 * (c & 1));
                     ++g;
@@ -193,7 +189,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         const int tid = threadIdx.x - 64;
         const uint32_t lut_lane = lut + (uint32_t)((lane & (LUT_COPIES - 1)) * 8);
         int g = 0;
-        for (int t = blockIdx.x; t < (PRE ? 0 : total) && !timed_out; t += gridDim.x) {
+        for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
             const Tile T = tile_of(t);
             for (int kb = 0; kb < T.nk; ++kb, ++g) {
                 const int s = g % LSTAGES, bs = g % BSTAGES;
@@ -238,7 +234,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
             if (lane == 0)
                 mbar_arrive(acc_empty + 8 * (c & 1));
         };
-        // Between chunk drains these warps decode too (packed variant).  A finished
+        // Between chunk drains these warps decode too.  A finished
         // chunk is drained before the next K block is decoded, so the MMA never
         // waits on a buffer these warps have not released while they wait on it.
         const int tid = threadIdx.x - 64;
@@ -252,7 +248,7 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
             for (int i = 0; i < HALF; ++i)
                 acc[i] = 0;
             int cn = gc;   // next chunk to drain
-            for (int kb = 0; kb < (PRE ? 0 : T.nk) && !timed_out; ++kb, ++g) {
+            for (int kb = 0; kb < T.nk && !timed_out; ++kb, ++g) {
                 while (cn < gc + nch) {
                     const bool ready =
                         __shfl_sync(0xffffffffu, (int)mbar_test(acc_full + 8 * (cn & 1), (cn >> 1) & 1), 0) != 0;
@@ -327,8 +323,8 @@ __global__ void codes_to_bf16_kernel(const int8_t *__restrict__ xq, __nv_bfloat1
 }
 
 // Weights expanded to bf16 [N, K] (row n = component n % 3 of packed row n / 3),
-// for the pre-decoded variant.  One thread per 16 packed bytes; the 16-copy
-// table of bf16 triples is the kernel's own.
+// the B operand of the SM-pair kernel (prefill_pair.cu).  One thread per 16
+// packed bytes; the 16-copy table of bf16 triples is the kernel's own.
 __global__ __launch_bounds__(256) void decode_bf16_kernel(const uint8_t *__restrict__ packed,
                                                           const int8_t *__restrict__ C, int N, int K,
                                                           __nv_bfloat16 *__restrict__ w)
@@ -429,8 +425,9 @@ static size_t align256(size_t v)
 }
 
 // From this many tokens the weights are expanded to bf16 once per call and the
-// GEMM reads them by bulk tensor copy: the expansion then costs less than
-// re-decoding every weight tile once per 128-token tile inside the GEMM.
+// SM-pair GEMM (prefill_pair.cu) reads them by bulk tensor copy: the expansion
+// then costs less than re-decoding every weight tile once per 128-token tile
+// inside the GEMM, the one-SM kernel here.
 constexpr int kPredecodeMinM = 384;
 
 bool prefill_predecode(int M)
@@ -535,24 +532,13 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    if (pre) {
-        // bf16 weights [N, K]: 64-column x 240-row boxes, 128-byte swizzle like the activations
-        const cuuint64_t dW[2] = {(cuuint64_t)a.K, (cuuint64_t)a.N};
-        const cuuint64_t sW[1] = {(cuuint64_t)a.K * 2};
-        const cuuint32_t boxW[2] = {BK, BN};
-        if (encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wdec, dW, sW, boxW, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    } else if (encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), dP, sP, boxP, es,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+    if (encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), dP, sP, boxP, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    }
 
-    const int smem_bytes = pre ? P_SMEM_BYTES : SMEM_BYTES;
-    e = pre ? cudaFuncSetAttribute(tc::prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)
-            : cudaFuncSetAttribute(tc::prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    const int smem_bytes = SMEM_BYTES;
+    e = cudaFuncSetAttribute(tc::prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess)
         return e;
     tc::Params p = tc::make_params(a, nsplit, kbps, part);
@@ -560,10 +546,7 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream
     if (tiles > 0x7FFFFFFFL)
         return cudaErrorInvalidValue;
     const long ctas = tiles < sms ? tiles : sms;   // persistent CTAs walk the tiles
-    if (pre)
-        tc::prefill_kernel<true><<<(unsigned)ctas, THREADS, smem_bytes, stream>>>(tm_act, tm_pk, p);
-    else
-        tc::prefill_kernel<false><<<(unsigned)ctas, THREADS, smem_bytes, stream>>>(tm_act, tm_pk, p);
+    tc::prefill_kernel<<<(unsigned)ctas, THREADS, smem_bytes, stream>>>(tm_act, tm_pk, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || nsplit == 1)
         return e;

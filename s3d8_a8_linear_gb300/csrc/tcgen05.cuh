@@ -38,15 +38,6 @@ constexpr int DECODERS = 14 * 32;   // warps 2-15 all decode (8-15 also drain)
 constexpr int DRAIN_WARP0 = 8;
 constexpr int HALF = BN / 2;             // 120 columns per epilogue thread
 
-// Variant with pre-decoded bf16 weights (both operands by bulk tensor copy): a
-// ring of PSTAGES (activation tile + weight tile), no packed tiles, no table.
-constexpr int PSTAGES = 4;
-constexpr int P_OFF_B = PSTAGES * A_BYTES;
-constexpr int P_OFF_BARS = P_OFF_B + PSTAGES * B_BYTES;
-constexpr int P_NBARS = 2 * PSTAGES + 4;
-constexpr int P_SMEM_BYTES = 1024 + P_OFF_BARS + P_NBARS * 8 + 16;
-static_assert(P_OFF_B % 1024 == 0 && P_SMEM_BYTES + 1024 <= 232448, "pre-decoded layout");
-
 static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0,
               "swizzled tiles must stay 1024-aligned");
 static_assert(OFF_P % 128 == 0 && P_BYTES % 128 == 0, "packed tiles 128-byte aligned");
