@@ -68,35 +68,37 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// Bulk tensor copy into this CTA's shared memory whose completion (tx bytes) is
-// signalled on `bar`, which may be the barrier of the other CTA of the pair.
-__device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+// Warp-wide pair forms (see the one-SM forms in tcgen05.cuh): the MMA with
+// M = 256 across the pair; the commit arrives on the barrier at offset `bar` in
+// both CTAs; the tensor copy completes on `bar`, which may be the barrier of the
+// other CTA of the pair.
+__device__ __forceinline__ void mma_bf16_pair_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3}], [%4];" ::"r"(dst),
-        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
-{
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
-// Arrive on the barrier at offset `bar` in both CTAs of the pair when the MMAs
-// issued so far by this thread have completed.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar)
+__device__ __forceinline__ void mma_commit_pair_elect(uint32_t bar)
 {
     const uint16_t mask = 0x3;
     asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}\n" ::"r"(
             bar),
         "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_2d_pair_elect(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];\n}\n" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
 
@@ -166,35 +168,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (warp == 0) {
             // ---- this CTA's halves of every K block, by bulk tensor copy; both CTAs'
             // copies complete on the even CTA's l_full, which expects both halves
-            if (lane == 0) {
+            {
                 const uint32_t full0 = map_to_rank(l_full, 0);
                 int issued = 0;
                 for (int t = cid; t < total && !timed_out; t += nclusters) {
                     const Tile T = tile_of(t);
                     for (int kb = 0; kb < T.nk; ++kb) {
                         const int s = issued % S;
-                        if (issued >= S && !mbar_wait_bounded(l_empty + 8 * s, ((issued / S) - 1) & 1)) {
+                        if (issued >= S && !warp_wait(l_empty + 8 * s, ((issued / S) - 1) & 1)) {
                             timed_out = true;
                             break;
                         }
                         if (rank == 0)
-                            mbar_arrive_expect_tx(l_full + 8 * s, 2 * (A_BYTES + B_HALF_BYTES));
+                            mbar_arrive_expect_tx_elect(l_full + 8 * s, 2 * (A_BYTES + B_HALF_BYTES));
                         const int kx = (T.kbase + kb) * BK;
-                        tma_2d_pair(base + s * A_BYTES, &tm_act, kx, T.m0 + (int)rank * BM, full0 + 8 * s);
-                        tma_2d_pair(base + PAIR_OFF_B + s * B_HALF_BYTES, &tm_w, kx, T.nt * BN + (int)rank * B_HALF,
-                                    full0 + 8 * s);
+                        tma_2d_pair_elect(base + s * A_BYTES, &tm_act, kx, T.m0 + (int)rank * BM, full0 + 8 * s);
+                        tma_2d_pair_elect(base + PAIR_OFF_B + s * B_HALF_BYTES, &tm_w, kx,
+                                          T.nt * BN + (int)rank * B_HALF, full0 + 8 * s);
                         ++issued;
                     }
                 }
                 // never leave with copies in flight: the last stages' MMAs (which
                 // needed every copy) have completed
                 for (int v = issued - S < 0 ? 0 : issued - S; v < issued; ++v)
-                    if (!mbar_wait_bounded(l_empty + 8 * (v % S), (v / S) & 1))
+                    if (!warp_wait(l_empty + 8 * (v % S), (v / S) & 1))
                         timed_out = true;
             }
         } else if (warp == 1 && rank == 0) {
-            // ---- MMA issuer of the pair ----------------------------------------------
-            if (lane == 0) {
+            // ---- MMA issuer of the pair: the whole warp runs the loop so that the
+            // descriptors stay warp-uniform; one elected lane issues -----------------
+            {
                 int g = 0, gc = 0;
                 const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                                        ((uint32_t)(PAIR_BM >> 4) << 24);
@@ -204,11 +207,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         const int s = g % S;
                         const int c = gc + kb / CHUNK_BLOCKS, kin = kb % CHUNK_BLOCKS;
                         const uint32_t d = tmem + (uint32_t)((c & 1) * 256);
-                        if (kin == 0 && c >= 2 && !mbar_wait_bounded(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
+                        if (kin == 0 && c >= 2 && !warp_wait(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
                             timed_out = true;
                             break;
                         }
-                        if (!mbar_wait_bounded(l_full + 8 * s, (g / S) & 1)) {
+                        if (!warp_wait(l_full + 8 * s, (g / S) & 1)) {
                             timed_out = true;
                             break;
                         }
@@ -216,17 +219,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         const uint32_t a = base + s * A_BYTES, b = base + PAIR_OFF_B + s * B_HALF_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_bf16_pair(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
-                                          (kin | kk) ? 1u : 0u);
-                        mma_commit_pair(l_empty + 8 * s);
+                            mma_bf16_pair_elect(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
+                                                (kin | kk) ? 1u : 0u);
+                        mma_commit_pair_elect(l_empty + 8 * s);
                         if (kin == CHUNK_BLOCKS - 1 || kb == T.nk - 1)
-                            mma_commit_pair(acc_full + 8 * (c & 1));
+                            mma_commit_pair_elect(acc_full + 8 * (c & 1));
                         ++g;
                     }
                     gc += (T.nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
                 }
                 // the tensor core must be done with both CTAs' memory before exit
-                if (g > 0 && !mbar_wait_bounded(l_empty + 8 * ((g - 1) % S), ((g - 1) / S) & 1))
+                if (g > 0 && !warp_wait(l_empty + 8 * ((g - 1) % S), ((g - 1) / S) & 1))
                     timed_out = true;
             }
         }

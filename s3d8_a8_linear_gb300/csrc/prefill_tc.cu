@@ -121,32 +121,33 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
     if (warp < DRAIN_WARP0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
     if (warp == 0) {
-        // ---- bulk tensor copies ------------------------------------------------
-        if (lane == 0) {
+        // ---- bulk tensor copies (whole warp; one elected lane issues) --------------
+        {
             int issued = 0;   // k-blocks issued by this CTA over all its tiles
             for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
                 const Tile T = tile_of(t);
                 for (int kb = 0; kb < T.nk; ++kb) {
                     const int s = issued % LST;
-                    if (issued >= LST && !mbar_wait_bounded(l_empty + 8 * s, ((issued / LST) - 1) & 1)) {
+                    if (issued >= LST && !warp_wait(l_empty + 8 * s, ((issued / LST) - 1) & 1)) {
                         timed_out = true;
                         break;
                     }
-                    mbar_arrive_expect_tx(l_full + 8 * s, A_BYTES + P_BYTES);
-                    tma_2d(base + OFF_A + s * A_BYTES, &tm_act, (T.kbase + kb) * BK, T.m0, l_full + 8 * s);
-                    tma_2d(base + OFF_P + s * P_BYTES, &tm_pk, (T.kbase + kb) * BK, T.nt * GROUPS,
-                           l_full + 8 * s);
+                    mbar_arrive_expect_tx_elect(l_full + 8 * s, A_BYTES + P_BYTES);
+                    tma_2d_elect(base + OFF_A + s * A_BYTES, &tm_act, (T.kbase + kb) * BK, T.m0, l_full + 8 * s);
+                    tma_2d_elect(base + OFF_P + s * P_BYTES, &tm_pk, (T.kbase + kb) * BK, T.nt * GROUPS,
+                                 l_full + 8 * s);
                     ++issued;
                 }
             }
             // never leave with copies in flight: wait (bounded) for the last ones
             for (int v = issued - LST < 0 ? 0 : issued - LST; v < issued; ++v)
-                if (!mbar_wait_bounded(l_full + 8 * (v % LST), (v / LST) & 1))
+                if (!warp_wait(l_full + 8 * (v % LST), (v / LST) & 1))
                     timed_out = true;
         }
     } else if (warp == 1) {
-        // ---- MMA issuer ----------------------------------------------------------
-        if (lane == 0) {
+        // ---- MMA issuer: the whole warp runs the loop so that the descriptors stay
+        // warp-uniform; one elected lane issues --------------------------------------
+        {
             int g = 0;    // k-blocks consumed by this CTA over all its tiles
             int gc = 0;   // chunks started by this CTA over all its tiles
             const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
@@ -157,12 +158,11 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
                     const int s = g % LST, bs = g % BSTAGES;
                     const int c = gc + kb / CHUNK_BLOCKS, kin = kb % CHUNK_BLOCKS;
                     const uint32_t d = tmem + (uint32_t)((c & 1) * 256);
-                    if (kin == 0 && c >= 2 && !mbar_wait_bounded(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
+                    if (kin == 0 && c >= 2 && !warp_wait(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) {
                         timed_out = true;
                         break;
                     }
-                    if (!mbar_wait_bounded(l_full + 8 * s, (g / LST) & 1) ||
-                        !mbar_wait_bounded(b_full + 8 * bs, (g / BSTAGES) & 1)) {
+                    if (!warp_wait(l_full + 8 * s, (g / LST) & 1) || !warp_wait(b_full + 8 * bs, (g / BSTAGES) & 1)) {
                         timed_out = true;
                         break;
                     }
@@ -170,18 +170,18 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
                     const uint32_t a = base + OFF_A + s * A_BYTES, b = base + O_B + bs * B_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_bf16(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
-                                 (kin | kk) ? 1u : 0u);
-                    mma_commit(l_empty + 8 * s);
-                    mma_commit(b_empty + 8 * bs);
+                        mma_bf16_elect(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
+                                       (kin | kk) ? 1u : 0u);
+                    mma_commit_elect(l_empty + 8 * s);
+                    mma_commit_elect(b_empty + 8 * bs);
                     if (kin == CHUNK_BLOCKS - 1 || kb == T.nk - 1)
-                        mma_commit(acc_full + 8 * (c & 1));
+                        mma_commit_elect(acc_full + 8 * (c & 1));
                     ++g;
                 }
                 gc += (T.nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
             }
             // the tensor core must be done with TMEM and shared memory before exit
-            if (g > 0 && !mbar_wait_bounded(l_empty + 8 * ((g - 1) % LST), ((g - 1) / LST) & 1))
+            if (g > 0 && !warp_wait(l_empty + 8 * ((g - 1) % LST), ((g - 1) / LST) & 1))
                 timed_out = true;
         }
     } else {
