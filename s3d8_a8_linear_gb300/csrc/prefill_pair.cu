@@ -162,6 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool timed_out = false;
+    pdl_launch_dependents();   // the split-K finish may be scheduled; it waits for this grid
 
     if (warp < DRAIN_WARP0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
@@ -169,6 +170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             // ---- this CTA's halves of every K block, by bulk tensor copy; both CTAs'
             // copies complete on the even CTA's l_full, which expects both halves
             {
+                pdl_wait();   // the activation codes and bf16 weights come from earlier kernels
                 const uint32_t full0 = map_to_rank(l_full, 0);
                 int issued = 0;
                 for (int t = cid; t < total && !timed_out; t += nclusters) {
@@ -333,8 +335,8 @@ cudaError_t launch_prefill_pair(const LinearArgs &a, const __nv_bfloat16 *act, c
         pairs = fit;
     (void)cudaGetLastError();
     const long clusters = tiles < pairs ? tiles : pairs;
-    prefill_pair_kernel<<<(unsigned)(2 * clusters), THREADS, PAIR_SMEM_BYTES, stream>>>(tm_act, tm_w, p);
-    return cudaGetLastError();
+    return launch_pdl(prefill_pair_kernel, dim3((unsigned)(2 * clusters)), dim3(THREADS), (size_t)PAIR_SMEM_BYTES,
+                      stream, tm_act, tm_w, p);
 }
 
 }  // namespace s3d8

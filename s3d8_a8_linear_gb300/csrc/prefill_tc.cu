@@ -117,12 +117,14 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool timed_out = false;
+    pdl_launch_dependents();   // the split-K finish may be scheduled; it waits for this grid
 
     if (warp < DRAIN_WARP0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
     if (warp == 0) {
         // ---- bulk tensor copies (whole warp; one elected lane issues) --------------
         {
+            pdl_wait();       // the activation codes come from the previous kernel
             int issued = 0;   // k-blocks issued by this CTA over all its tiles
             for (int t = blockIdx.x; t < total && !timed_out; t += gridDim.x) {
                 const Tile T = tile_of(t);
@@ -309,6 +311,7 @@ __device__ __forceinline__ void codes16_to_bf16(uint4 v, uint4 *dst)
 
 __global__ void codes_to_bf16_kernel(const int8_t *__restrict__ xq, __nv_bfloat16 *__restrict__ a, long n16)
 {
+    pdl_launch_dependents();   // the GEMM may set up meanwhile; it waits before reading a
     const uint4 *src = reinterpret_cast<const uint4 *>(xq);
     uint4 *dst = reinterpret_cast<uint4 *>(a);
     const long stride = (long)gridDim.x * blockDim.x;
@@ -329,6 +332,7 @@ __global__ __launch_bounds__(256) void decode_bf16_kernel(const uint8_t *__restr
                                                           const int8_t *__restrict__ C, int N, int K,
                                                           __nv_bfloat16 *__restrict__ w)
 {
+    pdl_launch_dependents();   // the GEMM may set up meanwhile; it waits before reading w
     __shared__ int8_t Cs[96];
     __shared__ uint2 lut[kLutEntries * LUT_COPIES];
     for (int i = threadIdx.x; i < 96; i += blockDim.x)
@@ -374,20 +378,59 @@ __global__ __launch_bounds__(256) void decode_bf16_kernel(const uint8_t *__restr
 
 // Split-K finish: out[m, n] (or acc) from the sum of the nsplit int32 partials.
 // Integer sums, so the order of the splits does not matter.
+// Split-K finish: sums the int32 partials [nsplit][M][N] and writes the raw
+// int32 result or the bf16 epilogue.  Threads take 4 consecutive columns of a row
+// (16-byte partial loads when N % 4 == 0), rows by grid stride: no division per
+// element.
 __global__ void finalize_kernel(const int32_t *__restrict__ part, int nsplit, int M, int N,
                                 const float *__restrict__ xscale, const __nv_bfloat16 *__restrict__ cs,
-                                __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc)
+                                __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc, int vec_in,
+                                int vec_out)
 {
+    pdl_wait();   // the partials are the previous kernel's output
     const size_t plane = (size_t)M * N;
-    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < plane; e += (size_t)gridDim.x * blockDim.x) {
-        int32_t v = 0;
-        for (int sp = 0; sp < nsplit; ++sp)
-            v += __ldg(part + (size_t)sp * plane + e);
-        if (acc) {
-            acc[e] = v;
-        } else {
-            const int m = (int)(e / (size_t)N), n = (int)(e - (size_t)m * N);
-            out[e] = epilogue_bf16(v, __ldg(xscale + m), cs[n]);
+    const int quads = (N + 3) / 4;
+    for (int m = blockIdx.y; m < M; m += gridDim.y) {
+        const size_t row = (size_t)m * N;
+        for (int qd = blockIdx.x * blockDim.x + threadIdx.x; qd < quads; qd += gridDim.x * blockDim.x) {
+            const int n0 = 4 * qd;
+            int32_t v[4] = {0, 0, 0, 0};
+            if (vec_in) {
+                for (int sp = 0; sp < nsplit; ++sp) {
+                    const int4 t = __ldg(reinterpret_cast<const int4 *>(part + sp * plane + row + n0));
+                    v[0] += t.x;
+                    v[1] += t.y;
+                    v[2] += t.z;
+                    v[3] += t.w;
+                }
+            } else {
+                for (int sp = 0; sp < nsplit; ++sp)
+                    for (int j = 0; j < 4; ++j)
+                        if (n0 + j < N)
+                            v[j] += __ldg(part + sp * plane + row + n0 + j);
+            }
+            if (acc) {
+                if (vec_out)
+                    *reinterpret_cast<int4 *>(acc + row + n0) = make_int4(v[0], v[1], v[2], v[3]);
+                else
+                    for (int j = 0; j < 4; ++j)
+                        if (n0 + j < N)
+                            acc[row + n0 + j] = v[j];
+            } else {
+                const float xs = __ldg(xscale + m);
+                __nv_bfloat16 o[4];
+                for (int j = 0; j < 4; ++j)
+                    o[j] = epilogue_bf16(v[j], xs, cs[n0 + j < N ? n0 + j : 0]);
+                if (vec_out) {
+                    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(o[0]) | ((uint32_t)__bfloat16_as_ushort(o[1]) << 16);
+                    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(o[2]) | ((uint32_t)__bfloat16_as_ushort(o[3]) << 16);
+                    *reinterpret_cast<uint2 *>(out + row + n0) = make_uint2(lo, hi);
+                } else {
+                    for (int j = 0; j < 4; ++j)
+                        if (n0 + j < N)
+                            out[row + n0 + j] = o[j];
+                }
+            }
         }
     }
 }
@@ -449,12 +492,14 @@ size_t prefill_workspace_bytes(int M, int N, int K, bool pre)
 
 cudaError_t launch_splitk_finalize(const int32_t *part, int nsplit, const LinearArgs &a, cudaStream_t stream)
 {
-    const size_t plane = (size_t)a.M * a.N;
-    long fgrid = (long)((plane + 255) / 256);
-    if (fgrid > (long)device_sm_count() * 16)
-        fgrid = (long)device_sm_count() * 16;
-    tc::finalize_kernel<<<(unsigned)fgrid, 256, 0, stream>>>(part, nsplit, a.M, a.N, a.xscale, a.cs, a.out, a.acc);
-    return cudaGetLastError();
+    const int quads = (a.N + 3) / 4;
+    const int vec_in = (a.N & 3) == 0 && ((uintptr_t)part & 15) == 0;
+    const int vec_out = (a.N & 3) == 0 && (a.acc ? ((uintptr_t)a.acc & 15) == 0 : ((uintptr_t)a.out & 7) == 0);
+    const int bx = (quads + 127) / 128;
+    const long rows_per = (long)device_sm_count() * 16 / (bx > 0 ? bx : 1);
+    const int by = (int)(a.M < rows_per ? a.M : (rows_per > 0 ? rows_per : 1));
+    return tc::launch_pdl(tc::finalize_kernel, dim3((unsigned)bx, (unsigned)by), dim3(128), 0, stream, part, nsplit,
+                          a.M, a.N, a.xscale, a.cs, a.out, a.acc, vec_in, vec_out);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -546,8 +591,8 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream
     if (tiles > 0x7FFFFFFFL)
         return cudaErrorInvalidValue;
     const long ctas = tiles < sms ? tiles : sms;   // persistent CTAs walk the tiles
-    tc::prefill_kernel<<<(unsigned)ctas, THREADS, smem_bytes, stream>>>(tm_act, tm_pk, p);
-    e = cudaGetLastError();
+    e = tc::launch_pdl(tc::prefill_kernel, dim3((unsigned)ctas), dim3(THREADS), (size_t)smem_bytes, stream, tm_act,
+                       tm_pk, p);
     if (e != cudaSuccess || nsplit == 1)
         return e;
     return launch_splitk_finalize(part, nsplit, a, stream);

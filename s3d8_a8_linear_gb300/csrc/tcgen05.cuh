@@ -90,6 +90,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32
         : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be scheduled,
+// and wait until the kernel before this one has completed (its memory visible).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Bounded wait taken by a whole warp: true only if every lane saw the phase.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
 {
@@ -229,6 +241,26 @@ __device__ __forceinline__ void store_tile_row(const Params &p, int split, int r
             if (nbase + i < p.N)
                 dst[i] = epilogue_bf16(acc[i], xs, p.cs[nbase + i]);
     }
+}
+
+// Launches `kernel` with programmatic stream serialization: it may be scheduled
+// while the previous kernel on the stream finishes, and must call pdl_wait()
+// before touching anything that kernel writes.
+template <typename Kernel, typename... Args>
+inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 inline Params make_params(const LinearArgs &a, int nsplit, int kbps, int32_t *part)
