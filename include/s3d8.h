@@ -63,8 +63,9 @@ typedef enum {
     S3D8_ERR_WORKSPACE = -6    /* workspace missing or smaller than required      */
 } s3d8_status;
 
-/* Algorithm choice for s3d8_linear_ex.  AUTO picks by M: GEMV up to 8 tokens,
- * SKINNY for 9..16, TC from 17. */
+/* Algorithm choice for s3d8_linear_ex.  AUTO picks by shape: GEMV up to 8
+ * tokens; SKINNY for 9..16 tokens when K <= 8192, and up to 32 tokens when also
+ * N >= 8192; TC otherwise. */
 typedef enum {
     S3D8_ALGO_AUTO = 0,
     S3D8_ALGO_GEMV = 1,    /* CUDA-core table decode + dp4a; bulk-copy rings up to 8 tokens      */

@@ -220,28 +220,28 @@ int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t
                                                   n, out, static_cast<cudaStream_t>(stream)));
 }
 
-// The algorithm AUTO runs (measured on GB300 on the 11B gate/up and down shapes):
-// the bulk-copy dp4a GEMV up to 8 tokens, the register-fragment mma.sync path
-// from 9 to 16 tokens, the tcgen05 GEMM from 17 tokens.
-constexpr int64_t kSkinnyMinM = 9;
-constexpr int64_t kTcMinM = 17;
-
-static int resolve_algo(int64_t M, int64_t K, int algo)
+// The algorithm AUTO runs (measured on GB300 on the 11B layer's shapes): the
+// bulk-copy dp4a GEMV up to 8 tokens; above that the register-fragment mma.sync
+// path while it is faster than the tcgen05 GEMM: up to 16 tokens for rows of at
+// most 8192 columns (its 1024-column K slices split longer rows into many
+// partial sums), and up to 32 tokens when the matrix is also wide (N >= 8192,
+// where the GEMM's 128-token tiles waste the most); the tcgen05 GEMM otherwise.
+static int resolve_algo(int64_t M, int64_t N, int64_t K, int algo)
 {
-    (void)K;
     if (algo != S3D8_ALGO_AUTO)
         return algo;
-    if (M >= kTcMinM)
-        return S3D8_ALGO_TC;
-    return M >= kSkinnyMinM ? S3D8_ALGO_SKINNY : S3D8_ALGO_GEMV;
+    if (M <= 8)
+        return S3D8_ALGO_GEMV;
+    if (K <= 8192 && (M <= 16 || (M <= 32 && N >= 8192)))
+        return S3D8_ALGO_SKINNY;
+    return S3D8_ALGO_TC;
 }
 
 size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo)
 {
-    (void)N;
     if (M <= 0 || K <= 0 || M > S3D8_MAX_M || K > S3D8_MAX_K)
         return 0;
-    const int r = resolve_algo(M, K, algo);
+    const int r = resolve_algo(M, N, K, algo);
     if (r == S3D8_ALGO_TC)
         return prefill_workspace_bytes((int)M, (int)N, (int)K, prefill_predecode((int)M));
     if (r == S3D8_ALGO_SKINNY && skinny_supported((int)M))
@@ -279,7 +279,7 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     const size_t need = s3d8_linear_workspace_size(M, N, K, algo);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return S3D8_ERR_WORKSPACE;
-    algo = resolve_algo(M, K, algo);
+    algo = resolve_algo(M, N, K, algo);
     if (algo == S3D8_ALGO_SKINNY && !skinny_supported((int)M))
         return S3D8_ERR_UNSUPPORTED;
 
