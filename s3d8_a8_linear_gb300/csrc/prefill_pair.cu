@@ -2,17 +2,16 @@
 //
 // Same exact scheme as the one-SM kernel in prefill_tc.cu (bf16 x bf16 -> fp32
 // per 1024-column chunk, drained into int32; weights pre-expanded to bf16 [N, K]),
-// but a cluster of two CTAs on two SMs computes a 256-token x 240-channel tile:
-// CTA r of the pair holds activation rows 128 r .. 128 r + 127 and weight rows
-// 120 r .. 120 r + 119 of the tile in its shared memory, the even CTA issues
-// M = 256, N = 240 MMAs that read both CTAs' halves, and each CTA's tensor
-// memory receives its own 128 rows of the accumulator.  Per SM and K block the
-// bulk copies bring 31 KB instead of 46 KB, which takes the one-SM kernel's
-// shared-memory traffic (about 145 bytes per clock at the tensor rate, above
-// the 128 the SM has) below the limit.
+// but a cluster of two CTAs on two SMs computes a 256-token x 256-channel tile
+// (the weights are bf16 rows here, so the tile need not hold whole packed
+// groups): CTA r of the pair holds activation rows 128 r .. 128 r + 127 and
+// weight rows 128 r .. 128 r + 127 of the tile in its shared memory, the even
+// CTA issues M = 256, N = 256 MMAs that read both CTAs' halves, and each CTA's
+// tensor memory receives its own 128 rows of the accumulator.  Per SM and K
+// block the bulk copies bring 32 KB, where a one-SM 128 x 256 tile would need 48.
 //
 // Roles (16 warps per CTA):
-//   warp 0       bulk tensor copies of this CTA's halves into a 7-stage ring,
+//   warp 0       bulk tensor copies of this CTA's halves into a 7-stage ring (32 KB stages),
 //                completing on the even CTA's barrier (cta_group::2 copies);
 //   warp 1       TMEM allocation for the pair (both CTAs, cta_group::2); in the
 //                even CTA the MMA issuer (one thread);
@@ -30,15 +29,22 @@ namespace tc {
 
 constexpr int PAIR_STAGES = 7;
 constexpr int PAIR_BM = 2 * BM;                    // 256 tokens per pair tile
-constexpr int B_HALF = BN / 2;                     // 120 weight rows per CTA
-constexpr int B_HALF_BYTES = B_HALF * BK * 2;      // 15 KiB
+constexpr int PAIR_BN = 256;                       // channels per pair tile at most (bf16 rows: no group alignment)
+constexpr int B_HALF = PAIR_BN / 2;                // weight rows per CTA at most
+constexpr int B_HALF_BYTES = B_HALF * BK * 2;      // 16 KiB stage slot
+constexpr int PH = PAIR_BN / 2;                    // accumulator columns per drain thread at most
+
+struct PairParams {
+    Params p;
+    int bn;   // channels per tile: 128, 192 or 256
+};
 constexpr int PAIR_OFF_B = PAIR_STAGES * A_BYTES;
 constexpr int PAIR_OFF_BARS = PAIR_OFF_B + PAIR_STAGES * B_HALF_BYTES;
 constexpr int PAIR_NBARS = 2 * PAIR_STAGES + 4;
 constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_OFF_BARS + PAIR_NBARS * 8 + 16;
 static_assert(B_HALF_BYTES % 1024 == 0 && PAIR_OFF_B % 1024 == 0, "swizzled tiles 1024-aligned");
 static_assert(PAIR_SMEM_BYTES + 1024 <= 232448, "shared memory budget");
-static_assert(B_HALF % 8 == 0 && BN % 16 == 0, "M = 256 MMAs need N a multiple of 16");
+static_assert(B_HALF % 8 == 0 && PAIR_BN % 16 == 0 && PAIR_BN <= 256, "M = 256 MMAs need N a multiple of 16");
 
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -104,8 +110,10 @@ __device__ __forceinline__ void tma_2d_pair_elect(uint32_t dst, const CUtensorMa
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
-                        Params p)
+                        PairParams pp)
 {
+    const Params &p = pp.p;
+    const int bn = pp.bn, bh = bn / 2;   // tile channels; per CTA and per drain thread
     constexpr int S = PAIR_STAGES;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -123,7 +131,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t rank = cluster_rank();
     const int cid = (int)blockIdx.x >> 1, nclusters = (int)gridDim.x >> 1;
     const int mtiles = (p.M + PAIR_BM - 1) / PAIR_BM;
-    const int ntiles = ((p.N + 2) / 3 + GROUPS - 1) / GROUPS;
+    const int ntiles = (p.N + bn - 1) / bn;
     const int nk_all = (p.K + BK - 1) / BK;
     const int total = mtiles * ntiles * p.nsplit;
     struct Tile {
@@ -182,11 +190,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                             break;
                         }
                         if (rank == 0)
-                            mbar_arrive_expect_tx_elect(l_full + 8 * s, 2 * (A_BYTES + B_HALF_BYTES));
+                            mbar_arrive_expect_tx_elect(l_full + 8 * s, 2 * (A_BYTES + bh * BK * 2));
                         const int kx = (T.kbase + kb) * BK;
                         tma_2d_pair_elect(base + s * A_BYTES, &tm_act, kx, T.m0 + (int)rank * BM, full0 + 8 * s);
                         tma_2d_pair_elect(base + PAIR_OFF_B + s * B_HALF_BYTES, &tm_w, kx,
-                                          T.nt * BN + (int)rank * B_HALF, full0 + 8 * s);
+                                          T.nt * bn + (int)rank * bh, full0 + 8 * s);
                         ++issued;
                     }
                 }
@@ -201,7 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             // descriptors stay warp-uniform; one elected lane issues -----------------
             {
                 int g = 0, gc = 0;
-                const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) |
                                        ((uint32_t)(PAIR_BM >> 4) << 24);
                 for (int t = cid; t < total && !timed_out; t += nclusters) {
                     const Tile T = tile_of(t);
@@ -241,13 +249,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int q = warp & 3;
         const int h = (warp - DRAIN_WARP0) >> 2;
         const uint32_t release = rank == 0 ? acc_empty : map_to_rank(acc_empty, 0);
-        int32_t acc[HALF];
+        int32_t acc[PH];
         int gc = 0;
         for (int t = cid; t < total && !timed_out; t += nclusters) {
             const Tile T = tile_of(t);
             const int nch = (T.nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
 #pragma unroll
-            for (int i = 0; i < HALF; ++i)
+            for (int i = 0; i < PH; ++i)
                 acc[i] = 0;
             for (int c = gc; c < gc + nch; ++c) {
                 if (!mbar_wait_bounded(acc_full + 8 * (c & 1), (c >> 1) & 1)) {
@@ -255,19 +263,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((c & 1) * 256 + h * HALF);
+                const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((c & 1) * 256 + h * bh);
 #pragma unroll
-                for (int gg = 0; gg < HALF / 24; ++gg) {
-                    float v[3][8];
+                for (int i = 0; i < PH / 32; ++i) {
+                    if (i * 32 < bh) {   // bh is uniform and a multiple of 32: the warp loads together
+                        float v[4][8];
 #pragma unroll
-                    for (int i = 0; i < 3; ++i)
-                        tmem_ld8(ta + (gg * 3 + i) * 8, v[i]);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        for (int u = 0; u < 4; ++u)
+                            tmem_ld8(ta + i * 32 + u * 8, v[u]);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                    for (int i = 0; i < 3; ++i)
+                        for (int u = 0; u < 4; ++u)
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            acc[(gg * 3 + i) * 8 + j] += __float2int_rn(v[i][j]);
+                            for (int j = 0; j < 8; ++j)
+                                acc[i * 32 + u * 8 + j] += __float2int_rn(v[u][j]);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -277,7 +287,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             gc += nch;
             const int row = T.m0 + (int)rank * BM + 32 * q + lane;
             if (!timed_out && row < p.M)
-                store_tile_row(p, T.split, row, T.nt * BN + h * HALF, acc);
+                store_tile_row<PH>(p, T.split, row, T.nt * bn + h * bh, acc, bh);
         }
     }
     if (timed_out)
@@ -290,6 +300,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 }  // namespace tc
+
+// Channels per pair tile: 256, 192 or 128 (each CTA's half then drains in whole
+// groups of 32 columns), the one that minimises the rounds of tiles the SM pairs run (time per tile taken as proportional to the
+// width plus a fixed 64 columns' worth), the widest on a tie.
+static int pair_tile_n(int M, int N, int nsplit)
+{
+    const long pairs = device_sm_count() / 2 > 0 ? device_sm_count() / 2 : 1;
+    const long mt = (long)((M + tc::PAIR_BM - 1) / tc::PAIR_BM) * nsplit;
+    int best = tc::PAIR_BN;
+    long best_cost = -1;
+    for (int bn = tc::PAIR_BN; bn >= 128; bn -= 64) {
+        const long tiles = mt * ((N + bn - 1) / bn);
+        const long cost = (tiles + pairs - 1) / pairs * (bn + 64);
+        if (best_cost < 0 || cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
 
 // SM-pair tensor-core GEMM on pre-expanded bf16 weights: act is the bf16 copy of
 // the activation codes [M, K], wdec the bf16 weights [N, K] (both in the
@@ -308,7 +338,8 @@ cudaError_t launch_prefill_pair(const LinearArgs &a, const __nv_bfloat16 *act, c
     const cuuint32_t boxA[2] = {BK, BM};
     const cuuint64_t dW[2] = {(cuuint64_t)a.K, (cuuint64_t)a.N};
     const cuuint64_t sW[1] = {(cuuint64_t)a.K * 2};
-    const cuuint32_t boxW[2] = {BK, B_HALF};
+    const int bn = pair_tile_n(a.M, a.N, nsplit);
+    const cuuint32_t boxW[2] = {BK, (cuuint32_t)(bn / 2)};
     if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(act), dA, sA, boxA, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
@@ -320,9 +351,10 @@ cudaError_t launch_prefill_pair(const LinearArgs &a, const __nv_bfloat16 *act, c
                                          PAIR_SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
-    Params p = make_params(a, nsplit, kbps, part);
-    const int G = (a.N + 2) / 3;
-    const long tiles = (long)((a.M + PAIR_BM - 1) / PAIR_BM) * (long)((G + GROUPS - 1) / GROUPS) * nsplit;
+    PairParams pp;
+    pp.p = make_params(a, nsplit, kbps, part);
+    pp.bn = bn;
+    const long tiles = (long)((a.M + PAIR_BM - 1) / PAIR_BM) * (long)((a.N + bn - 1) / bn) * nsplit;
     if (tiles > 0x7FFFFFFFL)
         return cudaErrorInvalidValue;
     long pairs = device_sm_count() / 2;
@@ -336,7 +368,7 @@ cudaError_t launch_prefill_pair(const LinearArgs &a, const __nv_bfloat16 *act, c
     (void)cudaGetLastError();
     const long clusters = tiles < pairs ? tiles : pairs;
     return launch_pdl(prefill_pair_kernel, dim3((unsigned)(2 * clusters)), dim3(THREADS), (size_t)PAIR_SMEM_BYTES,
-                      stream, tm_act, tm_w, p);
+                      stream, tm_act, tm_w, pp);
 }
 
 }  // namespace s3d8

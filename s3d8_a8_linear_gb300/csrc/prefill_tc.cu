@@ -440,9 +440,13 @@ __global__ void finalize_kernel(const int32_t *__restrict__ part, int nsplit, in
 // K split of the tensor-core GEMM when its output tiles alone cannot fill the
 // GPU: the number of 64-column blocks per split that minimises
 // waves x (blocks per CTA + a per-CTA fixed cost of about 4 blocks).
+static bool prefill_pairs(int M);
+
 static void tc_plan(int M, int N, int K, int sms, int &nsplit, int &kb_per_split)
 {
-    const long tiles = (long)((M + tc::BM - 1) / tc::BM) * (((N + 2) / 3 + tc::GROUPS - 1) / tc::GROUPS);
+    // CTAs per K range: 128 x 240 tiles on one SM, or 256 x 256 tiles on two
+    const long tiles = prefill_pairs(M) ? 2L * ((M + 255) / 256) * ((N + 255) / 256)
+                                        : (long)((M + tc::BM - 1) / tc::BM) * (((N + 2) / 3 + tc::GROUPS - 1) / tc::GROUPS);
     const int nk = (K + tc::BK - 1) / tc::BK;
     nsplit = 1;
     kb_per_split = nk;
@@ -476,6 +480,11 @@ constexpr int kPredecodeMinM = 384;
 bool prefill_predecode(int M)
 {
     return M >= kPredecodeMinM;
+}
+
+static bool prefill_pairs(int M)
+{
+    return prefill_predecode(M);
 }
 
 size_t prefill_workspace_bytes(int M, int N, int K, bool pre)

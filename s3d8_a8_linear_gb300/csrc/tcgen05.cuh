@@ -200,23 +200,26 @@ struct Params {
 
 // Writes one accumulator row segment of a tile: the int32 sums (to the split-K
 // partials or the raw int32 output) or the bf16 epilogue (x_s * acc) * W_s.
-// Columns nbase .. nbase + HALF - 1 of row `row`; columns >= N are skipped.
+// Columns nbase .. nbase + W - 1 of row `row`; columns >= N are skipped.
+// With a width `w` < W only the first w columns are written.
+template <int W = HALF>
 __device__ __forceinline__ void store_tile_row(const Params &p, int split, int row, int nbase,
-                                               const int32_t (&acc)[HALF])
+                                               const int32_t (&acc)[W], int w = W)
 {
-    const bool full = nbase + HALF <= p.N;
+    static_assert(W % 8 == 0, "vector stores take 8 columns");
+    const bool full = w == W && nbase + W <= p.N;
     int32_t *accp = p.part ? p.part + (size_t)split * p.M * p.N : p.acc;
     const bool vec_acc = p.part ? p.vec_part : p.vec_out;
     if (accp) {
         int32_t *dst = accp + (size_t)row * p.N + nbase;
         if (full && vec_acc) {
 #pragma unroll
-            for (int i = 0; i < HALF; i += 4)
+            for (int i = 0; i < W; i += 4)
                 *reinterpret_cast<int4 *>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
         } else {
 #pragma unroll
-            for (int i = 0; i < HALF; ++i)
-                if (nbase + i < p.N)
+            for (int i = 0; i < W; ++i)
+                if (i < w && nbase + i < p.N)
                     dst[i] = acc[i];
         }
         return;
@@ -225,7 +228,7 @@ __device__ __forceinline__ void store_tile_row(const Params &p, int split, int r
     __nv_bfloat16 *dst = p.out + (size_t)row * p.N + nbase;
     if (full && p.vec_out) {
 #pragma unroll
-        for (int i = 0; i < HALF; i += 8) {
+        for (int i = 0; i < W; i += 8) {
             uint32_t o[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -237,8 +240,8 @@ __device__ __forceinline__ void store_tile_row(const Params &p, int split, int r
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < HALF; ++i)
-            if (nbase + i < p.N)
+        for (int i = 0; i < W; ++i)
+            if (i < w && nbase + i < p.N)
                 dst[i] = epilogue_bf16(acc[i], xs, p.cs[nbase + i]);
     }
 }

@@ -266,7 +266,7 @@ TC_TILES = [(128, 240, 64), (129, 241, 1040), (300, 722, 2112), (256, 480, 3072)
             # TMA) and two SMs share each 256-token tile: the odd SM's rows past M,
             # partial pair tiles, one K block, split and unsplit K
             (384, 241, 1040), (520, 722, 2112), (768, 480, 3072), (400, 3, 16),
-            (1000, 1201, 4096), (2048, 96, 14336)]
+            (1000, 1201, 4096), (2048, 96, 14336), (640, 257, 1024), (512, 512, 2048)]
 
 
 @pytest.mark.parametrize("M,N,K", TC_TILES)
