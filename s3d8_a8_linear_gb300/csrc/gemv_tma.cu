@@ -320,6 +320,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
     // refilled while the second half is still being decoded.
     constexpr int kHalfBytes = kStage / kHalves;
     const int len0 = min(slice_len, kHalfBytes), len1 = slice_len - len0;
+    const uint64_t wpol = l2_evict_first_policy();   // packed bytes are read once per launch
     auto issue_slice = [&](int slot, int row) {
         if (lane == 0) {
             const uint8_t *src = job.packed + (size_t)row * K + slice_off;
@@ -327,10 +328,10 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
             const uint32_t b = bar0 + slot * kHalves * 8;
             fence_proxy_async_smem();   // this warp's earlier reads of the slot precede the refill
             mbar_arrive_expect_tx(b, (uint32_t)len0);
-            bulk_load(dst, src, (uint32_t)len0, b);
+            bulk_load_hint(dst, src, (uint32_t)len0, b, wpol);
             if (len1 > 0) {
                 mbar_arrive_expect_tx(b + 8, (uint32_t)len1);
-                bulk_load(dst + kHalfBytes, src + kHalfBytes, (uint32_t)len1, b + 8);
+                bulk_load_hint(dst + kHalfBytes, src + kHalfBytes, (uint32_t)len1, b + 8, wpol);
             }
         }
     };
@@ -456,7 +457,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
                 const uint8_t *src = job.packed + (size_t)next_row * K + slice_off;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(b, (uint32_t)len0);
-                bulk_load(ring + s * kStage, src, (uint32_t)len0, b);
+                bulk_load_hint(ring + s * kStage, src, (uint32_t)len0, b, wpol);
             }
             if (len1 > 0) {
                 if (!mbar_wait_bounded(b + 8, par)) {
@@ -473,7 +474,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
                     const uint8_t *src = job.packed + (size_t)next_row * K + slice_off + kHalfBytes;
                     fence_proxy_async_smem();
                     mbar_arrive_expect_tx(b + 8, (uint32_t)len1);
-                    bulk_load(ring + s * kStage + kHalfBytes, src, (uint32_t)len1, b + 8);
+                    bulk_load_hint(ring + s * kStage + kHalfBytes, src, (uint32_t)len1, b + 8, wpol);
                 }
             }
             ++consumed;
