@@ -149,15 +149,15 @@ __device__ __forceinline__ int quant_code(float x, float s, float r)
     return max(-127, min(127, __float2int_rn(t)));
 }
 
-// Eight bf16 values (one 16-byte chunk) -> eight codes (8 bytes).  The common
-// path is branch-free over the eight values and uses only full-rate FP32 adds,
-// multiplies and min/max: t = RN(x * r) is clamped to +-127 and rounded to the
-// nearest integer (ties to even) by adding 1.5 * 2^23, whose float encoding
-// then holds the two's-complement code in its low byte.  Clamping before
-// rounding gives the same code as rounding before clamping, because +-127 are
-// integers.  t - rint(t), exact in fp32, flags the rare near-ties, which are
-// redone with the exact quotient afterwards.  Out of line so that unrolled
-// prologue loops share one copy.
+// Eight bf16 values (one 16-byte chunk) -> eight codes (8 bytes), for values of
+// a row whose absmax a gives s = RN(a / 127).  The common path is branch-free
+// over the eight values and uses only full-rate FP32 multiplies and adds:
+// t = RN(x * r) is rounded to the nearest integer (ties to even) by adding
+// 1.5 * 2^23, whose float encoding then holds the two's-complement code in its
+// low byte.  No clamp is needed: |x| <= a, so |t| <= 127 (1 + 2^-24)^2 /
+// (1 - 2^-24) < 127.5 and rint(t) is already within +-127.  t - rint(t), exact
+// in fp32, flags the rare near-ties, which are redone with the exact quotient
+// afterwards (quant_code, which clamps).
 constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
 
 #ifdef S3D8_QUANT_NOINLINE
@@ -180,7 +180,7 @@ uint2 quant_chunk8(uint4 v, float s, float r)
     bool redo = s < kTinyScale;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        const float t = fminf(fmaxf(__fmul_rn(x[e], r), -127.0f), 127.0f);
+        const float t = __fmul_rn(x[e], r);
         const float y = __fadd_rn(t, kRoundMagic);
         const float d = __fsub_rn(t, __fsub_rn(y, kRoundMagic));   // t - rint(t)
         redo |= fabsf(fabsf(d) - 0.5f) < kTieMargin;

@@ -113,11 +113,13 @@ __device__ __forceinline__ void pdl_wait()
 // shared int8 codes and shared fp32 scales, by the whole CTA.  Same rule as the
 // standalone kernel.  The row is read once into registers (stage 1, issued
 // before the bulk weight copies so that it does not queue behind them) and
-// quantised from there (stage 2).
+// quantised from there (stage 2).  Instantiated for NS = 1, 2, 4 and 7 chunks
+// per thread, so that a short row runs a short prologue.
 constexpr int kActChunksPerThread = kUnionBytes / 8 / kTmaThreads;   // 16-byte chunks
 
+template <int NS>
 struct ActRegs {
-    uint4 v[kActChunksPerThread];
+    uint4 v[NS];
 };
 
 // Token (row of x) that 16-byte chunk c belongs to, for rows of per_row chunks:
@@ -134,11 +136,12 @@ __device__ __forceinline__ int chunk_token(int c, int per_row)
 
 // Volatile loads: all chunks leave at once, here, instead of being sunk one by
 // one to their first use (which would serialise their latencies).
-__device__ __forceinline__ void act_load(const __nv_bfloat16 *__restrict__ x, int M, int K, ActRegs &r)
+template <int NS>
+__device__ __forceinline__ void act_load(const __nv_bfloat16 *__restrict__ x, int M, int K, ActRegs<NS> &r)
 {
     const int chunks = M * K / 8;
 #pragma unroll
-    for (int i = 0; i < kActChunksPerThread; ++i) {
+    for (int i = 0; i < NS; ++i) {
         const int c = threadIdx.x + i * kTmaThreads;
         r.v[i] = c < chunks ? ldg_stream_v4(reinterpret_cast<const uint4 *>(x) + c)
                             : make_uint4(0u, 0u, 0u, 0u);
@@ -147,8 +150,8 @@ __device__ __forceinline__ void act_load(const __nv_bfloat16 *__restrict__ x, in
 
 // Phase A of the fused quantisation: per-warp absmax of each token's row part
 // held in `r`, written to red[warp * MT + m].
-template <int MT>
-__device__ __forceinline__ void act_amax_partial(const ActRegs &r, int M, int K, float *red)
+template <int MT, int NS>
+__device__ __forceinline__ void act_amax_partial(const ActRegs<NS> &r, int M, int K, float *red)
 {
     const int chunks = M * K / 8;
     const int per_row = K / 8;
@@ -158,7 +161,7 @@ __device__ __forceinline__ void act_amax_partial(const ActRegs &r, int M, int K,
     for (int m = 0; m < MT; ++m)
         amax[m] = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kActChunksPerThread; ++i) {
+    for (int i = 0; i < NS; ++i) {
         const int c = threadIdx.x + i * kTmaThreads;
         if (c < chunks) {
             const int m = chunk_token<MT>(c, per_row);
@@ -188,8 +191,8 @@ __device__ __forceinline__ void act_amax_partial(const ActRegs &r, int M, int K,
 // Phase B: every thread folds the warp maxima into the per-token scale
 // (absmax / 127, IEEE division) and writes the codes of its own chunks into
 // the shared row `xs`.  Thread 0 also publishes the scales.
-template <int MT>
-__device__ __forceinline__ void act_codes(const ActRegs &r, int M, int K, const float *red, int8_t *xs,
+template <int MT, int NS>
+__device__ __forceinline__ void act_codes(const ActRegs<NS> &r, int M, int K, const float *red, int8_t *xs,
                                           float *scale_s)
 {
     const int chunks = M * K / 8;
@@ -209,7 +212,7 @@ __device__ __forceinline__ void act_codes(const ActRegs &r, int M, int K, const 
             scale_s[m] = sc[m];
     }
 #pragma unroll
-    for (int i = 0; i < kActChunksPerThread; ++i) {
+    for (int i = 0; i < NS; ++i) {
         const int c = threadIdx.x + i * kTmaThreads;
         if (c < chunks) {
             const int m = chunk_token<MT>(c, per_row);
@@ -223,6 +226,23 @@ __device__ __forceinline__ void act_codes(const ActRegs &r, int M, int K, const 
             reinterpret_cast<uint2 *>(xs)[c] = quant_chunk8(r.v[i], s, inv);
         }
     }
+}
+
+// The fused quantisation with NS chunks per thread: loads x, runs issue_rest()
+// (the rest of the bulk copies, queued behind x), publishes the warp maxima,
+// then writes the codes and scales into shared memory.  Contains two CTA
+// barriers, the first of which also publishes the decode table.
+template <int MT, int NS, typename F>
+__device__ __forceinline__ void fused_quant(const __nv_bfloat16 *x, int M, int K, float *red, int8_t *xs,
+                                            float *scale_s, F issue_rest)
+{
+    ActRegs<NS> act;
+    act_load<NS>(x, M, K, act);
+    issue_rest();
+    act_amax_partial<MT, NS>(act, M, K, red);
+    __syncthreads();
+    act_codes<MT, NS>(act, M, K, red, xs, scale_s);
+    __syncthreads();
 }
 
 template <int MT, int CH>
@@ -358,13 +378,21 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
 
     // ---- activations -------------------------------------------------------------
     const bool fused = job.x != nullptr;
-    ActRegs act;
     uint32_t xr[MT][CH][4];
-    if (fused) {
-        act_load(job.x, M, K, act);
-        for (int i = kPrewaitSlices; i < kDepth && i < nmine0; ++i)   // rest of the ring, behind x
+    auto issue_rest = [&]() {   // rest of the ring, behind the activation loads
+        for (int i = kPrewaitSlices; i < kDepth && i < nmine0; ++i)
             issue_slice(issued++ % kDepth, row0 + rs + i * sets);
-        act_amax_partial<MT>(act, M, K, red);
+    };
+    if (fused) {
+        const int ns = (M * K / 8 + kTmaThreads - 1) / kTmaThreads;   // 16-byte chunks per thread
+        if (ns <= 1)
+            fused_quant<MT, 1>(job.x, M, K, red, xs, scale_s, issue_rest);
+        else if (ns <= 2)
+            fused_quant<MT, 2>(job.x, M, K, red, xs, scale_s, issue_rest);
+        else if (ns <= 4)
+            fused_quant<MT, 4>(job.x, M, K, red, xs, scale_s, issue_rest);
+        else
+            fused_quant<MT, kActChunksPerThread>(job.x, M, K, red, xs, scale_s, issue_rest);
     } else {
 #pragma unroll
         for (int m = 0; m < MT; ++m)
@@ -379,16 +407,13 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
                 xr[m][j][2] = v.z;
                 xr[m][j][3] = v.w;
             }
-        for (int i = kPrewaitSlices; i < kDepth && i < nmine0; ++i)   // rest of the ring, behind x
-            issue_slice(issued++ % kDepth, row0 + rs + i * sets);
+        issue_rest();
         if (threadIdx.x < MT)   // scales are read only for the bf16 output (none on the int32 path)
             scale_s[threadIdx.x] =
                 ((int)threadIdx.x < M && job.xscale != nullptr) ? job.xscale[threadIdx.x] : 0.0f;
+        __syncthreads();   // table written; scales published
     }
-    __syncthreads();   // table written; warp maxima (fused) or scales published
     if (fused) {
-        act_codes<MT>(act, M, K, red, xs, scale_s);
-        __syncthreads();
         if (b == 0) {   // optional copies of the codes and scales for the caller
             if (job.xq_out)
                 for (int c = threadIdx.x; c < M * K / 16; c += kTmaThreads)
