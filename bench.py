@@ -633,12 +633,15 @@ def device_matrix(torch, dev, gen, K, N):
                     torch.bfloat16))
 
 
-def decode_sweep_measure(torch, s3d8, dev, copies=8, reps=40):
+def decode_sweep_measure(torch, s3d8, dev, copies=8, reps=40, replays=5):
     """Batched decode (M = 8..64) on the gate/up and down shapes through
-    s3d8_linear (automatic algorithm choice), rotating `copies` weight copies."""
+    s3d8_linear (automatic algorithm choice), rotating `copies` weight copies.
+    The `reps` launches are captured in one CUDA graph and replayed, so that the
+    time is the device's and not the Python binding's per-call overhead."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
     res = {}
+    stream = torch.cuda.Stream(dev)
     for name, K, N in si.SWEEP_SHAPES:
         mats = [device_matrix(torch, dev, gen, K, N) for _ in range(copies)]
         for M in si.DECODE_SWEEP_M:
@@ -646,18 +649,25 @@ def decode_sweep_measure(torch, s3d8, dev, copies=8, reps=40):
             xq, xs = s3d8.quantize_act(x)
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = torch.empty((max(1, s3d8.workspace_size(M, N, K)),), dtype=torch.uint8, device=dev)
-            for m in mats:
+            for m in mats:   # eager warm-up (kernel attributes, first-touch)
                 s3d8.linear(m["packed"], m["C"], m["cs"], xq, xs, N, out=out, workspace=ws)
             torch.cuda.synchronize()
+
+            def body():
+                for i in range(reps):
+                    m = mats[i % copies]
+                    s3d8.linear(m["packed"], m["C"], m["cs"], xq, xs, N, out=out, workspace=ws)
+            g = capture(torch, stream, body)
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
-            t0.record()
-            for i in range(reps):
-                m = mats[i % copies]
-                s3d8.linear(m["packed"], m["C"], m["cs"], xq, xs, N, out=out, workspace=ws)
-            t1.record()
+            with torch.cuda.stream(stream):
+                g.replay()
+                t0.record(stream)
+                for _ in range(replays):
+                    g.replay()
+                t1.record(stream)
             t1.synchronize()
-            ms = t0.elapsed_time(t1) / reps
+            ms = t0.elapsed_time(t1) / (reps * replays)
             res[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2),
                                    "weight_gbs": round(weight_bytes(K, N) / (ms * 1e-3) / 1e9, 1),
                                    "tops": round(2 * M * N * K / (ms * 1e-3) / 1e12, 2)}
@@ -949,6 +959,8 @@ def main():
                     help="time the headline step only (no variants, e2e, sweeps); for profiling")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the M = 2048 tensor-core measurement and print it; for profiling")
+    ap.add_argument("--sweep-only", action="store_true",
+                    help="run only the batched-decode sweep (M = 8..64) and print it; for profiling")
     ap.add_argument("--encode-only", action="store_true",
                     help="run only the encoder and centroid-fit measurements and print them; "
                          "for profiling")
@@ -964,6 +976,13 @@ def main():
         import s3d8_a8_linear_gb300 as s3d8
         s3d8.load(build_if_missing=True)
         print(json.dumps(prefill_measure(torch, s3d8, torch.device("cuda:0"))))
+        return
+    if args.sweep_only:
+        import torch
+
+        import s3d8_a8_linear_gb300 as s3d8
+        s3d8.load(build_if_missing=True)
+        print(json.dumps(decode_sweep_measure(torch, s3d8, torch.device("cuda:0"))))
         return
     if args.encode_only:
         import torch
