@@ -64,13 +64,14 @@ typedef enum {
 } s3d8_status;
 
 /* Algorithm choice for s3d8_linear_ex.  AUTO picks by shape: GEMV up to 8
- * tokens; SKINNY for 9..16 tokens when K <= 8192, and up to 32 tokens when also
- * N >= 8192; TC otherwise. */
+ * tokens; TMEM for 9..32 tokens, and up to 64 tokens while its tiles fit in one
+ * wave on the device; TC otherwise.  SKINNY runs only on request. */
 typedef enum {
     S3D8_ALGO_AUTO = 0,
     S3D8_ALGO_GEMV = 1,    /* CUDA-core table decode + dp4a; bulk-copy rings up to 8 tokens      */
     S3D8_ALGO_SKINNY = 2,  /* table decode into mma.sync bf16 register fragments, 1..32 tokens   */
-    S3D8_ALGO_TC = 3       /* tcgen05 bf16 tensor-core GEMM with exact chunked int32 sums       */
+    S3D8_ALGO_TC = 3,      /* tcgen05 bf16 tensor-core GEMM with exact chunked int32 sums       */
+    S3D8_ALGO_TMEM = 4     /* tcgen05 fp16 GEMM, weights decoded into tensor memory, 1..64 tokens */
 } s3d8_algo;
 
 /*

@@ -19,7 +19,7 @@ import torch
 
 from . import _build
 
-ALGO_AUTO, ALGO_GEMV, ALGO_SKINNY, ALGO_TC = 0, 1, 2, 3
+ALGO_AUTO, ALGO_GEMV, ALGO_SKINNY, ALGO_TC, ALGO_TMEM = 0, 1, 2, 3, 4
 
 STATUS = {
     0: "ok",

@@ -221,19 +221,20 @@ int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t
 }
 
 // The algorithm AUTO runs (measured on GB300 on the 11B layer's shapes): the
-// bulk-copy dp4a GEMV up to 8 tokens; above that the register-fragment mma.sync
-// path while it is faster than the tcgen05 GEMM: up to 16 tokens for rows of at
-// most 8192 columns (its 1024-column K slices split longer rows into many
-// partial sums), and up to 32 tokens when the matrix is also wide (N >= 8192,
-// where the GEMM's 128-token tiles waste the most); the tcgen05 GEMM otherwise.
+// bulk-copy dp4a GEMV up to 8 tokens; the tcgen05 GEMM with the weights decoded
+// into tensor memory for 9..32 tokens, and up to 64 while its tiles fit in one
+// wave (with 48 or more tokens its K ranges are capped at 1024 columns, which on
+// long rows makes more tiles than SMs); the tcgen05 GEMM on shared-memory tiles
+// otherwise.  (The register-fragment mma.sync path is slower than the tensor-
+// memory path at every size it takes and runs only on request.)
 static int resolve_algo(int64_t M, int64_t N, int64_t K, int algo)
 {
     if (algo != S3D8_ALGO_AUTO)
         return algo;
     if (M <= 8)
         return S3D8_ALGO_GEMV;
-    if (K <= 8192 && (M <= 16 || (M <= 32 && N >= 8192)))
-        return S3D8_ALGO_SKINNY;
+    if (tmem_preferred((int)M, (int)N, (int)K))
+        return S3D8_ALGO_TMEM;
     return S3D8_ALGO_TC;
 }
 
@@ -246,6 +247,8 @@ size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo)
         return prefill_workspace_bytes((int)M, (int)N, (int)K, prefill_predecode((int)M));
     if (r == S3D8_ALGO_SKINNY && skinny_supported((int)M))
         return skinny_workspace_bytes((int)M, (int)N, (int)K);
+    if (r == S3D8_ALGO_TMEM && tmem_supported((int)M))
+        return tmem_workspace_bytes((int)M, (int)N, (int)K);
     return 0;
 }
 
@@ -259,7 +262,7 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
         st = check_mn(M, N);
     if (st != S3D8_OK)
         return st;
-    if (algo < S3D8_ALGO_AUTO || algo > S3D8_ALGO_TC)
+    if (algo < S3D8_ALGO_AUTO || algo > S3D8_ALGO_TMEM)
         return S3D8_ERR_INVALID_ARG;
     if (M == 0 || N == 0)
         return S3D8_OK;
@@ -282,6 +285,8 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     algo = resolve_algo(M, N, K, algo);
     if (algo == S3D8_ALGO_SKINNY && !skinny_supported((int)M))
         return S3D8_ERR_UNSUPPORTED;
+    if (algo == S3D8_ALGO_TMEM && !tmem_supported((int)M))
+        return S3D8_ERR_UNSUPPORTED;
 
     LinearArgs a;
     a.packed = packed;
@@ -302,6 +307,8 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
         return cuda_status(launch_prefill_tc(a, prefill_predecode(a.M), strm));
     if (algo == S3D8_ALGO_SKINNY)
         return cuda_status(launch_skinny(a, strm));
+    if (algo == S3D8_ALGO_TMEM)
+        return cuda_status(launch_tmem(a, strm));
     if (gemv_tma_supported(a.M, a.K))
         return cuda_status(launch_gemv_tma(a, strm));
     return cuda_status(launch_gemv(a, strm));

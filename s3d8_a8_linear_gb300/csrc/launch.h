@@ -86,5 +86,12 @@ cudaError_t launch_splitk_finalize(const int32_t *part, int nsplit, const Linear
 bool skinny_supported(int M);
 size_t skinny_workspace_bytes(int M, int N, int K);
 cudaError_t launch_skinny(const LinearArgs &a, cudaStream_t stream);
+// tcgen05 GEMM with the weights decoded into tensor memory (decode_tmem.cu):
+// 1..64 tokens.
+bool tmem_supported(int M);
+// AUTO takes it for 9..32 tokens, and up to 64 when its tiles fit in one wave.
+bool tmem_preferred(int M, int N, int K);
+size_t tmem_workspace_bytes(int M, int N, int K);
+cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream);
 
 }  // namespace s3d8

@@ -17,10 +17,10 @@ from gpu_util import (assert_out_close, bf16_bits, bf16_to_f64, dev, f32, guarde
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = [s3d8.ALGO_GEMV, s3d8.ALGO_SKINNY, s3d8.ALGO_TC]
-SKINNY_MAX_M = 32
+ALGOS = [s3d8.ALGO_GEMV, s3d8.ALGO_SKINNY, s3d8.ALGO_TC, s3d8.ALGO_TMEM]
+MAX_M = {s3d8.ALGO_SKINNY: 32, s3d8.ALGO_TMEM: 64}   # token limits of the bounded algorithms
 ALGO_IDS = {s3d8.ALGO_AUTO: "auto", s3d8.ALGO_GEMV: "gemv", s3d8.ALGO_SKINNY: "skinny",
-            s3d8.ALGO_TC: "tc"}
+            s3d8.ALGO_TC: "tc", s3d8.ALGO_TMEM: "tmem"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -210,8 +210,8 @@ def sample_positions(M, N, rng, count=1500):
 def test_sweep_sampled(shape, M, algo):
     """Batched decode (with 1 % activation outliers) and prefill sizes at full
     shape; the oracle computes a sample of outputs one by one."""
-    if algo == s3d8.ALGO_SKINNY and M > SKINNY_MAX_M:
-        pytest.skip("the register-fragment path takes up to 32 tokens")
+    if M > MAX_M.get(algo, M):
+        pytest.skip(f"{ALGO_IDS[algo]} takes up to {MAX_M[algo]} tokens")
     name, K, N = shape
     mat = si.matrix(name, K, N, seed=2)
     x = si.acts(M, K, seed=2, outliers=M <= 64)
@@ -311,6 +311,35 @@ def test_skinny_rejects_more_than_32_tokens():
     xq, xs = oracle.quantize_act(x)
     with pytest.raises(s3d8.S3D8Error) as e:
         gpu_acc(C, packed, xq, 9, s3d8.ALGO_SKINNY)
+    assert e.value.status == -3
+
+
+# Tensor-memory path: 128-row tiles (ragged last tile, N not a multiple of 3),
+# tiles of several 1024-column chunks (few K splits when there are many row
+# tiles), more tiles than SMs (a second tile per CTA), K ragged against the
+# 64-column block, and 1..64 tokens (N of the MMA 16..64).
+TMEM_CASES = [(1, 4, 16), (5, 241, 1040), (16, 722, 2112), (17, 1201, 3088), (33, 96, 256),
+              (64, 480, 14336), (8, 38401, 4096), (64, 61441, 256), (48, 3000, 1104)]
+
+
+@pytest.mark.parametrize("M,N,K", TMEM_CASES)
+def test_tmem_in_full(M, N, K):
+    C, packed, cs, x = rand_case(M, N, K, seed=M * 17 + N * 3 + K)
+    xq, xs = oracle.quantize_act(x)
+    ref, acc_o = oracle.linear(packed, C, cs, xq, xs, N)
+    np.testing.assert_array_equal(gpu_acc(C, packed, xq, N, s3d8.ALGO_TMEM), acc_o)
+    out, check = guarded((M, N), torch.bfloat16, 3.0, pad=65)
+    s3d8.linear(u8(packed), i8(C), bf16_bits(cs), i8(xq), f32(xs), N, out=out, algo=s3d8.ALGO_TMEM)
+    torch.cuda.synchronize()
+    check()
+    assert_out_close(bf16_to_f64(out), ref)
+
+
+def test_tmem_rejects_more_than_64_tokens():
+    C, packed, cs, x = rand_case(65, 9, 64, seed=10)
+    xq, xs = oracle.quantize_act(x)
+    with pytest.raises(s3d8.S3D8Error) as e:
+        gpu_acc(C, packed, xq, 9, s3d8.ALGO_TMEM)
     assert e.value.status == -3
 
 
