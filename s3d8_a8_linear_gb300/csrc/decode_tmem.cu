@@ -56,7 +56,7 @@ constexpr int LUT_BYTES = kLutEntries * 32 * 4;  // 32 KiB, one copy per lane
 constexpr int OFF_LUT = LST * STAGE;
 constexpr int OFF_BARS = OFF_LUT + LUT_BYTES;
 constexpr int TEAMS = 3;
-constexpr int NBARS = 2 * LST + 2 * TEAMS + 2;
+constexpr int NBARS = 2 * LST + TEAMS + 2;
 constexpr int SMEM_BYTES = 1024 + OFF_BARS + NBARS * 8 + 16;
 constexpr int THREADS = 512;
 constexpr int DEC_WARP0 = 4;
@@ -237,11 +237,11 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     const uint32_t lut = base + OFF_LUT;
     const uint32_t bars = base + OFF_BARS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BARS + NBARS * 8);
-    // full/empty: the ring's stages; a_full/a_empty: each team's A stage;
+    // full/empty: the ring's stages; a_full: each team's A stage is written;
     // acc_full: a chunk's sums are in D; acc_empty: D has been drained
     const uint32_t full = bars, empty = full + 8 * LST;
-    const uint32_t a_full = empty + 8 * LST, a_empty = a_full + 8 * TEAMS;
-    const uint32_t acc_full = a_empty + 8 * TEAMS, acc_empty = acc_full + 8;
+    const uint32_t a_full = empty + 8 * LST;
+    const uint32_t acc_full = a_full + 8 * TEAMS, acc_empty = acc_full + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nkb = (p.K + BK - 1) / BK;
 
@@ -252,7 +252,6 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
         }
         for (int t = 0; t < TEAMS; ++t) {
             mbar_init(a_full + 8 * t, 4);
-            mbar_init(a_empty + 8 * t, 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, DEC_WARPS);
@@ -313,8 +312,10 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
         for (Walk w = walk_begin(p, nkb); w.valid; walk_next(p, nkb, w)) {
             const int s = w.gkb % LST, t = w.gkb % TEAMS, use = w.gkb / TEAMS;
             const bool first = w.kb % CHUNK_BLOCKS == 0;
+            // (no wait for the ring stage here: the team signals a_full only after
+            // it has seen the stage's bulk copies complete)
             if ((first && w.gchunk >= 1 && !tc::warp_wait(acc_empty, (w.gchunk - 1) & 1)) ||
-                !tc::warp_wait(full + 8 * s, (w.gkb / LST) & 1) || !tc::warp_wait(a_full + 8 * t, use & 1)) {
+                !tc::warp_wait(a_full + 8 * t, use & 1)) {
                 timed_out = true;
                 break;
             }
@@ -329,7 +330,6 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                     mma_f16_tmem_a_elect(tmem + (uint32_t)(d * p.nt), acol + (uint32_t)(kk * A_STAGE_COLS + 8 * d),
                                          bdesc, idesc, (first && kk == 0) ? 0u : 1u);
             }
-            tc::mma_commit_elect(a_empty + 8 * t);
             tc::mma_commit_elect(empty + 8 * s);
             if (walk_chunk_last_block(w))
                 tc::mma_commit_elect(acc_full);
@@ -395,9 +395,14 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
             }
             if (timed_out || !w.valid)
                 break;
+            // the team's A stage is free once its previous block (3 back) has been
+            // released by the MMAs: that block's ring-stage barrier completes only
+            // with the MMAs' commit, and its next phase cannot complete before this
+            // wait (it needs this block's MMAs first)
             const int s = w.gkb % LST, use = w.gkb / TEAMS;
-            if (!tc::warp_wait(full + 8 * s, (w.gkb / LST) & 1) ||
-                (use >= 1 && !tc::warp_wait(a_empty + 8 * t, (use - 1) & 1))) {
+            const int prev = w.gkb - TEAMS;
+            if ((use >= 1 && !tc::warp_wait(empty + 8 * (prev % LST), (prev / LST) & 1)) ||
+                !tc::warp_wait(full + 8 * s, (w.gkb / LST) & 1)) {
                 timed_out = true;
                 break;
             }
