@@ -132,6 +132,9 @@ def test_other_entry_points_reject(lib):
     assert lib.s3d8_linear_acc_i32(A16, A16B, A16C, 2, 5, 32, A16 + 2, None, 0, 0, None) == -2
     assert lib.s3d8_linear_ex(A16, A16B, A16C, A16, A16B, 2, 3, 32, A16C, None, 0, 7, None) == -1
     assert lib.s3d8_linear_ex(A16, A16B, A16C, A16, A16B, 2, 3, 32, A16C, None, 0, -1, None) == -1
+    assert lib.s3d8_linear_ex(A16, A16B, A16C, A16, A16B, 2, 3, 32, A16C, None, 0, 5, None) == -1
+    # the tensor-memory algorithm takes at most 64 tokens
+    assert lib.s3d8_linear_ex(A16, A16B, A16C, A16, A16B, 65, 3, 32, A16C, None, 0, 4, None) == -3
     enc = lib.s3d8_encode
     WS = 16384
     assert enc(A16, A16B, 6, 24, A16C, A16, A16B, WS, None) == -1            # K % 16
