@@ -454,14 +454,20 @@ def gpu_arm(args):
     print(json.dumps(line))
 
 
-def e2e_measure(torch, s3d8, copies, dev, steps, nbuf=3):
+def e2e_measure(torch, s3d8, copies, dev, steps, group=4, sets=3):
     """Same metric through the Python binding, with each step's four activations
     copied in from pinned host memory and its seven outputs copied back to
-    pinned host memory.  Inputs and outputs each live in one contiguous buffer,
-    in nbuf rotating sets; 64 steps are captured in one CUDA graph over three streams
-    (copies in, layer launches, copies out), so the copy-in of step i+1 and the
-    copy-out of step i-1 run while step i computes.  Every step's copies are
-    inside the timed region."""
+    pinned host memory (one copy each way per step).  64 steps are captured in
+    one CUDA graph over three streams (copies in, layer launches, copies out),
+    in groups of `group` steps with `sets` rotating buffer sets per group: the
+    layer stream waits for a group's copy-ins (issued while the previous group
+    computes) once per group, and the copy-outs follow each group, so
+    consecutive launches inside a group still overlap through programmatic
+    dependent launch (a stream wait or event record between two launches stops
+    that overlap).  The synthetic steps are independent, so a group's inputs may
+    be copied before the previous group ends.  Every step's copies are inside
+    the timed region."""
+    nbuf = group * sets
     xk = list(ACT_K.items())
     kx = sum(K for _, K in xk)
     no = sum(N for _, _, N in si.LLAMA_11B_LAYER)
@@ -495,29 +501,33 @@ def e2e_measure(torch, s3d8, copies, dev, steps, nbuf=3):
     ks.synchronize()
 
     per = GRAPH_ROUNDS * COPIES
-    ev_in = [torch.cuda.Event() for _ in range(per)]
-    ev_k = [torch.cuda.Event() for _ in range(per)]
-    ev_out = [torch.cuda.Event() for _ in range(per)]
+    ngroups = per // group
+    ev_in = [torch.cuda.Event() for _ in range(ngroups)]
+    ev_k = [torch.cuda.Event() for _ in range(ngroups)]
+    ev_out = [torch.cuda.Event() for _ in range(ngroups)]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=ks):
         cin.wait_stream(ks)
         cout.wait_stream(ks)
-        for i in range(per):
-            b = i % nbuf
+        for gi in range(ngroups):
+            bufs = [(gi % sets) * group + j for j in range(group)]
             with torch.cuda.stream(cin):
-                if i >= nbuf:
-                    cin.wait_event(ev_k[i - nbuf])      # step i-nbuf has read x_all[b]
-                x_all[b].copy_(host_x[b], non_blocking=True)
-                ev_in[i].record(cin)
-            ks.wait_event(ev_in[i])
-            if i >= nbuf:
-                ks.wait_event(ev_out[i - nbuf])         # o_all[b] of step i-nbuf is copied out
-            steps_b[b].run(s3d8, copies[i % COPIES], "group1")
-            ev_k[i].record(ks)
+                if gi >= sets:
+                    cin.wait_event(ev_k[gi - sets])     # the set's last group has read its inputs
+                for b in bufs:
+                    x_all[b].copy_(host_x[b], non_blocking=True)
+                ev_in[gi].record(cin)
+            ks.wait_event(ev_in[gi])
+            if gi >= sets:
+                ks.wait_event(ev_out[gi - sets])        # the set's last outputs are copied out
+            for j, b in enumerate(bufs):
+                steps_b[b].run(s3d8, copies[(gi * group + j) % COPIES], "group1")
+            ev_k[gi].record(ks)
             with torch.cuda.stream(cout):
-                cout.wait_event(ev_k[i])
-                host_out[b].copy_(o_all[b], non_blocking=True)
-                ev_out[i].record(cout)
+                cout.wait_event(ev_k[gi])
+                for b in bufs:
+                    host_out[b].copy_(o_all[b], non_blocking=True)
+                ev_out[gi].record(cout)
         ks.wait_stream(cin)
         ks.wait_stream(cout)
     h2d = host_x[0].numel() * 2
@@ -540,9 +550,9 @@ def e2e_measure(torch, s3d8, copies, dev, steps, nbuf=3):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
             "steps": reps * per,
             "path": "Python binding (grouped launch); per step one pinned host->device copy of "
-                    "the four activations and one device->host copy of the seven outputs, "
-                    "in rotating buffer sets on their own streams so that they overlap the neighbouring "
-                    "steps' launches; 64 steps per CUDA graph"}
+                    "the four activations and one device->host copy of the seven outputs, on their "
+                    f"own streams, synchronised with the layer stream once per group of {group} steps "
+                    "(launches inside a group overlap); 64 steps per CUDA graph"}
 
 
 def prefill_measure(torch, s3d8, dev, M=2048, reps=3):
