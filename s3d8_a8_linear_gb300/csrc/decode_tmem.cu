@@ -202,7 +202,9 @@ __device__ __forceinline__ void decode_step(uint32_t tile, int row, int kk, uint
     }
 }
 
-// int8 codes -> fp16 (exact), 16 per thread and iteration.
+// int8 codes -> fp16 (exact), 16 per thread and iteration, without int-to-float
+// conversions: with b = code ^ 0x80 = v + 128, one byte permute builds the fp16
+// pair 0x64bb (1024 + b) for two codes and one packed subtract of 1152 leaves v.
 __global__ void codes_to_f16_kernel(const int8_t *__restrict__ xq, __half *__restrict__ a, long n16)
 {
     tc::pdl_launch_dependents();   // the GEMM may set up meanwhile; it waits before reading a
@@ -211,16 +213,12 @@ __global__ void codes_to_f16_kernel(const int8_t *__restrict__ xq, __half *__res
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
         const uint4 v = __ldg(src + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
         uint32_t o[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int8_t b0 = (int8_t)(w[j] & 0xFF), b1 = (int8_t)((w[j] >> 8) & 0xFF);
-            const int8_t b2 = (int8_t)((w[j] >> 16) & 0xFF), b3 = (int8_t)(w[j] >> 24);
-            o[2 * j] = (uint32_t)__half_as_ushort(__short2half_rn(b0)) |
-                       ((uint32_t)__half_as_ushort(__short2half_rn(b1)) << 16);
-            o[2 * j + 1] = (uint32_t)__half_as_ushort(__short2half_rn(b2)) |
-                           ((uint32_t)__half_as_ushort(__short2half_rn(b3)) << 16);
+            o[2 * j] = hsub2(prmt(w[j], 0x64646464u, 0x5140u), 0x64806480u);
+            o[2 * j + 1] = hsub2(prmt(w[j], 0x64646464u, 0x7362u), 0x64806480u);
         }
         dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);

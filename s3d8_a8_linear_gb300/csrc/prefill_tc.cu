@@ -292,18 +292,25 @@ __global__ __launch_bounds__(THREADS, 1) void prefill_kernel(const __grid_consta
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
 }
 
-// int8 codes -> bf16 (exact), the tensor-core A operand.  Two 16-byte loads in
-// flight per thread and iteration.
+// int8 codes -> bf16 (exact), the tensor-core A operand, without int-to-float
+// conversions: with b = code ^ 0x80 = v + 128 (0..255), one byte permute builds
+// the float 0x4B4000bb = 1.5 * 2^23 + b, one FP32 add of -(1.5 * 2^23 + 128)
+// leaves v exactly, and its upper 16 bits are v's bf16 (|v| <= 128 needs 8
+// significant bits); one more permute packs two of them.
 __device__ __forceinline__ void codes16_to_bf16(uint4 v, uint4 *dst)
 {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+    constexpr uint32_t kMagic = 0x4B400000u;
+    constexpr float kOff = -12583040.0f;   // -(1.5 * 2^23 + 128)
     uint32_t o[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int b0 = (int8_t)(w[j] & 0xFF), b1 = (int8_t)((w[j] >> 8) & 0xFF);
-        const int b2 = (int8_t)((w[j] >> 16) & 0xFF), b3 = (int8_t)(w[j] >> 24);
-        o[2 * j] = bf16_bits_of(b0) | (bf16_bits_of(b1) << 16);
-        o[2 * j + 1] = bf16_bits_of(b2) | (bf16_bits_of(b3) << 16);
+        float f[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            f[i] = __fadd_rn(__uint_as_float(prmt(w[j], kMagic, 0x7650u | (uint32_t)i)), kOff);
+        o[2 * j] = prmt(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
+        o[2 * j + 1] = prmt(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
     }
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
