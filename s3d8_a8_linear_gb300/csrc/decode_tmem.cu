@@ -14,9 +14,10 @@
 //   warp 0      bulk tensor copies: per 64-column block, the packed tile
 //               (128 rows x 64 bytes, 64-byte swizzle) and the fp16 codes
 //               tile (N rows x 128 bytes, 128-byte swizzle) into an 8-stage ring;
-//   warp 1      allocates tensor memory and issues the MMAs (one elected lane):
-//               12 per block (4 steps of 16 columns x 3 channels), after one
-//               wait for the block's decoded weights;
+//   warps 1-3   issue the MMAs, warp 1 + d those of channel d (one elected
+//               lane each; warp 1 also allocates tensor memory): 4 per block
+//               and warp, after one wait for the block's decoded weights (one
+//               issuing warp for all 12 MMAs of a block was slower);
 //   warps 4-15  three decoder teams of four warps; warp w owns tensor-memory
 //               lanes 32 (w % 4) .. + 31, i.e. packed rows 32 (w % 4) + lane.
 //               Team t decodes the blocks t, t + 3, ...: each thread reads its
@@ -246,12 +247,12 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < LST; ++s) {
             mbar_init(full + 8 * s, 1);
-            mbar_init(empty + 8 * s, 4 + 1);   // the block's team, and the MMAs
+            mbar_init(empty + 8 * s, 4 + 3);   // the block's team, and the three MMA warps
         }
         for (int t = 0; t < TEAMS; ++t) {
             mbar_init(a_full + 8 * t, 4);
         }
-        mbar_init(acc_full, 1);
+        mbar_init(acc_full, 3);
         mbar_init(acc_empty, DEC_WARPS);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -304,8 +305,11 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
         for (int v = issued - LST < 0 ? 0 : issued - LST; v < issued; ++v)
             if (!tc::warp_wait(full + 8 * (v % LST), (v / LST) & 1))
                 timed_out = true;
-    } else if (warp == 1) {
-        // ---- MMA issuer: block b belongs to team b % 3 (whole warp, one elected lane)
+    } else if (warp >= 1 && warp <= 3) {
+        // ---- MMA issuers: warp 1 + d issues channel d's MMAs into D_d (whole
+        // warp, one elected lane); the three accumulators are independent, so the
+        // warps need no ordering among themselves.  Block b belongs to team b % 3.
+        const int d = warp - 1;
         const uint32_t idesc = (1u << 4) | ((uint32_t)(p.nt >> 3) << 17) | ((uint32_t)(ROWS >> 4) << 24);
         for (Walk w = walk_begin(p, nkb); w.valid; walk_next(p, nkb, w)) {
             const int s = w.gkb % LST, t = w.gkb % TEAMS, use = w.gkb / TEAMS;
@@ -321,13 +325,9 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
             const uint32_t acol = tmem + (uint32_t)(p.a_col + t * 4 * A_STAGE_COLS);
             const uint32_t act = base + (uint32_t)(s * STAGE + PK_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bdesc = tc::sw128_desc(act + kk * 32);
-#pragma unroll
-                for (int d = 0; d < 3; ++d)
-                    mma_f16_tmem_a_elect(tmem + (uint32_t)(d * p.nt), acol + (uint32_t)(kk * A_STAGE_COLS + 8 * d),
-                                         bdesc, idesc, (first && kk == 0) ? 0u : 1u);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+                mma_f16_tmem_a_elect(tmem + (uint32_t)(d * p.nt), acol + (uint32_t)(kk * A_STAGE_COLS + 8 * d),
+                                     tc::sw128_desc(act + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
             tc::mma_commit_elect(empty + 8 * s);
             if (walk_chunk_last_block(w))
                 tc::mma_commit_elect(acc_full);
