@@ -63,9 +63,10 @@ typedef enum {
     S3D8_ERR_WORKSPACE = -6    /* workspace missing or smaller than required      */
 } s3d8_status;
 
-/* Algorithm choice for s3d8_linear_ex.  AUTO picks by shape: GEMV up to 8
- * tokens; TMEM for 9..32 tokens, and up to 64 tokens while its tiles fit in one
- * wave on the device; TC otherwise.  SKINNY runs only on request. */
+/* Algorithm choice for s3d8_linear_ex.  AUTO picks by shape: GEMV up to 4
+ * tokens (up to 8 when K > 8192); TMEM for 5..32 tokens otherwise, and up to 64
+ * tokens while its tiles fit in one wave on the device; TC otherwise.  SKINNY
+ * runs only on request. */
 typedef enum {
     S3D8_ALGO_AUTO = 0,
     S3D8_ALGO_GEMV = 1,    /* CUDA-core table decode + dp4a; bulk-copy rings up to 8 tokens      */

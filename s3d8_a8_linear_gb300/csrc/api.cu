@@ -221,9 +221,9 @@ int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t
 }
 
 // The algorithm AUTO runs (measured on GB300 on the 11B layer's shapes): the
-// bulk-copy dp4a GEMV up to 8 tokens; the tcgen05 GEMM with the weights decoded
-// into tensor memory for 9..32 tokens, and up to 64 while its tiles fit in one
-// wave (with 48 or more tokens its K ranges are capped at 1024 columns, which on
+// bulk-copy dp4a GEMV up to 4 tokens, and up to 8 on rows longer than 8192
+// columns; the tcgen05 GEMM with the weights decoded into tensor memory for
+// 5..32 tokens otherwise, and up to 64 while its tiles fit in one wave (with 48 or more tokens its K ranges are capped at 1024 columns, which on
 // long rows makes more tiles than SMs); the tcgen05 GEMM on shared-memory tiles
 // otherwise.  (The register-fragment mma.sync path is slower than the tensor-
 // memory path at every size it takes and runs only on request.)
@@ -231,10 +231,10 @@ static int resolve_algo(int64_t M, int64_t N, int64_t K, int algo)
 {
     if (algo != S3D8_ALGO_AUTO)
         return algo;
-    if (M <= 8)
-        return S3D8_ALGO_GEMV;
     if (tmem_preferred((int)M, (int)N, (int)K))
         return S3D8_ALGO_TMEM;
+    if (M <= 8)
+        return S3D8_ALGO_GEMV;
     return S3D8_ALGO_TC;
 }
 

@@ -468,7 +468,9 @@ bool tmem_supported(int M)
 
 bool tmem_preferred(int M, int N, int K)
 {
-    if (M < 9 || M > wt::MAX_NT)
+    // 5..8 tokens run the 8-token GEMV, whose dp4a work per byte is then the
+    // largest; on rows of at most 8192 columns this path is faster there too
+    if (M < 5 || M > wt::MAX_NT || (M <= 8 && K > 8192))
         return false;
     if (M <= 32)
         return true;
