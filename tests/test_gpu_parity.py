@@ -251,6 +251,33 @@ def test_int32_extremes(K, algo):
     assert acc_o[0, 0] == 16129 * K and acc_o[0, 3] == -16129 * K
 
 
+@pytest.mark.parametrize("M", [3, 40])
+def test_tmem_int32_extremes_across_chunks(M):
+    """The tensor-memory path at the int32 edge with tiles of many 1024-column
+    chunks (100 row tiles leave one K range per tile: 14 chunk sums carried in
+    int32 up to 16129 * 14336 = 231,225,344; with 40 tokens the K ranges are
+    capped at one chunk and the CTAs walk several tiles).  Every weight is +-127
+    with one sign per packed row, so acc[m, 3g + d] = sign(g) * 127 * sum_k xq[m, k]
+    in closed form; a sample is also checked against the oracle."""
+    C = np.full((32, 3), 127, np.int8)
+    K, N = 14336, 3 * 128 * 100
+    G = si.groups(N)
+    packed = np.full((G, K), oracle.pack_byte(9, 0, 0, 0), np.uint8)
+    packed[1::7] ^= 0x41              # every 7th packed row: all three weights negative
+    xq = np.full((M, K), 127, np.int8)
+    xq[1] = -127
+    xq[2, ::2] = -127                 # alternating signs: row sum 0
+    sign = np.ones(G, np.int64)
+    sign[1::7] = -1
+    want = 127 * xq.astype(np.int64).sum(axis=1)[:, None] * np.repeat(sign, 3)[None, :N]
+    got = gpu_acc(C, packed, xq, N, s3d8.ALGO_TMEM)
+    np.testing.assert_array_equal(got, want)
+    assert want[0, 0] == 16129 * K and want[0, 3] == -16129 * K
+    rng = np.random.default_rng(M)
+    ms, ns = sample_positions(M, N, rng, count=200)
+    np.testing.assert_array_equal(got[ms, ns], oracle.linear_acc_at(packed, C, xq, N, ms, ns))
+
+
 @pytest.mark.parametrize("algo", ALGOS, ids=lambda a: ALGO_IDS[a])
 def test_zero_activation_row_gives_zero(algo):
     C, packed, cs, x = rand_case(3, 30, 64, seed=4)
