@@ -223,9 +223,8 @@ int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t
 // The algorithm AUTO runs (measured on GB300 on the 11B layer's shapes): the
 // bulk-copy dp4a GEMV up to 4 tokens, and up to 8 on rows longer than 8192
 // columns; the tcgen05 GEMM with the weights decoded into tensor memory for
-// 5..32 tokens otherwise, and up to 64 while its tiles fit in one wave (with 48 or more tokens its K ranges are capped at 1024 columns, which on
-// long rows makes more tiles than SMs); the tcgen05 GEMM on shared-memory tiles
-// otherwise.  (The register-fragment mma.sync path is slower than the tensor-
+// 5..32 tokens otherwise, and up to 64 while its 128-row tiles fit in one wave;
+// the tcgen05 GEMM on shared-memory tiles otherwise.  (The register-fragment mma.sync path is slower than the tensor-
 // memory path at every size it takes and runs only on request.)
 static int resolve_algo(int64_t M, int64_t N, int64_t K, int algo)
 {

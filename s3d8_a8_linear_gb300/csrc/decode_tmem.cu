@@ -27,15 +27,17 @@
 //               value 1024 + xx) and one packed subtract of 1152; tcgen05.st
 //               writes them into the team's A stage.  Every team drains its own
 //               channel d = t of every 1024-column chunk: it adds the fp32 sums
-//               into int32 sums in tensor memory, and at the end of the tile
-//               writes them as int32 partials [split][M][N].
+//               into int32 sums (in tensor memory, or with 48..64 tokens in
+//               shared memory beside a 4-stage ring, where tensor memory has no
+//               room for them), and at the end of the tile writes them as int32
+//               partials [split][M][N].
 // The partials of the K splits are summed, and the epilogue applied, by the
 // split-K finish kernel.  Handing the MMA warp whole blocks matters: with one
 // handoff per 16-column step the issuing warp, sharing its scheduler with
 // three decoder warps, spent ~830 cycles per step on bookkeeping and waits.
 //
 // Tensor memory (512 columns): D_d at columns d * NT; int32 sums at 3 NT + d * NT
-// when a tile spans more than one chunk; then team t's A stage, 96 columns, at
+// when a tile spans more than one chunk and they fit; then team t's A stage, 96 columns, at
 // a_col + 96 t (step kk, channel d at + 24 kk + 8 d; 8 columns = 16 fp16 values,
 // row r in lane r, column c holding elements 2c (low half) and 2c + 1).
 #include <cuda_fp16.h>
@@ -52,13 +54,11 @@ constexpr int PK_BYTES = ROWS * BK;              // 8 KiB packed tile
 constexpr int MAX_NT = 64;                       // tokens per MMA (N), a multiple of 16
 constexpr int ACT_BYTES = MAX_NT * BK * 2;       // 8 KiB fp16 codes tile
 constexpr int STAGE = PK_BYTES + ACT_BYTES;
-constexpr int LST = 8;                           // ring stages
+constexpr int MAX_LST = 8;                       // ring stages (4 when the chunk sums live in shared memory)
 constexpr int LUT_BYTES = kLutEntries * 32 * 4;  // 32 KiB, one copy per lane
-constexpr int OFF_LUT = LST * STAGE;
-constexpr int OFF_BARS = OFF_LUT + LUT_BYTES;
+
 constexpr int TEAMS = 3;
-constexpr int NBARS = 2 * LST + TEAMS + 2;
-constexpr int SMEM_BYTES = 1024 + OFF_BARS + NBARS * 8 + 16;
+constexpr int NBARS = 2 * MAX_LST + TEAMS + 2;
 constexpr int THREADS = 512;
 constexpr int DEC_WARP0 = 4;
 constexpr int DEC_WARPS = TEAMS * 4;
@@ -66,7 +66,7 @@ constexpr int CHUNK_BLOCKS = 16;                 // 1024 columns per exact fp32 
 constexpr int A_STAGE_COLS = 24;                 // 3 channels x 8 columns
 
 static_assert(STAGE % 1024 == 0 && PK_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
-static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory budget");
+
 static_assert(3 * MAX_NT + TEAMS * 4 * A_STAGE_COLS <= 512, "tensor memory");
 
 struct Params {
@@ -77,6 +77,7 @@ struct Params {
     int kbps;
     int s_col;     // int32 sums at s_col + d * nt (tiles of more than one chunk)
     int a_col;     // team t's A stage (one 64-column block) at a_col + 96 t
+    int s_smem;    // chunk sums in shared memory (48..64 tokens, tiles of several chunks)
     const int8_t *C;
     int32_t *part; // [nsplit][M][N]
     int *status;
@@ -226,6 +227,9 @@ __global__ void codes_to_f16_kernel(const int8_t *__restrict__ xq, __half *__res
     }
 }
 
+// LST: ring stages (8, or 4 when the chunk sums live in shared memory); a
+// compile-time constant so that stage indices cost no division.
+template <int LST>
 __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constant__ CUtensorMap tm_act,
                                                             const __grid_constant__ CUtensorMap tm_pk, Params p)
 {
@@ -233,13 +237,19 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *smem = smem_raw + (base - raw);
-    const uint32_t lut = base + OFF_LUT;
-    const uint32_t bars = base + OFF_BARS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BARS + NBARS * 8);
+    // shared memory: ring, int32 chunk sums (s_smem only), table, barriers
+    constexpr bool SSUM = LST != MAX_LST;   // the 4-stage form keeps the chunk sums in shared memory
+    const int off_s = LST * STAGE;
+    const int off_lut = off_s + (SSUM ? 3 * p.nt * ROWS * 4 : 0);
+    const int off_bars = off_lut + LUT_BYTES;
+    const uint32_t lut = base + (uint32_t)off_lut;
+    const uint32_t bars = base + (uint32_t)off_bars;
+    int32_t *ssum = reinterpret_cast<int32_t *>(smem + off_s);   // [channel][token][row]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + off_bars + NBARS * 8);
     // full/empty: the ring's stages; a_full: each team's A stage is written;
     // acc_full: a chunk's sums are in D; acc_empty: D has been drained
-    const uint32_t full = bars, empty = full + 8 * LST;
-    const uint32_t a_full = empty + 8 * LST;
+    const uint32_t full = bars, empty = full + 8 * MAX_LST;
+    const uint32_t a_full = empty + 8 * MAX_LST;
     const uint32_t acc_full = a_full + 8 * TEAMS, acc_empty = acc_full + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nkb = (p.K + BK - 1) / BK;
@@ -361,9 +371,17 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                     float v[8];
                     uint32_t s8[8];
                     tc::tmem_ld8(tmem + lane_off + (uint32_t)(t * p.nt + cb * 8), v);
-                    if (!first_chunk)
+                    if (!first_chunk && !SSUM)
                         tmem_ld8u(tmem + lane_off + (uint32_t)(p.s_col + t * p.nt + cb * 8), s8);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    // sums in shared memory: entry (channel t, token, row), so a
+                    // warp's 32 rows are 32 consecutive words
+                    int32_t *srow = ssum + ((size_t)t * p.nt + cb * 8) * ROWS + row;
+                    if (!first_chunk && SSUM) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            s8[e] = (uint32_t)srow[e * ROWS];
+                    }
                     uint32_t sum[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
@@ -378,11 +396,15 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                                     p.part[((size_t)cw.split * p.M + tok) * p.N + n] = (int32_t)sum[e];
                             }
                         }
+                    } else if (SSUM) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            srow[e * ROWS] = (int32_t)sum[e];
                     } else {
                         tmem_st8(tmem + lane_off + (uint32_t)(p.s_col + t * p.nt + cb * 8), sum);
                     }
                 }
-                if (!last_chunk)
+                if (!last_chunk && !SSUM)
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc::tc_fence_before();
                 __syncwarp();
@@ -441,9 +463,7 @@ static size_t wt_align(size_t v)
 }
 
 // 128-row tiles, and K split into ranges so that row tiles x ranges fills the
-// SMs without a second wave.  Tiles of more than one 1024-column chunk keep
-// int32 sums in tensor memory next to D: with 48 or 64 tokens there is no room
-// for them beside the three A stages, so K ranges are then capped at one chunk.
+// SMs without a second wave.
 static void wt_plan(int M, int N, int K, int sms, int &rtiles, int &nsplit, int &kbps)
 {
     const int G = (N + 2) / 3;
@@ -455,9 +475,6 @@ static void wt_plan(int M, int N, int K, int sms, int &rtiles, int &nsplit, int 
     if (s > nkb)
         s = nkb;
     kbps = (nkb + s - 1) / s;
-    const int nt = (M + 15) / 16 * 16;
-    if (6 * nt + wt::TEAMS * 4 * wt::A_STAGE_COLS > 512 && kbps > wt::CHUNK_BLOCKS)
-        kbps = wt::CHUNK_BLOCKS;
     nsplit = (nkb + kbps - 1) / kbps;
 }
 
@@ -477,7 +494,7 @@ bool tmem_preferred(int M, int N, int K)
     const int sms = device_sm_count();
     int rtiles, nsplit, kbps;
     wt_plan(M, N, K, sms, rtiles, nsplit, kbps);
-    return (long)rtiles * nsplit <= sms;   // one wave of tiles
+    return (long)rtiles * nsplit <= sms;   // one wave of tiles (all but the widest matrices)
 }
 
 size_t tmem_workspace_bytes(int M, int N, int K)
@@ -529,9 +546,9 @@ cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream)
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(tmem_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess)
-        return e;
+    static_assert(1024 + MAX_LST * STAGE + LUT_BYTES + NBARS * 8 + 16 <= 232448 - 1024, "shared memory");
+    static_assert(1024 + 4 * STAGE + 3 * MAX_NT * ROWS * 4 + LUT_BYTES + NBARS * 8 + 16 <= 232448 - 1024,
+                  "shared memory");
     Params p;
     p.M = a.M;
     p.N = a.N;
@@ -541,10 +558,13 @@ cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream)
     p.rtiles = rtiles;
     p.nsplit = nsplit;
     p.kbps = kbps;
-    // tensor memory: D, then the int32 sums if a tile spans several chunks, then
-    // the three teams' A stages
+    // tensor memory: D, then the int32 chunk sums if a tile spans several chunks
+    // and they fit beside the three teams' A stages, then the A stages; with 48
+    // or 64 tokens the sums go to shared memory instead, next to a 4-stage ring
+    const bool multi = kbps > CHUNK_BLOCKS;
+    p.s_smem = multi && 6 * nt + TEAMS * 4 * A_STAGE_COLS > 512;
     p.s_col = 3 * nt;
-    p.a_col = kbps > CHUNK_BLOCKS ? 6 * nt : 3 * nt;
+    p.a_col = multi && !p.s_smem ? 6 * nt : 3 * nt;
     if (p.a_col + TEAMS * 4 * A_STAGE_COLS > 512)
         return cudaErrorInvalidValue;
     p.C = a.C;
@@ -552,8 +572,13 @@ cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream)
     p.status = a.status;
     const long tiles = (long)rtiles * nsplit;
     const long ctas = tiles < sms ? tiles : sms;   // persistent CTAs walk the tiles
-    e = tc::launch_pdl(tmem_a_kernel, dim3((unsigned)ctas), dim3(THREADS), (size_t)SMEM_BYTES, stream, tm_act,
-                       tm_pk, p);
+    const int lst = p.s_smem ? 4 : MAX_LST;
+    const int need = 1024 + lst * STAGE + (p.s_smem ? 3 * nt * ROWS * 4 : 0) + LUT_BYTES + NBARS * 8 + 16;
+    auto kernel = p.s_smem ? tmem_a_kernel<4> : tmem_a_kernel<MAX_LST>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+    if (e != cudaSuccess)
+        return e;
+    e = tc::launch_pdl(kernel, dim3((unsigned)ctas), dim3(THREADS), (size_t)need, stream, tm_act, tm_pk, p);
     if (e != cudaSuccess)
         return e;
     return launch_splitk_finalize(part, nsplit, a, stream);

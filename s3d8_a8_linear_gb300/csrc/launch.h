@@ -90,7 +90,7 @@ cudaError_t launch_skinny(const LinearArgs &a, cudaStream_t stream);
 // 1..64 tokens.
 bool tmem_supported(int M);
 // AUTO takes it for 9..32 tokens (5..8 too on rows of at most 8192 columns), and
-// up to 64 when its tiles fit in one wave.
+// up to 64 when its tiles fit in one wave (not with more 128-row tiles than SMs).
 bool tmem_preferred(int M, int N, int K);
 size_t tmem_workspace_bytes(int M, int N, int K);
 cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream);

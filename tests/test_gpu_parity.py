@@ -346,7 +346,8 @@ def test_skinny_rejects_more_than_32_tokens():
 # tiles), more tiles than SMs (a second tile per CTA), K ragged against the
 # 64-column block, and 1..64 tokens (N of the MMA 16..64).
 TMEM_CASES = [(1, 4, 16), (5, 241, 1040), (16, 722, 2112), (17, 1201, 3088), (33, 96, 256),
-              (64, 480, 14336), (8, 38401, 4096), (64, 61441, 256), (48, 3000, 1104)]
+              (64, 480, 14336), (8, 38401, 4096), (64, 61441, 256), (48, 3000, 1104),
+              (64, 29569, 1088)]   # 231 row tiles, 17-block tiles: chunk sums in shared memory
 
 
 @pytest.mark.parametrize("M,N,K", TMEM_CASES)
