@@ -266,6 +266,19 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
         mbar_init(acc_empty, DEC_WARPS);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // The copy warp starts the first stages' packed tiles at once, while the
+    // table is built: packed weights are never outputs of the kernel before
+    // this one (the codes tiles follow after the grid dependency).
+    const uint32_t tx = (uint32_t)PK_BYTES + (uint32_t)p.nt * BK * 2;
+    int pre = 0;
+    if (warp == 0) {
+        __syncwarp();   // lane 0's barrier initialisation
+        for (Walk w = walk_begin(p, nkb); w.valid && pre < LST; walk_next(p, nkb, w), ++pre) {
+            const uint32_t st = base + (uint32_t)(pre * STAGE);
+            tc::mbar_arrive_expect_tx_elect(full + 8 * pre, tx);
+            tc::tma_2d_elect(st, &tm_pk, (w.kbase + w.kb) * BK, w.rt * ROWS, full + 8 * pre);
+        }
+    }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
                          smem_addr(tmem_slot))
@@ -297,7 +310,6 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     if (warp == 0) {
         // ---- bulk tensor copies: packed tile + fp16 codes tile per 64-column block
         tc::pdl_wait();   // the fp16 codes are written by the kernel before this one
-        const uint32_t tx = (uint32_t)PK_BYTES + (uint32_t)p.nt * BK * 2;
         int issued = 0;
         for (Walk w = walk_begin(p, nkb); w.valid; walk_next(p, nkb, w), ++issued) {
             const int s = w.gkb % LST;
@@ -307,12 +319,15 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
             }
             const uint32_t st = base + (uint32_t)(s * STAGE);
             const int x = (w.kbase + w.kb) * BK;
-            tc::mbar_arrive_expect_tx_elect(full + 8 * s, tx);
-            tc::tma_2d_elect(st, &tm_pk, x, w.rt * ROWS, full + 8 * s);
+            if (w.gkb >= pre) {
+                tc::mbar_arrive_expect_tx_elect(full + 8 * s, tx);
+                tc::tma_2d_elect(st, &tm_pk, x, w.rt * ROWS, full + 8 * s);
+            }
             tc::tma_2d_elect(st + PK_BYTES, &tm_act, x, 0, full + 8 * s);
         }
         // never leave with copies in flight (only possible after a timeout)
-        for (int v = issued - LST < 0 ? 0 : issued - LST; v < issued; ++v)
+        const int hi = issued > pre ? issued : pre;
+        for (int v = hi - LST < 0 ? 0 : hi - LST; v < hi; ++v)
             if (!tc::warp_wait(full + 8 * (v % LST), (v / LST) & 1))
                 timed_out = true;
     } else if (warp >= 1 && warp <= 3) {
