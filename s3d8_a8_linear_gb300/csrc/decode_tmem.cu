@@ -204,6 +204,18 @@ __device__ __forceinline__ void decode_step(uint32_t tile, int row, int kk, uint
     }
 }
 
+// 2-D bulk tensor copy with an L2 cache policy (whole warp; one elected lane).
+__device__ __forceinline__ void tma_2d_hint_elect(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
+                                                  uint64_t policy)
+{
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+        "[%1, {%2, %3}], [%4], %5;\n}\n" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // int8 codes -> fp16 (exact), 16 per thread and iteration, without int-to-float
 // conversions: with b = code ^ 0x80 = v + 128, one byte permute builds the fp16
 // pair 0x64bb (1024 + b) for two codes and one packed subtract of 1152 leaves v.
@@ -271,12 +283,15 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     // this one (the codes tiles follow after the grid dependency).
     const uint32_t tx = (uint32_t)PK_BYTES + (uint32_t)p.nt * BK * 2;
     int pre = 0;
+    // packed bytes are read once: evict them first, keeping the codes tiles
+    // (read by every row tile of a K range) in L2
+    const uint64_t wpol = l2_evict_first_policy();
     if (warp == 0) {
         __syncwarp();   // lane 0's barrier initialisation
         for (Walk w = walk_begin(p, nkb); w.valid && pre < LST; walk_next(p, nkb, w), ++pre) {
             const uint32_t st = base + (uint32_t)(pre * STAGE);
             tc::mbar_arrive_expect_tx_elect(full + 8 * pre, tx);
-            tc::tma_2d_elect(st, &tm_pk, (w.kbase + w.kb) * BK, w.rt * ROWS, full + 8 * pre);
+            tma_2d_hint_elect(st, &tm_pk, (w.kbase + w.kb) * BK, w.rt * ROWS, full + 8 * pre, wpol);
         }
     }
     if (warp == 1) {
@@ -321,7 +336,7 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
             const int x = (w.kbase + w.kb) * BK;
             if (w.gkb >= pre) {
                 tc::mbar_arrive_expect_tx_elect(full + 8 * s, tx);
-                tc::tma_2d_elect(st, &tm_pk, x, w.rt * ROWS, full + 8 * s);
+                tma_2d_hint_elect(st, &tm_pk, x, w.rt * ROWS, full + 8 * s, wpol);
             }
             tc::tma_2d_elect(st + PK_BYTES, &tm_act, x, 0, full + 8 * s);
         }
