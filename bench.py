@@ -418,11 +418,12 @@ def gpu_arm(args):
         roofline["isolated_launch_us"] = round(iso_ms * 1e3, 3)
         roofline["isolated_achieved"] = round(step_bytes / (iso_ms * 1e-3) / 1e9, 1)
 
-    e2e = prefill = unpack = sweep = stack = encode = fit = None
+    e2e = prefill = unpack = quant = sweep = stack = encode = fit = None
     if not args.layer_only:
         e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 4000))
         prefill = prefill_measure(torch, s3d8, dev) if not args.skip_prefill else None
         unpack = unpack_measure(torch, s3d8, dev)
+        quant = quant_measure(torch, s3d8, dev)
         sweep = decode_sweep_measure(torch, s3d8, dev)
         stack = stack_measure(torch, s3d8, dev)
         encode = encode_measure(torch, s3d8, dev)
@@ -449,7 +450,7 @@ def gpu_arm(args):
         "device_status": status,
         "roofline": roofline, "variants": variants, "e2e": e2e, "prefill": prefill,
         "decode_sweep": sweep, "text_stack": stack, "spread": spread,
-        "unpack": unpack, "encode": encode, "fit": fit, "clocks": clocks, "cpu_baseline": cpu,
+        "unpack": unpack, "quantize": quant, "encode": encode, "fit": fit, "clocks": clocks, "cpu_baseline": cpu,
     }
     print(json.dumps(line))
 
@@ -753,6 +754,34 @@ def unpack_measure(torch, s3d8, dev, reps=20):
             "total_gbs": round((rd + N * K) / (ms * 1e-3) / 1e9, 1)}
 
 
+def quant_measure(torch, s3d8, dev, M=2048, K=14336, copies=4, reps=20):
+    """Standalone per-token activation quantisation at the prefill size of the
+    down projection's input (bf16 [2048, 14336], 58.7 MB in), rotating over
+    four input copies (235 MB, above L2).  Algorithmic bytes: 2MK read, MK + 4M
+    written."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    xs = [torch.randn((M, K), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+          for _ in range(copies)]
+    xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+    xscale = torch.empty((M,), dtype=torch.float32, device=dev)
+    for i in range(copies):
+        s3d8.quantize_act(xs[i], xq, xscale)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(reps):
+        s3d8.quantize_act(xs[i % copies], xq, xscale)
+    t1.record()
+    t1.synchronize()
+    ms = t0.elapsed_time(t1) / reps
+    nbytes = 2 * M * K + M * K + 4 * M
+    del xs
+    return {"shape": f"bf16 [{M}, {K}]", "us": round(ms * 1e3, 2),
+            "algorithmic_bytes": nbytes, "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+
+
 def encode_measure(torch, s3d8, dev, reps=3):
     """Direct-cast encoder over the seven matrices of one 11B decoder layer
     (218 M bf16 weights, 436 MB, larger than L2), weights N(0, 0.02) drawn on
@@ -971,6 +1000,9 @@ def main():
                     help="run only the M = 2048 tensor-core measurement and print it; for profiling")
     ap.add_argument("--sweep-only", action="store_true",
                     help="run only the batched-decode sweep (M = 8..64) and print it; for profiling")
+    ap.add_argument("--aux-only", action="store_true",
+                    help="run only the standalone unpack and quantisation measurements and print "
+                         "them; for profiling")
     ap.add_argument("--encode-only", action="store_true",
                     help="run only the encoder and centroid-fit measurements and print them; "
                          "for profiling")
@@ -993,6 +1025,15 @@ def main():
         import s3d8_a8_linear_gb300 as s3d8
         s3d8.load(build_if_missing=True)
         print(json.dumps(decode_sweep_measure(torch, s3d8, torch.device("cuda:0"))))
+        return
+    if args.aux_only:
+        import torch
+
+        import s3d8_a8_linear_gb300 as s3d8
+        s3d8.load(build_if_missing=True)
+        dev = torch.device("cuda:0")
+        print(json.dumps({"unpack": unpack_measure(torch, s3d8, dev),
+                          "quantize": quant_measure(torch, s3d8, dev)}))
         return
     if args.encode_only:
         import torch

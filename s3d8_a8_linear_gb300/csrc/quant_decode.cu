@@ -5,8 +5,9 @@
 namespace s3d8 {
 
 // ---------------------------------------------------------------------------
-// Per-token absmax INT8 quantisation.  One CTA per row (grid-stride over rows),
-// 16-byte vector loads, two passes over the row (the second hits L1/L2).
+// Per-token absmax INT8 quantisation.  Rows of more than 16384 columns: one CTA
+// per row (grid-stride over rows), 16-byte vector loads, two passes over the row
+// (the second hits L1/L2).  Shorter rows: quantize_act_rows_kernel below.
 // xscale = absmax / 127 with IEEE division; q = rint(x / xscale), ties to even,
 // clamped to +-127 (quant_code: one multiply by RN(1/xscale), exact division
 // only near ties); a zero row gives scale 0 and codes 0.
@@ -55,11 +56,75 @@ __global__ __launch_bounds__(kQuantThreads) void quantize_act_kernel(
     }
 }
 
+// Rows of at most NS * kQuantThreads 16-byte chunks (K <= 2048 NS): one CTA per
+// row, the whole row held in registers.  Every load of a thread leaves before
+// the first is used, so a row costs one memory latency, and the block scheduler
+// deals rows to SMs as they free up (no grid-stride tail).  Same arithmetic as
+// quantize_act_kernel.
+template <int NS>
+__global__ __launch_bounds__(kQuantThreads) void quantize_act_rows_kernel(
+    const __nv_bfloat16 *__restrict__ x, int K, int8_t *__restrict__ xq, float *__restrict__ xscale)
+{
+    __shared__ float red[kQuantThreads / 32];
+    const int chunks = K / 8;
+    const size_t m = blockIdx.x;
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + m * K);
+    uint4 v[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        const int c = threadIdx.x + i * kQuantThreads;
+        v[i] = c < chunks ? ldg_stream_v4(row + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
+            amax = fmaxf(amax, fabsf(__low2float(h)));
+            amax = fmaxf(amax, fabsf(__high2float(h)));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < kQuantThreads / 32; ++i)
+        amax = fmaxf(amax, red[i]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    const float r = s > 0.0f ? __frcp_rn(s) : 0.0f;
+    if (threadIdx.x == 0)
+        xscale[m] = s;
+    uint2 *qrow = reinterpret_cast<uint2 *>(xq + m * K);
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        const int c = threadIdx.x + i * kQuantThreads;
+        if (c < chunks)
+            qrow[c] = quant_chunk8(v[i], s, r);
+    }
+}
+
 cudaError_t launch_quantize_act(const __nv_bfloat16 *x, int M, int K, int8_t *xq, float *xscale,
                                 cudaStream_t stream)
 {
-    const int grid = M < device_sm_count() * 8 ? M : device_sm_count() * 8;
-    quantize_act_kernel<<<grid, kQuantThreads, 0, stream>>>(x, M, K, xq, xscale);
+    const int chunks = K / 8;
+    if (chunks <= kQuantThreads)
+        quantize_act_rows_kernel<1><<<M, kQuantThreads, 0, stream>>>(x, K, xq, xscale);
+    else if (chunks <= 2 * kQuantThreads)
+        quantize_act_rows_kernel<2><<<M, kQuantThreads, 0, stream>>>(x, K, xq, xscale);
+    else if (chunks <= 4 * kQuantThreads)
+        quantize_act_rows_kernel<4><<<M, kQuantThreads, 0, stream>>>(x, K, xq, xscale);
+    else if (chunks <= 8 * kQuantThreads)
+        quantize_act_rows_kernel<8><<<M, kQuantThreads, 0, stream>>>(x, K, xq, xscale);
+    else {
+        const int grid = M < device_sm_count() * 8 ? M : device_sm_count() * 8;
+        quantize_act_kernel<<<grid, kQuantThreads, 0, stream>>>(x, M, K, xq, xscale);
+    }
     return cudaGetLastError();
 }
 

@@ -56,7 +56,13 @@ def gpu_acc(C, packed, xq, N, algo):
 
 @pytest.mark.parametrize("M,K,outliers", [(4, 256, False), (1, 16, False), (3, 48, False),
                                           (1, 4096, False), (1, 14336, False), (7, 1040, True),
-                                          (64, 14336, True), (2048, 14336, False)])
+                                          (64, 14336, True), (2048, 14336, False),
+                                          # both sides of each row-width class of the
+                                          # standalone kernel (2048 / 4096 / 8192 / 16384
+                                          # columns held in registers, longer rows two-pass)
+                                          (2, 2048, False), (3, 2064, True), (2, 8192, True),
+                                          (3, 8208, False), (3, 16384, True), (2, 16400, True),
+                                          (2, 40960, False)])
 def test_quantize_act_bitexact(M, K, outliers):
     rng = np.random.default_rng(M * 7 + K)
     x = si.activations(rng, M, K, outliers)
