@@ -149,6 +149,32 @@ __device__ __forceinline__ int quant_code(float x, float s, float r)
     return max(-127, min(127, __float2int_rn(t)));
 }
 
+// Per-lane unsigned 16-bit maximum of two packed pairs.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Absolute maximum of the eight bf16 values of a 16-byte chunk, folded into m
+// (two 16-bit lanes of bf16 bit patterns, start from 0).  With the sign bits
+// cleared, the bit patterns of finite bf16 values order like their magnitudes,
+// so a per-lane unsigned maximum is exact and needs no conversion to fp32.
+__device__ __forceinline__ uint32_t absmax_bf16x8(uint4 v, uint32_t m)
+{
+    m = max_u16x2(m, v.x & 0x7FFF7FFFu);
+    m = max_u16x2(m, v.y & 0x7FFF7FFFu);
+    m = max_u16x2(m, v.z & 0x7FFF7FFFu);
+    return max_u16x2(m, v.w & 0x7FFF7FFFu);
+}
+
+// The fp32 value of the larger of m's two lanes.
+__device__ __forceinline__ float absmax_bf16x2_value(uint32_t m)
+{
+    return __uint_as_float(max(m >> 16, m & 0xFFFFu) << 16);
+}
+
 // Eight bf16 values (one 16-byte chunk) -> eight codes (8 bytes), for values of
 // a row whose absmax a gives s = RN(a / 127).  The common path is branch-free
 // over the eight values and uses only full-rate FP32 multiplies and adds:
@@ -159,6 +185,9 @@ __device__ __forceinline__ int quant_code(float x, float s, float r)
 // in fp32, flags the rare near-ties, which are redone with the exact quotient
 // afterwards (quant_code, which clamps).
 constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
+// |t - rint(t)| <= 0.5, so t lies within kTieMargin of a half-integer exactly
+// when |t - rint(t)| > 0.5 - kTieMargin: one compare per value.
+constexpr float kTieFloor = 0.5f - kTieMargin;
 
 #ifdef S3D8_QUANT_NOINLINE
 static __device__ __noinline__
@@ -183,7 +212,7 @@ uint2 quant_chunk8(uint4 v, float s, float r)
         const float t = __fmul_rn(x[e], r);
         const float y = __fadd_rn(t, kRoundMagic);
         const float d = __fsub_rn(t, __fsub_rn(y, kRoundMagic));   // t - rint(t)
-        redo |= fabsf(fabsf(d) - 0.5f) < kTieMargin;
+        redo |= fabsf(d) > kTieFloor;
         b[e] = __float_as_uint(y);
     }
     if (redo) {

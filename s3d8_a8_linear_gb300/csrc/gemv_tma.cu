@@ -165,13 +165,7 @@ __device__ __forceinline__ void act_amax_partial(const ActRegs<NS> &r, int M, in
         const int c = threadIdx.x + i * kTmaThreads;
         if (c < chunks) {
             const int m = chunk_token<MT>(c, per_row);
-            const uint32_t w[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
-            float a = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
-                a = fmaxf(a, fmaxf(fabsf(__low2float(h)), fabsf(__high2float(h))));
-            }
+            const float a = absmax_bf16x2_value(absmax_bf16x8(r.v[i], 0u));
 #pragma unroll
             for (int mm = 0; mm < MT; ++mm)
                 if (mm == m)

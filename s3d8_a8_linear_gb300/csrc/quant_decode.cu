@@ -22,17 +22,10 @@ __global__ __launch_bounds__(kQuantThreads) void quantize_act_kernel(
     const int chunks = K / 8;  // 8 bf16 per 16 bytes; K % 16 == 0
     for (int m = blockIdx.x; m < M; m += gridDim.x) {
         const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
-        float amax = 0.0f;
-        for (int c = threadIdx.x; c < chunks; c += kQuantThreads) {
-            const uint4 v = __ldg(row + c);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
-                amax = fmaxf(amax, fabsf(__low2float(h)));
-                amax = fmaxf(amax, fabsf(__high2float(h)));
-            }
-        }
+        uint32_t m2 = 0u;
+        for (int c = threadIdx.x; c < chunks; c += kQuantThreads)
+            m2 = absmax_bf16x8(__ldg(row + c), m2);
+        float amax = absmax_bf16x2_value(m2);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -75,17 +68,11 @@ __global__ __launch_bounds__(kQuantThreads) void quantize_act_rows_kernel(
         const int c = threadIdx.x + i * kQuantThreads;
         v[i] = c < chunks ? ldg_stream_v4(row + c) : make_uint4(0u, 0u, 0u, 0u);
     }
-    float amax = 0.0f;
+    uint32_t m2 = 0u;
 #pragma unroll
-    for (int i = 0; i < NS; ++i) {
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
-            amax = fmaxf(amax, fabsf(__low2float(h)));
-            amax = fmaxf(amax, fabsf(__high2float(h)));
-        }
-    }
+    for (int i = 0; i < NS; ++i)
+        m2 = absmax_bf16x8(v[i], m2);
+    float amax = absmax_bf16x2_value(m2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
