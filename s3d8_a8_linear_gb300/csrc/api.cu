@@ -6,40 +6,46 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 namespace s3d8 {
 
 __device__ int g_device_status;  // sticky S3D8_ERR_TIMEOUT set by bounded waits
 
 static constexpr int kMaxDevices = 64;
 
+// Both caches below are filled on first use per device; threads that race on
+// the first call store the same value, and the atomics make that well defined.
 int device_sm_count()
 {
-    static int cached[kMaxDevices] = {0};
+    static std::atomic<int> cached[kMaxDevices];   // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 148;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 int *device_status_ptr()
 {
-    static int *cached[kMaxDevices] = {nullptr};
+    static std::atomic<int *> cached[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return nullptr;
-    if (!cached[dev]) {
+    int *ptr = cached[dev].load(std::memory_order_relaxed);
+    if (!ptr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess)
             return nullptr;
-        cached[dev] = static_cast<int *>(p);
+        ptr = static_cast<int *>(p);
+        cached[dev].store(ptr, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return ptr;
 }
 
 }  // namespace s3d8

@@ -27,6 +27,8 @@
 // one chunk while the other drains.  Every mbarrier wait is bounded.
 #include "tcgen05.cuh"
 
+#include <atomic>
+
 namespace s3d8 {
 
 namespace tc {
@@ -523,19 +525,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder_fn());
 }
 
-// The driver's cuTensorMapEncodeTiled, looked up once through the runtime.
+// The driver's cuTensorMapEncodeTiled, looked up through the runtime until a
+// lookup succeeds, then cached (racing threads store the same pointer).
 void *tensor_map_encoder_fn()
 {
-    static void *fn = nullptr;
-    if (!fn) {
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load(std::memory_order_relaxed);
+    if (!f) {
         cudaDriverEntryPointQueryResult q;
-        void *f = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = f;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f, std::memory_order_relaxed);
     }
-    return fn;
+    return f;
 }
 
 cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream)
