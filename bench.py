@@ -50,7 +50,10 @@ import s3d8_inputs as si  # noqa: E402
 METRIC = "S3D8 linear weight GB/s (M=1) & INT8 TOPS (prefill), % of roofline"
 UNIT = "GB/s"
 COPIES = 8
-GRAPH_ROUNDS = 8
+# Longest run of headline steps captured in one CUDA graph: a timed region of at
+# most this many steps is exactly one graph replay; longer regions replay it and
+# then a graph holding the remainder.
+MAX_GRAPH_STEPS = 512
 WORKLOAD = ("Llama-3.2-11B text decoder layer, decode M=1: S3D8 linears q 4096->4096, "
             "k/v 4096->1024, o 4096->4096, gate/up 4096->14336, down 14336->4096")
 
@@ -67,6 +70,12 @@ def linear_bytes(M, K, N):
 
 LAYER_WEIGHT_BYTES = sum(weight_bytes(K, N) for _, K, N in si.LLAMA_11B_LAYER)
 ACT_K = {"attn": 4096, "o": 4096, "mlp": 4096, "down": 14336}
+# The workload both arms print, word for word: step i streams layer copy i mod 8.
+CONFIG = {"workload": WORKLOAD, "M": 1, "weight_bytes_per_step": LAYER_WEIGHT_BYTES,
+          "weight_copies": COPIES,
+          "l2": f"inputs larger than L2: step i streams layer copy i mod {COPIES} "
+                f"({COPIES * LAYER_WEIGHT_BYTES / 1e6:.0f} MB of weights in all, over 4x the "
+                "129 MB L2); one L2 flush before the timed region"}
 
 
 def load_peaks():
@@ -282,6 +291,27 @@ def make_timing_events(torch, n):
         return None
 
 
+def l2_flush(torch, dev, _buf={}):
+    """Writes a buffer larger than the 129 MB L2, so that no weight line of an
+    earlier step is still cached when a timed region starts."""
+    if "b" not in _buf:
+        _buf["b"] = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    _buf["b"].fill_(1)
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def gpu_arm(args):
     import torch
 
@@ -306,79 +336,77 @@ def gpu_arm(args):
                 step.run(s3d8, copies[r], mode)
     stream.synchronize()
 
-    # One graph holds the COPIES consecutive steps (one per weight copy), the way a
-    # decode loop captures its layers; consecutive launches inside it overlap
-    # through programmatic dependent launch.  Single-step graphs cover the rest.
-    def run_all(mode, rounds):
-        for _ in range(rounds):
-            for r in range(COPIES):
-                step.run(s3d8, copies[r], mode)
+    # The timed region is exactly args.steps headline steps: one graph of
+    # consecutive grouped launches (step i on layer copy i mod 8) if that is at
+    # most MAX_GRAPH_STEPS, else replays of a MAX_GRAPH_STEPS graph and one graph
+    # with the remainder.  Inside a graph consecutive launches overlap through
+    # programmatic dependent launch; at a graph boundary they cannot.
+    def run_steps(mode, n):
+        for i in range(n):
+            step.run(s3d8, copies[i % COPIES], mode)
 
-    # The headline graph holds GRAPH_ROUNDS passes over the copies (64 steps), so
-    # that graph boundaries (where consecutive launches cannot overlap) are rare.
-    multi = {mode: capture(torch, stream, lambda mode=mode: run_all(mode, GRAPH_ROUNDS if mode == "group1" else 1))
-             for mode in ("group1", "group4", "separate")}
-    per_graph = {mode: COPIES * (GRAPH_ROUNDS if mode == "group1" else 1) for mode in multi}
-    single = [capture(torch, stream, lambda r=r: step.run(s3d8, copies[r], "group1"))
-              for r in range(COPIES)]
+    per_graph = min(args.steps, MAX_GRAPH_STEPS)
+    full, rest = divmod(args.steps, per_graph)
+    main_g = capture(torch, stream, lambda: run_steps("group1", per_graph))
+    rest_g = capture(torch, stream, lambda: run_steps("group1", rest)) if rest else None
     torch.cuda.synchronize()
 
-    def replay_steps(mode, steps):
-        full, rest = divmod(steps, per_graph[mode])
+    def timed_replays(graphs):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             t0.record(stream)
-            for _ in range(full):
-                multi[mode].replay()
-            for r in range(rest):
-                single[r % COPIES].replay()
+            for g in graphs:
+                g.replay()
             t1.record(stream)
         t1.synchronize()
-        return t0.elapsed_time(t1) / steps
+        return t0.elapsed_time(t1)
 
-    replay_steps("group1", max(args.warmup, 3))
+    # warm-up: at least args.warmup steps of the same graph
+    with torch.cuda.stream(stream):
+        for _ in range((args.warmup + per_graph - 1) // per_graph):
+            main_g.replay()
+    stream.synchronize()
 
     # ---- timed region: exactly args.steps steps of the headline structure ----
+    # The L2 flush is queued on the stream just before the start event, so that
+    # the GPU is still busy with it while the host submits the graph: the region
+    # then starts with the first launch, not with the host's submission latency.
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    ms_step = replay_steps("group1", args.steps)
+    with torch.cuda.stream(stream):
+        l2_flush(torch, dev)
+    ms_step = timed_replays([main_g] * full + ([rest_g] if rest_g else [])) / args.steps
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
 
-    # ---- spread: 64-step graph replays timed one by one, median and a 95 %
+    # ---- spread: replays of the same graph timed one by one, median and a 95 %
     # bootstrap interval of the per-step time (outside the timed region) ------
     spread = None
     if not args.layer_only:
-        blocks = []
-        with torch.cuda.stream(stream):
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(60)]
-            for a, b in evs:
-                a.record(stream)
-                multi["group1"].replay()
-                b.record(stream)
-            stream.synchronize()
-            blocks = [a.elapsed_time(b) / per_graph["group1"] for a, b in evs]
-        spread = bootstrap_median(blocks)
-        spread["block_steps"] = per_graph["group1"]
+        samples = [timed_replays([main_g]) / per_graph for _ in range(60)]
+        spread = bootstrap_median(samples)
+        spread["block_steps"] = per_graph
 
     # ---- other launch structures (same weights, same rotation) --------------
     variants = {}
     for mode in (() if args.layer_only else ("group4", "separate")):
-        n = max(COPIES, (args.steps // 4) // COPIES * COPIES)
-        replay_steps(mode, COPIES * 4)
-        ms = replay_steps(mode, n)
+        n = max(COPIES, min(per_graph, MAX_GRAPH_STEPS // 4) // COPIES * COPIES)
+        g = capture(torch, stream, lambda mode=mode, n=n: run_steps(mode, n))
+        timed_replays([g])
+        ms = timed_replays([g]) / n
         variants[mode] = {"ms_per_step": round(ms, 6), "launches_per_step": n_launches(mode),
+                          "steps_per_graph": n,
                           "value": round(LAYER_WEIGHT_BYTES / (ms * 1e-3) / 1e9, 1)}
+        del g
 
-    # ---- per-launch duration of the grouped kernel (events inside graphs) -----
-    launch_ms, launch_bytes = [], []
+    # ---- per-launch duration of the grouped kernel bracketed alone by events --
+    launch_ms = []
     evgraphs = []
     for r in range(COPIES):
         ev = make_timing_events(torch, 1)
@@ -393,12 +421,11 @@ def gpu_arm(args):
                     g.replay()
                 stream.synchronize()
                 launch_ms += [ev[0][0].elapsed_time(ev[0][1]) for _, ev in evgraphs]
-        launch_bytes = [group_bytes([n for n, _, _ in si.LLAMA_11B_LAYER])] * len(launch_ms)
     status = s3d8.device_status()
 
     ms_step = max_over_ranks(torch, ms_step, dev, world)
     value = job_value(world, ms_step)
-    hbm_peak, _, peak_kind = load_peaks()
+    hbm_peak, bf16_peak, peak_kind = load_peaks()
     # The timed region runs nothing but the grouped kernel, one launch per step, so
     # its average launch duration there is the region's event time / launches.
     # Launches bracketed one by one by events (no overlap with neighbours) are
@@ -420,11 +447,15 @@ def gpu_arm(args):
 
     e2e = prefill = unpack = quant = sweep = stack = encode = fit = None
     if not args.layer_only:
-        e2e = e2e_measure(torch, s3d8, copies, dev, min(args.steps, 4000))
-        prefill = prefill_measure(torch, s3d8, dev) if not args.skip_prefill else None
+        e2e = e2e_measure(torch, s3d8, copies, dev, args.steps, per_graph)
+        if not args.skip_prefill:
+            psampler = ClockSampler(local)
+            psampler.start()
+            prefill = prefill_measure(torch, s3d8, dev, bf16_peak)
+            prefill["clocks"] = psampler.stop()
         unpack = unpack_measure(torch, s3d8, dev)
         quant = quant_measure(torch, s3d8, dev)
-        sweep = decode_sweep_measure(torch, s3d8, dev)
+        sweep = decode_sweep_measure(torch, s3d8, dev, hbm_peak, bf16_peak)
         stack = stack_measure(torch, s3d8, dev)
         encode = encode_measure(torch, s3d8, dev)
         fit = fit_measure(torch, s3d8, dev)
@@ -437,15 +468,14 @@ def gpu_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic (seeded S3D8 fields, bf16 N(0,1) activations; no trained weights)",
-        "config": {"workload": WORKLOAD, "M": 1, "weight_bytes_per_step": LAYER_WEIGHT_BYTES,
-                   "weight_copies": COPIES,
-                   "l2": f"inputs larger than L2: {COPIES} rotating layer copies "
-                         f"({COPIES * LAYER_WEIGHT_BYTES / 1e6:.0f} MB of weights)",
-                   "launch": "one grouped launch per step (7 projections, activation "
-                             "quantisation fused); 64 consecutive steps (8 passes over the 8 "
-                             "rotating copies) captured in one CUDA graph, consecutive launches "
-                             "overlapping by programmatic dependent launch",
-                   "parallelism": f"replicas x{world}"},
+        "config": dict(CONFIG),
+        "parallelism": f"replicas x{world}",
+        "launch": (f"one grouped launch per step (7 projections, activation quantisation fused); "
+                   f"the {args.steps} timed steps are "
+                   + (f"one CUDA graph of {per_graph} consecutive launches" if full == 1 and not rest
+                      else f"{full} replays of a {per_graph}-step CUDA graph"
+                      + (f" and one {rest}-step graph" if rest else ""))
+                   + ", consecutive launches overlapping by programmatic dependent launch"),
         "gpu_launches": args.steps * n_launches("group1"),
         "device_status": status,
         "roofline": roofline, "variants": variants, "e2e": e2e, "prefill": prefill,
@@ -455,19 +485,20 @@ def gpu_arm(args):
     print(json.dumps(line))
 
 
-def e2e_measure(torch, s3d8, copies, dev, steps, group=4, sets=3):
+def e2e_measure(torch, s3d8, copies, dev, steps, per_graph, group=4, sets=3):
     """Same metric through the Python binding, with each step's four activations
     copied in from pinned host memory and its seven outputs copied back to
-    pinned host memory (one copy each way per step).  64 steps are captured in
-    one CUDA graph over three streams (copies in, layer launches, copies out),
-    in groups of `group` steps with `sets` rotating buffer sets per group: the
-    layer stream waits for a group's copy-ins (issued while the previous group
-    computes) once per group, and the copy-outs follow each group, so
-    consecutive launches inside a group still overlap through programmatic
-    dependent launch (a stream wait or event record between two launches stops
-    that overlap).  The synthetic steps are independent, so a group's inputs may
-    be copied before the previous group ends.  Every step's copies are inside
-    the timed region."""
+    pinned host memory (one copy each way per step), over exactly `steps` steps
+    in the same graph structure as the headline (graphs of `per_graph` steps,
+    step i on layer copy i mod 8).  Each graph runs on three streams (copies in,
+    layer launches, copies out), in groups of `group` steps with `sets` rotating
+    buffer sets per group: the layer stream waits for a group's copy-ins (issued
+    while the previous group computes) once per group, and the copy-outs follow
+    each group, so consecutive launches inside a group still overlap through
+    programmatic dependent launch (a stream wait or event record between two
+    launches stops that overlap).  The synthetic steps are independent, so a
+    group's inputs may be copied before the previous group ends.  Every step's
+    copies are inside the timed region."""
     nbuf = group * sets
     xk = list(ACT_K.items())
     kx = sum(K for _, K in xk)
@@ -501,91 +532,129 @@ def e2e_measure(torch, s3d8, copies, dev, steps, group=4, sets=3):
                 steps_b[b].run(s3d8, copies[r], "group1")
     ks.synchronize()
 
-    per = GRAPH_ROUNDS * COPIES
-    ngroups = per // group
-    ev_in = [torch.cuda.Event() for _ in range(ngroups)]
-    ev_k = [torch.cuda.Event() for _ in range(ngroups)]
-    ev_out = [torch.cuda.Event() for _ in range(ngroups)]
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=ks):
-        cin.wait_stream(ks)
-        cout.wait_stream(ks)
-        for gi in range(ngroups):
-            bufs = [(gi % sets) * group + j for j in range(group)]
-            with torch.cuda.stream(cin):
+    def capture_steps(n):
+        """A graph of n steps with their copies (groups of `group` steps)."""
+        groups_ = [list(range(i, min(n, i + group))) for i in range(0, n, group)]
+        ev_in = [torch.cuda.Event() for _ in groups_]
+        ev_k = [torch.cuda.Event() for _ in groups_]
+        ev_out = [torch.cuda.Event() for _ in groups_]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=ks):
+            cin.wait_stream(ks)
+            cout.wait_stream(ks)
+            for gi, idx in enumerate(groups_):
+                bufs = [(gi % sets) * group + j for j in range(len(idx))]
+                with torch.cuda.stream(cin):
+                    if gi >= sets:
+                        cin.wait_event(ev_k[gi - sets])     # the set's last group has read its inputs
+                    for b in bufs:
+                        x_all[b].copy_(host_x[b], non_blocking=True)
+                    ev_in[gi].record(cin)
+                ks.wait_event(ev_in[gi])
                 if gi >= sets:
-                    cin.wait_event(ev_k[gi - sets])     # the set's last group has read its inputs
-                for b in bufs:
-                    x_all[b].copy_(host_x[b], non_blocking=True)
-                ev_in[gi].record(cin)
-            ks.wait_event(ev_in[gi])
-            if gi >= sets:
-                ks.wait_event(ev_out[gi - sets])        # the set's last outputs are copied out
-            for j, b in enumerate(bufs):
-                steps_b[b].run(s3d8, copies[(gi * group + j) % COPIES], "group1")
-            ev_k[gi].record(ks)
-            with torch.cuda.stream(cout):
-                cout.wait_event(ev_k[gi])
-                for b in bufs:
-                    host_out[b].copy_(o_all[b], non_blocking=True)
-                ev_out[gi].record(cout)
-        ks.wait_stream(cin)
-        ks.wait_stream(cout)
+                    ks.wait_event(ev_out[gi - sets])        # the set's last outputs are copied out
+                for i, b in zip(idx, bufs):
+                    steps_b[b].run(s3d8, copies[i % COPIES], "group1")
+                ev_k[gi].record(ks)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(ev_k[gi])
+                    for b in bufs:
+                        host_out[b].copy_(o_all[b], non_blocking=True)
+                    ev_out[gi].record(cout)
+            ks.wait_stream(cin)
+            ks.wait_stream(cout)
+        return g
+
+    full, rest = divmod(steps, per_graph)
+    main_g = capture_steps(per_graph)
+    rest_g = capture_steps(rest) if rest else None
     h2d = host_x[0].numel() * 2
     d2h = host_out[0].numel() * 2
-    reps = max(1, steps // per)
     with torch.cuda.stream(ks):
         for _ in range(2):
-            g.replay()
+            main_g.replay()
     ks.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(ks):
+        l2_flush(torch, dev)    # keeps the GPU busy while the graph is submitted
         t0.record(ks)
-        for _ in range(reps):
-            g.replay()
+        for _ in range(full):
+            main_g.replay()
+        if rest_g is not None:
+            rest_g.replay()
         t1.record(ks)
     t1.synchronize()
-    ms = t0.elapsed_time(t1) / (reps * per)
+    ms = t0.elapsed_time(t1) / steps
     return {"value": round(LAYER_WEIGHT_BYTES / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
-            "steps": reps * per,
+            "steps": steps,
             "path": "Python binding (grouped launch); per step one pinned host->device copy of "
                     "the four activations and one device->host copy of the seven outputs, on their "
                     f"own streams, synchronised with the layer stream once per group of {group} steps "
-                    "(launches inside a group overlap); 64 steps per CUDA graph"}
+                    f"(launches inside a group overlap); the same {per_graph}-step graphs as the "
+                    "headline"}
 
 
-def prefill_measure(torch, s3d8, dev, M=2048, reps=3):
-    res = {}
-    tot_ops, tot_ms = 0, 0.0
-    for name, K, N in si.SWEEP_SHAPES:
-        mat = si.matrix(name, K, N, seed=3)
-        packed = torch.from_numpy(mat.packed).to(dev)
-        C = torch.from_numpy(mat.C).to(dev)
-        cs = to_dev_bf16(mat.chan_scale, dev)
-        x = to_dev_bf16(si.acts(M, K, seed=3), dev)
-        xq, xs = s3d8.quantize_act(x)
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        ws = torch.empty((s3d8.workspace_size(M, N, K),), dtype=torch.uint8, device=dev)
-        s3d8.linear(packed, C, cs, xq, xs, N, out=out, workspace=ws)
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for _ in range(reps):
-            s3d8.linear(packed, C, cs, xq, xs, N, out=out, workspace=ws)
-        t1.record()
-        t1.synchronize()
-        ms = t0.elapsed_time(t1) / reps
-        ops = 2 * M * N * K
-        res[name] = {"M": M, "K": K, "N": N, "us": round(ms * 1e3, 1),
-                     "tops": round(ops / (ms * 1e-3) / 1e12, 2)}
-        tot_ops += ops
-        tot_ms += ms
-    res["tops"] = round(tot_ops / (tot_ms * 1e-3) / 1e12, 2)
-    res["unit"] = "TOPS (int8 multiply-adds x2)"
-    res["two_step"] = two_step_measure(torch, s3d8, dev, M, reps)
+def prefill_measure(torch, s3d8, dev, bf16_peak, Ms=None, reps=20, copies=2):
+    """The tensor-core path at the prefill sizes (M = 512 and 2048) on the gate/up
+    and down shapes, through s3d8_linear (automatic algorithm), alternating
+    between `copies` weight copies; 3 warm-up calls, then `reps` calls timed
+    with CUDA events.  Roofline: the tensor engine the path runs on (bf16
+    tcgen05.mma kind::f16, exact int32 sums from fp32 chunks), against the
+    measured bf16 dense peak (burst: the calls are timed without a long
+    sustained load); the fraction of the INT8 library GEMM rate measured on the
+    same shapes (the pages' two-step method's GEMM) is reported beside it."""
+    Ms = si.PREFILL_M if Ms is None else Ms
+    two_step = two_step_measure(torch, s3d8, dev, max(Ms), 3)
+    # the chip's INT8 tensor rate as the library GEMM reaches it on these shapes
+    int8_peak = max(2 * max(Ms) * K * N / (two_step[name]["int8_gemm_us"] * 1e-6) / 1e12
+                    for name, K, N in si.SWEEP_SHAPES)
+    res = {"unit": "TOPS (int8 multiply-adds x2)", "engine": "tcgen05.mma kind::f16 (bf16), exact int32",
+           "peak_tflops": bf16_peak, "int8_library_peak_tops": round(int8_peak, 1),
+           "int8_library": "torch._int_mm (cuBLASLt int8 x int8 -> int32) on the same shapes at "
+                           f"M = {max(Ms)}, the fastest of the two"}
+    for M in Ms:
+        tot_ops, tot_ms = 0, 0.0
+        for name, K, N in si.SWEEP_SHAPES:
+            mats = [si.matrix(name, K, N, seed=3, index=i) for i in range(copies)]
+            w = [dict(packed=torch.from_numpy(m.packed).to(dev), C=torch.from_numpy(m.C).to(dev),
+                      cs=to_dev_bf16(m.chan_scale, dev)) for m in mats]
+            x = to_dev_bf16(si.acts(M, K, seed=3), dev)
+            xq, xs = s3d8.quantize_act(x)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty((max(1, s3d8.workspace_size(M, N, K)),), dtype=torch.uint8, device=dev)
+
+            def call(i):
+                m = w[i % copies]
+                s3d8.linear(m["packed"], m["C"], m["cs"], xq, xs, N, out=out, workspace=ws)
+
+            for i in range(3):
+                call(i)
+            torch.cuda.synchronize()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for i in range(reps):
+                call(i)
+            t1.record()
+            t1.synchronize()
+            ms = t0.elapsed_time(t1) / reps
+            ops = 2 * M * N * K
+            tops = ops / (ms * 1e-3) / 1e12
+            res[f"{name}_M{M}"] = {"M": M, "K": K, "N": N, "us": round(ms * 1e3, 1),
+                                   "tops": round(tops, 2),
+                                   "roofline": {"bound": "tensor", "achieved": round(tops, 1),
+                                                "peak": bf16_peak, "unit": "TFLOP/s",
+                                                "frac": round(tops / bf16_peak, 4),
+                                                "frac_of_int8_library": round(tops / int8_peak, 2)}}
+            tot_ops += ops
+            tot_ms += ms
+            del w, mats
+        tops = tot_ops / (tot_ms * 1e-3) / 1e12
+        res[f"M{M}"] = {"tops": round(tops, 2), "frac": round(tops / bf16_peak, 4)}
+    res["tops"] = res[f"M{max(Ms)}"]["tops"]
+    res["two_step"] = two_step
     return res
 
 
@@ -644,13 +713,18 @@ def device_matrix(torch, dev, gen, K, N):
                     torch.bfloat16))
 
 
-def decode_sweep_measure(torch, s3d8, dev, copies=28, reps=56, replays=5):
+def decode_sweep_measure(torch, s3d8, dev, hbm_peak, bf16_peak, copies=28, reps=56, replays=5):
     """Batched decode (M = 8..64) on the gate/up and down shapes through
     s3d8_linear (automatic algorithm choice), rotating `copies` weight copies
     (28 x 19.6 MB = 549 MB, over four times the 129 MB L2, so that every launch
     streams its weights from HBM).
     The `reps` launches are captured in one CUDA graph and replayed, so that the
-    time is the device's and not the Python binding's per-call overhead."""
+    time is the device's and not the Python binding's per-call overhead.
+    Roofline per entry: the larger of the HBM time of the algorithmic bytes
+    (weights, scales, table, codes, token scales, bf16 outputs) at the measured
+    copy bandwidth and the tensor time of 2 M N K operations at the measured
+    bf16 dense peak (the engine of the tensor-core paths); frac = that bound /
+    the measured time."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
     res = {}
@@ -681,9 +755,15 @@ def decode_sweep_measure(torch, s3d8, dev, copies=28, reps=56, replays=5):
                 t1.record(stream)
             t1.synchronize()
             ms = t0.elapsed_time(t1) / (reps * replays)
+            hbm_us = linear_bytes(M, K, N) / (hbm_peak * 1e9) * 1e6
+            tensor_us = 2 * M * N * K / (bf16_peak * 1e12) * 1e6
+            bound_us = max(hbm_us, tensor_us)
             res[f"{name}_M{M}"] = {"us": round(ms * 1e3, 2),
                                    "weight_gbs": round(weight_bytes(K, N) / (ms * 1e-3) / 1e9, 1),
-                                   "tops": round(2 * M * N * K / (ms * 1e-3) / 1e12, 2)}
+                                   "tops": round(2 * M * N * K / (ms * 1e-3) / 1e12, 2),
+                                   "bound": "hbm" if hbm_us >= tensor_us else "tensor",
+                                   "bound_us": round(bound_us, 3),
+                                   "frac": round(bound_us / (ms * 1e3), 4)}
         del mats
     return res
 
@@ -945,7 +1025,7 @@ def cpu_baseline(seconds, max_steps=None):
     return {"value": round(multi, 4), "unit": UNIT, "cores": cores,
             "kind": "oracle", "seconds": round(el + el2, 2),
             "single_thread_value": round(single, 4),
-            "host": f"{platform.machine()}, {cores} cores",
+            "host": f"{cpu_model()} ({platform.machine()}), {cores} cores",
             "sample": f"{m} full layer steps at M=1 (4 activation quantisations + 7 linears) with "
                       f"the plain C oracle on {cores} threads (each linear split into {cores} "
                       f"packed-row slices); single-threaded: {n} steps"}
@@ -956,17 +1036,18 @@ def reference_arm(args):
     if rank != 0:
         return
     import oracle
-    mats = si.layer_matrices(layer=0, seed=0)
+    # the same workload as the GPU arm: step i streams layer copy i mod 8
+    copies = [si.layer_matrices(layer=r, seed=0) for r in range(COPIES)]
     xs_bits = {k: si.acts(1, K, seed=0, index=i) for i, (k, K) in enumerate(ACT_K.items())}
     oracle.lib()
     import concurrent.futures as cf
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
-        for _ in range(args.warmup):
-            oracle_layer_step_threads(oracle, mats, xs_bits, pool, cores)
+        for i in range(args.warmup):
+            oracle_layer_step_threads(oracle, copies[i % COPIES], xs_bits, pool, cores)
         t0 = time.perf_counter()
-        for _ in range(args.steps):
-            oracle_layer_step_threads(oracle, mats, xs_bits, pool, cores)
+        for i in range(args.steps):
+            oracle_layer_step_threads(oracle, copies[i % COPIES], xs_bits, pool, cores)
         el = time.perf_counter() - t0
     ms = el * 1e3 / args.steps
     value = LAYER_WEIGHT_BYTES / (ms * 1e-3) / 1e9
@@ -975,9 +1056,10 @@ def reference_arm(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8",
-        "data": "synthetic (seeded S3D8 fields, bf16 N(0,1) activations)",
-        "config": {"workload": WORKLOAD, "M": 1, "weight_bytes_per_step": LAYER_WEIGHT_BYTES},
+        "data": "synthetic (seeded S3D8 fields, bf16 N(0,1) activations; no trained weights)",
+        "config": dict(CONFIG),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "host": f"{cpu_model()}, {cores} cores",
                          "sample": f"{args.steps} full layer steps at M=1, the plain C oracle "
                                    f"on {cores} threads (each linear split into {cores} "
                                    "packed-row slices)"},
@@ -1019,14 +1101,17 @@ def main():
 
         import s3d8_a8_linear_gb300 as s3d8
         s3d8.load(build_if_missing=True)
-        print(json.dumps(prefill_measure(torch, s3d8, torch.device("cuda:0"))))
+        _, bf16_peak, _ = load_peaks()
+        print(json.dumps(prefill_measure(torch, s3d8, torch.device("cuda:0"), bf16_peak)))
         return
     if args.sweep_only:
         import torch
 
         import s3d8_a8_linear_gb300 as s3d8
         s3d8.load(build_if_missing=True)
-        print(json.dumps(decode_sweep_measure(torch, s3d8, torch.device("cuda:0"))))
+        hbm_peak, bf16_peak, _ = load_peaks()
+        print(json.dumps(decode_sweep_measure(torch, s3d8, torch.device("cuda:0"), hbm_peak,
+                                              bf16_peak)))
         return
     if args.aux_only:
         import torch

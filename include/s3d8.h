@@ -281,26 +281,31 @@ int s3d8_selftest_wait_timeout(int64_t polls, void *stream);
 #define S3D8_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /*
- * The tensor-core linear (s3d8_linear_ex with S3D8_ALGO_TC: same kernels, same
- * results, same argument layouts and alignment rules) for callers that cannot
- * allocate device memory: code inside an allocator or memory-pool callback, a
- * real-time loop that must never wait on the driver's allocator, or a host that
- * owns all device memory itself.  It calls no cudaMalloc or cudaFree and no
- * allocating library routine.  Instead of caller workspace it uses a fixed
- * scratch array of S3D8_NOALLOC_SCRATCH_BYTES compiled into the library, which
- * every GPU that loads the library holds until the process exits.  The paper
- * has no counterpart; this is a deployment convenience.
- *   - Shapes whose tensor-core workspace (s3d8_linear_workspace_size with
- *     S3D8_ALGO_TC) exceeds S3D8_NOALLOC_SCRATCH_BYTES are rejected with
- *     S3D8_ERR_WORKSPACE before any launch: the bf16 activation copy needs
- *     2 * M * K + 256 bytes (so M <= 2047 at K = 4096), plus the int32 partial
- *     sums when a small M splits K.
+ * The tensor-core linear, with the same results, argument layouts and alignment
+ * rules as s3d8_linear_ex with S3D8_ALGO_TC (the int32 sums are exact on both,
+ * and the bf16 epilogue is the same), for callers that cannot allocate device
+ * memory: code inside an allocator or memory-pool callback, a real-time loop
+ * that must never wait on the driver's allocator, or a host that owns all
+ * device memory itself.  It calls no cudaMalloc or cudaFree and no allocating
+ * library routine.  Instead of caller workspace it uses a fixed scratch array of
+ * S3D8_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads the library holds until the process exits.  The paper has no
+ * counterpart; this is a deployment convenience.
+ *   - Kernel: always the one-SM tensor-core GEMM that decodes the packed weight
+ *     tiles itself (S3D8_ALGO_TC takes it below 384 tokens); it never expands
+ *     the weights into scratch, so its scratch need does not grow with N.
+ *   - Scratch need: the bf16 copy of the activation codes, 2 * M * K + 256
+ *     bytes, plus int32 partial sums (nsplit * M * N * 4 bytes) when the output
+ *     tiles cannot fill the GPU and K is split.  Shapes beyond
+ *     S3D8_NOALLOC_SCRATCH_BYTES are rejected with S3D8_ERR_WORKSPACE before any
+ *     launch; without a K split that is M <= 4095 at K = 4096.
  *   - The first call on a device looks up the scratch array's device address
  *     (once per device, with that device current); make that first call before
  *     any stream capture.
- *   - All calls on a device share the one array.  Calls that overlap on the GPU
- *     (on different streams, or from several threads without ordering) race on
- *     it and give wrong results; order them on one stream.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents (each call overwrites what it reads).  Calls that overlap on the
+ *     GPU (on different streams, or from several threads without ordering) race
+ *     on it and give wrong results; order them on one stream.
  * Inputs and outputs are still the caller's device memory, as in s3d8_linear.
  */
 int s3d8_linear_tc_noalloc(const uint8_t *packed, const int8_t *centroids,

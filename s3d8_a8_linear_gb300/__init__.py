@@ -284,13 +284,15 @@ def linear(packed: torch.Tensor, centroids: torch.Tensor, chan_scale: torch.Tens
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=packed.device)
     ws, ws_bytes = _workspace(M, N, K, algo, packed.device, workspace)
-    st = load().s3d8_linear_ex(
-        _dev(packed, "packed", torch.uint8), _dev(centroids, "centroids", torch.int8, (32, 3)),
-        _dev(chan_scale, "chan_scale", torch.bfloat16, (N,)), _dev(xq, "xq", torch.int8, (M, K)),
-        _dev(xscale, "xscale", torch.float32, (M,)), M, N, K,
-        _dev(out, "out", torch.bfloat16, (M, N)),
-        None if ws is None else ws.data_ptr(), ws_bytes, algo, _stream(packed.device))
-    _check("s3d8_linear_ex", st)
+    args = (_dev(packed, "packed", torch.uint8), _dev(centroids, "centroids", torch.int8, (32, 3)),
+            _dev(chan_scale, "chan_scale", torch.bfloat16, (N,)), _dev(xq, "xq", torch.int8, (M, K)),
+            _dev(xscale, "xscale", torch.float32, (M,)), M, N, K,
+            _dev(out, "out", torch.bfloat16, (M, N)),
+            None if ws is None else ws.data_ptr(), ws_bytes)
+    if algo == ALGO_AUTO:   # the plain entry point: the library picks the algorithm
+        _check("s3d8_linear", load().s3d8_linear(*args, _stream(packed.device)))
+    else:
+        _check("s3d8_linear_ex", load().s3d8_linear_ex(*args, algo, _stream(packed.device)))
     return out
 
 

@@ -448,14 +448,13 @@ __global__ void finalize_kernel(const int32_t *__restrict__ part, int nsplit, in
 
 // K split of the tensor-core GEMM when its output tiles alone cannot fill the
 // GPU: the number of 64-column blocks per split that minimises
-// waves x (blocks per CTA + a per-CTA fixed cost of about 4 blocks).
-static bool prefill_pairs(int M);
-
-static void tc_plan(int M, int N, int K, int sms, int &nsplit, int &kb_per_split)
+// waves x (blocks per CTA + a per-CTA fixed cost of about 4 blocks).  `pairs`
+// names the kernel the plan is for: the SM-pair GEMM (256 x 256 tiles on two
+// SMs) or the one-SM GEMM (128 x 240 tiles).
+static void tc_plan(int M, int N, int K, int sms, bool pairs, int &nsplit, int &kb_per_split)
 {
-    // CTAs per K range: 128 x 240 tiles on one SM, or 256 x 256 tiles on two
-    const long tiles = prefill_pairs(M) ? 2L * ((M + 255) / 256) * ((N + 255) / 256)
-                                        : (long)((M + tc::BM - 1) / tc::BM) * (((N + 2) / 3 + tc::GROUPS - 1) / tc::GROUPS);
+    const long tiles = pairs ? 2L * ((M + 255) / 256) * ((N + 255) / 256)
+                             : (long)((M + tc::BM - 1) / tc::BM) * (((N + 2) / 3 + tc::GROUPS - 1) / tc::GROUPS);
     const int nk = (K + tc::BK - 1) / tc::BK;
     nsplit = 1;
     kb_per_split = nk;
@@ -491,15 +490,12 @@ bool prefill_predecode(int M)
     return M >= kPredecodeMinM;
 }
 
-static bool prefill_pairs(int M)
-{
-    return prefill_predecode(M);
-}
-
+// `pre` selects the kernel: the SM-pair GEMM on pre-expanded weights, or the
+// one-SM GEMM that decodes packed tiles itself (at any M).
 size_t prefill_workspace_bytes(int M, int N, int K, bool pre)
 {
     int nsplit, kbps;
-    tc_plan(M, N, K, device_sm_count(), nsplit, kbps);
+    tc_plan(M, N, K, device_sm_count(), pre, nsplit, kbps);
     size_t bytes = align256((size_t)M * K * 2) + 256;
     if (nsplit > 1)
         bytes += align256((size_t)nsplit * M * N * 4);
@@ -548,7 +544,7 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream
     if (!a.ws || a.ws_bytes < prefill_workspace_bytes(a.M, a.N, a.K, pre))
         return cudaErrorInvalidValue;
     int nsplit, kbps;
-    tc_plan(a.M, a.N, a.K, device_sm_count(), nsplit, kbps);
+    tc_plan(a.M, a.N, a.K, device_sm_count(), pre, nsplit, kbps);
     auto encode = tensor_map_encoder();
     if (!encode)
         return cudaErrorNotSupported;

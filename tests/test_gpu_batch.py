@@ -32,7 +32,9 @@ def mat_dev(m):
 
 def test_layer_fused_m1():
     """The seven projections of a decoder layer in one launch, activations
-    quantised inside the launch, each compared in full with the oracle."""
+    quantised inside the launch, each compared in full with the oracle: the
+    bf16 outputs within the parity tolerance, and, from a second launch that
+    writes int32 accumulators instead, the exact sums bit for bit."""
     mats = si.layer_matrices(layer=3, seed=1)
     acts = {a: si.acts(1, K, seed=1, index=i) for i, (a, K) in
             enumerate({"attn": 4096, "o": 4096, "mlp": 4096, "down": 14336}.items())}
@@ -43,16 +45,19 @@ def test_layer_fused_m1():
             qref[a] = oracle.quantize_act(acts[a])
         xq_o, xs_o = qref[a]
         ref, acc_o = oracle.linear(m.packed, m.C, m.chan_scale, xq_o, xs_o, m.N)
-        refs.append((m.name, ref, a))
+        refs.append((m.name, ref, a, acc_o))
         j = mat_dev(m)
         j["x"] = bf16_bits(acts[a])
         j["xq_out"] = torch.empty((1, m.K), dtype=torch.int8, device=dev())
         j["xscale_out"] = torch.empty((1,), dtype=torch.float32, device=dev())
         jobs.append(j)
     outs = s3d8.linear_batch(jobs, 1)
+    acc_jobs = [dict(j, acc=torch.empty((1, j["N"]), dtype=torch.int32, device=dev())) for j in jobs]
+    accs = s3d8.linear_batch(acc_jobs, 1)
     torch.cuda.synchronize()
-    for (name, ref, a), j, out in zip(refs, jobs, outs):
+    for (name, ref, a, acc_o), j, out, acc in zip(refs, jobs, outs, accs):
         assert_out_close(bf16_to_f64(out), ref)
+        np.testing.assert_array_equal(to_np(acc).astype(np.int64), acc_o, err_msg=name)
         np.testing.assert_array_equal(to_np(j["xq_out"]), qref[a][0], err_msg=name)
         np.testing.assert_array_equal(to_np(j["xscale_out"]), qref[a][1], err_msg=name)
 

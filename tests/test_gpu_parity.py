@@ -191,6 +191,48 @@ def test_tiny_config(algo):
                      ref)
 
 
+def _plain_linear(packed, C, cs, xq, xs, N):
+    """out through the exported s3d8_linear symbol itself, called with ctypes
+    (workspace sized by s3d8_linear_workspace_size with the automatic choice)."""
+    M, K = xq.shape
+    lib = s3d8.load()
+    need = int(lib.s3d8_linear_workspace_size(M, N, K, s3d8.ALGO_AUTO))
+    ws = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev())
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev())
+    st = lib.s3d8_linear(packed.data_ptr(), C.data_ptr(), cs.data_ptr(), xq.data_ptr(),
+                         xs.data_ptr(), M, N, K, out.data_ptr(), ws.data_ptr() if need else None,
+                         need, torch.cuda.current_stream().cuda_stream)
+    assert st == 0, lib.s3d8_status_string(st)
+    return out
+
+
+def test_plain_entry_point_s3d8_linear():
+    """The literal boundary call s3d8_linear on the small case (K=256, N=96,
+    M=4) and on two projections of an 11B layer at M = 1 (gate 4096 -> 14336,
+    down 14336 -> 4096): within tolerance of the oracle, and bit for bit equal
+    to s3d8_linear_ex with the automatic algorithm."""
+    mat, x = si.tiny_case(0)
+    cases = [(mat, x)]
+    for m in si.layer_matrices(layer=0, seed=0):
+        if m.name in ("gate", "down"):
+            cases.append((m, si.acts(1, m.K, seed=0, index=len(cases))))
+    for mat, x in cases:
+        xq, xs = oracle.quantize_act(x)
+        ref, _ = oracle.linear(mat.packed, mat.C, mat.chan_scale, xq, xs, mat.N)
+        args = (u8(mat.packed), i8(mat.C), bf16_bits(mat.chan_scale), i8(xq), f32(xs))
+        got = _plain_linear(*args, mat.N)
+        ex = torch.empty_like(got)
+        M, K = xq.shape
+        ws = torch.empty((max(1, s3d8.workspace_size(M, mat.N, K)),), dtype=torch.uint8, device=dev())
+        st = s3d8.load().s3d8_linear_ex(*(a.data_ptr() for a in args), M, mat.N, K, ex.data_ptr(),
+                                        ws.data_ptr(), ws.numel(), s3d8.ALGO_AUTO,
+                                        torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+        torch.cuda.synchronize()
+        assert_out_close(bf16_to_f64(got), ref)
+        np.testing.assert_array_equal(to_np(got.view(torch.int16)), to_np(ex.view(torch.int16)))
+
+
 @pytest.mark.parametrize("algo", [s3d8.ALGO_AUTO] + ALGOS, ids=lambda a: ALGO_IDS[a])
 def test_llama_layer_decode_m1_full(algo):
     """Every projection of one 11B decoder layer at M = 1, compared in full."""
