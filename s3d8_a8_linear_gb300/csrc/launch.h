@@ -71,16 +71,19 @@ cudaError_t launch_wait_timeout(int polls, int *status, cudaStream_t stream);
 bool gemv_group_job_ok(int M, int K, bool fused);
 cudaError_t launch_gemv_group(GroupArgs &g, cudaStream_t stream);
 cudaError_t launch_gemv_tma(const LinearArgs &a, cudaStream_t stream);
-// Tensor-core path; `pre` expands the weights to bf16 in the workspace first and
-// feeds both operands by bulk tensor copy (large M), otherwise the weight tile
-// is decoded from packed bytes inside the GEMM.
-bool prefill_predecode(int M);
-size_t prefill_workspace_bytes(int M, int N, int K, bool pre);
-cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream);
-// Split-K finish shared by the tensor-core and skinny paths: sums int32 partials
-// [nsplit][M][N] into a.out (epilogue) or a.acc.
+// Tensor-core path, three kernels: one SM per tile (decoding packed tiles
+// itself), SM pairs decoding packed tiles themselves, or SM pairs on weights
+// expanded to bf16 in the workspace first.  prefill_kind(M) picks by token count.
+constexpr int kTcOneSm = 0, kTcPairFused = 1, kTcPairExpanded = 2;
+int prefill_kind(int M);
+size_t prefill_workspace_bytes(int M, int N, int K, int kind);
+cudaError_t launch_prefill_tc(const LinearArgs &a, int kind, cudaStream_t stream);
 cudaError_t launch_prefill_pair(const LinearArgs &a, const __nv_bfloat16 *act, const __nv_bfloat16 *wdec,
                                 int32_t *part, int nsplit, int kbps, cudaStream_t stream);
+cudaError_t launch_prefill_fused(const LinearArgs &a, const __nv_bfloat16 *act, int32_t *part, int nsplit, int kbps,
+                                 cudaStream_t stream);
+// Split-K finish shared by the tensor-core and skinny paths: sums int32 partials
+// [nsplit][M][N] into a.out (epilogue) or a.acc.
 cudaError_t launch_splitk_finalize(const int32_t *part, int nsplit, const LinearArgs &a, cudaStream_t stream);
 // mma.sync path for a few tokens (1..32), weights decoded into register fragments.
 bool skinny_supported(int M);

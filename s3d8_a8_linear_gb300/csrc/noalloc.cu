@@ -67,7 +67,7 @@ int s3d8_linear_tc_noalloc(const uint8_t *packed, const int8_t *centroids, const
     if (((uintptr_t)packed & 15) || ((uintptr_t)xq & 15) || ((uintptr_t)chan_scale_bf16 & 1) ||
         ((uintptr_t)xscale & 3) || ((uintptr_t)out_bf16 & 1))
         return S3D8_ERR_ALIGNMENT;
-    if (prefill_workspace_bytes((int)M, (int)N, (int)K, false) > (size_t)S3D8_NOALLOC_SCRATCH_BYTES)
+    if (prefill_workspace_bytes((int)M, (int)N, (int)K, kTcOneSm) > (size_t)S3D8_NOALLOC_SCRATCH_BYTES)
         return S3D8_ERR_WORKSPACE;
 
     void *scratch = nullptr;
@@ -89,5 +89,5 @@ int s3d8_linear_tc_noalloc(const uint8_t *packed, const int8_t *centroids, const
     a.status = device_status_ptr();
     if (!a.status)
         return S3D8_ERR_CUDA;
-    return launch_prefill_tc(a, false, static_cast<cudaStream_t>(stream)) == cudaSuccess ? S3D8_OK : S3D8_ERR_CUDA;
+    return launch_prefill_tc(a, kTcOneSm, static_cast<cudaStream_t>(stream)) == cudaSuccess ? S3D8_OK : S3D8_ERR_CUDA;
 }

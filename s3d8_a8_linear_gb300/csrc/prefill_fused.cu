@@ -1,0 +1,389 @@
+// Prefill-regime S3D8 linear on SM pairs with the S3D8 unpack inside the GEMM:
+// tcgen05.mma.cta_group::2 on fp32-exact bf16 chunks, like the one-SM kernel in
+// prefill_tc.cu, with no bf16 copy of the weights anywhere.
+//
+// A cluster of two CTAs on two SMs computes a 256-token x 240-channel tile:
+// CTA r of the pair holds activation rows 128 r .. 128 r + 127 of the tile (by
+// bulk tensor copy from the bf16 copy of the codes) and decodes packed rows
+// 40 r .. 40 r + 39 of the tile's 80 (channels 120 r .. 120 r + 119) from
+// packed bytes into its half of the bf16 weight tile; the even CTA issues
+// M = 256, N = 240 MMAs that read both CTAs' halves, and each CTA's tensor
+// memory receives its own 128 rows of the accumulator.  Per SM and K block the
+// bulk copies bring 16 KiB of activations and 2.5 KiB of packed bytes.
+//
+// Roles (16 warps per CTA):
+//   warp 0       bulk tensor copies of this CTA's activation halves into a
+//                5-stage ring, completing on the even CTA's full barrier
+//                (cta_group::2 copies);
+//   warp 1       TMEM allocation for the pair (both CTAs, cta_group::2); in the
+//                even CTA the MMA issuer (one elected lane);
+//   warp 2       bulk tensor copies of this CTA's packed halves into a 16-stage
+//                ring on its own barriers, so that decoding runs ahead of the
+//                MMAs by the whole ring;
+//   warps 3-7    decode: two 8-byte units (one packed row, 8 columns) each per K
+//                block, written into the 128-byte-swizzled K-major bf16 half of
+//                the stage; then a proxy fence (generic writes -> the tensor
+//                core's async proxy) and an arrive on the even CTA's full
+//                barrier, which completes with 1 + 10 arrivals (the even CTA's
+//                copy-issuing lane, 5 decoder warps x 2 CTAs) and both copies'
+//                bytes, so that the MMA issuer waits and commits once per K block;
+//   warps 8-15   drain this CTA's accumulator rows per chunk into int32
+//                (setmaxnreg 176) and write the epilogue.  They release the TMEM
+//                buffer to the even CTA's MMA issuer (16 arrivals: 8 warps x 2
+//                CTAs).  (Decoding in these warps too, between drains, made them
+//                the slowest decoders: the 120 sums they hold leave the decode
+//                too few registers.)
+// MMA completion is committed to the barriers of both CTAs at once
+// (multicast).  Every mbarrier wait is bounded; both CTAs reach the closing
+// cluster barrier on every path, so neither leaves while the other may still
+// touch its memory.
+#include "tcgen05.cuh"
+
+namespace s3d8 {
+
+namespace tc {
+
+constexpr int FUSED_STAGES = 5;                       // ring of stages: activation half + decoded weight half
+constexpr int FUSED_PSTAGES = 16;                     // ring of packed halves (decoded ahead of the MMA)
+constexpr int FUSED_LUT_COPIES = 8;                   // table copies (two lanes of a half-warp share one)
+constexpr int FUSED_LUT_BYTES = kLutEntries * FUSED_LUT_COPIES * 8;   // 16 KiB
+constexpr int FUSED_BM = 2 * BM;                      // 256 tokens per pair tile
+constexpr int FUSED_GROUPS = GROUPS / 2;              // 40 packed rows per CTA
+constexpr int FUSED_BH = 3 * FUSED_GROUPS;             // 120 weight rows (channels) per CTA
+constexpr int FUSED_BN = 2 * FUSED_BH;                 // 240 channels per pair tile
+constexpr int FUSED_P_BYTES = FUSED_GROUPS * BK;       // 2.5 KiB packed bytes per stage
+constexpr int FUSED_B_BYTES = FUSED_BH * BK * 2;       // 15 KiB decoded half tile
+constexpr int FUSED_DEC_WARP0 = 3;                    // decoders: warps 3-7
+constexpr int FUSED_DEC_WARPS = 5;
+constexpr int FUSED_DECODERS = FUSED_DEC_WARPS * 32;   // two units each per K block
+constexpr int FUSED_OFF_A = 0;
+constexpr int FUSED_OFF_B = FUSED_OFF_A + FUSED_STAGES * A_BYTES;
+constexpr int FUSED_OFF_P = FUSED_OFF_B + FUSED_STAGES * FUSED_B_BYTES;
+constexpr int FUSED_OFF_LUT = FUSED_OFF_P + FUSED_PSTAGES * FUSED_P_BYTES;
+constexpr int FUSED_OFF_BARS = FUSED_OFF_LUT + FUSED_LUT_BYTES;
+constexpr int FUSED_NBARS = 2 * FUSED_STAGES + 2 * FUSED_PSTAGES + 4;
+constexpr int FUSED_SMEM_BYTES = 1024 + FUSED_OFF_BARS + FUSED_NBARS * 8 + 16;
+static_assert(FUSED_B_BYTES % 1024 == 0 && FUSED_OFF_B % 1024 == 0 && A_BYTES % 1024 == 0,
+              "swizzled tiles 1024-aligned");
+static_assert(FUSED_OFF_P % 128 == 0 && FUSED_P_BYTES % 128 == 0 && FUSED_OFF_LUT % 16 == 0, "packed tiles aligned");
+static_assert(FUSED_SMEM_BYTES + 1024 <= 232448, "shared memory budget");
+static_assert(FUSED_BH % 8 == 0 && FUSED_BN % 16 == 0 && FUSED_BN <= 256, "M = 256 MMAs need N a multiple of 16");
+static_assert(2 * FUSED_DECODERS == FUSED_GROUPS * 8, "two decode units per decoder thread and K block");
+static_assert(FUSED_BH == HALF, "each drain thread holds the sums of one CTA half's columns");
+static_assert(FUSED_DEC_WARP0 + FUSED_DEC_WARPS == DRAIN_WARP0, "decoders are warps 3-7, before the drain warps");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    prefill_fused_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_pk,
+                        Params p)
+{
+    constexpr int S = FUSED_STAGES, PS = FUSED_PSTAGES;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *smem = smem_raw + (base - raw);
+    const uint32_t lut = base + FUSED_OFF_LUT;
+    const uint32_t bars = base + FUSED_OFF_BARS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + FUSED_OFF_BARS + FUSED_NBARS * 8);
+    // full[S] (even CTA: both CTAs' activation halves of the stage landed and
+    // both CTAs' decoded halves written: 1 + 10 arrivals and the copies' bytes),
+    // empty[S] (the pair's MMAs are done with the stage; both CTAs), p_full[PS]
+    // (this CTA's packed half landed), p_empty[PS] (this CTA's decoders are done
+    // with it), acc_full[2] (chunk in TMEM), acc_empty[2] (even CTA: both CTAs
+    // drained it).  One barrier per stage and direction keeps the MMA issuer at
+    // one wait and one commit per K block.
+    const uint32_t full = bars, empty = full + 8 * S;
+    const uint32_t p_full = empty + 8 * S, p_empty = p_full + 8 * PS;
+    const uint32_t acc_full = p_empty + 8 * PS, acc_empty = acc_full + 16;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int cid = (int)blockIdx.x >> 1, nclusters = (int)gridDim.x >> 1;
+    const int mtiles = (p.M + FUSED_BM - 1) / FUSED_BM;
+    const int ntiles = ((p.N + 2) / 3 + GROUPS - 1) / GROUPS;
+    const int nk_all = (p.K + BK - 1) / BK;
+    const int total = mtiles * ntiles * p.nsplit;
+    struct Tile {
+        int m0, nt, split, kbase, nk;
+    };
+    // consecutive tile indices share the channel tile, so the pairs working at
+    // one time read its packed bytes from L2
+    auto tile_of = [&](int t) {
+        Tile T;
+        const int mt = t % mtiles, rest = t / mtiles;
+        T.nt = rest % ntiles;
+        T.split = rest / ntiles;
+        T.m0 = mt * FUSED_BM;
+        T.kbase = T.split * p.kb_per_split;
+        T.nk = min(p.kb_per_split, nk_all - T.kbase);
+        return T;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full + 8 * s, 1 + 2 * FUSED_DEC_WARPS);
+            mbar_init(empty + 8 * s, 1);
+        }
+        for (int s = 0; s < PS; ++s) {
+            mbar_init(p_full + 8 * s, 1);
+            mbar_init(p_empty + 8 * s, FUSED_DEC_WARPS);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(acc_full + 8 * i, 1);
+            mbar_init(acc_empty + 8 * i, 16);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_addr(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    // decode table: byte -> [bf16 w0 | bf16 w1 << 16, bf16 w2], 8 copies (two
+    // lanes of a half-warp per copy)
+    {
+        __shared__ int8_t Cs[96];
+        for (int i = threadIdx.x; i < 96; i += THREADS)
+            Cs[i] = p.C[i];
+        __syncthreads();
+        uint2 *t = reinterpret_cast<uint2 *>(smem + FUSED_OFF_LUT);
+        for (int i = threadIdx.x; i < kLutEntries * FUSED_LUT_COPIES; i += THREADS) {
+            const uint32_t e = expanded_entry(Cs, (uint32_t)(i / FUSED_LUT_COPIES));
+            const int w0 = (int8_t)(e & 0xFF), w1 = (int8_t)((e >> 8) & 0xFF), w2 = (int8_t)((e >> 16) & 0xFF);
+            t[i] = make_uint2(bf16_bits_of(w0) | (bf16_bits_of(w1) << 16), bf16_bits_of(w2));
+        }
+    }
+    tc_fence_before();
+    cluster_sync();   // both CTAs' barriers initialised, the pair's TMEM allocated, tables built
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool timed_out = false;
+    pdl_launch_dependents();   // the split-K finish may be scheduled; it waits for this grid
+
+    // decode of K block g (this CTA's half) into the decoded half of stage g % S,
+    // after its packed bytes have landed and the MMAs are done with the stage's
+    // last use; the warp then releases the packed stage and signals the even CTA
+    const uint32_t lut_lane = lut + (uint32_t)((lane & (FUSED_LUT_COPIES - 1)) * 8);
+    const uint32_t full0 = map_to_rank(full, 0);
+    auto decode_block = [&](int g) -> bool {
+        const int ps = g % PS, s = g % S;
+        if (!mbar_wait_bounded(p_full + 8 * ps, (g / PS) & 1) ||
+            (g >= S && !mbar_wait_bounded(empty + 8 * s, ((g / S) - 1) & 1)))
+            return false;
+        decode_tile2<FUSED_LUT_COPIES>(base + FUSED_OFF_P + ps * FUSED_P_BYTES, base + FUSED_OFF_B + s * FUSED_B_BYTES,
+                                      lut_lane, (int)threadIdx.x - 32 * FUSED_DEC_WARP0, FUSED_DECODERS);
+        fence_proxy_async_smem();   // generic writes -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(p_empty + 8 * ps);
+            mbar_arrive_remote(full0 + 8 * s);
+        }
+        return true;
+    };
+
+    if (warp < DRAIN_WARP0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+        if (warp == 0) {
+            // ---- this CTA's activation half of every K block, by bulk tensor
+            // copy, completing on the even CTA's full barrier (which expects both
+            // halves' bytes)
+            pdl_wait();   // the bf16 activation codes come from the kernel before
+            int issued = 0;
+            for (int t = cid; t < total && !timed_out; t += nclusters) {
+                const Tile T = tile_of(t);
+                for (int kb = 0; kb < T.nk; ++kb) {
+                    const int s = issued % S;
+                    if (issued >= S && !warp_wait(empty + 8 * s, ((issued / S) - 1) & 1)) {
+                        timed_out = true;
+                        break;
+                    }
+                    if (rank == 0)
+                        mbar_arrive_expect_tx_elect(full + 8 * s, 2 * A_BYTES);
+                    tma_2d_pair_elect(base + FUSED_OFF_A + s * A_BYTES, &tm_act, (T.kbase + kb) * BK,
+                                      T.m0 + (int)rank * BM, full0 + 8 * s);
+                    ++issued;
+                }
+            }
+            // never leave with copies in flight: the last stages' MMAs (which
+            // needed every copy of both CTAs) have completed
+            for (int v = issued - S < 0 ? 0 : issued - S; v < issued; ++v)
+                if (!warp_wait(empty + 8 * (v % S), (v / S) & 1))
+                    timed_out = true;
+        } else if (warp == 2) {
+            // ---- this CTA's packed half of every K block (packed weights are
+            // never outputs of the kernel before: no grid-dependency wait)
+            int issued = 0;
+            for (int t = cid; t < total && !timed_out; t += nclusters) {
+                const Tile T = tile_of(t);
+                for (int kb = 0; kb < T.nk; ++kb) {
+                    const int s = issued % PS;
+                    if (issued >= PS && !warp_wait(p_empty + 8 * s, ((issued / PS) - 1) & 1)) {
+                        timed_out = true;
+                        break;
+                    }
+                    mbar_arrive_expect_tx_elect(p_full + 8 * s, FUSED_P_BYTES);
+                    tma_2d_elect(base + FUSED_OFF_P + s * FUSED_P_BYTES, &tm_pk, (T.kbase + kb) * BK,
+                                 T.nt * GROUPS + (int)rank * FUSED_GROUPS, p_full + 8 * s);
+                    ++issued;
+                }
+            }
+            for (int v = issued - PS < 0 ? 0 : issued - PS; v < issued; ++v)
+                if (!warp_wait(p_full + 8 * (v % PS), (v / PS) & 1))
+                    timed_out = true;
+        } else if (warp == 1) {
+            if (rank == 0) {
+                // ---- MMA issuer of the pair: the whole warp runs the loop so that
+                // the descriptors stay warp-uniform; one elected lane issues -------
+                int g = 0, gc = 0;
+                const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(FUSED_BN >> 3) << 17) |
+                                       ((uint32_t)(FUSED_BM >> 4) << 24);
+                for (int t = cid; t < total && !timed_out; t += nclusters) {
+                    const Tile T = tile_of(t);
+                    for (int kb = 0; kb < T.nk; ++kb) {
+                        const int s = g % S;
+                        const int c = gc + kb / CHUNK_BLOCKS, kin = kb % CHUNK_BLOCKS;
+                        const uint32_t d = tmem + (uint32_t)((c & 1) * 256);
+                        if ((kin == 0 && c >= 2 && !warp_wait(acc_empty + 8 * (c & 1), ((c >> 1) - 1) & 1)) ||
+                            !warp_wait(full + 8 * s, (g / S) & 1)) {
+                            timed_out = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a = base + FUSED_OFF_A + s * A_BYTES;
+                        const uint32_t b = base + FUSED_OFF_B + s * FUSED_B_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            mma_bf16_pair_elect(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
+                                                (kin | kk) ? 1u : 0u);
+                        mma_commit_pair_elect(empty + 8 * s);
+                        if (kin == CHUNK_BLOCKS - 1 || kb == T.nk - 1)
+                            mma_commit_pair_elect(acc_full + 8 * (c & 1));
+                        ++g;
+                    }
+                    gc += (T.nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
+                }
+                // the tensor core must be done with both CTAs' memory before exit
+                if (g > 0 && !warp_wait(empty + 8 * ((g - 1) % S), ((g - 1) / S) & 1))
+                    timed_out = true;
+            }
+        } else if (warp >= FUSED_DEC_WARP0) {
+            // ---- decode (warps 3-7) -----------------------------------------------
+            int g = 0;
+            for (int t = cid; t < total && !timed_out; t += nclusters) {
+                const int nk = tile_of(t).nk;
+                for (int kb = 0; kb < nk; ++kb, ++g)
+                    if (!decode_block(g)) {
+                        timed_out = true;
+                        break;
+                    }
+            }
+        }
+    } else {
+        // ---- drain this CTA's accumulator rows (warps 8-15), then the epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
+        const int q = warp & 3;
+        const int h = (warp - DRAIN_WARP0) >> 2;   // which 120 of the 240 columns
+        const uint32_t release = rank == 0 ? acc_empty : map_to_rank(acc_empty, 0);
+        int32_t acc[HALF];
+        // fp32 chunk c in TMEM -> int32 registers; then release its buffer
+        auto drain = [&](int c) {
+            tc_fence_after();
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((c & 1) * 256 + h * HALF);
+#pragma unroll
+            for (int gg = 0; gg < HALF / 24; ++gg) {
+                float v[3][8];
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+                    tmem_ld8(ta + (gg * 3 + i) * 8, v[i]);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        acc[(gg * 3 + i) * 8 + j] += __float2int_rn(v[i][j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_remote(release + 8 * (c & 1));
+        };
+        int gc = 0;   // first chunk of the current tile
+        for (int t = cid; t < total && !timed_out; t += nclusters) {
+            const Tile T = tile_of(t);
+            const int nch = (T.nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
+#pragma unroll
+            for (int i = 0; i < HALF; ++i)
+                acc[i] = 0;
+            int cn = gc;   // next chunk to drain
+            for (; cn < gc + nch && !timed_out; ++cn) {
+                if (!mbar_wait_bounded(acc_full + 8 * (cn & 1), (cn >> 1) & 1)) {
+                    timed_out = true;
+                    break;
+                }
+                drain(cn);
+            }
+            gc += nch;
+            const int row = T.m0 + (int)rank * BM + 32 * q + lane;
+            if (!timed_out && row < p.M)
+                store_tile_row(p, T.split, row, T.nt * FUSED_BN + h * HALF, acc);
+        }
+    }
+    if (timed_out)
+        record_timeout(p.status);
+    tc_fence_before();
+    cluster_sync();   // no CTA leaves while its pair may still signal or read it
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+}
+
+}  // namespace tc
+
+// SM-pair tensor-core GEMM on packed weights: act is the bf16 copy of the
+// activation codes [M, K] (in the workspace), part the split-K partials or null.
+cudaError_t launch_prefill_fused(const LinearArgs &a, const __nv_bfloat16 *act, int32_t *part, int nsplit, int kbps,
+                                cudaStream_t stream)
+{
+    using namespace tc;
+    auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder_fn());
+    if (!encode)
+        return cudaErrorNotSupported;
+    const int G = (a.N + 2) / 3;
+    CUtensorMap tm_act, tm_pk;
+    const cuuint32_t es[2] = {1, 1};
+    const cuuint64_t dA[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    const cuuint64_t sA[1] = {(cuuint64_t)a.K * 2};
+    const cuuint32_t boxA[2] = {BK, BM};
+    const cuuint64_t dP[2] = {(cuuint64_t)a.K, (cuuint64_t)G};
+    const cuuint64_t sP[1] = {(cuuint64_t)a.K};
+    const cuuint32_t boxP[2] = {BK, FUSED_GROUPS};
+    if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(act), dA, sA, boxA, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), dP, sP, boxP, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         FUSED_SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    const Params p = make_params(a, nsplit, kbps, part);
+    const long tiles = (long)((a.M + FUSED_BM - 1) / FUSED_BM) * (long)((G + GROUPS - 1) / GROUPS) * nsplit;
+    if (tiles > 0x7FFFFFFFL)
+        return cudaErrorInvalidValue;
+    long pairs = device_sm_count() / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = FUSED_SMEM_BYTES;
+    int fit = 0;   // pairs the GPU can hold at once (not every SM may find a partner)
+    if (cudaOccupancyMaxActiveClusters(&fit, prefill_fused_kernel, &cfg) == cudaSuccess && fit > 0 && fit < pairs)
+        pairs = fit;
+    (void)cudaGetLastError();
+    const long clusters = tiles < pairs ? tiles : pairs;
+    return launch_pdl(prefill_fused_kernel, dim3((unsigned)(2 * clusters)), dim3(THREADS), (size_t)FUSED_SMEM_BYTES,
+                      stream, tm_act, tm_pk, p);
+}
+
+}  // namespace s3d8

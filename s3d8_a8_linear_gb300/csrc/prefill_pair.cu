@@ -46,68 +46,6 @@ static_assert(B_HALF_BYTES % 1024 == 0 && PAIR_OFF_B % 1024 == 0, "swizzled tile
 static_assert(PAIR_SMEM_BYTES + 1024 <= 232448, "shared memory budget");
 static_assert(B_HALF % 8 == 0 && PAIR_BN % 16 == 0 && PAIR_BN <= 256, "M = 256 MMAs need N a multiple of 16");
 
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// shared::cluster address of the same shared-memory offset in CTA `rank`
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Arrive on a barrier of another CTA of the cluster (default release semantics
-// at CTA scope, as for a local arrive; the tensor-core side is ordered by the
-// tcgen05 fences around it).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// Warp-wide pair forms (see the one-SM forms in tcgen05.cuh): the MMA with
-// M = 256 across the pair; the commit arrives on the barrier at offset `bar` in
-// both CTAs; the tensor copy completes on `bar`, which may be the barrier of the
-// other CTA of the pair.
-__device__ __forceinline__ void mma_bf16_pair_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
-{
-    asm volatile(
-        "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
-        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit_pair_elect(uint32_t bar)
-{
-    const uint16_t mask = 0x3;
-    asm volatile(
-        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
-        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}\n" ::"r"(
-            bar),
-        "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_2d_pair_elect(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
-{
-    asm volatile(
-        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
-        "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
-        "{%2, %3}], [%4];\n}\n" ::"r"(dst),
-        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
                         PairParams pp)

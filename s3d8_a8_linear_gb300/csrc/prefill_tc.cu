@@ -8,8 +8,10 @@
 // After each chunk the fp32 accumulator is drained into int32 registers.
 //
 // This file holds the one-SM kernel that decodes packed weight tiles itself
-// (below 384 tokens) and the host side of both tensor-core paths; from 384
-// tokens the weights are expanded to bf16 first and prefill_pair.cu runs.
+// (below 384 tokens) and the host side of the three tensor-core kernels: from
+// 384 tokens the SM-pair kernel that decodes the packed tiles itself
+// (prefill_fused.cu), and from 1024 tokens the SM-pair kernel on weights
+// expanded to bf16 once per call (prefill_pair.cu).
 //
 // Tile: 128 tokens (MMA M) x 240 output channels (MMA N; 80 whole packed groups)
 // per CTA, K in blocks of 64.  Sixteen warps in four warpgroups:
@@ -448,13 +450,15 @@ __global__ void finalize_kernel(const int32_t *__restrict__ part, int nsplit, in
 
 // K split of the tensor-core GEMM when its output tiles alone cannot fill the
 // GPU: the number of 64-column blocks per split that minimises
-// waves x (blocks per CTA + a per-CTA fixed cost of about 4 blocks).  `pairs`
-// names the kernel the plan is for: the SM-pair GEMM (256 x 256 tiles on two
-// SMs) or the one-SM GEMM (128 x 240 tiles).
-static void tc_plan(int M, int N, int K, int sms, bool pairs, int &nsplit, int &kb_per_split)
+// waves x (blocks per CTA + a per-CTA fixed cost of about 4 blocks).  CTAs per
+// K range: 128 x 240 tiles on one SM, 256 x 240 tiles on two (fused), or
+// 256 x 256 tiles on two (expanded weights).
+static void tc_plan(int M, int N, int K, int sms, int kind, int &nsplit, int &kb_per_split)
 {
-    const long tiles = pairs ? 2L * ((M + 255) / 256) * ((N + 255) / 256)
-                             : (long)((M + tc::BM - 1) / tc::BM) * (((N + 2) / 3 + tc::GROUPS - 1) / tc::GROUPS);
+    const long gtiles = ((N + 2) / 3 + tc::GROUPS - 1) / tc::GROUPS;
+    const long tiles = kind == kTcPairExpanded ? 2L * ((M + 255) / 256) * ((N + 255) / 256)
+                       : kind == kTcPairFused  ? 2L * ((M + 255) / 256) * gtiles
+                                               : (long)((M + tc::BM - 1) / tc::BM) * gtiles;
     const int nk = (K + tc::BK - 1) / tc::BK;
     nsplit = 1;
     kb_per_split = nk;
@@ -479,27 +483,30 @@ static size_t align256(size_t v)
     return (v + 255) & ~(size_t)255;
 }
 
-// From this many tokens the weights are expanded to bf16 once per call and the
-// SM-pair GEMM (prefill_pair.cu) reads them by bulk tensor copy: the expansion
-// then costs less than re-decoding every weight tile once per 128-token tile
-// inside the GEMM, the one-SM kernel here.
-constexpr int kPredecodeMinM = 384;
+// The kernel for M tokens.  From 384 tokens the SM pairs' 256-token tiles
+// decode each packed weight tile once per 256 tokens instead of once per 128;
+// from 1024 tokens expanding the weights to bf16 once per call costs less than
+// decoding them once per 256-token tile inside the GEMM (measured on GB300 at
+// 512 and 2048 tokens on the 11B shapes: the fused kernel is 1.4-1.6x faster
+// at 512, the expanded one 1.4-1.5x faster at 2048).
+constexpr int kPairsMinM = 384;
+constexpr int kExpandMinM = 1024;
 
-bool prefill_predecode(int M)
+int prefill_kind(int M)
 {
-    return M >= kPredecodeMinM;
+    return M >= kExpandMinM ? kTcPairExpanded : M >= kPairsMinM ? kTcPairFused : kTcOneSm;
 }
 
-// `pre` selects the kernel: the SM-pair GEMM on pre-expanded weights, or the
-// one-SM GEMM that decodes packed tiles itself (at any M).
-size_t prefill_workspace_bytes(int M, int N, int K, bool pre)
+// Workspace: the bf16 copy of the activation codes, then the split-K partials,
+// then (expanded kind only) the bf16 weights [N, K].
+size_t prefill_workspace_bytes(int M, int N, int K, int kind)
 {
     int nsplit, kbps;
-    tc_plan(M, N, K, device_sm_count(), pre, nsplit, kbps);
+    tc_plan(M, N, K, device_sm_count(), kind, nsplit, kbps);
     size_t bytes = align256((size_t)M * K * 2) + 256;
     if (nsplit > 1)
         bytes += align256((size_t)nsplit * M * N * 4);
-    if (pre)
+    if (kind == kTcPairExpanded)
         bytes += align256((size_t)N * K * 2);
     return bytes;
 }
@@ -538,13 +545,14 @@ void *tensor_map_encoder_fn()
     return f;
 }
 
-cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream)
+cudaError_t launch_prefill_tc(const LinearArgs &a, int kind, cudaStream_t stream)
 {
     using namespace tc;
-    if (!a.ws || a.ws_bytes < prefill_workspace_bytes(a.M, a.N, a.K, pre))
+    if (!a.ws || a.ws_bytes < prefill_workspace_bytes(a.M, a.N, a.K, kind))
         return cudaErrorInvalidValue;
+    const bool pre = kind == kTcPairExpanded;
     int nsplit, kbps;
-    tc_plan(a.M, a.N, a.K, device_sm_count(), pre, nsplit, kbps);
+    tc_plan(a.M, a.N, a.K, device_sm_count(), kind, nsplit, kbps);
     auto encode = tensor_map_encoder();
     if (!encode)
         return cudaErrorNotSupported;
@@ -573,9 +581,10 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, bool pre, cudaStream_t stream
             return e;
     }
 
-    if (pre) {
-        // pre-expanded weights: the SM-pair kernel (256-token tiles on two SMs)
-        e = launch_prefill_pair(a, act, wdec, part, nsplit, kbps, stream);
+    if (kind != kTcOneSm) {
+        // the SM-pair kernels (256-token tiles on two SMs)
+        e = pre ? launch_prefill_pair(a, act, wdec, part, nsplit, kbps, stream)
+                : launch_prefill_fused(a, act, part, nsplit, kbps, stream);
         if (e != cudaSuccess || nsplit == 1)
             return e;
         return launch_splitk_finalize(part, nsplit, a, stream);

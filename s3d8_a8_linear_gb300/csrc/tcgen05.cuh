@@ -108,6 +108,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
 }
 
+// Bounded wait taken for the whole warp by lane 0 alone: one phase test per
+// round instead of 32, which keeps the barrier unit free for the other warps'
+// waits and arrivals.  __syncwarp orders the other lanes' later accesses after
+// lane 0's acquire.  All lanes must call it together.
+__device__ __forceinline__ bool warp_wait_one(uint32_t bar, uint32_t parity)
+{
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0)
+        ok = mbar_wait_bounded(bar, parity) ? 1 : 0;
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -134,13 +147,16 @@ __device__ __forceinline__ uint32_t bf16_bits_of(int v)
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn((float)v));
 }
 
-// Expands this thread's share of a 80 x 64 packed tile (units u = t, t + nthr, ...;
+// Expands this thread's share of an NG x 64 packed tile (units u = t, t + nthr, ...;
 // one unit = one group's 8 bytes at one 16-byte column chunk) into the
 // 128-byte-swizzled K-major bf16 tile: element (n, k) at n * 128 +
 // ((k / 8) ^ (n % 8)) * 16 + (k % 8) * 2.
+// The table holds COPIES copies of each 8-byte entry side by side (entry b of
+// copy c at 8 (COPIES b + c)); `lut_lane` = table + 8 (lane % COPIES).
+template <int NG = GROUPS, int COPIES = LUT_COPIES>
 __device__ __forceinline__ void decode_tile(uint32_t ptile, uint32_t btile, uint32_t lut_lane, int t, int nthr)
 {
-    for (int u = t; u < GROUPS * 8; u += nthr) {
+    for (int u = t; u < NG * 8; u += nthr) {
         const int gl = u >> 3, j = u & 7;   // group, 16-byte chunk (8 k)
         uint32_t pk0, pk1;
         asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(pk0), "=r"(pk1) : "r"(ptile + gl * 64 + j * 8));
@@ -150,7 +166,7 @@ __device__ __forceinline__ void decode_tile(uint32_t ptile, uint32_t btile, uint
             const uint32_t byte = ((i < 4 ? pk0 : pk1) >> (8 * (i & 3))) & 0xFFu;
             asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
                          : "=r"(e[i].x), "=r"(e[i].y)
-                         : "r"(lut_lane + byte * (LUT_COPIES * 8)));
+                         : "r"(lut_lane + byte * (COPIES * 8)));
         }
         uint32_t w[3][4];
 #pragma unroll
@@ -163,6 +179,53 @@ __device__ __forceinline__ void decode_tile(uint32_t ptile, uint32_t btile, uint
         for (int d = 0; d < 3; ++d) {
             const int n = 3 * gl + d;
             const uint32_t addr = btile + n * 128 + (((uint32_t)j ^ (uint32_t)(n & 7)) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[d][0]), "r"(w[d][1]),
+                         "r"(w[d][2]), "r"(w[d][3])
+                         : "memory");
+        }
+    }
+}
+
+// As decode_tile for a 40 x 64 packed tile (320 units) and nthr = 160 threads:
+// each thread expands units t and t + 160 with their lookups interleaved, so that
+// the two table-load chains overlap.
+template <int COPIES>
+__device__ __forceinline__ void decode_tile2(uint32_t ptile, uint32_t btile, uint32_t lut_lane, int t, int nthr)
+{
+    uint32_t pk[2][2];
+    int gl[2], j[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int u = t + h * nthr;
+        gl[h] = u >> 3;
+        j[h] = u & 7;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                     : "=r"(pk[h][0]), "=r"(pk[h][1])
+                     : "r"(ptile + gl[h] * 64 + j[h] * 8));
+    }
+    uint2 e[2][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t byte = (pk[h][i >> 2] >> (8 * (i & 3))) & 0xFFu;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(e[h][i].x), "=r"(e[h][i].y)
+                         : "r"(lut_lane + byte * (COPIES * 8)));
+        }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t w[3][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            w[0][q] = prmt(e[h][2 * q].x, e[h][2 * q + 1].x, 0x5410);
+            w[1][q] = prmt(e[h][2 * q].x, e[h][2 * q + 1].x, 0x7632);
+            w[2][q] = prmt(e[h][2 * q].y, e[h][2 * q + 1].y, 0x5410);
+        }
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const int n = 3 * gl[h] + d;
+            const uint32_t addr = btile + n * 128 + (((uint32_t)j[h] ^ (uint32_t)(n & 7)) << 4);
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[d][0]), "r"(w[d][1]),
                          "r"(w[d][2]), "r"(w[d][3])
                          : "memory");
@@ -264,6 +327,71 @@ inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// ---- SM-pair (cluster of two CTAs) building blocks, shared by the two pair
+// kernels (prefill_pair.cu, prefill_fused.cu) ---------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on a barrier of another CTA of the cluster (default release semantics
+// at CTA scope, as for a local arrive; the tensor-core side is ordered by the
+// tcgen05 fences around it).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Warp-wide pair forms (see the one-SM forms in tcgen05.cuh): the MMA with
+// M = 256 across the pair; the commit arrives on the barrier at offset `bar` in
+// both CTAs; the tensor copy completes on `bar`, which may be the barrier of the
+// other CTA of the pair.
+__device__ __forceinline__ void mma_bf16_pair_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_pair_elect(uint32_t bar)
+{
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n}\n" ::"r"(
+            bar),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_2d_pair_elect(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];\n}\n" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 
 inline Params make_params(const LinearArgs &a, int nsplit, int kbps, int32_t *part)

@@ -337,19 +337,22 @@ def test_zero_activation_row_gives_zero(algo):
 
 TC_TILES = [(128, 240, 64), (129, 241, 1040), (300, 722, 2112), (256, 480, 3072),
             (1, 3, 16), (17, 1201, 1024),
-            # from 384 tokens the weights are expanded to bf16 first (both operands by
-            # TMA) and two SMs share each 256-token tile: the odd SM's rows past M,
-            # partial pair tiles, one K block, split and unsplit K
+            # from 384 tokens two SMs share each 256-token tile (240 channels, each
+            # SM decoding its 40 packed rows; from 1024 tokens 256 channels of
+            # weights expanded to bf16 first): the odd SM's rows past M, partial
+            # pair tiles, one K block, split and unsplit K, both sides of 1024
             (384, 241, 1040), (520, 722, 2112), (768, 480, 3072), (400, 3, 16),
-            (1000, 1201, 4096), (2048, 96, 14336), (640, 257, 1024), (512, 512, 2048)]
+            (1000, 1201, 4096), (2048, 96, 14336), (640, 257, 1024), (512, 512, 2048),
+            (1023, 722, 2112), (1024, 241, 1040), (1300, 3, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", TC_TILES)
 def test_tc_tiles_and_tails(M, N, K):
     """Tensor-core path in full against the oracle: whole and ragged 128-token and
     240-channel tiles, K ragged against the 64-column block and the 1024-column
-    exact chunk, with the weight tiles decoded inside the GEMM (small M) and
-    pre-expanded to bf16 (M >= 384)."""
+    exact chunk, on one SM per tile (small M) and on SM pairs (M >= 384:
+    decoding the weight tiles inside the GEMM below 1024 tokens, on weights
+    expanded to bf16 first from 1024)."""
     C, packed, cs, x = rand_case(M, N, K, seed=M * 7919 + N * 31 + K)
     xq, xs = oracle.quantize_act(x)
     ref, acc_o = oracle.linear(packed, C, cs, xq, xs, N)
@@ -419,10 +422,10 @@ def test_tmem_rejects_more_than_64_tokens():
     assert e.value.status == -3
 
 
-@pytest.mark.parametrize("M", [130, 390])
+@pytest.mark.parametrize("M", [130, 390, 1100])
 def test_tc_unaligned_outputs(M):
     """Output views that are only 2- (bf16) or 4-byte (int32) aligned take the
-    scalar store path and still match (one-SM and SM-pair kernels)."""
+    scalar store path and still match (one-SM and both SM-pair kernels)."""
     N, K = 480, 256
     C, packed, cs, x = rand_case(M, N, K, seed=5)
     xq, xs = oracle.quantize_act(x)
@@ -438,12 +441,12 @@ def test_tc_unaligned_outputs(M):
     np.testing.assert_array_equal(to_np(acc).astype(np.int64), acc_o)
 
 
-@pytest.mark.parametrize("M", [200, 400])
+@pytest.mark.parametrize("M", [200, 400, 1030])
 def test_tc_adversarial_chunk_sums(M):
     """Every product +16129 over 1024 columns is the largest partial sum an exact
     fp32 chunk holds (16,516,096 < 2^24); two chunks in a row must still add
-    exactly in int32 (K = 2048 + 1024 + 16).  One SM per tile (200 tokens) and
-    SM pairs on pre-expanded weights (400)."""
+    exactly in int32 (K = 2048 + 1024 + 16).  One SM per tile (200 tokens), SM
+    pairs decoding packed tiles (400) and SM pairs on expanded weights (1030)."""
     C = np.full((32, 3), 127, np.int8)
     N, K = 243, 3088
     packed = np.full((si.groups(N), K), oracle.pack_byte(3, 0, 0, 0), np.uint8)
