@@ -58,10 +58,7 @@ constexpr int MAX_LST = 8;                       // ring stages (4 when the chun
 constexpr int LUT_BYTES = kLutEntries * 32 * 4;  // 32 KiB, one copy per lane
 
 constexpr int TEAMS = 3;
-constexpr int NBARS = 3 * MAX_LST + TEAMS + 2;
-// Shared memory requested by the 8-stage form, which carves its ring around a
-// 64 KiB-aligned wide table (see tmem_a_kernel).
-constexpr int WIDE_DYN_SMEM = 232448 - 4096;
+constexpr int NBARS = 2 * MAX_LST + TEAMS + 2;
 constexpr int THREADS = 512;
 constexpr int DEC_WARP0 = 4;
 constexpr int DEC_WARPS = TEAMS * 4;
@@ -187,10 +184,6 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b)
 // channels' fp16 pairs: a[d][c] holds the weights of columns 2c and 2c + 1.
 // The packed tile row `row` (64 bytes) sits at tile + 64 row with its 16-byte
 // units permuted by the 64-byte swizzle (unit u at u ^ ((row >> 1) & 3)).
-// WIDE: the table has a 256-byte entry stride in a 64 KiB-aligned window, and
-// `lut_lane` = window | 4 lane, so that one byte permute forms each lookup
-// address; otherwise entries are 128 bytes apart (lut_lane = table + 4 lane).
-template <bool WIDE>
 __device__ __forceinline__ void decode_step(uint32_t tile, int row, int kk, uint32_t lut_lane,
                                             uint32_t (&a)[3][8])
 {
@@ -199,12 +192,8 @@ __device__ __forceinline__ void decode_step(uint32_t tile, int row, int kk, uint
     uint32_t L[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        if (WIDE) {
-            L[i] = lds_u32_nv(prmt(w[i >> 2], lut_lane, 0x7604u | ((uint32_t)(i & 3) << 4)));
-        } else {
-            const uint32_t byte = prmt(w[i >> 2], 0u, 0x4440u | (uint32_t)(i & 3));
-            L[i] = lds_u32_nv(mad_lo_u32(byte, 128u, lut_lane));
-        }
+        const uint32_t byte = prmt(w[i >> 2], 0u, 0x4440u | (uint32_t)(i & 3));
+        L[i] = lds_u32_nv(mad_lo_u32(byte, 128u, lut_lane));
     }
     constexpr uint32_t kBias = 0x64806480u;   // fp16 (1152, 1152)
 #pragma unroll
@@ -260,39 +249,19 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *smem = smem_raw + (base - raw);
-    // shared memory.  4-stage form: ring, int32 chunk sums, compact table,
-    // barriers.  8-stage form (WIDE): the wide table (64 KiB) sits in the first
-    // 64 KiB-aligned window of the dynamic shared memory, the ring stages below
-    // it as far as they fit and the rest above it, then the barriers.
+    // shared memory: ring, int32 chunk sums (s_smem only), table, barriers
     constexpr bool SSUM = LST != MAX_LST;   // the 4-stage form keeps the chunk sums in shared memory
-    constexpr bool WIDE = !SSUM;
     const int off_s = LST * STAGE;
-    uint32_t lut, bars, hi = 0;
-    int n_below = LST;
-    if (WIDE) {
-        lut = wide_lut_window(raw);
-        n_below = (int)min((lut - base) / (uint32_t)STAGE, (uint32_t)LST);
-        hi = lut + kWideLutBytes;
-        bars = hi + (uint32_t)((LST - n_below) * STAGE);
-        if (bars + NBARS * 8 + 16 > raw + (uint32_t)WIDE_DYN_SMEM) {   // the host requests enough
-            if (threadIdx.x == 0 && p.status)
-                atomicExch(p.status, -3);
-            return;
-        }
-    } else {
-        lut = base + (uint32_t)(off_s + 3 * p.nt * ROWS * 4);
-        bars = lut + (uint32_t)LUT_BYTES;
-    }
-    auto stage_at = [&](int s) -> uint32_t {
-        return s < n_below ? base + (uint32_t)(s * STAGE) : hi + (uint32_t)((s - n_below) * STAGE);
-    };
+    const int off_lut = off_s + (SSUM ? 3 * p.nt * ROWS * 4 : 0);
+    const int off_bars = off_lut + LUT_BYTES;
+    const uint32_t lut = base + (uint32_t)off_lut;
+    const uint32_t bars = base + (uint32_t)off_bars;
     int32_t *ssum = reinterpret_cast<int32_t *>(smem + off_s);   // [channel][token][row]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + (bars + NBARS * 8 - raw));
-    // full: a stage's packed tile has landed; full_act: its fp16 codes tile has
-    // landed; empty: the stage is consumed; a_full: each team's A stage is
-    // written; acc_full: a chunk's sums are in D; acc_empty: D has been drained
-    const uint32_t full = bars, empty = full + 8 * MAX_LST, full_act = empty + 8 * MAX_LST;
-    const uint32_t a_full = full_act + 8 * MAX_LST;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + off_bars + NBARS * 8);
+    // full/empty: the ring's stages; a_full: each team's A stage is written;
+    // acc_full: a chunk's sums are in D; acc_empty: D has been drained
+    const uint32_t full = bars, empty = full + 8 * MAX_LST;
+    const uint32_t a_full = empty + 8 * MAX_LST;
     const uint32_t acc_full = a_full + 8 * TEAMS, acc_empty = acc_full + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nkb = (p.K + BK - 1) / BK;
@@ -300,7 +269,6 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < LST; ++s) {
             mbar_init(full + 8 * s, 1);
-            mbar_init(full_act + 8 * s, 1);
             mbar_init(empty + 8 * s, 4 + 3);   // the block's team, and the three MMA warps
         }
         for (int t = 0; t < TEAMS; ++t) {
@@ -312,9 +280,8 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     }
     // The copy warp starts the first stages' packed tiles at once, while the
     // table is built: packed weights are never outputs of the kernel before
-    // this one (the codes tiles follow after the grid dependency, on their own
-    // barriers, so that decoding does not wait for them).
-    const uint32_t tx_act = (uint32_t)p.nt * BK * 2;
+    // this one (the codes tiles follow after the grid dependency).
+    const uint32_t tx = (uint32_t)PK_BYTES + (uint32_t)p.nt * BK * 2;
     int pre = 0;
     // packed bytes are read once: evict them first, keeping the codes tiles
     // (read by every row tile of a K range) in L2
@@ -322,8 +289,9 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     if (warp == 0) {
         __syncwarp();   // lane 0's barrier initialisation
         for (Walk w = walk_begin(p, nkb); w.valid && pre < LST; walk_next(p, nkb, w), ++pre) {
-            tc::mbar_arrive_expect_tx_elect(full + 8 * pre, (uint32_t)PK_BYTES);
-            tma_2d_hint_elect(stage_at(pre), &tm_pk, (w.kbase + w.kb) * BK, w.rt * ROWS, full + 8 * pre, wpol);
+            const uint32_t st = base + (uint32_t)(pre * STAGE);
+            tc::mbar_arrive_expect_tx_elect(full + 8 * pre, tx);
+            tma_2d_hint_elect(st, &tm_pk, (w.kbase + w.kb) * BK, w.rt * ROWS, full + 8 * pre, wpol);
         }
     }
     if (warp == 1) {
@@ -339,10 +307,9 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
         for (int i = threadIdx.x; i < 96; i += THREADS)
             Cs[i] = p.C[i];
         __syncthreads();
-        const uint32_t stride = WIDE ? 256u : 128u;
         for (int i = threadIdx.x; i < kLutEntries * 8; i += THREADS) {
             const uint32_t e = (expanded_entry(Cs, (uint32_t)(i >> 3)) ^ 0x00808080u) | 0x64000000u;
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(lut + (uint32_t)(i >> 3) * stride +
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(lut + (uint32_t)(i >> 3) * 128u +
                                                                            (uint32_t)(i & 7) * 16u),
                          "r"(e)
                          : "memory");
@@ -365,24 +332,19 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                 timed_out = true;
                 break;
             }
-            const uint32_t st = stage_at(s);
+            const uint32_t st = base + (uint32_t)(s * STAGE);
             const int x = (w.kbase + w.kb) * BK;
             if (w.gkb >= pre) {
-                tc::mbar_arrive_expect_tx_elect(full + 8 * s, (uint32_t)PK_BYTES);
+                tc::mbar_arrive_expect_tx_elect(full + 8 * s, tx);
                 tma_2d_hint_elect(st, &tm_pk, x, w.rt * ROWS, full + 8 * s, wpol);
             }
-            tc::mbar_arrive_expect_tx_elect(full_act + 8 * s, tx_act);
-            tc::tma_2d_elect(st + PK_BYTES, &tm_act, x, 0, full_act + 8 * s);
+            tc::tma_2d_elect(st + PK_BYTES, &tm_act, x, 0, full + 8 * s);
         }
-        // never leave with copies in flight (only possible after a timeout):
-        // the packed tiles of the first `pre` stages were issued before the loop
-        const int top = issued > pre ? issued : pre;
-        for (int v = top - LST < 0 ? 0 : top - LST; v < top; ++v) {
+        // never leave with copies in flight (only possible after a timeout)
+        const int hi = issued > pre ? issued : pre;
+        for (int v = hi - LST < 0 ? 0 : hi - LST; v < hi; ++v)
             if (!tc::warp_wait(full + 8 * (v % LST), (v / LST) & 1))
                 timed_out = true;
-            if (v < issued && !tc::warp_wait(full_act + 8 * (v % LST), (v / LST) & 1))
-                timed_out = true;
-        }
     } else if (warp >= 1 && warp <= 3) {
         // ---- MMA issuers: warp 1 + d issues channel d's MMAs into D_d (whole
         // warp, one elected lane); the three accumulators are independent, so the
@@ -395,13 +357,13 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
             // (no wait for the ring stage here: the team signals a_full only after
             // it has seen the stage's bulk copies complete)
             if ((first && w.gchunk >= 1 && !tc::warp_wait(acc_empty, (w.gchunk - 1) & 1)) ||
-                !tc::warp_wait(a_full + 8 * t, use & 1) || !tc::warp_wait(full_act + 8 * s, (w.gkb / LST) & 1)) {
+                !tc::warp_wait(a_full + 8 * t, use & 1)) {
                 timed_out = true;
                 break;
             }
             tc::tc_fence_after();
             const uint32_t acol = tmem + (uint32_t)(p.a_col + t * 4 * A_STAGE_COLS);
-            const uint32_t act = stage_at(s) + (uint32_t)PK_BYTES;
+            const uint32_t act = base + (uint32_t)(s * STAGE + PK_BYTES);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_f16_tmem_a_elect(tmem + (uint32_t)(d * p.nt), acol + (uint32_t)(kk * A_STAGE_COLS + 8 * d),
@@ -416,7 +378,7 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
         // chunk (or at the end)
         const int t = (warp - DEC_WARP0) / 4, q = warp & 3;
         const int row = 32 * q + lane;
-        const uint32_t lut_lane = WIDE ? (lut | ((uint32_t)lane << 2)) : lut + (uint32_t)lane * 4u;
+        const uint32_t lut_lane = lut + (uint32_t)lane * 4u;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const uint32_t acol = tmem + lane_off + (uint32_t)(p.a_col + t * 4 * A_STAGE_COLS);
         Walk w = walk_begin(p, nkb);
@@ -494,11 +456,11 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                 timed_out = true;
                 break;
             }
-            const uint32_t pk = stage_at(s);
+            const uint32_t pk = base + (uint32_t)(s * STAGE);
 #pragma unroll 1
             for (int kk = 0; kk < 4; ++kk) {
                 uint32_t a[3][8];
-                decode_step<WIDE>(pk, row, kk, lut_lane, a);
+                decode_step(pk, row, kk, lut_lane, a);
 #pragma unroll
                 for (int d = 0; d < 3; ++d)
                     tmem_st8(acol + (uint32_t)(kk * A_STAGE_COLS + 8 * d), a[d]);
@@ -614,8 +576,7 @@ cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream)
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    // 8-stage form: at worst 1 KiB of alignment, the table window and the ring
-    static_assert(1024 + 0x10000 + MAX_LST * STAGE + NBARS * 8 + 16 <= WIDE_DYN_SMEM, "shared memory");
+    static_assert(1024 + MAX_LST * STAGE + LUT_BYTES + NBARS * 8 + 16 <= 232448 - 1024, "shared memory");
     static_assert(1024 + 4 * STAGE + 3 * MAX_NT * ROWS * 4 + LUT_BYTES + NBARS * 8 + 16 <= 232448 - 1024,
                   "shared memory");
     Params p;
@@ -641,7 +602,8 @@ cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream)
     p.status = a.status;
     const long tiles = (long)rtiles * nsplit;
     const long ctas = tiles < sms ? tiles : sms;   // persistent CTAs walk the tiles
-    const int need = p.s_smem ? 1024 + 4 * STAGE + 3 * nt * ROWS * 4 + LUT_BYTES + NBARS * 8 + 16 : WIDE_DYN_SMEM;
+    const int lst = p.s_smem ? 4 : MAX_LST;
+    const int need = 1024 + lst * STAGE + (p.s_smem ? 3 * nt * ROWS * 4 : 0) + LUT_BYTES + NBARS * 8 + 16;
     auto kernel = p.s_smem ? tmem_a_kernel<4> : tmem_a_kernel<MAX_LST>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
     if (e != cudaSuccess)
