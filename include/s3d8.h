@@ -65,12 +65,13 @@ typedef enum {
 
 /* Algorithm choice for s3d8_linear_ex.  AUTO picks by shape: GEMV up to 4
  * tokens (up to 8 when K > 8192); TMEM for 5..32 tokens otherwise, and up to 64
- * tokens while its tiles fit in one wave on the device; TC otherwise.  SKINNY
- * runs only on request. */
+ * tokens while its tiles fit in one wave on the device; TC otherwise.  The value
+ * 2 (a register-fragment mma.sync path, slower than TMEM at every size it took)
+ * is retired and stays reserved: it returns S3D8_ERR_UNSUPPORTED. */
 typedef enum {
     S3D8_ALGO_AUTO = 0,
     S3D8_ALGO_GEMV = 1,    /* CUDA-core table decode + dp4a; bulk-copy rings up to 8 tokens      */
-    S3D8_ALGO_SKINNY = 2,  /* table decode into mma.sync bf16 register fragments, 1..32 tokens   */
+    S3D8_ALGO_SKINNY = 2,  /* retired: S3D8_ERR_UNSUPPORTED                                      */
     S3D8_ALGO_TC = 3,      /* tcgen05 bf16 tensor-core GEMM with exact chunked int32 sums       */
     S3D8_ALGO_TMEM = 4     /* tcgen05 fp16 GEMM, weights decoded into tensor memory, 1..64 tokens */
 } s3d8_algo;

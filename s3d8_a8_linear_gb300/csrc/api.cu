@@ -230,8 +230,7 @@ int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t
 // bulk-copy dp4a GEMV up to 4 tokens, and up to 8 on rows longer than 8192
 // columns; the tcgen05 GEMM with the weights decoded into tensor memory for
 // 5..32 tokens otherwise, and up to 64 while its 128-row tiles fit in one wave;
-// the tcgen05 GEMM on shared-memory tiles otherwise.  (The register-fragment mma.sync path is slower than the tensor-
-// memory path at every size it takes and runs only on request.)
+// the tcgen05 GEMM on shared-memory tiles otherwise.
 static int resolve_algo(int64_t M, int64_t N, int64_t K, int algo)
 {
     if (algo != S3D8_ALGO_AUTO)
@@ -250,8 +249,6 @@ size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo)
     const int r = resolve_algo(M, N, K, algo);
     if (r == S3D8_ALGO_TC)
         return prefill_workspace_bytes((int)M, (int)N, (int)K, prefill_kind((int)M));
-    if (r == S3D8_ALGO_SKINNY && skinny_supported((int)M))
-        return skinny_workspace_bytes((int)M, (int)N, (int)K);
     if (r == S3D8_ALGO_TMEM && tmem_supported((int)M))
         return tmem_workspace_bytes((int)M, (int)N, (int)K);
     return 0;
@@ -288,7 +285,7 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     if (need > 0 && (!workspace || workspace_bytes < need))
         return S3D8_ERR_WORKSPACE;
     algo = resolve_algo(M, N, K, algo);
-    if (algo == S3D8_ALGO_SKINNY && !skinny_supported((int)M))
+    if (algo == S3D8_ALGO_SKINNY)   // retired: slower than TMEM at every size it took
         return S3D8_ERR_UNSUPPORTED;
     if (algo == S3D8_ALGO_TMEM && !tmem_supported((int)M))
         return S3D8_ERR_UNSUPPORTED;
@@ -310,8 +307,6 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     if (algo == S3D8_ALGO_TC)
         return cuda_status(launch_prefill_tc(a, prefill_kind(a.M), strm));
-    if (algo == S3D8_ALGO_SKINNY)
-        return cuda_status(launch_skinny(a, strm));
     if (algo == S3D8_ALGO_TMEM)
         return cuda_status(launch_tmem(a, strm));
     if (gemv_tma_supported(a.M, a.K))

@@ -82,13 +82,9 @@ cudaError_t launch_prefill_pair(const LinearArgs &a, const __nv_bfloat16 *act, c
                                 int32_t *part, int nsplit, int kbps, cudaStream_t stream);
 cudaError_t launch_prefill_fused(const LinearArgs &a, const __nv_bfloat16 *act, int32_t *part, int nsplit, int kbps,
                                  cudaStream_t stream);
-// Split-K finish shared by the tensor-core and skinny paths: sums int32 partials
+// Split-K finish shared by the tensor-core paths: sums int32 partials
 // [nsplit][M][N] into a.out (epilogue) or a.acc.
 cudaError_t launch_splitk_finalize(const int32_t *part, int nsplit, const LinearArgs &a, cudaStream_t stream);
-// mma.sync path for a few tokens (1..32), weights decoded into register fragments.
-bool skinny_supported(int M);
-size_t skinny_workspace_bytes(int M, int N, int K);
-cudaError_t launch_skinny(const LinearArgs &a, cudaStream_t stream);
 // tcgen05 GEMM with the weights decoded into tensor memory (decode_tmem.cu):
 // 1..64 tokens.
 bool tmem_supported(int M);

@@ -17,8 +17,8 @@ from gpu_util import (assert_out_close, bf16_bits, bf16_to_f64, dev, f32, guarde
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = [s3d8.ALGO_GEMV, s3d8.ALGO_SKINNY, s3d8.ALGO_TC, s3d8.ALGO_TMEM]
-MAX_M = {s3d8.ALGO_SKINNY: 32, s3d8.ALGO_TMEM: 64}   # token limits of the bounded algorithms
+ALGOS = [s3d8.ALGO_GEMV, s3d8.ALGO_TC, s3d8.ALGO_TMEM]
+MAX_M = {s3d8.ALGO_TMEM: 64}   # token limits of the bounded algorithms
 ALGO_IDS = {s3d8.ALGO_AUTO: "auto", s3d8.ALGO_GEMV: "gemv", s3d8.ALGO_SKINNY: "skinny",
             s3d8.ALGO_TC: "tc", s3d8.ALGO_TMEM: "tmem"}
 
@@ -364,28 +364,10 @@ def test_tc_tiles_and_tails(M, N, K):
     assert_out_close(bf16_to_f64(out), ref)
 
 
-SKINNY_CASES = [(5, 241, 1040), (16, 722, 2112), (17, 1201, 3088), (32, 96, 256), (24, 480, 14336),
-                (1, 4, 16), (9, 3000, 256)]
-
-
-@pytest.mark.parametrize("M,N,K", SKINNY_CASES)
-def test_skinny_in_full(M, N, K):
-    """The register-fragment mma.sync path in full against the oracle: one and two
-    token tiles, ragged 128-row CTA ranges and 8-row warp blocks, K ragged against
-    the 256-column ring stage, split and unsplit K."""
-    C, packed, cs, x = rand_case(M, N, K, seed=M * 131 + N * 7 + K)
-    xq, xs = oracle.quantize_act(x)
-    ref, acc_o = oracle.linear(packed, C, cs, xq, xs, N)
-    np.testing.assert_array_equal(gpu_acc(C, packed, xq, N, s3d8.ALGO_SKINNY), acc_o)
-    out, check = guarded((M, N), torch.bfloat16, 3.0, pad=65)
-    s3d8.linear(u8(packed), i8(C), bf16_bits(cs), i8(xq), f32(xs), N, out=out, algo=s3d8.ALGO_SKINNY)
-    torch.cuda.synchronize()
-    check()
-    assert_out_close(bf16_to_f64(out), ref)
-
-
-def test_skinny_rejects_more_than_32_tokens():
-    C, packed, cs, x = rand_case(33, 9, 64, seed=9)
+def test_retired_algorithm_value_is_rejected():
+    """Algorithm value 2 (the retired register-fragment path) returns
+    S3D8_ERR_UNSUPPORTED before any launch."""
+    C, packed, cs, x = rand_case(16, 9, 64, seed=9)
     xq, xs = oracle.quantize_act(x)
     with pytest.raises(s3d8.S3D8Error) as e:
         gpu_acc(C, packed, xq, 9, s3d8.ALGO_SKINNY)
