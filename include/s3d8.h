@@ -60,7 +60,8 @@ typedef enum {
     S3D8_ERR_UNSUPPORTED = -3, /* algorithm not available for this shape/device   */
     S3D8_ERR_CUDA = -4,        /* a CUDA call or kernel launch failed             */
     S3D8_ERR_TIMEOUT = -5,     /* a bounded device-side wait ran out (sticky)     */
-    S3D8_ERR_WORKSPACE = -6    /* workspace missing or smaller than required      */
+    S3D8_ERR_WORKSPACE = -6,   /* workspace missing or smaller than required      */
+    S3D8_ERR_BOUNDS = -7       /* debug build only: an in-kernel bounds check failed (sticky) */
 } s3d8_status;
 
 /* Algorithm choice for s3d8_linear_ex.  AUTO picks by shape: GEMV up to 4

@@ -29,6 +29,7 @@ STATUS = {
     -4: "CUDA error",
     -5: "timeout",
     -6: "workspace",
+    -7: "bounds check failed (debug build)",
 }
 
 _lib = None
@@ -51,8 +52,13 @@ class S3D8Error(RuntimeError):
         self.status = status
 
 
+def _debug_variant() -> bool:
+    """S3D8_LIBRARY=debug selects the build with in-kernel bounds checks."""
+    return os.environ.get("S3D8_LIBRARY", "") == "debug"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.DEBUG_LIB if _debug_variant() else _build.LIB
 
 
 def load(build_if_missing: bool = False):
@@ -60,13 +66,14 @@ def load(build_if_missing: bool = False):
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(_build.LIB):
-        if not build_if_missing:
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing and not _debug_variant():
             raise RuntimeError(
-                f"S3D8 CUDA library missing at {_build.LIB}; build it with "
+                f"S3D8 CUDA library missing at {path}; build it with "
                 "`python -c 'import __graft_entry__ as g; g.build()'`")
-        _build.build()
-    L = ctypes.CDLL(_build.LIB)
+        _build.build(debug=_debug_variant())
+    L = ctypes.CDLL(path)
     P, I64, SZ, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
     L.s3d8_quantize_act.argtypes = [P, I64, I64, P, P, P]
     L.s3d8_decode.argtypes = [P, P, I64, I64, P, P]

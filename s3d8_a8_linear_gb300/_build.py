@@ -18,6 +18,12 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libs3d8.so")
+# The debug-checks variant: every kernel compiled with S3D8_DEBUG_CHECKS, whose
+# in-kernel bounds checks record S3D8_ERR_BOUNDS instead of touching memory out
+# of range.  Built on request only (build(debug=True)); the binding loads it when
+# the environment variable S3D8_LIBRARY is "debug".
+DEBUG_OUT = os.path.join(OUT, "debug")
+DEBUG_LIB = os.path.join(OUT, "libs3d8_debug.so")
 HEADER = os.path.join(ROOT, "include", "s3d8.h")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -42,20 +48,22 @@ def _inputs_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def up_to_date() -> bool:
-    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _inputs_mtime()
+def up_to_date(lib: str = LIB) -> bool:
+    return os.path.exists(lib) and os.path.getmtime(lib) >= _inputs_mtime()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile every CUDA source for sm_103a and link ``libs3d8.so``."""
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags=None, debug: bool = False) -> str:
+    """Compile every CUDA source for sm_103a and link ``libs3d8.so`` (or, with
+    debug=True, ``libs3d8_debug.so`` with the in-kernel bounds checks)."""
+    lib, out = (DEBUG_LIB, DEBUG_OUT) if debug else (LIB, OUT)
+    if not force and up_to_date(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(OUT, exist_ok=True)
-    flags = NVCC_FLAGS + ARCH + list(extra_flags or [])
+    os.makedirs(out, exist_ok=True)
+    flags = NVCC_FLAGS + ARCH + list(extra_flags or []) + (["-DS3D8_DEBUG_CHECKS"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,13 +75,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

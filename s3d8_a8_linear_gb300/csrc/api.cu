@@ -90,6 +90,7 @@ const char *s3d8_status_string(int status)
     case S3D8_ERR_CUDA: return "CUDA error";
     case S3D8_ERR_TIMEOUT: return "device-side wait timed out";
     case S3D8_ERR_WORKSPACE: return "workspace missing or too small";
+    case S3D8_ERR_BOUNDS: return "in-kernel bounds check failed (debug build)";
     default: return "unknown status";
     }
 }

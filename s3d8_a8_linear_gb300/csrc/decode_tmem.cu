@@ -418,7 +418,7 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                         sum[e] = (uint32_t)(__float2int_rn(v[e]) + (first_chunk ? 0 : (int)s8[e]));
                     if (last_chunk) {
                         const int n = 3 * g + t;
-                        if (g < p.G && n < p.N) {
+                        if (g < p.G && n < p.N && dcheck(p.status, cw.split < p.nsplit)) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const int tok = cb * 8 + e;
@@ -427,10 +427,12 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                             }
                         }
                     } else if (SSUM) {
+                        if (dcheck(p.status, (t * p.nt + cb * 8 + 7) * ROWS + row < 3 * p.nt * ROWS)) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            srow[e * ROWS] = (int32_t)sum[e];
-                    } else {
+                            for (int e = 0; e < 8; ++e)
+                                srow[e * ROWS] = (int32_t)sum[e];
+                        }
+                    } else if (dcheck(p.status, p.s_col + t * p.nt + cb * 8 + 8 <= 512)) {
                         tmem_st8(tmem + lane_off + (uint32_t)(p.s_col + t * p.nt + cb * 8), sum);
                     }
                 }
@@ -457,6 +459,10 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                 break;
             }
             const uint32_t pk = base + (uint32_t)(s * STAGE);
+            if (!dcheck(p.status, s < LST && p.a_col + t * 4 * A_STAGE_COLS + 4 * A_STAGE_COLS <= 512)) {
+                timed_out = true;
+                break;
+            }
 #pragma unroll 1
             for (int kk = 0; kk < 4; ++kk) {
                 uint32_t a[3][8];

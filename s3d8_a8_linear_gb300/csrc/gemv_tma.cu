@@ -336,7 +336,9 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
     const int len0 = min(slice_len, kHalfBytes), len1 = slice_len - len0;
     const uint64_t wpol = l2_evict_first_policy();   // packed bytes are read once per launch
     auto issue_slice = [&](int slot, int row) {
-        if (lane == 0) {
+        if (lane == 0 && dcheck(g.status, slot >= 0 && slot < kDepth && row >= 0 && row < G &&
+                                               slice_off + slice_len <= K &&
+                                               ring + (uint32_t)((slot + 1) * kStage) <= dyn + (uint32_t)smem_size)) {
             const uint8_t *src = job.packed + (size_t)row * K + slice_off;
             const uint32_t dst = ring + slot * kStage;
             const uint32_t b = bar0 + slot * kHalves * 8;
@@ -472,7 +474,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
             else
                 SliceCompute<MT, CH>::template run<false, 0, CH / 2>(st, nch, lane_base, xr, acc);
             __syncwarp();
-            if (refill && lane == 0) {   // first half of the slot is free: refill it
+            if (refill && lane == 0 && dcheck(g.status, next_row < G)) {   // first half of the slot is free: refill it
                 const uint8_t *src = job.packed + (size_t)next_row * K + slice_off;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(b, (uint32_t)len0);
@@ -489,7 +491,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
                 else
                     SliceCompute<MT, CH>::template run<false, CH / 2, CH>(st, nch, lane_base, xr, acc);
                 __syncwarp();
-                if (refill && lane == 0) {
+                if (refill && lane == 0 && dcheck(g.status, next_row < G)) {
                     const uint8_t *src = job.packed + (size_t)next_row * K + slice_off + kHalfBytes;
                     fence_proxy_async_smem();
                     mbar_arrive_expect_tx(b + 8, (uint32_t)len1);
@@ -510,13 +512,13 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
             if (leader && idx < NV) {
                 const int m = idx / 3, n = 3 * row + (idx - 3 * m);
                 if (T == 1) {
-                    if (m < M && n < N) {
+                    if (m < M && n < N && dcheck(g.status, row < G)) {
                         if (job.acc)
                             job.acc[(size_t)m * N + n] = sum;
                         else
                             job.out[(size_t)m * N + n] = epilogue_bf16(sum, xsc[m], job.cs[n]);
                     }
-                } else {
+                } else if (dcheck(g.status, (lrow - r0) * NV + idx < range_rows * NV)) {
                     atomicAdd(&sacc[(lrow - r0) * NV + idx], sum);
                 }
             }
@@ -526,7 +528,7 @@ __global__ __launch_bounds__(kTmaThreads, 1) void gemv_group_kernel(GroupArgs g,
             for (int e = threadIdx.x; e < nrow * NV; e += kTmaThreads) {
                 const int rl = e / NV, idx = e - rl * NV;
                 const int m = idx / 3, n = 3 * (row0 + r0 + rl) + (idx - 3 * m);
-                if (m < M && n < N) {
+                if (m < M && n < N && dcheck(g.status, row0 + r0 + rl < G)) {
                     if (job.acc)
                         job.acc[(size_t)m * N + n] = sacc[e];
                     else

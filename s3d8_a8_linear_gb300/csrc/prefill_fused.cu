@@ -167,7 +167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t full0 = map_to_rank(full, 0);
     auto decode_block = [&](int g) -> bool {
         const int ps = g % PS, s = g % S;
-        if (!mbar_wait_bounded(p_full + 8 * ps, (g / PS) & 1) ||
+        if (!dcheck(p.status, ps < PS && s < S) || !mbar_wait_bounded(p_full + 8 * ps, (g / PS) & 1) ||
             (g >= S && !mbar_wait_bounded(empty + 8 * s, ((g / S) - 1) & 1)))
             return false;
         decode_tile2<FUSED_LUT_COPIES>(base + FUSED_OFF_P + ps * FUSED_P_BYTES, base + FUSED_OFF_B + s * FUSED_B_BYTES,

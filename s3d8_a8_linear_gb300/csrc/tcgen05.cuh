@@ -270,6 +270,8 @@ __device__ __forceinline__ void store_tile_row(const Params &p, int split, int r
                                                const int32_t (&acc)[W], int w = W)
 {
     static_assert(W % 8 == 0, "vector stores take 8 columns");
+    if (!dcheck(p.status, row >= 0 && row < p.M && nbase >= 0 && (p.part == nullptr || split < p.nsplit)))
+        return;
     const bool full = w == W && nbase + W <= p.N;
     int32_t *accp = p.part ? p.part + (size_t)split * p.M * p.N : p.acc;
     const bool vec_acc = p.part ? p.vec_part : p.vec_out;

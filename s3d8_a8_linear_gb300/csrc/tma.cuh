@@ -11,6 +11,25 @@ namespace s3d8 {
 
 constexpr int kWaitPolls = 1 << 22;
 constexpr int kStatusTimeout = -5;  // S3D8_ERR_TIMEOUT
+constexpr int kStatusBounds = -7;   // S3D8_ERR_BOUNDS
+
+// In-kernel bounds check of the debug build (S3D8_DEBUG_CHECKS): a failed
+// check records S3D8_ERR_BOUNDS in the device status word and returns false, so
+// that the caller skips the access; nothing traps.  In the normal build it is
+// `true` and costs nothing.
+#ifdef S3D8_DEBUG_CHECKS
+__device__ __forceinline__ bool dcheck(int *status, bool ok)
+{
+    if (!ok && status)
+        atomicExch(status, kStatusBounds);
+    return ok;
+}
+#else
+__device__ __forceinline__ bool dcheck(int *, bool)
+{
+    return true;
+}
+#endif
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {

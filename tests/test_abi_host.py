@@ -63,9 +63,20 @@ def test_library_exports_every_declared_symbol(lib):
         getattr(lib, fn)
 
 
+def test_debug_build_exports_the_same_symbols():
+    """The debug-checks variant (in-kernel bounds checks) builds here and exports
+    every declared entry point too."""
+    path = _build.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (s3d8_[a-z0-9_]+)$", out, flags=re.M))
+    missing = [fn for fn in declared_functions() if fn not in exported]
+    assert not missing, f"declared but not exported by the debug build: {missing}"
+
+
 def test_status_strings(lib):
     for code, word in ((0, b"ok"), (-1, b"invalid"), (-2, b"misaligned"), (-3, b"unsupported"),
-                       (-4, b"CUDA"), (-5, b"timed out"), (-6, b"workspace")):
+                       (-4, b"CUDA"), (-5, b"timed out"), (-6, b"workspace"), (-7, b"bounds")):
         assert word in lib.s3d8_status_string(code)
     assert lib.s3d8_version() >= 100
 
