@@ -1076,7 +1076,9 @@ def main():
     ap.add_argument("--layer-only", action="store_true",
                     help="time the headline step only (no variants, e2e, sweeps); for profiling")
     ap.add_argument("--prefill-only", action="store_true",
-                    help="run only the M = 2048 tensor-core measurement and print it; for profiling")
+                    help="run only the prefill tensor-core measurement and print it; for profiling")
+    ap.add_argument("--prefill-tokens", type=int, nargs="+", default=None,
+                    help="token counts for --prefill-only (default: 512 and 2048)")
     ap.add_argument("--sweep-only", action="store_true",
                     help="run only the batched-decode sweep (M = 8..64) and print it; for profiling")
     ap.add_argument("--aux-only", action="store_true",
@@ -1097,7 +1099,8 @@ def main():
         import s3d8_a8_linear_gb300 as s3d8
         s3d8.load(build_if_missing=True)
         _, bf16_peak, _ = load_peaks()
-        print(json.dumps(prefill_measure(torch, s3d8, torch.device("cuda:0"), bf16_peak)))
+        print(json.dumps(prefill_measure(torch, s3d8, torch.device("cuda:0"), bf16_peak,
+                                         Ms=args.prefill_tokens)))
         return
     if args.sweep_only:
         import torch
