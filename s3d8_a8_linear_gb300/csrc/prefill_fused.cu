@@ -1,12 +1,13 @@
 // Prefill-regime S3D8 linear on SM pairs with the S3D8 unpack inside the GEMM:
-// tcgen05.mma.cta_group::2 on fp32-exact bf16 chunks, like the one-SM kernel in
-// prefill_tc.cu, with no bf16 copy of the weights anywhere.
+// tcgen05.mma.cta_group::2 kind::f16 on fp16 operands (every int8 value is an
+// fp16 value) with exact fp32 chunks, like the one-SM kernel in prefill_tc.cu,
+// and no 16-bit copy of the weights anywhere.
 //
 // A cluster of two CTAs on two SMs computes a 256-token x 240-channel tile:
 // CTA r of the pair holds activation rows 128 r .. 128 r + 127 of the tile (by
-// bulk tensor copy from the bf16 copy of the codes) and decodes packed rows
+// bulk tensor copy from the fp16 copy of the codes) and decodes packed rows
 // 40 r .. 40 r + 39 of the tile's 80 (channels 120 r .. 120 r + 119) from
-// packed bytes into its half of the bf16 weight tile; the even CTA issues
+// packed bytes into its half of the fp16 weight tile; the even CTA issues
 // M = 256, N = 240 MMAs that read both CTAs' halves, and each CTA's tensor
 // memory receives its own 128 rows of the accumulator.  Per SM and K block the
 // bulk copies bring 16 KiB of activations and 2.5 KiB of packed bytes.
@@ -17,12 +18,14 @@
 //                (cta_group::2 copies);
 //   warp 1       TMEM allocation for the pair (both CTAs, cta_group::2); in the
 //                even CTA the MMA issuer (one elected lane);
-//   warp 2       bulk tensor copies of this CTA's packed halves into a 16-stage
+//   warp 2       bulk tensor copies of this CTA's packed halves into a 12-stage
 //                ring on its own barriers, so that decoding runs ahead of the
 //                MMAs by the whole ring;
 //   warps 3-7    decode: two 8-byte units (one packed row, 8 columns) each per K
-//                block, written into the 128-byte-swizzled K-major bf16 half of
-//                the stage; then a proxy fence (generic writes -> the tensor
+//                block, written into the 128-byte-swizzled K-major fp16 half of
+//                the stage (one 4-byte lookup per packed byte in a lane-
+//                replicated table of biased weights, a byte permute and a packed
+//                fp16 subtract per two weights); then a proxy fence (generic writes -> the tensor
 //                core's async proxy) and an arrive on the even CTA's full
 //                barrier, which completes with 1 + 10 arrivals (the even CTA's
 //                copy-issuing lane, 5 decoder warps x 2 CTAs) and both copies'
@@ -44,9 +47,8 @@ namespace s3d8 {
 namespace tc {
 
 constexpr int FUSED_STAGES = 5;                       // ring of stages: activation half + decoded weight half
-constexpr int FUSED_PSTAGES = 16;                     // ring of packed halves (decoded ahead of the MMA)
-constexpr int FUSED_LUT_COPIES = 8;                   // table copies (two lanes of a half-warp share one)
-constexpr int FUSED_LUT_BYTES = kLutEntries * FUSED_LUT_COPIES * 8;   // 16 KiB
+constexpr int FUSED_PSTAGES = 12;                     // ring of packed halves (decoded ahead of the MMA)
+constexpr int FUSED_LUT_BYTES = kLutEntries * 32 * 4;  // 32 KiB: one 4-byte entry per byte and lane
 constexpr int FUSED_BM = 2 * BM;                      // 256 tokens per pair tile
 constexpr int FUSED_GROUPS = GROUPS / 2;              // 40 packed rows per CTA
 constexpr int FUSED_BH = 3 * FUSED_GROUPS;             // 120 weight rows (channels) per CTA
@@ -71,6 +73,55 @@ static_assert(FUSED_BH % 8 == 0 && FUSED_BN % 16 == 0 && FUSED_BN <= 256, "M = 2
 static_assert(2 * FUSED_DECODERS == FUSED_GROUPS * 8, "two decode units per decoder thread and K block");
 static_assert(FUSED_BH == HALF, "each drain thread holds the sums of one CTA half's columns");
 static_assert(FUSED_DEC_WARP0 + FUSED_DEC_WARPS == DRAIN_WARP0, "decoders are warps 3-7, before the drain warps");
+
+// Decodes the units t and t + nthr (8-byte units: packed row u / 8, columns
+// 8 (u % 8) .. + 7 of the K block) of a packed half into fp16 weights.  Each of
+// the unit's 8 bytes is one table lookup [w0 + 128, w1 + 128, w2 + 128, 0x64];
+// a byte permute of two lookups forms the fp16 pair 0x64xx (1024 + xx) of one
+// channel for two adjacent columns, and a packed subtract of 1152 leaves the
+// weights.  The 16 bytes of channel d (row n = 3 g + d of the half tile) are one
+// 16-byte chunk of the 128-byte-swizzled K-major tile.
+__device__ __forceinline__ void decode_units_f16(uint32_t ptile, uint32_t btile, uint32_t lut_lane, int t, int nthr)
+{
+    uint32_t pk[2][2];
+    int gl[2], j[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int u = t + h * nthr;
+        gl[h] = u >> 3;
+        j[h] = u & 7;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                     : "=r"(pk[h][0]), "=r"(pk[h][1])
+                     : "r"(ptile + gl[h] * 64 + j[h] * 8));
+    }
+    uint32_t L[2][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t byte = prmt(pk[h][i >> 2], 0u, 0x4440u | (uint32_t)(i & 3));
+            L[h][i] = lds_u32_nv(mad_lo_u32(byte, 128u, lut_lane));
+        }
+    constexpr uint32_t kBias = 0x64806480u;   // fp16 (1152, 1152)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t w[3][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            w[0][q] = f16x2_sub(prmt(L[h][2 * q], L[h][2 * q + 1], 0x7430u), kBias);
+            w[1][q] = f16x2_sub(prmt(L[h][2 * q], L[h][2 * q + 1], 0x7531u), kBias);
+            w[2][q] = f16x2_sub(prmt(L[h][2 * q], L[h][2 * q + 1], 0x7632u), kBias);
+        }
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const int n = 3 * gl[h] + d;
+            const uint32_t addr = btile + n * 128 + (((uint32_t)j[h] ^ (uint32_t)(n & 7)) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[d][0]), "r"(w[d][1]),
+                         "r"(w[d][2]), "r"(w[d][3])
+                         : "memory");
+        }
+    }
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     prefill_fused_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_pk,
@@ -139,18 +190,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
-    // decode table: byte -> [bf16 w0 | bf16 w1 << 16, bf16 w2], 8 copies (two
-    // lanes of a half-warp per copy)
+    // decode table: byte -> [w0 + 128, w1 + 128, w2 + 128, 0x64], one copy per
+    // lane (entry b of lane l at lut + 128 b + 4 l), so that a warp's lookups
+    // fall in 32 different banks whatever the bytes
     {
         __shared__ int8_t Cs[96];
         for (int i = threadIdx.x; i < 96; i += THREADS)
             Cs[i] = p.C[i];
         __syncthreads();
-        uint2 *t = reinterpret_cast<uint2 *>(smem + FUSED_OFF_LUT);
-        for (int i = threadIdx.x; i < kLutEntries * FUSED_LUT_COPIES; i += THREADS) {
-            const uint32_t e = expanded_entry(Cs, (uint32_t)(i / FUSED_LUT_COPIES));
-            const int w0 = (int8_t)(e & 0xFF), w1 = (int8_t)((e >> 8) & 0xFF), w2 = (int8_t)((e >> 16) & 0xFF);
-            t[i] = make_uint2(bf16_bits_of(w0) | (bf16_bits_of(w1) << 16), bf16_bits_of(w2));
+        for (int i = threadIdx.x; i < kLutEntries * 8; i += THREADS) {
+            const uint32_t e = (expanded_entry(Cs, (uint32_t)(i >> 3)) ^ 0x00808080u) | 0x64000000u;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(lut + (uint32_t)(i >> 3) * 128u +
+                                                                           (uint32_t)(i & 7) * 16u),
+                         "r"(e)
+                         : "memory");
         }
     }
     tc_fence_before();
@@ -163,15 +216,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // decode of K block g (this CTA's half) into the decoded half of stage g % S,
     // after its packed bytes have landed and the MMAs are done with the stage's
     // last use; the warp then releases the packed stage and signals the even CTA
-    const uint32_t lut_lane = lut + (uint32_t)((lane & (FUSED_LUT_COPIES - 1)) * 8);
+    const uint32_t lut_lane = lut + (uint32_t)lane * 4u;
     const uint32_t full0 = map_to_rank(full, 0);
     auto decode_block = [&](int g) -> bool {
         const int ps = g % PS, s = g % S;
         if (!dcheck(p.status, ps < PS && s < S) || !mbar_wait_bounded(p_full + 8 * ps, (g / PS) & 1) ||
             (g >= S && !mbar_wait_bounded(empty + 8 * s, ((g / S) - 1) & 1)))
             return false;
-        decode_tile2<FUSED_LUT_COPIES>(base + FUSED_OFF_P + ps * FUSED_P_BYTES, base + FUSED_OFF_B + s * FUSED_B_BYTES,
-                                      lut_lane, (int)threadIdx.x - 32 * FUSED_DEC_WARP0, FUSED_DECODERS);
+        decode_units_f16(base + FUSED_OFF_P + ps * FUSED_P_BYTES, base + FUSED_OFF_B + s * FUSED_B_BYTES, lut_lane,
+                         (int)threadIdx.x - 32 * FUSED_DEC_WARP0, FUSED_DECODERS);
         fence_proxy_async_smem();   // generic writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) {
@@ -187,7 +240,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             // ---- this CTA's activation half of every K block, by bulk tensor
             // copy, completing on the even CTA's full barrier (which expects both
             // halves' bytes)
-            pdl_wait();   // the bf16 activation codes come from the kernel before
+            pdl_wait();   // the fp16 activation codes come from the kernel before
             int issued = 0;
             for (int t = cid; t < total && !timed_out; t += nclusters) {
                 const Tile T = tile_of(t);
@@ -235,7 +288,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 // ---- MMA issuer of the pair: the whole warp runs the loop so that
                 // the descriptors stay warp-uniform; one elected lane issues -------
                 int g = 0, gc = 0;
-                const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(FUSED_BN >> 3) << 17) |
+                // fp32 accumulator, fp16 A and B (format 0), K-major, N and M
+                const uint32_t idesc = (1u << 4) | ((uint32_t)(FUSED_BN >> 3) << 17) |
                                        ((uint32_t)(FUSED_BM >> 4) << 24);
                 for (int t = cid; t < total && !timed_out; t += nclusters) {
                     const Tile T = tile_of(t);
@@ -253,7 +307,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         const uint32_t b = base + FUSED_OFF_B + s * FUSED_B_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_bf16_pair_elect(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
+                            mma_f16_pair_elect(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
                                                 (kin | kk) ? 1u : 0u);
                         mma_commit_pair_elect(empty + 8 * s);
                         if (kin == CHUNK_BLOCKS - 1 || kb == T.nk - 1)
@@ -339,9 +393,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 }  // namespace tc
 
-// SM-pair tensor-core GEMM on packed weights: act is the bf16 copy of the
+// SM-pair tensor-core GEMM on packed weights: act_f16 is the fp16 copy of the
 // activation codes [M, K] (in the workspace), part the split-K partials or null.
-cudaError_t launch_prefill_fused(const LinearArgs &a, const __nv_bfloat16 *act, int32_t *part, int nsplit, int kbps,
+cudaError_t launch_prefill_fused(const LinearArgs &a, const uint16_t *act_f16, int32_t *part, int nsplit, int kbps,
                                 cudaStream_t stream)
 {
     using namespace tc;
@@ -357,7 +411,7 @@ cudaError_t launch_prefill_fused(const LinearArgs &a, const __nv_bfloat16 *act, 
     const cuuint64_t dP[2] = {(cuuint64_t)a.K, (cuuint64_t)G};
     const cuuint64_t sP[1] = {(cuuint64_t)a.K};
     const cuuint32_t boxP[2] = {BK, FUSED_GROUPS};
-    if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(act), dA, sA, boxA, es,
+    if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(act_f16), dA, sA, boxA, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
         encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), dP, sP, boxP, es,

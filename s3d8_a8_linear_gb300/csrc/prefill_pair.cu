@@ -167,7 +167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         const uint32_t a = base + s * A_BYTES, b = base + PAIR_OFF_B + s * B_HALF_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_bf16_pair_elect(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
+                            mma_f16_pair_elect(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
                                                 (kin | kk) ? 1u : 0u);
                         mma_commit_pair_elect(l_empty + 8 * s);
                         if (kin == CHUNK_BLOCKS - 1 || kb == T.nk - 1)

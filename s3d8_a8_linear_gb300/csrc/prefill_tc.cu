@@ -336,6 +336,33 @@ __global__ void codes_to_bf16_kernel(const int8_t *__restrict__ xq, __nv_bfloat1
     }
 }
 
+// int8 codes -> fp16 (exact), the A operand of the fused SM-pair kernel: with
+// b = code ^ 0x80 = v + 128, one byte permute builds the fp16 pair 0x64bb
+// (1024 + b) for two codes, and one packed fp16 subtract of 1152 leaves v
+// (fp16 holds every integer of magnitude up to 2048).
+__device__ __forceinline__ void codes16_to_f16(uint4 v, uint4 *dst)
+{
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        o[2 * j] = f16x2_sub(prmt(w[j], 0x64646464u, 0x5140u), 0x64806480u);
+        o[2 * j + 1] = f16x2_sub(prmt(w[j], 0x64646464u, 0x7362u), 0x64806480u);
+    }
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__global__ void codes_to_f16_kernel(const int8_t *__restrict__ xq, uint16_t *__restrict__ a, long n16)
+{
+    pdl_launch_dependents();   // the GEMM may set up meanwhile; it waits before reading a
+    const uint4 *src = reinterpret_cast<const uint4 *>(xq);
+    uint4 *dst = reinterpret_cast<uint4 *>(a);
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+        codes16_to_f16(__ldg(src + i), dst + 2 * i);
+}
+
 // Weights expanded to bf16 [N, K] (row n = component n % 3 of packed row n / 3),
 // the B operand of the SM-pair kernel (prefill_pair.cu).  One thread per 16
 // packed bytes; the 16-copy table of bf16 triples is the kernel's own.
@@ -566,7 +593,11 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, int kind, cudaStream_t stream
     int cgrid = (int)((n16 + 511) / 512);
     if (cgrid > sms * 16)
         cgrid = sms * 16;
-    tc::codes_to_bf16_kernel<<<cgrid, 256, 0, stream>>>(a.xq, act, n16);
+    // the fused SM-pair kernel multiplies fp16 operands, the others bf16
+    if (kind == kTcPairFused)
+        tc::codes_to_f16_kernel<<<cgrid, 256, 0, stream>>>(a.xq, reinterpret_cast<uint16_t *>(act), n16);
+    else
+        tc::codes_to_bf16_kernel<<<cgrid, 256, 0, stream>>>(a.xq, act, n16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
@@ -584,7 +615,7 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, int kind, cudaStream_t stream
     if (kind != kTcOneSm) {
         // the SM-pair kernels (256-token tiles on two SMs)
         e = pre ? launch_prefill_pair(a, act, wdec, part, nsplit, kbps, stream)
-                : launch_prefill_fused(a, act, part, nsplit, kbps, stream);
+                : launch_prefill_fused(a, reinterpret_cast<const uint16_t *>(act), part, nsplit, kbps, stream);
         if (e != cudaSuccess || nsplit == 1)
             return e;
         return launch_splitk_finalize(part, nsplit, a, stream);

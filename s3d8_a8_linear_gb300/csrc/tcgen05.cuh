@@ -186,51 +186,12 @@ __device__ __forceinline__ void decode_tile(uint32_t ptile, uint32_t btile, uint
     }
 }
 
-// As decode_tile for a 40 x 64 packed tile (320 units) and nthr = 160 threads:
-// each thread expands units t and t + 160 with their lookups interleaved, so that
-// the two table-load chains overlap.
-template <int COPIES>
-__device__ __forceinline__ void decode_tile2(uint32_t ptile, uint32_t btile, uint32_t lut_lane, int t, int nthr)
+// Packed fp16 subtract a - b (two lanes), round to nearest.
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b)
 {
-    uint32_t pk[2][2];
-    int gl[2], j[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int u = t + h * nthr;
-        gl[h] = u >> 3;
-        j[h] = u & 7;
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                     : "=r"(pk[h][0]), "=r"(pk[h][1])
-                     : "r"(ptile + gl[h] * 64 + j[h] * 8));
-    }
-    uint2 e[2][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t byte = (pk[h][i >> 2] >> (8 * (i & 3))) & 0xFFu;
-            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                         : "=r"(e[h][i].x), "=r"(e[h][i].y)
-                         : "r"(lut_lane + byte * (COPIES * 8)));
-        }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t w[3][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            w[0][q] = prmt(e[h][2 * q].x, e[h][2 * q + 1].x, 0x5410);
-            w[1][q] = prmt(e[h][2 * q].x, e[h][2 * q + 1].x, 0x7632);
-            w[2][q] = prmt(e[h][2 * q].y, e[h][2 * q + 1].y, 0x5410);
-        }
-#pragma unroll
-        for (int d = 0; d < 3; ++d) {
-            const int n = 3 * gl[h] + d;
-            const uint32_t addr = btile + n * 128 + (((uint32_t)j[h] ^ (uint32_t)(n & 7)) << 4);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[d][0]), "r"(w[d][1]),
-                         "r"(w[d][2]), "r"(w[d][3])
-                         : "memory");
-        }
-    }
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
@@ -366,7 +327,9 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 // M = 256 across the pair; the commit arrives on the barrier at offset `bar` in
 // both CTAs; the tensor copy completes on `bar`, which may be the barrier of the
 // other CTA of the pair.
-__device__ __forceinline__ void mma_bf16_pair_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+// tcgen05.mma.cta_group::2.kind::f16 (bf16 or fp16 operands, as the
+// instruction descriptor says) issued by one elected lane of the warp.
+__device__ __forceinline__ void mma_f16_pair_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
 {
     asm volatile(
         "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
