@@ -21,8 +21,11 @@ Printed JSON (one line, rank 0):
   e2e        the same metric with per-step host->device copies of the
              activations from pinned memory and device->host copies of the
              seven outputs, through the Python binding;
-  prefill    INT8 tensor-op rate of the same library at M = 2048 on the
-             gate/up and down shapes;
+  prefill    INT8 tensor-op rate of the same library at M = 512 and 2048 on
+             the gate/up and down shapes, with the fraction of the measured
+             bf16 tensor peak (the engine the path runs on);
+  decode_sweep  the batched-decode sizes (M = 8..64) with their roofline
+             fractions;
   cpu_baseline  the plain CPU oracle, timed on this host on a bounded sample.
 
 `--impl reference` times the CPU oracle alone on the same workload.
