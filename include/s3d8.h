@@ -73,7 +73,7 @@ typedef enum {
     S3D8_ALGO_AUTO = 0,
     S3D8_ALGO_GEMV = 1,    /* CUDA-core table decode + dp4a; bulk-copy rings up to 8 tokens      */
     S3D8_ALGO_SKINNY = 2,  /* retired: S3D8_ERR_UNSUPPORTED                                      */
-    S3D8_ALGO_TC = 3,      /* tcgen05 bf16 tensor-core GEMM with exact chunked int32 sums       */
+    S3D8_ALGO_TC = 3,      /* tcgen05 16-bit tensor-core GEMM with exact chunked int32 sums    */
     S3D8_ALGO_TMEM = 4     /* tcgen05 fp16 GEMM, weights decoded into tensor memory, 1..64 tokens */
 } s3d8_algo;
 

@@ -249,7 +249,7 @@ size_t s3d8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int algo)
         return 0;
     const int r = resolve_algo(M, N, K, algo);
     if (r == S3D8_ALGO_TC)
-        return prefill_workspace_bytes((int)M, (int)N, (int)K, prefill_kind((int)M));
+        return prefill_workspace_bytes((int)M, (int)N, (int)K, prefill_kind((int)M, (int)K));
     if (r == S3D8_ALGO_TMEM && tmem_supported((int)M))
         return tmem_workspace_bytes((int)M, (int)N, (int)K);
     return 0;
@@ -307,7 +307,7 @@ static int linear_common(const uint8_t *packed, const int8_t *centroids, const v
     a.status = device_status_ptr();
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     if (algo == S3D8_ALGO_TC)
-        return cuda_status(launch_prefill_tc(a, prefill_kind(a.M), strm));
+        return cuda_status(launch_prefill_tc(a, prefill_kind(a.M, a.K), strm));
     if (algo == S3D8_ALGO_TMEM)
         return cuda_status(launch_tmem(a, strm));
     if (gemv_tma_supported(a.M, a.K))

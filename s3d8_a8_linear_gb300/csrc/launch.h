@@ -73,9 +73,10 @@ cudaError_t launch_gemv_group(GroupArgs &g, cudaStream_t stream);
 cudaError_t launch_gemv_tma(const LinearArgs &a, cudaStream_t stream);
 // Tensor-core path, three kernels: one SM per tile (decoding packed tiles
 // itself), SM pairs decoding packed tiles themselves, or SM pairs on weights
-// expanded to bf16 in the workspace first.  prefill_kind(M) picks by token count.
+// expanded to bf16 in the workspace first.  prefill_kind(M, K) picks by token
+// count and row length.
 constexpr int kTcOneSm = 0, kTcPairFused = 1, kTcPairExpanded = 2;
-int prefill_kind(int M);
+int prefill_kind(int M, int K);
 size_t prefill_workspace_bytes(int M, int N, int K, int kind);
 cudaError_t launch_prefill_tc(const LinearArgs &a, int kind, cudaStream_t stream);
 cudaError_t launch_prefill_pair(const LinearArgs &a, const __nv_bfloat16 *act, const __nv_bfloat16 *wdec,

@@ -240,8 +240,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }  // namespace tc
 
 // Channels per pair tile: 256, 192 or 128 (each CTA's half then drains in whole
-// groups of 32 columns), the one that minimises the rounds of tiles the SM pairs run (time per tile taken as proportional to the
-// width plus a fixed 64 columns' worth), the widest on a tie.
+// groups of 32 columns), the one that minimises the rounds of tiles the SM
+// pairs run, time per tile taken as proportional to the width plus a fixed 192
+// columns' worth, the widest on a tie.  (With 64 columns' worth the model chose
+// 192-channel tiles for gate/up at 1536 and 1792 tokens, measured 4% slower
+// than 256; with 192 it picks the faster width on both 11B shapes at 1280,
+// 1536 and 1792 tokens.)
 static int pair_tile_n(int M, int N, int nsplit)
 {
     const long pairs = device_sm_count() / 2 > 0 ? device_sm_count() / 2 : 1;
@@ -250,7 +254,7 @@ static int pair_tile_n(int M, int N, int nsplit)
     long best_cost = -1;
     for (int bn = tc::PAIR_BN; bn >= 128; bn -= 64) {
         const long tiles = mt * ((N + bn - 1) / bn);
-        const long cost = (tiles + pairs - 1) / pairs * (bn + 64);
+        const long cost = (tiles + pairs - 1) / pairs * (bn + 192);
         if (best_cost < 0 || cost < best_cost) {
             best = bn;
             best_cost = cost;

@@ -510,18 +510,24 @@ static size_t align256(size_t v)
     return (v + 255) & ~(size_t)255;
 }
 
-// The kernel for M tokens.  From 384 tokens the SM pairs' 256-token tiles
-// decode each packed weight tile once per 256 tokens instead of once per 128;
-// from 1024 tokens expanding the weights to bf16 once per call costs less than
-// decoding them once per 256-token tile inside the GEMM (measured on GB300 at
-// 512 and 2048 tokens on the 11B shapes: the fused kernel is 1.4-1.6x faster
-// at 512, the expanded one 1.4-1.5x faster at 2048).
+// The kernel for M tokens of K columns.  From 384 tokens the SM pairs'
+// 256-token tiles decode each packed weight tile once per 256 tokens instead of
+// once per 128.  Expanding the weights to bf16 once per call pays off at more
+// tokens: from 896 on rows of up to 8192 columns, from 1280 on longer rows,
+// whose expanded tiles (activation and weight rows of 2 K bytes each) overflow
+// L2 when the SM pairs stream them at once.  Measured on GB300 on the 11B
+// shapes (us, fused / expanded): gate/up (K 4096) 512: 78.8 / 141.9, 768:
+// 106.6 / 104.1, 896: 135.0 / 107.1, 2048: 224.1 / 171.9; down (K 14336) 1023:
+// 109.9 / 163.3, 1280: 200.1 / 173.2, 2048: 206.5 / 186.5.
 constexpr int kPairsMinM = 384;
-constexpr int kExpandMinM = 1024;
+constexpr int kExpandMinMShortK = 896;
+constexpr int kExpandMinMLongK = 1280;
+constexpr int kLongK = 8192;
 
-int prefill_kind(int M)
+int prefill_kind(int M, int K)
 {
-    return M >= kExpandMinM ? kTcPairExpanded : M >= kPairsMinM ? kTcPairFused : kTcOneSm;
+    const int expand_min = K > kLongK ? kExpandMinMLongK : kExpandMinMShortK;
+    return M >= expand_min ? kTcPairExpanded : M >= kPairsMinM ? kTcPairFused : kTcOneSm;
 }
 
 // Workspace: the bf16 copy of the activation codes, then the split-K partials,

@@ -233,7 +233,9 @@ __device__ __forceinline__ void store_tile_row(const Params &p, int split, int r
     static_assert(W % 8 == 0, "vector stores take 8 columns");
     if (!dcheck(p.status, row >= 0 && row < p.M && nbase >= 0 && (p.part == nullptr || split < p.nsplit)))
         return;
-    const bool full = w == W && nbase + W <= p.N;
+    // whole 8-column groups inside N take the vector stores (w is a multiple of 8
+    // for every tile width the kernels use; narrower tiles skip the groups >= w)
+    const bool full = w % 8 == 0 && nbase + w <= p.N;
     int32_t *accp = p.part ? p.part + (size_t)split * p.M * p.N : p.acc;
     const bool vec_acc = p.part ? p.vec_part : p.vec_out;
     if (accp) {
@@ -241,7 +243,8 @@ __device__ __forceinline__ void store_tile_row(const Params &p, int split, int r
         if (full && vec_acc) {
 #pragma unroll
             for (int i = 0; i < W; i += 4)
-                *reinterpret_cast<int4 *>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                if (i < w)
+                    *reinterpret_cast<int4 *>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
         } else {
 #pragma unroll
             for (int i = 0; i < W; ++i)
@@ -255,6 +258,8 @@ __device__ __forceinline__ void store_tile_row(const Params &p, int split, int r
     if (full && p.vec_out) {
 #pragma unroll
         for (int i = 0; i < W; i += 8) {
+            if (i >= w)
+                break;
             uint32_t o[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
