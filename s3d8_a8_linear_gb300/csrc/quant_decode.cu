@@ -4,6 +4,79 @@
 
 namespace s3d8 {
 
+// Two fp32 lanes in one 64-bit register, and the packed fp32 operations on
+// them: mul.rn / add.rn / sub.rn .f32x2 round each lane exactly as the scalar
+// instruction does (no flush to zero), at one issue slot per two values.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// As quant_chunk8, with the multiply and the two rounding steps on value pairs
+// (f32x2): the same result bit for bit, in fewer issue slots.  The standalone
+// quantisation kernels use it (measured 26.5 -> 25.6 us on bf16 [2048, 14336]);
+// the GEMV's fused prologue keeps the scalar form, which measured 1% faster
+// there.
+static __device__ __forceinline__
+uint2 quant_chunk8_x2(uint4 v, float s, float r)
+{
+    if (s == 0.0f)
+        return make_uint2(0u, 0u);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint64_t r2 = f32x2_pack(r, r), m2 = f32x2_pack(kRoundMagic, kRoundMagic);
+    float x[8];
+    uint32_t b[8];
+    bool redo = s < kTinyScale;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // values 2j and 2j + 1 (the two halves of word j) as one pair
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        const uint64_t t2 = f32x2_mul(f32x2_pack(x[2 * j], x[2 * j + 1]), r2);
+        const uint64_t y2 = f32x2_add(t2, m2);
+        const uint64_t d2 = f32x2_sub(t2, f32x2_sub(y2, m2));   // t - rint(t), per lane
+        float d0, d1, y0, y1;
+        f32x2_unpack(d2, d0, d1);
+        f32x2_unpack(y2, y0, y1);
+        redo |= fabsf(d0) > kTieFloor;
+        redo |= fabsf(d1) > kTieFloor;
+        b[2 * j] = __float_as_uint(y0);
+        b[2 * j + 1] = __float_as_uint(y1);
+    }
+    if (redo) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            b[e] = (uint32_t)quant_code(x[e], s, r);
+    }
+    const uint32_t lo = prmt(prmt(b[0], b[1], 0x0040), prmt(b[2], b[3], 0x0040), 0x5410);
+    const uint32_t hi = prmt(prmt(b[4], b[5], 0x0040), prmt(b[6], b[7], 0x0040), 0x5410);
+    return make_uint2(lo, hi);
+}
+
+
 // ---------------------------------------------------------------------------
 // Per-token absmax INT8 quantisation.  Rows of more than 16384 columns: one CTA
 // per row (grid-stride over rows), 16-byte vector loads, two passes over the row
@@ -44,7 +117,7 @@ __global__ __launch_bounds__(kQuantThreads) void quantize_act_kernel(
         uint2 *qrow = reinterpret_cast<uint2 *>(xq + (size_t)m * K);
         for (int c = threadIdx.x; c < chunks; c += kQuantThreads) {
             const uint4 v = __ldg(row + c);
-            qrow[c] = quant_chunk8(v, s, r);
+            qrow[c] = quant_chunk8_x2(v, s, r);
         }
     }
 }
@@ -92,7 +165,7 @@ __global__ __launch_bounds__(kQuantThreads) void quantize_act_rows_kernel(
     for (int i = 0; i < NS; ++i) {
         const int c = threadIdx.x + i * kQuantThreads;
         if (c < chunks)
-            qrow[c] = quant_chunk8(v[i], s, r);
+            qrow[c] = quant_chunk8_x2(v[i], s, r);
     }
 }
 
