@@ -608,9 +608,9 @@ def prefill_measure(torch, s3d8, dev, bf16_peak, Ms=None, reps=20, copies=2):
     # the chip's INT8 tensor rate as the library GEMM reaches it on these shapes
     int8_peak = max(2 * max(Ms) * K * N / (two_step[name]["int8_gemm_us"] * 1e-6) / 1e12
                     for name, K, N in si.SWEEP_SHAPES)
-    res = {"unit": "TOPS (int8 multiply-adds x2)", "engine": "tcgen05.mma kind::f16 (bf16), exact int32",
+    res = {"unit": "TOPS (int8 multiply-adds x2)", "engine": "tcgen05.mma kind::f16 (fp16 operands below the expansion size, bf16 above), exact int32",
            "peak_tflops": bf16_peak, "int8_library_peak_tops": round(int8_peak, 1),
-           "int8_library": "torch._int_mm (cuBLASLt int8 x int8 -> int32) on the same shapes at "
+           "int8_library": "torch._int_mm (PyTorch's CUTLASS int8 x int8 -> int32 mma.sync GEMM) on the same shapes at "
                            f"M = {max(Ms)}, the fastest of the two"}
     for M in Ms:
         tot_ops, tot_ms = 0, 0.0
@@ -659,7 +659,7 @@ def prefill_measure(torch, s3d8, dev, bf16_peak, Ms=None, reps=20, copies=2):
 def two_step_measure(torch, s3d8, dev, M, reps):
     """The pages' prefill method, for comparison: a standalone unpack to dense
     int8 weights (s3d8_decode), then a library GEMM on the dense weights, either
-    INT8 x INT8 -> int32 (torch._int_mm, cuBLASLt) or the same codes as bf16
+    INT8 x INT8 -> int32 (torch._int_mm, a CUTLASS mma.sync GEMM) or the same codes as bf16
     (torch.matmul, cuBLAS).  The epilogue is left out, so these times are lower
     bounds for the two-step layer."""
     out = {}
