@@ -12,15 +12,17 @@
 //
 // Per CTA (one SM, 16 warps):
 //   warp 0      bulk tensor copies: per 64-column block, the packed tile
-//               (128 rows x 64 bytes, 64-byte swizzle) and the fp16 codes
-//               tile (N rows x 128 bytes, 128-byte swizzle) into an 8-stage ring;
+//               (128 rows x 64 bytes, 64-byte swizzle) and the int8 codes tile
+//               (N rows x 64 bytes) into an 8-stage ring;
 //   warps 1-3   issue the MMAs, warp 1 + d those of channel d (one elected
 //               lane each; warp 1 also allocates tensor memory): 4 per block
 //               and warp, after one wait for the block's decoded weights (one
 //               issuing warp for all 12 MMAs of a block was slower);
 //   warps 4-15  three decoder teams of four warps; warp w owns tensor-memory
 //               lanes 32 (w % 4) .. + 31, i.e. packed rows 32 (w % 4) + lane.
-//               Team t decodes the blocks t, t + 3, ...: each thread reads its
+//               Team t decodes the blocks t, t + 3, ...: it first turns the
+//               block's int8 codes tile into the fp16 B operand (128-byte
+//               swizzle) in the same stage, then each thread reads its
 //               row's 64 packed bytes, looks each up in a lane-replicated table
 //               of biased weights [w0 + 128, w1 + 128, w2 + 128, 0x64], and
 //               builds fp16 pairs with one byte permute (0x64xx is the fp16
@@ -52,8 +54,9 @@ constexpr int ROWS = 128;                        // packed rows per tile (the MM
 constexpr int BK = 64;                           // columns per k-block
 constexpr int PK_BYTES = ROWS * BK;              // 8 KiB packed tile
 constexpr int MAX_NT = 64;                       // tokens per MMA (N), a multiple of 16
-constexpr int ACT_BYTES = MAX_NT * BK * 2;       // 8 KiB fp16 codes tile
-constexpr int STAGE = PK_BYTES + ACT_BYTES;
+constexpr int ACT_BYTES = MAX_NT * BK * 2;       // 8 KiB fp16 codes tile (the MMA's B operand)
+constexpr int ACT8_BYTES = MAX_NT * BK;          // 4 KiB int8 codes tile, as copied
+constexpr int STAGE = PK_BYTES + ACT_BYTES + ACT8_BYTES;
 constexpr int MAX_LST = 8;                       // ring stages (4 when the chunk sums live in shared memory)
 constexpr int LUT_BYTES = kLutEntries * 32 * 4;  // 32 KiB, one copy per lane
 
@@ -65,7 +68,7 @@ constexpr int DEC_WARPS = TEAMS * 4;
 constexpr int CHUNK_BLOCKS = 16;                 // 1024 columns per exact fp32 chunk
 constexpr int A_STAGE_COLS = 24;                 // 3 channels x 8 columns
 
-static_assert(STAGE % 1024 == 0 && PK_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
+static_assert(STAGE % 1024 == 0 && PK_BYTES % 1024 == 0 && ACT_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
 
 static_assert(3 * MAX_NT + TEAMS * 4 * A_STAGE_COLS <= 512, "tensor memory");
 
@@ -216,26 +219,29 @@ __device__ __forceinline__ void tma_2d_hint_elect(uint32_t dst, const CUtensorMa
         : "memory");
 }
 
-// int8 codes -> fp16 (exact), 16 per thread and iteration, without int-to-float
+// The stage's int8 codes tile (nt rows x 64 bytes, as copied) -> the fp16 B
+// operand tile (nt rows x 128 bytes, 128-byte swizzle: 16-byte chunk j of row r
+// at r * 128 + (j ^ (r % 8)) * 16), by the 128 threads of a decoder team (thread
+// i takes 8-code chunks i, i + 128, ...).  Exact without int-to-float
 // conversions: with b = code ^ 0x80 = v + 128, one byte permute builds the fp16
-// pair 0x64bb (1024 + b) for two codes and one packed subtract of 1152 leaves v.
-__global__ void codes_to_f16_kernel(const int8_t *__restrict__ xq, __half *__restrict__ a, long n16)
+// pair 0x64bb (1024 + b) for two codes, and one packed subtract of 1152 leaves v.
+__device__ __forceinline__ void codes_tile_to_f16(uint32_t act8, uint32_t act16, int nt, int i)
 {
-    tc::pdl_launch_dependents();   // the GEMM may set up meanwhile; it waits before reading a
-    const uint4 *src = reinterpret_cast<const uint4 *>(xq);
-    uint4 *dst = reinterpret_cast<uint4 *>(a);
-    const long stride = (long)gridDim.x * blockDim.x;
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-        const uint4 v = __ldg(src + i);
-        const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-        uint32_t o[8];
+    for (int c = i; c < nt * 8; c += 128) {
+        const int r = c >> 3, j = c & 7;
+        uint32_t v0, v1;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(act8 + (uint32_t)(c * 8)));
+        const uint32_t w[2] = {v0 ^ 0x80808080u, v1 ^ 0x80808080u};
+        uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            o[2 * j] = hsub2(prmt(w[j], 0x64646464u, 0x5140u), 0x64806480u);
-            o[2 * j + 1] = hsub2(prmt(w[j], 0x64646464u, 0x7362u), 0x64806480u);
+        for (int q = 0; q < 2; ++q) {
+            o[2 * q] = hsub2(prmt(w[q], 0x64646464u, 0x5140u), 0x64806480u);
+            o[2 * q + 1] = hsub2(prmt(w[q], 0x64646464u, 0x7362u), 0x64806480u);
         }
-        dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(act16 + (uint32_t)(r * 128) +
+                                                                       (((uint32_t)j ^ (uint32_t)(r & 7)) << 4)),
+                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                     : "memory");
     }
 }
 
@@ -281,7 +287,7 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     // The copy warp starts the first stages' packed tiles at once, while the
     // table is built: packed weights are never outputs of the kernel before
     // this one (the codes tiles follow after the grid dependency).
-    const uint32_t tx = (uint32_t)PK_BYTES + (uint32_t)p.nt * BK * 2;
+    const uint32_t tx = (uint32_t)PK_BYTES + (uint32_t)p.nt * BK;
     int pre = 0;
     // packed bytes are read once: evict them first, keeping the codes tiles
     // (read by every row tile of a K range) in L2
@@ -323,8 +329,8 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
     tc::pdl_launch_dependents();   // the split-K finish may be scheduled; it waits for this grid
 
     if (warp == 0) {
-        // ---- bulk tensor copies: packed tile + fp16 codes tile per 64-column block
-        tc::pdl_wait();   // the fp16 codes are written by the kernel before this one
+        // ---- bulk tensor copies: packed tile + int8 codes tile per 64-column block
+        tc::pdl_wait();   // the codes may be written by the kernel before this one
         int issued = 0;
         for (Walk w = walk_begin(p, nkb); w.valid; walk_next(p, nkb, w), ++issued) {
             const int s = w.gkb % LST;
@@ -338,7 +344,7 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                 tc::mbar_arrive_expect_tx_elect(full + 8 * s, tx);
                 tma_2d_hint_elect(st, &tm_pk, x, w.rt * ROWS, full + 8 * s, wpol);
             }
-            tc::tma_2d_elect(st + PK_BYTES, &tm_act, x, 0, full + 8 * s);
+            tc::tma_2d_elect(st + PK_BYTES + ACT_BYTES, &tm_act, x, 0, full + 8 * s);
         }
         // never leave with copies in flight (only possible after a timeout)
         const int hi = issued > pre ? issued : pre;
@@ -459,10 +465,14 @@ __global__ __launch_bounds__(THREADS, 1) void tmem_a_kernel(const __grid_constan
                 break;
             }
             const uint32_t pk = base + (uint32_t)(s * STAGE);
-            if (!dcheck(p.status, s < LST && p.a_col + t * 4 * A_STAGE_COLS + 4 * A_STAGE_COLS <= 512)) {
+            if (!dcheck(p.status, s < LST && p.a_col + t * 4 * A_STAGE_COLS + 4 * A_STAGE_COLS <= 512 &&
+                                      p.nt <= MAX_NT)) {
                 timed_out = true;
                 break;
             }
+            // the block's codes as the fp16 B operand, for the async proxy (the MMAs)
+            codes_tile_to_f16(pk + PK_BYTES + ACT_BYTES, pk + PK_BYTES, p.nt, row);
+            fence_proxy_async_smem();
 #pragma unroll 1
             for (int kk = 0; kk < 4; ++kk) {
                 uint32_t a[3][8];
@@ -537,7 +547,7 @@ size_t tmem_workspace_bytes(int M, int N, int K)
 {
     int rtiles, nsplit, kbps;
     wt_plan(M, N, K, device_sm_count(), rtiles, nsplit, kbps);
-    return 256 + wt_align((size_t)M * K * 2) + wt_align((size_t)nsplit * M * N * 4);
+    return 256 + wt_align((size_t)nsplit * M * N * 4);
 }
 
 cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream)
@@ -555,28 +565,19 @@ cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream)
     wt_plan(a.M, a.N, a.K, sms, rtiles, nsplit, kbps);
     const int G = (a.N + 2) / 3;
     const int nt = (a.M + 15) / 16 * 16;
-    __half *act = reinterpret_cast<__half *>(((uintptr_t)a.ws + 255) & ~(uintptr_t)255);
-    int32_t *part = reinterpret_cast<int32_t *>(reinterpret_cast<unsigned char *>(act) +
-                                                wt_align((size_t)a.M * a.K * 2));
+    int32_t *part = reinterpret_cast<int32_t *>(((uintptr_t)a.ws + 255) & ~(uintptr_t)255);
 
-    const long n16 = (long)a.M * a.K / 16;
-    long cgrid = (n16 + 255) / 256;
-    if (cgrid > (long)sms * 8)
-        cgrid = (long)sms * 8;
-    codes_to_f16_kernel<<<(unsigned)cgrid, 256, 0, stream>>>(a.xq, act, n16);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return e;
-
+    // the int8 codes [M, K] themselves: the decoder teams turn each block's tile
+    // into the fp16 operand in shared memory
     CUtensorMap tm_act, tm_pk;
     const cuuint64_t dA[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
-    const cuuint64_t sA[1] = {(cuuint64_t)a.K * 2};
+    const cuuint64_t sA[1] = {(cuuint64_t)a.K};
     const cuuint32_t boxA[2] = {BK, (cuuint32_t)nt}, es[2] = {1, 1};
     const cuuint64_t dP[2] = {(cuuint64_t)a.K, (cuuint64_t)G};
     const cuuint64_t sP[1] = {(cuuint64_t)a.K};
     const cuuint32_t boxP[2] = {BK, ROWS};
-    if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, act, dA, sA, boxA, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(a.xq), dA, sA, boxA, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
         encode(&tm_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), dP, sP, boxP, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -611,7 +612,7 @@ cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream)
     const int lst = p.s_smem ? 4 : MAX_LST;
     const int need = 1024 + lst * STAGE + (p.s_smem ? 3 * nt * ROWS * 4 : 0) + LUT_BYTES + NBARS * 8 + 16;
     auto kernel = p.s_smem ? tmem_a_kernel<4> : tmem_a_kernel<MAX_LST>;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
     if (e != cudaSuccess)
         return e;
     e = tc::launch_pdl(kernel, dim3((unsigned)ctas), dim3(THREADS), (size_t)need, stream, tm_act, tm_pk, p);
