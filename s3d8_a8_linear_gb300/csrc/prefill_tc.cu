@@ -425,6 +425,9 @@ __global__ void finalize_kernel(const int32_t *__restrict__ part, int nsplit, in
                                 __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc, int vec_in,
                                 int vec_out)
 {
+    // The next kernel may set up meanwhile (it waits for this grid before it
+    // reads or writes anything this kernel touches).
+    pdl_launch_dependents();
     pdl_wait();   // the partials are the previous kernel's output
     const size_t plane = (size_t)M * N;
     const int quads = (N + 3) / 4;
@@ -434,12 +437,21 @@ __global__ void finalize_kernel(const int32_t *__restrict__ part, int nsplit, in
             const int n0 = 4 * qd;
             int32_t v[4] = {0, 0, 0, 0};
             if (vec_in) {
-                for (int sp = 0; sp < nsplit; ++sp) {
-                    const int4 t = __ldg(reinterpret_cast<const int4 *>(part + sp * plane + row + n0));
-                    v[0] += t.x;
-                    v[1] += t.y;
-                    v[2] += t.z;
-                    v[3] += t.w;
+                // eight partials' loads in flight at once, not one L2 round trip each
+                for (int sp0 = 0; sp0 < nsplit; sp0 += 8) {
+                    int4 t[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        t[j] = sp0 + j < nsplit
+                                   ? __ldg(reinterpret_cast<const int4 *>(part + (sp0 + j) * plane + row + n0))
+                                   : make_int4(0, 0, 0, 0);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        v[0] += t[j].x;
+                        v[1] += t[j].y;
+                        v[2] += t[j].z;
+                        v[3] += t[j].w;
+                    }
                 }
             } else {
                 for (int sp = 0; sp < nsplit; ++sp)
