@@ -65,7 +65,7 @@ typedef enum {
 } s3d8_status;
 
 /* Algorithm choice for s3d8_linear_ex.  AUTO picks by shape: GEMV up to 4
- * tokens (up to 8 when K > 8192); TMEM for 5..32 tokens otherwise, and up to 64
+ * tokens; TMEM for 5..32 tokens, and up to 64
  * tokens while its tiles fit in one wave on the device; TC otherwise.  The value
  * 2 (a register-fragment mma.sync path, slower than TMEM at every size it took)
  * is retired and stays reserved: it returns S3D8_ERR_UNSUPPORTED. */

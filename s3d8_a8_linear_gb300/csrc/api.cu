@@ -228,9 +228,9 @@ int s3d8_selftest_scaled_abs(const void *x_bf16, const void *alpha_bf16, int64_t
 }
 
 // The algorithm AUTO runs (measured on GB300 on the 11B layer's shapes): the
-// bulk-copy dp4a GEMV up to 4 tokens, and up to 8 on rows longer than 8192
-// columns; the tcgen05 GEMM with the weights decoded into tensor memory for
-// 5..32 tokens otherwise, and up to 64 while its 128-row tiles fit in one wave;
+// bulk-copy dp4a GEMV up to 4 tokens; the tcgen05 GEMM with the weights
+// decoded into tensor memory for 5..32 tokens, and up to 64 while its 128-row
+// tiles fit in one wave;
 // the tcgen05 GEMM on shared-memory tiles otherwise.
 static int resolve_algo(int64_t M, int64_t N, int64_t K, int algo)
 {

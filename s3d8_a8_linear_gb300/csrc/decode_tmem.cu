@@ -531,9 +531,11 @@ bool tmem_supported(int M)
 
 bool tmem_preferred(int M, int N, int K)
 {
-    // 5..8 tokens run the 8-token GEMV, whose dp4a work per byte is then the
-    // largest; on rows of at most 8192 columns this path is faster there too
-    if (M < 5 || M > wt::MAX_NT || (M <= 8 && K > 8192))
+    // from 5 tokens the grouped GEMV runs its 8-token form, whose dp4a work per
+    // byte is the largest; this path is faster there on both 11B shapes (graph-
+    // timed on GB300 at 5, 6 and 8 tokens: gate/up 14.4 against 16.8-17.1 us,
+    // down 16.3-16.8 against 18.0-18.1 us)
+    if (M < 5 || M > wt::MAX_NT)
         return false;
     if (M <= 32)
         return true;
