@@ -590,7 +590,10 @@ bool gemv_tma_supported(int M, int K)
 // Cost = packed bytes, plus for jobs that quantise their activations in-kernel
 // the longer prologue of a long row, in bytes a CTA would have streamed in that
 // time (measured on GB300: about 1.2 us more at K = 14336 than at K = 4096, at
-// about 32 KB per microsecond per SM).
+// about 32 KB per microsecond per SM), times 1.08 for rows cut into several
+// slices (their CTAs streamed ~8% fewer bytes per microsecond in a per-CTA
+// timeline of the 11B layer: shorter last slices and the shared-memory row
+// sums; with the factor the layer step went from 19.41 to 19.24 us).
 static void split_ctas(const GroupArgs &g, int ctas, int *cta_begin)
 {
     const int kStage = stage_bytes(g.M);
@@ -608,6 +611,8 @@ static void split_ctas(const GroupArgs &g, int ctas, int *cta_begin)
             const double est_ctas = ctas * bytes[j] / raw;
             bytes[j] += est_ctas * 1.2 * (g.jobs[j].K - 4096) / 10240.0 * 32768.0;
         }
+        if (T > 1)
+            bytes[j] *= 1.08;
         cap[j] = (int)(G * T < ctas ? G * T : ctas);
         total += bytes[j];
     }
