@@ -10,8 +10,9 @@
 // This file holds the one-SM kernel that decodes packed weight tiles itself
 // (below 384 tokens) and the host side of the three tensor-core kernels: from
 // 384 tokens the SM-pair kernel that decodes the packed tiles itself
-// (prefill_fused.cu), and from 1024 tokens the SM-pair kernel on weights
-// expanded to bf16 once per call (prefill_pair.cu).
+// (prefill_fused.cu, fp16 operands), and from 896 tokens (1280 on rows longer
+// than 8192 columns) the SM-pair kernel on weights expanded to bf16 once per
+// call (prefill_pair.cu).
 //
 // Tile: 128 tokens (MMA M) x 240 output channels (MMA N; 80 whole packed groups)
 // per CTA, K in blocks of 64.  Sixteen warps in four warpgroups:
