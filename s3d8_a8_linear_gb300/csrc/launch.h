@@ -82,7 +82,7 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, int kind, cudaStream_t stream
 cudaError_t launch_prefill_pair(const LinearArgs &a, const __nv_bfloat16 *act, const __nv_bfloat16 *wdec,
                                 int32_t *part, int nsplit, int kbps, cudaStream_t stream);
 cudaError_t launch_prefill_fused(const LinearArgs &a, const uint16_t *act_f16, int32_t *part, int nsplit, int kbps,
-                                 cudaStream_t stream);
+                                 int g2, cudaStream_t stream);
 // Split-K finish shared by the tensor-core paths: sums int32 partials
 // [nsplit][M][N] into a.out (epilogue) or a.acc.
 cudaError_t launch_splitk_finalize(const int32_t *part, int nsplit, const LinearArgs &a, cudaStream_t stream);

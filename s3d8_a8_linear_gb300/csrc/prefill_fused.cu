@@ -50,29 +50,35 @@ constexpr int FUSED_STAGES = 5;                       // ring of stages: activat
 constexpr int FUSED_PSTAGES = 12;                     // ring of packed halves (decoded ahead of the MMA)
 constexpr int FUSED_LUT_BYTES = kLutEntries * 32 * 4;  // 32 KiB: one 4-byte entry per byte and lane
 constexpr int FUSED_BM = 2 * BM;                      // 256 tokens per pair tile
-constexpr int FUSED_GROUPS = GROUPS / 2;              // 40 packed rows per CTA
-constexpr int FUSED_BH = 3 * FUSED_GROUPS;             // 120 weight rows (channels) per CTA
-constexpr int FUSED_BN = 2 * FUSED_BH;                 // 240 channels per pair tile
-constexpr int FUSED_P_BYTES = FUSED_GROUPS * BK;       // 2.5 KiB packed bytes per stage
-constexpr int FUSED_B_BYTES = FUSED_BH * BK * 2;       // 15 KiB decoded half tile
-constexpr int FUSED_DEC_WARP0 = 3;                    // decoders: warps 3-7
-constexpr int FUSED_DEC_WARPS = 5;
-constexpr int FUSED_DECODERS = FUSED_DEC_WARPS * 32;   // two units each per K block
-constexpr int FUSED_OFF_A = 0;
-constexpr int FUSED_OFF_B = FUSED_OFF_A + FUSED_STAGES * A_BYTES;
-constexpr int FUSED_OFF_P = FUSED_OFF_B + FUSED_STAGES * FUSED_B_BYTES;
-constexpr int FUSED_OFF_LUT = FUSED_OFF_P + FUSED_PSTAGES * FUSED_P_BYTES;
-constexpr int FUSED_OFF_BARS = FUSED_OFF_LUT + FUSED_LUT_BYTES;
+constexpr int FUSED_DEC_WARP0 = 3;                    // decoders: warps 3.. (4 or 5 of them)
 constexpr int FUSED_NBARS = 2 * FUSED_STAGES + 2 * FUSED_PSTAGES + 4;
-constexpr int FUSED_SMEM_BYTES = 1024 + FUSED_OFF_BARS + FUSED_NBARS * 8 + 16;
-static_assert(FUSED_B_BYTES % 1024 == 0 && FUSED_OFF_B % 1024 == 0 && A_BYTES % 1024 == 0,
-              "swizzled tiles 1024-aligned");
-static_assert(FUSED_OFF_P % 128 == 0 && FUSED_P_BYTES % 128 == 0 && FUSED_OFF_LUT % 16 == 0, "packed tiles aligned");
-static_assert(FUSED_SMEM_BYTES + 1024 <= 232448, "shared memory budget");
-static_assert(FUSED_BH % 8 == 0 && FUSED_BN % 16 == 0 && FUSED_BN <= 256, "M = 256 MMAs need N a multiple of 16");
-static_assert(2 * FUSED_DECODERS == FUSED_GROUPS * 8, "two decode units per decoder thread and K block");
-static_assert(FUSED_BH == HALF, "each drain thread holds the sums of one CTA half's columns");
-static_assert(FUSED_DEC_WARP0 + FUSED_DEC_WARPS == DRAIN_WARP0, "decoders are warps 3-7, before the drain warps");
+
+// The pair tile for G2 packed rows per CTA: 40 (256 tokens x 240 channels, five
+// decoder warps, 120 columns per drain thread) or 32 (256 x 192, four decoder
+// warps, 96 columns), whichever covers the matrix in fewer rounds of tiles
+// over the SM pairs (fused_tile_groups).
+template <int G2>
+struct FusedTile {
+    static constexpr int TILE_GROUPS = 2 * G2;                 // packed rows per pair tile
+    static constexpr int BH = 3 * G2;                          // weight rows (channels) per CTA
+    static constexpr int BN = 2 * BH;                          // channels per pair tile
+    static constexpr int P_BYTES = G2 * BK;                    // packed bytes per stage
+    static constexpr int B_BYTES = BH * BK * 2;                // decoded half tile
+    static constexpr int DEC_WARPS = G2 / 8;                   // two 8-byte units per thread and K block
+    static constexpr int DECODERS = DEC_WARPS * 32;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + FUSED_STAGES * A_BYTES;
+    static constexpr int OFF_P = OFF_B + FUSED_STAGES * B_BYTES;
+    static constexpr int OFF_LUT = OFF_P + FUSED_PSTAGES * P_BYTES;
+    static constexpr int OFF_BARS = OFF_LUT + FUSED_LUT_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + OFF_BARS + FUSED_NBARS * 8 + 16;
+    static_assert(B_BYTES % 1024 == 0 && OFF_B % 1024 == 0 && A_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
+    static_assert(OFF_P % 128 == 0 && P_BYTES % 128 == 0 && OFF_LUT % 16 == 0, "packed tiles aligned");
+    static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory budget");
+    static_assert(BH % 24 == 0 && BN % 16 == 0 && BN <= 256, "M = 256 MMAs need N a multiple of 16");
+    static_assert(2 * DECODERS == G2 * 8, "two decode units per decoder thread and K block");
+    static_assert(FUSED_DEC_WARP0 + DEC_WARPS <= DRAIN_WARP0, "decoders before the drain warps");
+};
 
 // Decodes the units t and t + nthr (8-byte units: packed row u / 8, columns
 // 8 (u % 8) .. + 7 of the K block) of a packed half into fp16 weights.  Each of
@@ -123,18 +129,20 @@ __device__ __forceinline__ void decode_units_f16(uint32_t ptile, uint32_t btile,
     }
 }
 
+template <int G2>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     prefill_fused_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_pk,
                         Params p)
 {
     constexpr int S = FUSED_STAGES, PS = FUSED_PSTAGES;
+    using F = FusedTile<G2>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *smem = smem_raw + (base - raw);
-    const uint32_t lut = base + FUSED_OFF_LUT;
-    const uint32_t bars = base + FUSED_OFF_BARS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + FUSED_OFF_BARS + FUSED_NBARS * 8);
+    const uint32_t lut = base + F::OFF_LUT;
+    const uint32_t bars = base + F::OFF_BARS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + F::OFF_BARS + FUSED_NBARS * 8);
     // full[S] (even CTA: both CTAs' activation halves of the stage landed and
     // both CTAs' decoded halves written: 1 + 10 arrivals and the copies' bytes),
     // empty[S] (the pair's MMAs are done with the stage; both CTAs), p_full[PS]
@@ -150,7 +158,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t rank = cluster_rank();
     const int cid = (int)blockIdx.x >> 1, nclusters = (int)gridDim.x >> 1;
     const int mtiles = (p.M + FUSED_BM - 1) / FUSED_BM;
-    const int ntiles = ((p.N + 2) / 3 + GROUPS - 1) / GROUPS;
+    const int ntiles = ((p.N + 2) / 3 + F::TILE_GROUPS - 1) / F::TILE_GROUPS;
     const int nk_all = (p.K + BK - 1) / BK;
     const int total = mtiles * ntiles * p.nsplit;
     struct Tile {
@@ -171,12 +179,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full + 8 * s, 1 + 2 * FUSED_DEC_WARPS);
+            mbar_init(full + 8 * s, 1 + 2 * F::DEC_WARPS);
             mbar_init(empty + 8 * s, 1);
         }
         for (int s = 0; s < PS; ++s) {
             mbar_init(p_full + 8 * s, 1);
-            mbar_init(p_empty + 8 * s, FUSED_DEC_WARPS);
+            mbar_init(p_empty + 8 * s, F::DEC_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full + 8 * i, 1);
@@ -223,8 +231,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (!dcheck(p.status, ps < PS && s < S) || !mbar_wait_bounded(p_full + 8 * ps, (g / PS) & 1) ||
             (g >= S && !mbar_wait_bounded(empty + 8 * s, ((g / S) - 1) & 1)))
             return false;
-        decode_units_f16(base + FUSED_OFF_P + ps * FUSED_P_BYTES, base + FUSED_OFF_B + s * FUSED_B_BYTES, lut_lane,
-                         (int)threadIdx.x - 32 * FUSED_DEC_WARP0, FUSED_DECODERS);
+        decode_units_f16(base + F::OFF_P + ps * F::P_BYTES, base + F::OFF_B + s * F::B_BYTES, lut_lane,
+                         (int)threadIdx.x - 32 * FUSED_DEC_WARP0, F::DECODERS);
         fence_proxy_async_smem();   // generic writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) {
@@ -252,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     }
                     if (rank == 0)
                         mbar_arrive_expect_tx_elect(full + 8 * s, 2 * A_BYTES);
-                    tma_2d_pair_elect(base + FUSED_OFF_A + s * A_BYTES, &tm_act, (T.kbase + kb) * BK,
+                    tma_2d_pair_elect(base + F::OFF_A + s * A_BYTES, &tm_act, (T.kbase + kb) * BK,
                                       T.m0 + (int)rank * BM, full0 + 8 * s);
                     ++issued;
                 }
@@ -274,9 +282,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         timed_out = true;
                         break;
                     }
-                    mbar_arrive_expect_tx_elect(p_full + 8 * s, FUSED_P_BYTES);
-                    tma_2d_elect(base + FUSED_OFF_P + s * FUSED_P_BYTES, &tm_pk, (T.kbase + kb) * BK,
-                                 T.nt * GROUPS + (int)rank * FUSED_GROUPS, p_full + 8 * s);
+                    mbar_arrive_expect_tx_elect(p_full + 8 * s, F::P_BYTES);
+                    tma_2d_elect(base + F::OFF_P + s * F::P_BYTES, &tm_pk, (T.kbase + kb) * BK,
+                                 T.nt * F::TILE_GROUPS + (int)rank * G2, p_full + 8 * s);
                     ++issued;
                 }
             }
@@ -289,7 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 // the descriptors stay warp-uniform; one elected lane issues -------
                 int g = 0, gc = 0;
                 // fp32 accumulator, fp16 A and B (format 0), K-major, N and M
-                const uint32_t idesc = (1u << 4) | ((uint32_t)(FUSED_BN >> 3) << 17) |
+                const uint32_t idesc = (1u << 4) | ((uint32_t)(F::BN >> 3) << 17) |
                                        ((uint32_t)(FUSED_BM >> 4) << 24);
                 for (int t = cid; t < total && !timed_out; t += nclusters) {
                     const Tile T = tile_of(t);
@@ -303,8 +311,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a = base + FUSED_OFF_A + s * A_BYTES;
-                        const uint32_t b = base + FUSED_OFF_B + s * FUSED_B_BYTES;
+                        const uint32_t a = base + F::OFF_A + s * A_BYTES;
+                        const uint32_t b = base + F::OFF_B + s * F::B_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk)
                             mma_f16_pair_elect(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc,
@@ -320,7 +328,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (g > 0 && !warp_wait(empty + 8 * ((g - 1) % S), ((g - 1) / S) & 1))
                     timed_out = true;
             }
-        } else if (warp >= FUSED_DEC_WARP0) {
+        } else if (warp >= FUSED_DEC_WARP0 && warp < FUSED_DEC_WARP0 + F::DEC_WARPS) {
             // ---- decode (warps 3-7) -----------------------------------------------
             int g = 0;
             for (int t = cid; t < total && !timed_out; t += nclusters) {
@@ -338,13 +346,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int q = warp & 3;
         const int h = (warp - DRAIN_WARP0) >> 2;   // which 120 of the 240 columns
         const uint32_t release = rank == 0 ? acc_empty : map_to_rank(acc_empty, 0);
-        int32_t acc[HALF];
+        int32_t acc[F::BH];
         // fp32 chunk c in TMEM -> int32 registers; then release its buffer
         auto drain = [&](int c) {
             tc_fence_after();
-            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((c & 1) * 256 + h * HALF);
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((c & 1) * 256 + h * F::BH);
 #pragma unroll
-            for (int gg = 0; gg < HALF / 24; ++gg) {
+            for (int gg = 0; gg < F::BH / 24; ++gg) {
                 float v[3][8];
 #pragma unroll
                 for (int i = 0; i < 3; ++i)
@@ -366,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const Tile T = tile_of(t);
             const int nch = (T.nk + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
 #pragma unroll
-            for (int i = 0; i < HALF; ++i)
+            for (int i = 0; i < F::BH; ++i)
                 acc[i] = 0;
             int cn = gc;   // next chunk to drain
             for (; cn < gc + nch && !timed_out; ++cn) {
@@ -379,7 +387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             gc += nch;
             const int row = T.m0 + (int)rank * BM + 32 * q + lane;
             if (!timed_out && row < p.M)
-                store_tile_row(p, T.split, row, T.nt * FUSED_BN + h * HALF, acc);
+                store_tile_row<F::BH>(p, T.split, row, T.nt * F::BN + h * F::BH, acc);
         }
     }
     if (timed_out)
@@ -393,12 +401,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 }  // namespace tc
 
-// SM-pair tensor-core GEMM on packed weights: act_f16 is the fp16 copy of the
-// activation codes [M, K] (in the workspace), part the split-K partials or null.
-cudaError_t launch_prefill_fused(const LinearArgs &a, const uint16_t *act_f16, int32_t *part, int nsplit, int kbps,
-                                cudaStream_t stream)
+template <int G2>
+static cudaError_t launch_fused_tile(const LinearArgs &a, const uint16_t *act_f16, int32_t *part, int nsplit,
+                                     int kbps, cudaStream_t stream)
 {
     using namespace tc;
+    using F = FusedTile<G2>;
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder_fn());
     if (!encode)
         return cudaErrorNotSupported;
@@ -410,7 +418,7 @@ cudaError_t launch_prefill_fused(const LinearArgs &a, const uint16_t *act_f16, i
     const cuuint32_t boxA[2] = {BK, BM};
     const cuuint64_t dP[2] = {(cuuint64_t)a.K, (cuuint64_t)G};
     const cuuint64_t sP[1] = {(cuuint64_t)a.K};
-    const cuuint32_t boxP[2] = {BK, FUSED_GROUPS};
+    const cuuint32_t boxP[2] = {BK, G2};
     if (encode(&tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(act_f16), dA, sA, boxA, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
@@ -418,26 +426,41 @@ cudaError_t launch_prefill_fused(const LinearArgs &a, const uint16_t *act_f16, i
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FUSED_SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(prefill_fused_kernel<G2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         F::SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
     const Params p = make_params(a, nsplit, kbps, part);
-    const long tiles = (long)((a.M + FUSED_BM - 1) / FUSED_BM) * (long)((G + GROUPS - 1) / GROUPS) * nsplit;
+    const long tiles = (long)((a.M + FUSED_BM - 1) / FUSED_BM) * (long)((G + F::TILE_GROUPS - 1) / F::TILE_GROUPS) *
+                       nsplit;
     if (tiles > 0x7FFFFFFFL)
         return cudaErrorInvalidValue;
     long pairs = device_sm_count() / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * pairs));
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = FUSED_SMEM_BYTES;
+    cfg.dynamicSmemBytes = F::SMEM_BYTES;
     int fit = 0;   // pairs the GPU can hold at once (not every SM may find a partner)
-    if (cudaOccupancyMaxActiveClusters(&fit, prefill_fused_kernel, &cfg) == cudaSuccess && fit > 0 && fit < pairs)
+    if (cudaOccupancyMaxActiveClusters(&fit, prefill_fused_kernel<G2>, &cfg) == cudaSuccess && fit > 0 &&
+        fit < pairs)
         pairs = fit;
     (void)cudaGetLastError();
     const long clusters = tiles < pairs ? tiles : pairs;
-    return launch_pdl(prefill_fused_kernel, dim3((unsigned)(2 * clusters)), dim3(THREADS), (size_t)FUSED_SMEM_BYTES,
-                      stream, tm_act, tm_pk, p);
+    return launch_pdl(prefill_fused_kernel<G2>, dim3((unsigned)(2 * clusters)), dim3(THREADS),
+                      (size_t)F::SMEM_BYTES, stream, tm_act, tm_pk, p);
+}
+
+// SM-pair tensor-core GEMM on packed weights: act_f16 is the fp16 copy of the
+// activation codes [M, K] (in the workspace), part the split-K partials or null;
+// g2 = packed rows per CTA of the tile (fused_tile_groups).
+cudaError_t launch_prefill_fused(const LinearArgs &a, const uint16_t *act_f16, int32_t *part, int nsplit, int kbps,
+                                 int g2, cudaStream_t stream)
+{
+    if (g2 == 32)
+        return launch_fused_tile<32>(a, act_f16, part, nsplit, kbps, stream);
+    if (g2 == 40)
+        return launch_fused_tile<40>(a, act_f16, part, nsplit, kbps, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace s3d8

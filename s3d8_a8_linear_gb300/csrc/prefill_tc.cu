@@ -10,7 +10,7 @@
 // This file holds the one-SM kernel that decodes packed weight tiles itself
 // (below 384 tokens) and the host side of the three tensor-core kernels: from
 // 384 tokens the SM-pair kernel that decodes the packed tiles itself
-// (prefill_fused.cu, fp16 operands), and from 896 tokens (1280 on rows longer
+// (prefill_fused.cu, fp16 operands), and from 769 tokens (1025 on rows longer
 // than 8192 columns) the SM-pair kernel on weights expanded to bf16 once per
 // call (prefill_pair.cu).
 //
@@ -490,20 +490,14 @@ __global__ void finalize_kernel(const int32_t *__restrict__ part, int nsplit, in
 
 // K split of the tensor-core GEMM when its output tiles alone cannot fill the
 // GPU: the number of 64-column blocks per split that minimises
-// waves x (blocks per CTA + a per-CTA fixed cost of about 4 blocks).  CTAs per
-// K range: 128 x 240 tiles on one SM, 256 x 240 tiles on two (fused), or
-// 256 x 256 tiles on two (expanded weights).
-static void tc_plan(int M, int N, int K, int sms, int kind, int &nsplit, int &kb_per_split)
+// waves x (blocks per CTA + a per-CTA fixed cost of about 4 blocks), for
+// `tiles` CTAs per K range.  Returns that cost.
+static double split_plan(long tiles, int nk, int sms, int &nsplit, int &kb_per_split)
 {
-    const long gtiles = ((N + 2) / 3 + tc::GROUPS - 1) / tc::GROUPS;
-    const long tiles = kind == kTcPairExpanded ? 2L * ((M + 255) / 256) * ((N + 255) / 256)
-                       : kind == kTcPairFused  ? 2L * ((M + 255) / 256) * gtiles
-                                               : (long)((M + tc::BM - 1) / tc::BM) * gtiles;
-    const int nk = (K + tc::BK - 1) / tc::BK;
     nsplit = 1;
     kb_per_split = nk;
     if (tiles >= sms)
-        return;
+        return (double)((tiles + sms - 1) / sms) * (nk + 4);
     double best = 1e30;
     for (int s = 1; s <= 16 && s <= nk; ++s) {
         const int kbps = (nk + s - 1) / s;
@@ -516,6 +510,47 @@ static void tc_plan(int M, int N, int K, int sms, int kind, int &nsplit, int &kb
             kb_per_split = kbps;
         }
     }
+    return best;
+}
+
+// Packed rows per CTA of the fused SM-pair kernel's tile: 40 (256 tokens x 240
+// channels) or 32 (256 x 192), whichever gives the lower split-plan cost times
+// the tile's width (+ 48 columns of fixed cost per tile).  On gate/up at 512
+// tokens 40 makes 120 pair tiles for 76 SM pairs (two rounds for 1.6 rounds of
+// work), 32 makes 150 (two rounds of shorter tiles).
+int fused_tile_groups(int M, int N, int K, int sms)
+{
+    const long mt = (M + 255) / 256;
+    const long G = (N + 2) / 3;
+    const int nk = (K + tc::BK - 1) / tc::BK;
+    int best_g2 = 40;
+    double best = 1e30;
+    for (int g2 = 40; g2 >= 32; g2 -= 8) {
+        int ns, kb;
+        const double c = split_plan(2 * mt * ((G + 2 * g2 - 1) / (2 * g2)), nk, sms, ns, kb) * (6.0 * g2 + 48.0);
+        if (c < best - 1e-9) {
+            best = c;
+            best_g2 = g2;
+        }
+    }
+    return best_g2;
+}
+
+// CTAs per K range: 128 x 240 tiles on one SM, 256 x 240 or 256 x 192 tiles on
+// two (fused), or 256 x 256 tiles on two (expanded weights).
+static void tc_plan(int M, int N, int K, int sms, int kind, int &nsplit, int &kb_per_split)
+{
+    const long G = (N + 2) / 3;
+    long tiles;
+    if (kind == kTcPairExpanded) {
+        tiles = 2L * ((M + 255) / 256) * ((N + 255) / 256);
+    } else if (kind == kTcPairFused) {
+        const int g2 = fused_tile_groups(M, N, K, sms);
+        tiles = 2L * ((M + 255) / 256) * ((G + 2 * g2 - 1) / (2 * g2));
+    } else {
+        tiles = (long)((M + tc::BM - 1) / tc::BM) * ((G + tc::GROUPS - 1) / tc::GROUPS);
+    }
+    split_plan(tiles, (K + tc::BK - 1) / tc::BK, sms, nsplit, kb_per_split);
 }
 
 static size_t align256(size_t v)
@@ -525,16 +560,17 @@ static size_t align256(size_t v)
 
 // The kernel for M tokens of K columns.  From 384 tokens the SM pairs'
 // 256-token tiles decode each packed weight tile once per 256 tokens instead of
-// once per 128.  Expanding the weights to bf16 once per call pays off at more
-// tokens: from 896 on rows of up to 8192 columns, from 1280 on longer rows,
-// whose expanded tiles (activation and weight rows of 2 K bytes each) overflow
-// L2 when the SM pairs stream them at once.  Measured on GB300 on the 11B
-// shapes (us, fused / expanded): gate/up (K 4096) 512: 78.8 / 141.9, 768:
-// 106.6 / 104.1, 896: 135.0 / 107.1, 2048: 224.1 / 171.9; down (K 14336) 1023:
-// 109.9 / 163.3, 1280: 200.1 / 173.2, 2048: 206.5 / 186.5.
+// once per 128.  Expanding the weights to bf16 once per call pays off once the
+// fused kernel needs a fourth row of 256-token tiles on rows of up to 8192
+// columns (from 769 tokens), or a fifth on longer rows (from 1025), whose
+// expanded tiles (activation and weight rows of 2 K bytes each) overflow L2
+// when the SM pairs stream them at once.  Measured on GB300 on the 11B shapes
+// (us, fused / expanded): gate/up (K 4096) 512: 70.5 / 141.9, 768: 97.4 /
+// 104.1, 895: 124.8 / 107.1, 2048: 224.1 / 171.9; down (K 14336) 1023:
+// 109.5 / 163.3, 1279: 194.8 / 173.2 (at 1280), 2048: 206.5 / 186.5.
 constexpr int kPairsMinM = 384;
-constexpr int kExpandMinMShortK = 896;
-constexpr int kExpandMinMLongK = 1280;
+constexpr int kExpandMinMShortK = 769;
+constexpr int kExpandMinMLongK = 1025;
 constexpr int kLongK = 8192;
 
 int prefill_kind(int M, int K)
@@ -634,7 +670,8 @@ cudaError_t launch_prefill_tc(const LinearArgs &a, int kind, cudaStream_t stream
     if (kind != kTcOneSm) {
         // the SM-pair kernels (256-token tiles on two SMs)
         e = pre ? launch_prefill_pair(a, act, wdec, part, nsplit, kbps, stream)
-                : launch_prefill_fused(a, reinterpret_cast<const uint16_t *>(act), part, nsplit, kbps, stream);
+                : launch_prefill_fused(a, reinterpret_cast<const uint16_t *>(act), part, nsplit, kbps,
+                                       fused_tile_groups(a.M, a.N, a.K, device_sm_count()), stream);
         if (e != cudaSuccess || nsplit == 1)
             return e;
         return launch_splitk_finalize(part, nsplit, a, stream);
