@@ -89,8 +89,8 @@ cudaError_t launch_splitk_finalize(const int32_t *part, int nsplit, const Linear
 // tcgen05 GEMM with the weights decoded into tensor memory (decode_tmem.cu):
 // 1..64 tokens.
 bool tmem_supported(int M);
-// AUTO takes it for 9..32 tokens (5..8 too on rows of at most 8192 columns), and
-// up to 64 when its tiles fit in one wave (not with more 128-row tiles than SMs).
+// AUTO takes it for 5..32 tokens, and up to 64 when its tiles fit in one wave
+// (not with more 128-row tiles than SMs).
 bool tmem_preferred(int M, int N, int K);
 size_t tmem_workspace_bytes(int M, int N, int K);
 cudaError_t launch_tmem(const LinearArgs &a, cudaStream_t stream);

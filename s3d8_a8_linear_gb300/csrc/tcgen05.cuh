@@ -108,19 +108,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
 }
 
-// Bounded wait taken for the whole warp by lane 0 alone: one phase test per
-// round instead of 32, which keeps the barrier unit free for the other warps'
-// waits and arrivals.  __syncwarp orders the other lanes' later accesses after
-// lane 0's acquire.  All lanes must call it together.
-__device__ __forceinline__ bool warp_wait_one(uint32_t bar, uint32_t parity)
-{
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0)
-        ok = mbar_wait_bounded(bar, parity) ? 1 : 0;
-    __syncwarp();
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
