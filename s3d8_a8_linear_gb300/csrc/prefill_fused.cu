@@ -14,13 +14,13 @@
 //
 // Roles (16 warps per CTA):
 //   warp 0       bulk tensor copies of this CTA's activation halves into a
-//                5-stage ring, completing on the even CTA's full barrier
-//                (cta_group::2 copies);
+//                ring of 5 stages (6 with 192-channel tiles), completing on the
+//                even CTA's full barrier (cta_group::2 copies);
 //   warp 1       TMEM allocation for the pair (both CTAs, cta_group::2); in the
 //                even CTA the MMA issuer (one elected lane);
-//   warp 2       bulk tensor copies of this CTA's packed halves into a 12-stage
-//                ring on its own barriers, so that decoding runs ahead of the
-//                MMAs by the whole ring;
+//   warp 2       bulk tensor copies of this CTA's packed halves into a ring of
+//                12 stages (8 with 192-channel tiles) on its own barriers, so
+//                that decoding runs ahead of the MMAs by the whole ring;
 //   warps 3-7    decode: two 8-byte units (one packed row, 8 columns) each per K
 //                block, written into the 128-byte-swizzled K-major fp16 half of
 //                the stage (one 4-byte lookup per packed byte in a lane-
@@ -46,12 +46,9 @@ namespace s3d8 {
 
 namespace tc {
 
-constexpr int FUSED_STAGES = 5;                       // ring of stages: activation half + decoded weight half
-constexpr int FUSED_PSTAGES = 12;                     // ring of packed halves (decoded ahead of the MMA)
 constexpr int FUSED_LUT_BYTES = kLutEntries * 32 * 4;  // 32 KiB: one 4-byte entry per byte and lane
 constexpr int FUSED_BM = 2 * BM;                      // 256 tokens per pair tile
 constexpr int FUSED_DEC_WARP0 = 3;                    // decoders: warps 3.. (4 or 5 of them)
-constexpr int FUSED_NBARS = 2 * FUSED_STAGES + 2 * FUSED_PSTAGES + 4;
 
 // The pair tile for G2 packed rows per CTA: 40 (256 tokens x 240 channels, five
 // decoder warps, 120 columns per drain thread) or 32 (256 x 192, four decoder
@@ -66,12 +63,19 @@ struct FusedTile {
     static constexpr int B_BYTES = BH * BK * 2;                // decoded half tile
     static constexpr int DEC_WARPS = G2 / 8;                   // two 8-byte units per thread and K block
     static constexpr int DECODERS = DEC_WARPS * 32;
+    // rings: stages of activation half + decoded weight half, and of packed
+    // halves (decoded ahead of the MMAs); with 192-channel tiles a sixth stage
+    // fits beside 8 packed stages (gate/up at 512 tokens 70.7 -> 69.1-69.4 us,
+    // at 768 tokens 97.7 -> 95.7-96.1 us; 6 packed stages measured the same)
+    static constexpr int STAGES = G2 == 32 ? 6 : 5;
+    static constexpr int PSTAGES = G2 == 32 ? 8 : 12;
+    static constexpr int NBARS = 2 * STAGES + 2 * PSTAGES + 4;
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + FUSED_STAGES * A_BYTES;
-    static constexpr int OFF_P = OFF_B + FUSED_STAGES * B_BYTES;
-    static constexpr int OFF_LUT = OFF_P + FUSED_PSTAGES * P_BYTES;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_P = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_LUT = OFF_P + PSTAGES * P_BYTES;
     static constexpr int OFF_BARS = OFF_LUT + FUSED_LUT_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + OFF_BARS + FUSED_NBARS * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 + OFF_BARS + NBARS * 8 + 16;
     static_assert(B_BYTES % 1024 == 0 && OFF_B % 1024 == 0 && A_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
     static_assert(OFF_P % 128 == 0 && P_BYTES % 128 == 0 && OFF_LUT % 16 == 0, "packed tiles aligned");
     static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory budget");
@@ -134,15 +138,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     prefill_fused_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_pk,
                         Params p)
 {
-    constexpr int S = FUSED_STAGES, PS = FUSED_PSTAGES;
     using F = FusedTile<G2>;
+    constexpr int S = F::STAGES, PS = F::PSTAGES;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *smem = smem_raw + (base - raw);
     const uint32_t lut = base + F::OFF_LUT;
     const uint32_t bars = base + F::OFF_BARS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + F::OFF_BARS + FUSED_NBARS * 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + F::OFF_BARS + F::NBARS * 8);
     // full[S] (even CTA: both CTAs' activation halves of the stage landed and
     // both CTAs' decoded halves written: 1 + 10 arrivals and the copies' bytes),
     // empty[S] (the pair's MMAs are done with the stage; both CTAs), p_full[PS]
