@@ -13,23 +13,27 @@
 // bulk copies bring 16 KiB of activations and 2.5 KiB of packed bytes.
 //
 // Roles (16 warps per CTA):
-//   warp 0       bulk tensor copies of this CTA's activation halves into a
-//                ring of 5 stages (6 with 192-channel tiles), completing on the
-//                even CTA's full barrier (cta_group::2 copies);
+//   warp 0       bulk tensor copies, per K block, of this CTA's packed half
+//                (completing on its own barrier) and activation half (cta_group::2
+//                copy, completing on the even CTA's full barrier) into a ring of
+//                6 or 5 stages (32 or 40 packed rows per CTA);
 //   warp 1       TMEM allocation for the pair (both CTAs, cta_group::2); in the
 //                even CTA the MMA issuer (one elected lane);
-//   warp 2       bulk tensor copies of this CTA's packed halves into a ring of
-//                12 stages (8 with 192-channel tiles) on its own barriers, so
-//                that decoding runs ahead of the MMAs by the whole ring;
-//   warps 3-7    decode: two 8-byte units (one packed row, 8 columns) each per K
-//                block, written into the 128-byte-swizzled K-major fp16 half of
-//                the stage (one 4-byte lookup per packed byte in a lane-
-//                replicated table of biased weights, a byte permute and a packed
-//                fp16 subtract per two weights); then a proxy fence (generic writes -> the tensor
-//                core's async proxy) and an arrive on the even CTA's full
-//                barrier, which completes with 1 + 10 arrivals (the even CTA's
-//                copy-issuing lane, 5 decoder warps x 2 CTAs) and both copies'
-//                bytes, so that the MMA issuer waits and commits once per K block;
+//   warps 3-6    decode (3-7 with 40 packed rows per CTA): two 8-byte units (one packed row, 8 columns) each per K block,
+//                written into the 128-byte-swizzled K-major fp16 half of the
+//                stage (one 4-byte lookup per packed byte in a lane-replicated
+//                table of biased weights, a byte permute and a packed fp16
+//                subtract per two weights); then a proxy fence (generic writes ->
+//                the tensor core's async proxy) and an arrive on the even CTA's
+//                full barrier, which completes with 1 + 2 x decoder warps
+//                arrivals (the even CTA's copy-issuing lane, the decoders of
+//                both CTAs) and both activation copies' bytes, so that the MMA
+//                issuer waits and commits once per K block.  A decoder warp waits
+//                on one barrier (the packed half landed) and arrives on one per
+//                block: at ~100 cycles per barrier operation for a warp that has
+//                nothing else to overlap them with, the earlier separate packed
+//                ring (a wait for the packed half, a wait for the stage, two
+//                arrives) spent ~460 of the ~780 cycles each block took;
 //   warps 8-15   drain this CTA's accumulator rows per chunk into int32
 //                (setmaxnreg 176) and write the epilogue.  They release the TMEM
 //                buffer to the even CTA's MMA issuer (16 arrivals: 8 warps x 2
@@ -48,7 +52,6 @@ namespace tc {
 
 constexpr int FUSED_LUT_BYTES = kLutEntries * 32 * 4;  // 32 KiB: one 4-byte entry per byte and lane
 constexpr int FUSED_BM = 2 * BM;                      // 256 tokens per pair tile
-constexpr int FUSED_DEC_WARP0 = 3;                    // decoders: warps 3.. (4 or 5 of them)
 
 // The pair tile for G2 packed rows per CTA: 40 (256 tokens x 240 channels, five
 // decoder warps, 120 columns per drain thread) or 32 (256 x 192, four decoder
@@ -63,17 +66,15 @@ struct FusedTile {
     static constexpr int B_BYTES = BH * BK * 2;                // decoded half tile
     static constexpr int DEC_WARPS = G2 / 8;                   // two 8-byte units per thread and K block
     static constexpr int DECODERS = DEC_WARPS * 32;
-    // rings: stages of activation half + decoded weight half, and of packed
-    // halves (decoded ahead of the MMAs); with 192-channel tiles a sixth stage
-    // fits beside 8 packed stages (gate/up at 512 tokens 70.7 -> 69.1-69.4 us,
-    // at 768 tokens 97.7 -> 95.7-96.1 us; 6 packed stages measured the same)
+    // ring stages of activation half + packed half + decoded weight half, as
+    // many as fit beside the table
     static constexpr int STAGES = G2 == 32 ? 6 : 5;
-    static constexpr int PSTAGES = G2 == 32 ? 8 : 12;
-    static constexpr int NBARS = 2 * STAGES + 2 * PSTAGES + 4;
+    __device__ static int decoder_index(int w) { return w >= 3 && w < 3 + DEC_WARPS ? w - 3 : -1; }
+    static constexpr int NBARS = 3 * STAGES + 4;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_P = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_LUT = OFF_P + PSTAGES * P_BYTES;
+    static constexpr int OFF_LUT = OFF_P + STAGES * P_BYTES;
     static constexpr int OFF_BARS = OFF_LUT + FUSED_LUT_BYTES;
     static constexpr int SMEM_BYTES = 1024 + OFF_BARS + NBARS * 8 + 16;
     static_assert(B_BYTES % 1024 == 0 && OFF_B % 1024 == 0 && A_BYTES % 1024 == 0, "swizzled tiles 1024-aligned");
@@ -81,7 +82,7 @@ struct FusedTile {
     static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory budget");
     static_assert(BH % 24 == 0 && BN % 16 == 0 && BN <= 256, "M = 256 MMAs need N a multiple of 16");
     static_assert(2 * DECODERS == G2 * 8, "two decode units per decoder thread and K block");
-    static_assert(FUSED_DEC_WARP0 + DEC_WARPS <= DRAIN_WARP0, "decoders before the drain warps");
+    static_assert(DEC_WARPS >= 4 && DEC_WARPS <= 5, "four or five decoder warps (warps 3..7)");
 };
 
 // Decodes the units t and t + nthr (8-byte units: packed row u / 8, columns
@@ -139,7 +140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         Params p)
 {
     using F = FusedTile<G2>;
-    constexpr int S = F::STAGES, PS = F::PSTAGES;
+    constexpr int S = F::STAGES;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -148,15 +149,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t bars = base + F::OFF_BARS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + F::OFF_BARS + F::NBARS * 8);
     // full[S] (even CTA: both CTAs' activation halves of the stage landed and
-    // both CTAs' decoded halves written: 1 + 10 arrivals and the copies' bytes),
-    // empty[S] (the pair's MMAs are done with the stage; both CTAs), p_full[PS]
-    // (this CTA's packed half landed), p_empty[PS] (this CTA's decoders are done
-    // with it), acc_full[2] (chunk in TMEM), acc_empty[2] (even CTA: both CTAs
-    // drained it).  One barrier per stage and direction keeps the MMA issuer at
-    // one wait and one commit per K block.
-    const uint32_t full = bars, empty = full + 8 * S;
-    const uint32_t p_full = empty + 8 * S, p_empty = p_full + 8 * PS;
-    const uint32_t acc_full = p_empty + 8 * PS, acc_empty = acc_full + 16;
+    // both CTAs' decoded halves written: 1 + 2 x decoder warps arrivals and the
+    // copies' bytes), empty[S] (the pair's MMAs are done with the stage; both
+    // CTAs), p_full[S] (this CTA's packed half of the stage landed: its copy is
+    // issued after empty, so the stage's decoded half is free too), acc_full[2]
+    // (chunk in TMEM), acc_empty[2] (even CTA: both CTAs drained it).  The MMA
+    // issuer waits and commits once per K block, a decoder warp waits once and
+    // arrives once.
+    const uint32_t full = bars, empty = full + 8 * S, p_full = empty + 8 * S;
+    const uint32_t acc_full = p_full + 8 * S, acc_empty = acc_full + 16;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -185,10 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(full + 8 * s, 1 + 2 * F::DEC_WARPS);
             mbar_init(empty + 8 * s, 1);
-        }
-        for (int s = 0; s < PS; ++s) {
             mbar_init(p_full + 8 * s, 1);
-            mbar_init(p_empty + 8 * s, F::DEC_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full + 8 * i, 1);
@@ -226,32 +224,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     pdl_launch_dependents();   // the split-K finish may be scheduled; it waits for this grid
 
     // decode of K block g (this CTA's half) into the decoded half of stage g % S,
-    // after its packed bytes have landed and the MMAs are done with the stage's
-    // last use; the warp then releases the packed stage and signals the even CTA
+    // once its packed bytes have landed (copied after the MMAs were done with the
+    // stage's last use); the warp then signals the even CTA
     const uint32_t lut_lane = lut + (uint32_t)lane * 4u;
     const uint32_t full0 = map_to_rank(full, 0);
     auto decode_block = [&](int g) -> bool {
-        const int ps = g % PS, s = g % S;
-        if (!dcheck(p.status, ps < PS && s < S) || !mbar_wait_bounded(p_full + 8 * ps, (g / PS) & 1) ||
-            (g >= S && !mbar_wait_bounded(empty + 8 * s, ((g / S) - 1) & 1)))
+        const int s = g % S;
+        if (!dcheck(p.status, s < S) || !mbar_wait_bounded(p_full + 8 * s, (g / S) & 1))
             return false;
-        decode_units_f16(base + F::OFF_P + ps * F::P_BYTES, base + F::OFF_B + s * F::B_BYTES, lut_lane,
-                         (int)threadIdx.x - 32 * FUSED_DEC_WARP0, F::DECODERS);
+        decode_units_f16(base + F::OFF_P + s * F::P_BYTES, base + F::OFF_B + s * F::B_BYTES, lut_lane,
+                         32 * F::decoder_index(warp) + lane, F::DECODERS);
         fence_proxy_async_smem();   // generic writes -> visible to the tensor core
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(p_empty + 8 * ps);
+        if (lane == 0)
             mbar_arrive_remote(full0 + 8 * s);
-        }
         return true;
     };
 
     if (warp < DRAIN_WARP0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
         if (warp == 0) {
-            // ---- this CTA's activation half of every K block, by bulk tensor
-            // copy, completing on the even CTA's full barrier (which expects both
-            // halves' bytes)
+            // ---- this CTA's packed half and activation half of every K block, by
+            // bulk tensor copy: the packed half completes on this CTA's p_full,
+            // both CTAs' activation halves on the even CTA's full barrier (which
+            // expects both halves' bytes).  Packed weights are never outputs of
+            // the kernel before, so the first stages' packed halves are requested
+            // before the grid-dependency wait.
+            auto issue_packed = [&](int s, const Tile &T, int kb) {
+                mbar_arrive_expect_tx_elect(p_full + 8 * s, F::P_BYTES);
+                tma_2d_elect(base + F::OFF_P + s * F::P_BYTES, &tm_pk, (T.kbase + kb) * BK,
+                             T.nt * F::TILE_GROUPS + (int)rank * G2, p_full + 8 * s);
+            };
+            int early = 0;   // packed halves issued before the wait (blocks 0 .. early - 1)
+            for (int t = cid; t < total && early < S; t += nclusters) {
+                const Tile T = tile_of(t);
+                for (int kb = 0; kb < T.nk && early < S; ++kb)
+                    issue_packed(early++, T, kb);
+            }
             pdl_wait();   // the fp16 activation codes come from the kernel before
             int issued = 0;
             for (int t = cid; t < total && !timed_out; t += nclusters) {
@@ -262,6 +271,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         timed_out = true;
                         break;
                     }
+                    if (issued >= early)
+                        issue_packed(s, T, kb);
                     if (rank == 0)
                         mbar_arrive_expect_tx_elect(full + 8 * s, 2 * A_BYTES);
                     tma_2d_pair_elect(base + F::OFF_A + s * A_BYTES, &tm_act, (T.kbase + kb) * BK,
@@ -270,30 +281,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 }
             }
             // never leave with copies in flight: the last stages' MMAs (which
-            // needed every copy of both CTAs) have completed
+            // needed every copy of both CTAs) have completed; packed halves issued
+            // early for blocks the loop never reached (a timeout) have landed
             for (int v = issued - S < 0 ? 0 : issued - S; v < issued; ++v)
                 if (!warp_wait(empty + 8 * (v % S), (v / S) & 1))
                     timed_out = true;
-        } else if (warp == 2) {
-            // ---- this CTA's packed half of every K block (packed weights are
-            // never outputs of the kernel before: no grid-dependency wait)
-            int issued = 0;
-            for (int t = cid; t < total && !timed_out; t += nclusters) {
-                const Tile T = tile_of(t);
-                for (int kb = 0; kb < T.nk; ++kb) {
-                    const int s = issued % PS;
-                    if (issued >= PS && !warp_wait(p_empty + 8 * s, ((issued / PS) - 1) & 1)) {
-                        timed_out = true;
-                        break;
-                    }
-                    mbar_arrive_expect_tx_elect(p_full + 8 * s, F::P_BYTES);
-                    tma_2d_elect(base + F::OFF_P + s * F::P_BYTES, &tm_pk, (T.kbase + kb) * BK,
-                                 T.nt * F::TILE_GROUPS + (int)rank * G2, p_full + 8 * s);
-                    ++issued;
-                }
-            }
-            for (int v = issued - PS < 0 ? 0 : issued - PS; v < issued; ++v)
-                if (!warp_wait(p_full + 8 * (v % PS), (v / PS) & 1))
+            for (int v = issued; v < early; ++v)
+                if (!warp_wait(p_full + 8 * v, 0))
                     timed_out = true;
         } else if (warp == 1) {
             if (rank == 0) {
@@ -332,8 +326,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (g > 0 && !warp_wait(empty + 8 * ((g - 1) % S), ((g - 1) / S) & 1))
                     timed_out = true;
             }
-        } else if (warp >= FUSED_DEC_WARP0 && warp < FUSED_DEC_WARP0 + F::DEC_WARPS) {
-            // ---- decode (warps 3-7) -----------------------------------------------
+        } else if (F::decoder_index(warp) >= 0) {
+            // ---- decode ---------------------------------------------------------------
             int g = 0;
             for (int t = cid; t < total && !timed_out; t += nclusters) {
                 const int nk = tile_of(t).nk;

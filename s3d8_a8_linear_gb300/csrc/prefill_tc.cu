@@ -10,7 +10,7 @@
 // This file holds the one-SM kernel that decodes packed weight tiles itself
 // (below 384 tokens) and the host side of the three tensor-core kernels: from
 // 384 tokens the SM-pair kernel that decodes the packed tiles itself
-// (prefill_fused.cu, fp16 operands), and from 769 tokens (1025 on rows longer
+// (prefill_fused.cu, fp16 operands), and from 1537 tokens (2049 on rows longer
 // than 8192 columns) the SM-pair kernel on weights expanded to bf16 once per
 // call (prefill_pair.cu).
 //
@@ -31,6 +31,7 @@
 #include "tcgen05.cuh"
 
 #include <atomic>
+
 
 namespace s3d8 {
 
@@ -515,19 +516,26 @@ static double split_plan(long tiles, int nk, int sms, int &nsplit, int &kb_per_s
 
 // Packed rows per CTA of the fused SM-pair kernel's tile: 40 (256 tokens x 240
 // channels) or 32 (256 x 192), whichever gives the lower split-plan cost times
-// the tile's width (+ 48 columns of fixed cost per tile).  On gate/up at 512
-// tokens 40 makes 120 pair tiles for 76 SM pairs (two rounds for 1.6 rounds of
-// work), 32 makes 150 (two rounds of shorter tiles).
+// the tile's measured time per K block.  On gate/up at 512 tokens 40 makes 120
+// pair tiles for 76 SM pairs (two rounds for 1.6 rounds of work), 32 makes 150
+// (two rounds of shorter tiles).
 int fused_tile_groups(int M, int N, int K, int sms)
 {
     const long mt = (M + 255) / 256;
     const long G = (N + 2) / 3;
     const int nk = (K + tc::BK - 1) / tc::BK;
+    // time per K block of one pair tile, relative, as measured on GB300 at 512
+    // tokens (gate/up: 0.483 us per block with 32 packed rows per CTA, 0.548 us
+    // with 40; a 24-row tile with three decoder warps, 0.385 us, lost on rounds
+    // at every size and was dropped)
+    const int g2s[2] = {40, 32};
+    const double block_cost[2] = {910.0, 800.0};
     int best_g2 = 40;
     double best = 1e30;
-    for (int g2 = 40; g2 >= 32; g2 -= 8) {
+    for (int i = 0; i < 2; ++i) {
+        const int g2 = g2s[i];
         int ns, kb;
-        const double c = split_plan(2 * mt * ((G + 2 * g2 - 1) / (2 * g2)), nk, sms, ns, kb) * (6.0 * g2 + 48.0);
+        const double c = split_plan(2 * mt * ((G + 2 * g2 - 1) / (2 * g2)), nk, sms, ns, kb) * block_cost[i];
         if (c < best - 1e-9) {
             best = c;
             best_g2 = g2;
@@ -561,16 +569,17 @@ static size_t align256(size_t v)
 // The kernel for M tokens of K columns.  From 384 tokens the SM pairs'
 // 256-token tiles decode each packed weight tile once per 256 tokens instead of
 // once per 128.  Expanding the weights to bf16 once per call pays off once the
-// fused kernel needs a fourth row of 256-token tiles on rows of up to 8192
-// columns (from 769 tokens), or a fifth on longer rows (from 1025), whose
-// expanded tiles (activation and weight rows of 2 K bytes each) overflow L2
-// when the SM pairs stream them at once.  Measured on GB300 on the 11B shapes
-// (us, fused / expanded): gate/up (K 4096) 512: 70.5 / 141.9, 768: 97.4 /
-// 104.1, 895: 124.8 / 107.1, 2048: 224.1 / 171.9; down (K 14336) 1023:
-// 109.5 / 163.3, 1279: 194.8 / 173.2 (at 1280), 2048: 206.5 / 186.5.
+// fused kernel needs a seventh row of 256-token tiles on rows of up to 8192
+// columns (from 1537 tokens); on longer rows, whose expanded tiles (activation
+// and weight rows of 2 K bytes each) overflow L2 when the SM pairs stream them
+// at once, the fused kernel was faster at every size measured, up to 2048
+// tokens.  Measured on GB300 on the 11B shapes (us, fused / expanded): gate/up
+// (K 4096) 1024: 105.9 / 107.9, 1536: 148.8 / 150.5, 1792: 173.8 / 168.0,
+// 2048: 199.4 / 172.6; down (K 14336) 1536: 162.7 / 177.1, 2048: 181.8 /
+// 187.7.
 constexpr int kPairsMinM = 384;
-constexpr int kExpandMinMShortK = 769;
-constexpr int kExpandMinMLongK = 1025;
+constexpr int kExpandMinMShortK = 1537;
+constexpr int kExpandMinMLongK = 2049;
 constexpr int kLongK = 8192;
 
 int prefill_kind(int M, int K)

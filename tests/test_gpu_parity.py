@@ -338,8 +338,8 @@ def test_zero_activation_row_gives_zero(algo):
 TC_TILES = [(128, 240, 64), (129, 241, 1040), (300, 722, 2112), (256, 480, 3072),
             (1, 3, 16), (17, 1201, 1024),
             # from 384 tokens two SMs share each 256-token tile (240 or 192
-            # channels, each SM decoding its 40 or 32 packed rows, fp16); from 769
-            # tokens on rows of up to 8192 columns and from 1025 on longer rows,
+            # channels, each SM decoding its 40 or 32 packed rows, fp16); from 1537
+            # tokens on rows of up to 8192 columns and from 2049 on longer rows,
             # 256 channels of weights expanded to bf16 first: the odd SM's rows
             # past M, partial pair tiles, one K block, split and unsplit K, both
             # sides of both boundaries
@@ -347,9 +347,10 @@ TC_TILES = [(128, 240, 64), (129, 241, 1040), (300, 722, 2112), (256, 480, 3072)
             (1000, 1201, 4096), (2048, 96, 14336), (640, 257, 1024), (512, 512, 2048),
             (768, 722, 2112), (769, 241, 1040), (1024, 96, 14336), (1025, 96, 14336),
             (1023, 722, 2112), (1024, 241, 1040), (1300, 3, 64),
+            (1536, 241, 1040), (1537, 241, 1040), (2049, 96, 14336), (1700, 3, 64),
             # expanded-weight tiles narrower than 256 channels (192 and 128: each
             # drain thread writes 96 or 64 columns) with 16-byte aligned rows
-            (1100, 5000, 128), (1024, 1024, 64)]
+            (1600, 1344, 128), (1600, 1024, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", TC_TILES)
@@ -357,7 +358,7 @@ def test_tc_tiles_and_tails(M, N, K):
     """Tensor-core path in full against the oracle: whole and ragged 128-token and
     240-channel tiles, K ragged against the 64-column block and the 1024-column
     exact chunk, on one SM per tile (small M) and on SM pairs (M >= 384:
-    decoding the weight tiles inside the GEMM below 769 tokens, or 1025 on rows
+    decoding the weight tiles inside the GEMM below 1537 tokens, or 2049 on rows
     longer than 8192 columns; on weights expanded to bf16 first above)."""
     C, packed, cs, x = rand_case(M, N, K, seed=M * 7919 + N * 31 + K)
     xq, xs = oracle.quantize_act(x)

@@ -10,7 +10,7 @@ ordinary entry point (s3d8_linear_ex with the tensor-core algorithm) bit for
 bit, call after call, although every call reuses the same scratch.  Shapes of
 384 tokens and more are included: there the ordinary entry point runs an
 SM-pair GEMM (decoding packed tiles itself, or on pre-expanded weights from
-769 tokens on these rows), while this one keeps the one-SM GEMM and that
+1537 tokens on these rows), while this one keeps the one-SM GEMM and that
 kernel's own K-split plan.  Kept in a file that pytest collects last.
 """
 import numpy as np
