@@ -228,10 +228,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // stage's last use); the warp then signals the even CTA
     const uint32_t lut_lane = lut + (uint32_t)lane * 4u;
     const uint32_t full0 = map_to_rank(full, 0);
+    // The next block's packed half is tested (without blocking) before this
+    // block's decode, so that the test's latency hides behind the decode; when it
+    // has landed the next call skips its wait.  The phase tested cannot be an
+    // older one (that completed with the other parity) nor a later one (that
+    // needs this warp's decode of the next block first).
+    bool next_landed = false;
     auto decode_block = [&](int g) -> bool {
         const int s = g % S;
-        if (!dcheck(p.status, s < S) || !mbar_wait_bounded(p_full + 8 * s, (g / S) & 1))
+        if (!dcheck(p.status, s < S) || (!next_landed && !mbar_wait_bounded(p_full + 8 * s, (g / S) & 1)))
             return false;
+        next_landed = mbar_test(p_full + 8 * ((g + 1) % S), ((g + 1) / S) & 1);
         decode_units_f16(base + F::OFF_P + s * F::P_BYTES, base + F::OFF_B + s * F::B_BYTES, lut_lane,
                          32 * F::decoder_index(warp) + lane, F::DECODERS);
         fence_proxy_async_smem();   // generic writes -> visible to the tensor core
