@@ -191,6 +191,19 @@ def test_linear_workspace_sizes(lib):
     assert ws(64, 4096, 14336, 4) > 0
 
 
+def test_tc_workspace_marks_the_weight_expansion(lib):
+    """The tensor-core workspace holds a 16-bit copy of the weights [N, K] only
+    where the path expands them first: from 1537 tokens on rows of up to 8192
+    columns, from 2049 on longer rows (below, the SM pairs decode the packed
+    tiles inside the GEMM); the 16-bit activation copy grows with M throughout."""
+    ws = lib.s3d8_linear_workspace_size
+    for N, K, last_fused in ((14336, 4096, 1536), (4096, 14336, 2048), (14336, 8192, 1536), (14336, 8208, 2048)):
+        before, after = ws(last_fused, N, K, 3), ws(last_fused + 1, N, K, 3)
+        assert before < N * K * 2 + last_fused * K * 2, (N, K)
+        assert after >= N * K * 2 + (last_fused + 1) * K * 2, (N, K)
+        assert ws(384, N, K, 3) < N * K * 2
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
 
